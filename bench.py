@@ -1,0 +1,424 @@
+#!/usr/bin/env python3
+"""Benchmark of the Palimpsa dual-state recurrence on GB300.
+
+Default workload ("decode"): B=256, H=32, d_k=128, d_v=64, bf16 inputs, fp32
+state. One step = the whole job: a 512-token chunked prefill (forward_chunked)
+that leaves mu, I resident in HBM, then 1024 recurrent decode steps
+(palimpsa_step) on that state. The metric is head-tokens processed per second
+(B*H*(512 + 1024) per step); the dominant kernel is the decode step, bound by
+HBM bandwidth (it streams the 537 MB state in and out every token).
+
+Other workloads (``--workload small_layer|layer_760m|long_context|tiny``): one
+step = one chunked forward over the whole configuration (ALU-bound).
+
+Prints ONE JSON line on rank 0. ``--impl reference`` times the fp64 CPU oracle
+on a bounded sample of the same workload instead.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "Palimpsa scan throughput (B·H·T tokens/s) and % of GB300 HBM roofline"
+UNIT = "head-tokens/s"
+FALLBACK_HBM_GBS = 6800.0
+SM_COUNT_GB300 = 152
+MUFU_RCP_PER_CLK_PER_SM = 16     # SFU reciprocal issue rate per SM (one per element-token)
+
+
+# ----------------------------------------------------------------------------- helpers
+
+def _dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def _measured_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as f:
+            return json.load(f), "measured"
+    except Exception:
+        return {"hbm_gbs": FALLBACK_HBM_GBS, "sm_max_mhz": 2070.0}, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi clock/throttle sampling during the timed region."""
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.out = os.path.join("/tmp", f"palimpsa_clocks_{os.getpid()}.csv")
+
+    def __enter__(self):
+        try:
+            self.fh = open(self.out, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "200"], stdout=self.fh, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+            self.fh.close()
+
+    def summary(self):
+        if self.proc is None or not os.path.exists(self.out):
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        rows = []
+        with open(self.out) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) >= 8:
+                    rows.append(parts)
+        try:
+            os.remove(self.out)
+        except OSError:
+            pass
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+
+        def num(x):
+            try:
+                return float(x)
+            except ValueError:
+                return None
+        sm = [num(r[0]) for r in rows if num(r[0]) is not None]
+        mx = [num(r[1]) for r in rows if num(r[1]) is not None]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[4 + i].lower().startswith("active")})
+        pw = [num(r[2]) for r in rows if num(r[2]) is not None]
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(rows), "power_w_max": max(pw) if pw else None}
+
+
+# ----------------------------------------------------------------------------- byte / work accounting
+
+def decode_step_bytes(B, H, dk, dv, in_bytes):
+    """Algorithmic HBM bytes of one palimpsa_step launch: mu and I read and written
+    (16 B per state element) plus q, k, v, beta, d_t in and y out."""
+    state = B * H * dv * dk * 4 * 2 * 2
+    inputs = B * H * (2 * dk + 2 * dv) * in_bytes + B * H * 4 + 2 * H * 4
+    out = B * H * dv * 4
+    return state + inputs + out
+
+
+def forward_bytes(B, H, T, dk, dv, in_bytes):
+    """Algorithmic HBM bytes of one forward_chunked launch: every input once, y
+    once, the final state written once (the initial state is synthesised)."""
+    per_tok = (2 * dk + 2 * dv) * in_bytes + 4 + dv * 4
+    return B * H * T * per_tok + B * H * dv * dk * 4 * 2 + 2 * H * 4
+
+
+# ----------------------------------------------------------------------------- our implementation
+
+def run_ours(args, ws, rank, local):
+    import torch
+    import torch.distributed as dist
+
+    import metaplastic_linear_attention_gb300 as pal
+    from metaplastic_linear_attention_gb300 import build_lib
+    from metaplastic_linear_attention_gb300 import synthetic as syn
+
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if ws > 1:
+        dist.init_process_group("nccl", device_id=dev)
+    build_lib.build()
+    pal.load_library()
+    wl = syn.WORKLOADS[args.workload]
+    seed = wl.seed + 1000 * rank           # each rank an independent replica (weak scaling)
+    inp = syn.sequence_inputs(wl, device=dev, seed=seed)
+    B, H, T, dk, dv = wl.B, wl.H, wl.T, wl.d_k, wl.d_v
+    in_bytes = 2 if wl.bf16 else 4
+    S = wl.steps
+    dec = syn.decode_inputs(wl, S, device=dev, seed=seed) if S else None
+    f32 = torch.float32
+    y_pre = torch.empty((B, H, T, dv), dtype=f32, device=dev)
+    mu = torch.empty((B, H, dv, dk), dtype=f32, device=dev)
+    I = torch.empty((B, H, dv, dk), dtype=f32, device=dev)
+    y_dec = torch.empty((max(S, 1), B, H, dv), dtype=f32, device=dev)
+    stream = torch.cuda.current_stream()
+
+    ev = []
+
+    def one_step(record=False):
+        e0 = torch.cuda.Event(enable_timing=True) if record else None
+        e1 = torch.cuda.Event(enable_timing=True) if record else None
+        e2 = torch.cuda.Event(enable_timing=True) if record else None
+        if record:
+            e0.record(stream)
+        pal.palimpsa_forward_chunked(inp["q"], inp["k"], inp["v"], inp["beta"], inp["d_t"], inp["A"],
+                                     inp["I_prior"], y=y_pre, mu_T=mu, I_T=I, chunk=wl.chunk)
+        if record:
+            e1.record(stream)
+        for s in range(S):
+            pal.palimpsa_step(dec["q"][s], dec["k"][s], dec["v"][s], dec["beta"][s], dec["d_t"][s], inp["A"],
+                              inp["I_prior"], mu, I, y=y_dec[s])
+        if record:
+            e2.record(stream)
+            ev.append((e0, e1, e2))
+
+    for _ in range(args.warmup):
+        one_step()
+    torch.cuda.synchronize()
+    st = pal.palimpsa_get_device_status()
+    if st != 0:
+        raise RuntimeError(f"device status after warm-up: {pal.palimpsa_status_string(st)}")
+
+    if ws > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    with ClockSampler(local) as clk:
+        t_start.record(stream)
+        for _ in range(args.steps):
+            one_step(record=True)
+        t_end.record(stream)
+        torch.cuda.synchronize()
+    if ws > 1:
+        dist.barrier()
+    ms_total = t_start.elapsed_time(t_end)
+    pre_ms = [a.elapsed_time(b) for a, b, _ in ev]
+    dec_ms = [b.elapsed_time(c) for _, b, c in ev]
+    if ws > 1:
+        t = torch.tensor([ms_total], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms_total = float(t.item())
+    clocks = clk.summary()
+    st = pal.palimpsa_get_device_status()
+    if st != 0:
+        raise RuntimeError(f"device status after timing: {pal.palimpsa_status_string(st)}")
+
+    ms_step = ms_total / args.steps
+    head_tokens = B * H * (T + S)
+    value = head_tokens * ws / (ms_step / 1e3)
+
+    peaks, peak_kind = _measured_peaks()
+    hbm_peak = float(peaks.get("hbm_gbs", FALLBACK_HBM_GBS))
+    kernels = {}
+    fwd_avg_ms = statistics.mean(pre_ms)
+    fb = forward_bytes(B, H, T, dk, dv, in_bytes)
+    E_fwd = B * H * T * dv * dk
+    sm_max = float(peaks.get("sm_max_mhz", 2070.0))
+    alu_peak = SM_COUNT_GB300 * MUFU_RCP_PER_CLK_PER_SM * sm_max * 1e6 / 1e9   # G element-updates/s
+    kernels["palimpsa_fwd_chunked"] = {
+        "launches_per_step": 1, "avg_ms": fwd_avg_ms,
+        "head_tokens_per_s": B * H * T / (fwd_avg_ms / 1e3),
+        "hbm_gbs": fb / (fwd_avg_ms / 1e3) / 1e9,
+        "alu": {"achieved": E_fwd / (fwd_avg_ms / 1e3) / 1e9, "peak": alu_peak, "unit": "G element-updates/s",
+                "frac": E_fwd / (fwd_avg_ms / 1e3) / 1e9 / alu_peak},
+    }
+    if S:
+        dec_avg_ms = statistics.mean(dec_ms) / S
+        db = decode_step_bytes(B, H, dk, dv, in_bytes)
+        ach = db / (dec_avg_ms / 1e3) / 1e9
+        kernels["palimpsa_step"] = {"launches_per_step": S, "avg_ms": dec_avg_ms,
+                                    "head_tokens_per_s": B * H / (dec_avg_ms / 1e3), "hbm_gbs": ach,
+                                    "bytes_per_launch": db}
+        roofline = {"bound": "hbm", "kernel": "palimpsa_step", "achieved": ach, "peak": hbm_peak, "unit": "GB/s",
+                    "frac": ach / hbm_peak, "traffic": args.traffic, "peak_source": f"{peak_kind} hbm_gbs",
+                    "bytes_per_launch": db}
+    else:
+        a = kernels["palimpsa_fwd_chunked"]["alu"]
+        roofline = {"bound": "alu", "kernel": "palimpsa_fwd_chunked", "achieved": a["achieved"], "peak": alu_peak,
+                    "unit": "G element-updates/s", "frac": a["frac"], "traffic": args.traffic,
+                    "peak_source": f"{SM_COUNT_GB300} SMs x {MUFU_RCP_PER_CLK_PER_SM} rcp/clk x {sm_max:.0f} MHz"}
+
+    e2e = None
+    if not args.no_e2e:
+        e2e = run_e2e(args, wl, inp, dec, dev, pal, ws)
+
+    cpu = None
+    if rank == 0 and not args.no_cpu_baseline:
+        cpu = cpu_baseline(wl, args.cpu_seconds)
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+            "config": {"workload": _describe(wl), "B": B, "H": H, "T_prefill": T, "decode_steps": S, "d_k": dk,
+                       "d_v": dv, "inputs": "bf16" if wl.bf16 else "f32", "state": "f32",
+                       "head_tokens_per_step": head_tokens,
+                       "l2": "inputs larger than L2 (state alone is %.0f MB)" % (B * H * dv * dk * 8 / 1e6),
+                       "parallelism": f"replicas x{ws}" if ws > 1 else "single GPU"},
+            "roofline": roofline, "kernels": kernels, "cpu_baseline": cpu, "e2e": e2e,
+            "gpu_launches": (1 + S) * args.steps, "clocks": clocks,
+        }
+        print(json.dumps(line), flush=True)
+    if ws > 1:
+        dist.destroy_process_group()
+
+
+def _describe(wl):
+    if wl.steps:
+        return (f"{wl.name}: B={wl.B} H={wl.H} d_k={wl.d_k} d_v={wl.d_v}, {wl.T}-token chunked prefill + "
+                f"{wl.steps} decode steps, {'bf16' if wl.bf16 else 'fp32'} inputs, fp32 state")
+    return (f"{wl.name}: B={wl.B} H={wl.H} T={wl.T} d_k={wl.d_k} d_v={wl.d_v}, chunked forward, "
+            f"{'bf16' if wl.bf16 else 'fp32'} inputs, fp32 state")
+
+
+def run_e2e(args, wl, inp, dec, dev, pal, ws):
+    """Same job through the public calls with pinned HOST inputs and outputs:
+    every step copies its inputs host->device and its y device->host."""
+    import torch
+    import torch.distributed as dist
+
+    B, H, T, dk, dv, S = wl.B, wl.H, wl.T, wl.d_k, wl.d_v, wl.steps
+    h_inp = {k: v.to("cpu").pin_memory() for k, v in inp.items()}
+    h_dec = {k: v.to("cpu").pin_memory() for k, v in dec.items()} if S else None
+    h_ypre = torch.empty((B, H, T, dv), dtype=torch.float32, pin_memory=True)
+    h_ydec = torch.empty((max(S, 1), B, H, dv), dtype=torch.float32, pin_memory=True)
+    mu = torch.empty((B, H, dv, dk), dtype=torch.float32, device=dev)
+    I = torch.empty_like(mu)
+
+    def one_step():
+        pal.palimpsa_forward_chunked(h_inp["q"], h_inp["k"], h_inp["v"], h_inp["beta"], h_inp["d_t"], h_inp["A"],
+                                     h_inp["I_prior"], y=h_ypre, mu_T=mu, I_T=I, chunk=wl.chunk)
+        for s in range(S):
+            pal.palimpsa_step(h_dec["q"][s], h_dec["k"][s], h_dec["v"][s], h_dec["beta"][s], h_dec["d_t"][s],
+                              h_inp["A"], h_inp["I_prior"], mu, I, y=h_ydec[s])
+
+    for _ in range(args.warmup):
+        one_step()
+    torch.cuda.synchronize()
+    if ws > 1:
+        dist.barrier()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        one_step()
+    torch.cuda.synchronize()
+    el = time.perf_counter() - t0
+    if ws > 1:
+        t = torch.tensor([el], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        el = float(t.item())
+    h2d = sum(v.numel() * v.element_size() for v in h_inp.values())
+    h2d += 2 * H * 4 * S  # A and I_prior go with every step call
+    if S:
+        h2d += sum(v.numel() * v.element_size() for v in h_dec.values())
+    d2h = h_ypre.numel() * 4 + (S * B * H * dv * 4 if S else 0)
+    value = B * H * (T + S) * ws / (el / args.steps)
+    return {"value": value, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+            "ms_per_step": el / args.steps * 1e3, "timer": "host wall clock around device-synchronised steps"}
+
+
+# ----------------------------------------------------------------------------- the oracle (CPU baseline)
+
+def _oracle_sample(wl, n_heads, seed=12345):
+    """A bounded sample of the workload for the fp64 oracle: n_heads heads over the
+    whole token stream (prefill followed by the decode tokens, which the oracle
+    treats as one continuous scan: a decode step is one token of the recurrence)."""
+    import numpy as np
+    import torch
+
+    from metaplastic_linear_attention_gb300 import synthetic as syn
+    Ttot = wl.T + wl.steps
+    sub = wl.with_(B=1, H=n_heads, T=Ttot, steps=0)
+    x = syn.sequence_inputs(sub, seed=seed)
+    f = syn.as_float64_numpy
+    return [f(x[k]) for k in ("q", "k", "v", "beta", "d_t", "A", "I_prior")], n_heads * Ttot
+
+
+def cpu_baseline(wl, seconds):
+    import oracle
+    threads = oracle.max_threads()
+    args1, ht1 = _oracle_sample(wl, 1)
+    t0 = time.perf_counter()
+    oracle.forward(*args1)
+    t1 = time.perf_counter() - t0
+    n = max(1, min(wl.B * wl.H, int(seconds / max(t1, 1e-3))))
+    args_n, ht = _oracle_sample(wl, n)
+    t0 = time.perf_counter()
+    oracle.forward(*args_n)
+    el = time.perf_counter() - t0
+    return {"value": ht / el, "unit": UNIT, "cores": threads, "kind": "oracle",
+            "sample": f"{n} head(s) x {wl.T + wl.steps} tokens (d_k={wl.d_k}, d_v={wl.d_v}) of the {wl.name} "
+                      f"workload, fp64 C oracle, {el:.1f} s"}
+
+
+def run_reference(args, ws, rank):
+    """--impl reference: the fp64 CPU oracle on the host cores, on a bounded sample of
+    the same workload per step (rank 0 only)."""
+    if rank != 0:
+        return
+    import oracle
+    from metaplastic_linear_attention_gb300 import synthetic as syn
+    wl = syn.WORKLOADS[args.workload]
+    oracle.build()
+    threads = oracle.max_threads()
+    args1, _ = _oracle_sample(wl, 1)
+    t0 = time.perf_counter()
+    oracle.forward(*args1)
+    t1 = time.perf_counter() - t0
+    per_step = max(0.5, min(args.ref_step_seconds, 150.0 / max(1, args.steps + args.warmup)))
+    n = max(1, min(wl.B * wl.H, int(per_step / max(t1, 1e-3))))
+    sample, ht = _oracle_sample(wl, n)
+    for _ in range(args.warmup):
+        oracle.forward(*sample)
+    times = []
+    for _ in range(args.steps):
+        t0 = time.perf_counter()
+        oracle.forward(*sample)
+        times.append(time.perf_counter() - t0)
+    el = sum(times)
+    value = ht * args.steps / el
+    desc = (f"{n} head(s) x {wl.T + wl.steps} tokens of the {wl.name} workload per step, fp64 C oracle "
+            f"({threads} threads)")
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": el / args.steps * 1e3,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": _describe(wl), "sample": desc},
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": threads, "kind": "oracle", "sample": desc},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    p = argparse.ArgumentParser(description=__doc__.split("\n\n")[0])
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=5)
+    p.add_argument("--warmup", type=int, default=3)
+    p.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    p.add_argument("--workload", default="decode",
+                   choices=["decode", "small_layer", "layer_760m", "long_context", "tiny"])
+    p.add_argument("--no-e2e", action="store_true")
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--cpu-seconds", type=float, default=12.0, help="target oracle time for cpu_baseline")
+    p.add_argument("--ref-step-seconds", type=float, default=4.0)
+    p.add_argument("--traffic", type=float, default=None,
+                   help="DRAM bytes per launch of the dominant kernel from an ncu capture (else null)")
+    args = p.parse_args()
+    if args.warmup < 3:
+        p.error("--warmup must be >= 3")
+    ws, rank, local = _dist_env()
+    if args.impl == "reference":
+        run_reference(args, ws, rank)
+        return
+    run_ours(args, ws, rank, local)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,161 @@
+/*
+ * palimpsa.h — C ABI of the GB300 (sm_103a) Palimpsa dual-state recurrence.
+ *
+ * The operation is the metaplastic linear attention of Bonnet, Lohoff,
+ * Finkbeiner, Shiqerukaj and Neftci, "Learning to Remember, Learn, and Forget
+ * in Attention-Based Models" (ICML 2026). Per head it keeps a memory mean
+ * mu and an elementwise precision ("importance") I, both d_v x d_k, and for
+ * every token t:
+ *
+ *   alpha_t = exp(-A * d_t)                                   (slide 5; paper Sec. 2.2)
+ *   I_t     = alpha_t I_{t-1} + (1 - alpha_t) I_prior + beta_t (x) k_t^2
+ *   mu_t    = alpha_t (I_{t-1} / I_t) (.) mu_{t-1}
+ *             + (1 / I_t) (.) [(beta_t (.) v_t) (x) k_t]       (slide 7; paper Eq. 5)
+ *   y_t     = mu_t q_t                                         (slide 4; paper Eq. 2)
+ *
+ * Squares, divisions and (.) are elementwise; (x) is an outer product with the
+ * value index i as the row and the key index j as the column. The read y_t
+ * uses the state after token t's write. The chunked entry point evaluates the
+ * same recurrence through the natural parameters M = I (.) mu and I (slide 9;
+ * paper App. A.12); the step entry point is the recurrent inference update of
+ * one token (slide 22; paper App. A.13, Fig. 7).
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ * - Memory: every array argument is a DEVICE pointer owned by the caller;
+ *   nothing is copied, retained or freed. All arrays are dense row-major.
+ * - Alignment: every array pointer must be 16-byte aligned, except d_t, A and
+ *   I_prior (4-byte aligned). Misaligned pointers give PALIMPSA_ERR_ALIGN.
+ * - Sizes: 1 <= B, H; d_k in {64, 128}; d_v a multiple of 8 in [8, 256].
+ * - Input dtype: q, k, v, beta are PALIMPSA_F32 (float) or PALIMPSA_BF16
+ *   (__nv_bfloat16, upcast exactly to fp32). d_t, A, I_prior, the state and
+ *   y are always fp32. All arithmetic is fp32.
+ * - Streams: work is enqueued on `cuda_stream` (a cudaStream_t, NULL = the
+ *   legacy default stream) on the CURRENT device; the call returns without
+ *   synchronising. Argument checks run on the host before anything is
+ *   enqueued: when a call returns an error nothing was launched and no output
+ *   was written.
+ * - Domain: A > 0, I_prior > 0, d_t >= 0, beta >= 0 and I0 > 0 (all finite)
+ *   are preconditions. The kernels test them as they read the inputs; a
+ *   violation leaves that call's outputs unspecified and latches
+ *   PALIMPSA_ERR_DOMAIN into the device status word (palimpsa_get_device_status).
+ * - Errors are returned as status codes; nothing aborts and no C++ exception
+ *   crosses this interface. A CUDA launch failure returns PALIMPSA_ERR_CUDA.
+ * - Thread safety: calls may be made from several host threads; the debug
+ *   setters below are process-wide.
+ */
+#ifndef PALIMPSA_H
+#define PALIMPSA_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define PALIMPSA_ABI_VERSION 1
+
+typedef enum {
+  PALIMPSA_F32 = 0,  /* float                                 */
+  PALIMPSA_BF16 = 1  /* bfloat16 (1-8-7), upcast exactly to fp32 */
+} palimpsa_dtype;
+
+typedef enum {
+  PALIMPSA_OK = 0,
+  PALIMPSA_ERR_NULL = 1,        /* a required pointer is NULL                         */
+  PALIMPSA_ERR_SHAPE = 2,       /* a size is out of range or overflows                */
+  PALIMPSA_ERR_ALIGN = 3,       /* a pointer is not aligned as required               */
+  PALIMPSA_ERR_DTYPE = 4,       /* unknown palimpsa_dtype                             */
+  PALIMPSA_ERR_DOMAIN = 5,      /* (device status) an input broke a precondition      */
+  PALIMPSA_ERR_UNSUPPORTED = 6, /* d_k, d_v or chunk not supported by this build      */
+  PALIMPSA_ERR_CUDA = 7,        /* a CUDA runtime call failed                         */
+  PALIMPSA_ERR_TIMEOUT = 8      /* (device status) a bounded device wait gave up      */
+} palimpsa_status;
+
+/*
+ * palimpsa_forward_chunked — the recurrence over T tokens for B x H heads.
+ *
+ * Defined by slide 7 / paper Eq. (5) (state update), slide 4 / Eq. (2)
+ * (readout) and slide 9 / App. A.12 (chunked scan of the natural parameters:
+ * chunks of `chunk` tokens are staged on chip, the state is carried from one
+ * chunk to the next). The result does not depend on `chunk`.
+ *
+ *   q, k     [B, H, T, d_k]  in_dtype
+ *   v, beta  [B, H, T, d_v]  in_dtype, beta >= 0 (per value channel)
+ *   d_t      [B, H, T]       fp32, >= 0
+ *   A        [H]             fp32, > 0   (alpha = exp(-A d_t))
+ *   I_prior  [H]             fp32, > 0   (prior precision, one per head)
+ *   mu0, I0  [B, H, d_v, d_k] fp32 initial state, or NULL: mu0 = NULL means
+ *            mu0 = 0; I0 = NULL means I0 = I_prior. I0 > 0.
+ *   y        [B, H, T, d_v]  fp32 output, y[b,h,t,i] = sum_j mu_t[i,j] q_t[j]
+ *   mu_T, I_T [B, H, d_v, d_k] fp32 final state. mu_T may be the same pointer
+ *            as mu0 and I_T the same as I0 (in-place update); any other
+ *            overlap between inputs and outputs is undefined.
+ *   T >= 0. T = 0 copies the initial state to (mu_T, I_T); q, k, v, beta,
+ *            d_t and y are then not read and may be NULL.
+ *   chunk    0 (library default) or one of {16, 32, 64}.
+ */
+palimpsa_status palimpsa_forward_chunked(
+    const void* q, const void* k, const void* v, const void* beta,
+    const float* d_t, const float* A, const float* I_prior,
+    const float* mu0, const float* I0,
+    float* y, float* mu_T, float* I_T,
+    int B, int H, int T, int d_k, int d_v, int chunk,
+    palimpsa_dtype in_dtype, void* cuda_stream);
+
+/*
+ * palimpsa_step — one recurrent (decode) token for B x H heads, in place.
+ *
+ * The recurrent inference update of slide 22 / paper App. A.13 (Fig. 7):
+ * Eq. (5) and the readout for a single token, the state read from and written
+ * back to HBM.
+ *
+ *   q, k     [B, H, d_k]     in_dtype
+ *   v, beta  [B, H, d_v]     in_dtype, beta >= 0
+ *   d_t      [B, H]          fp32, >= 0
+ *   A        [H]             fp32, > 0
+ *   I_prior  [H]             fp32, > 0
+ *   mu, I    [B, H, d_v, d_k] fp32 state, updated in place (I > 0)
+ *   y        [B, H, d_v]     fp32 output (must not overlap the state)
+ */
+palimpsa_status palimpsa_step(
+    const void* q, const void* k, const void* v, const void* beta,
+    const float* d_t, const float* A, const float* I_prior,
+    float* mu, float* I, float* y,
+    int B, int H, int d_k, int d_v,
+    palimpsa_dtype in_dtype, void* cuda_stream);
+
+/* Static English text for a status code (never NULL). */
+const char* palimpsa_status_string(palimpsa_status s);
+
+/*
+ * palimpsa_get_device_status — synchronises `cuda_stream`, then reads and
+ * clears the current device's status word, which kernels latch when a
+ * bounded wait gives up (PALIMPSA_ERR_TIMEOUT) or an input breaks a
+ * precondition (PALIMPSA_ERR_DOMAIN). Returns PALIMPSA_OK when nothing was
+ * latched, the latched code (TIMEOUT before DOMAIN) otherwise, or
+ * PALIMPSA_ERR_CUDA when the synchronisation itself fails.
+ */
+palimpsa_status palimpsa_get_device_status(void* cuda_stream);
+
+/* PALIMPSA_ABI_VERSION of the loaded library. */
+int palimpsa_abi_version(void);
+
+/*
+ * Failure-detection controls (process-wide; for tests).
+ * palimpsa_set_wait_timeout_ns sets how long a kernel waits for a staged copy
+ * before it records PALIMPSA_ERR_TIMEOUT and returns (default 2e9 ns).
+ * palimpsa_debug_withhold_first_copy(1) makes the next chunked launches skip
+ * issuing their first staged copy, so that their wait can never be satisfied
+ * and must run out; 0 restores normal operation. Neither changes results
+ * otherwise.
+ */
+void palimpsa_set_wait_timeout_ns(uint64_t ns);
+void palimpsa_debug_withhold_first_copy(int on);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PALIMPSA_H */

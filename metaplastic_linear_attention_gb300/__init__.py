@@ -1,0 +1,26 @@
+"""GB300-native Palimpsa dual-state recurrence (metaplastic linear attention).
+
+Per head the recurrence keeps a memory mean mu and an elementwise precision I
+(both d_v x d_k); each token makes a beta-weighted write whose per-element
+plasticity is set by I, the gate alpha = exp(-A d_t) discounts I toward
+I_prior, and the output is y_t = mu_t q_t (Bonnet et al., "Learning to
+Remember, Learn, and Forget in Attention-Based Models", Eq. (5)).
+
+The computation lives in ``libpalimpsa.so`` (hand-written sm_103a kernels
+behind the C ABI of ``include/palimpsa.h``); this package is its thin binding
+plus the seeded synthetic-input generator.
+"""
+from .binding import (  # noqa: F401
+    PALIMPSA_BF16,
+    PALIMPSA_F32,
+    PalimpsaError,
+    library_path,
+    load_library,
+    palimpsa_abi_version,
+    palimpsa_debug_withhold_first_copy,
+    palimpsa_forward_chunked,
+    palimpsa_get_device_status,
+    palimpsa_set_wait_timeout_ns,
+    palimpsa_status_string,
+    palimpsa_step,
+)

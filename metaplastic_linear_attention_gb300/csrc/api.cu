@@ -1,0 +1,147 @@
+// C ABI layer: argument validation, the per-device status word, debug
+// controls, and dispatch to the kernels' launchers. Declared in palimpsa.h.
+#include <atomic>
+#include <cstdint>
+#include <mutex>
+
+#include "../../include/palimpsa.h"
+#include "palimpsa_internal.cuh"
+
+namespace palimpsa {
+
+// One status word per device, latched by kernels (kStatus* bits).
+__device__ unsigned int g_status_word;
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+std::mutex g_status_mu;
+unsigned int* g_status_ptr[kMaxDevices] = {};
+std::atomic<unsigned long long> g_wait_timeout_ns{2000000000ull};
+std::atomic<int> g_withhold_first_copy{0};
+
+// Device address of the current device's status word (looked up once per
+// device with that device current).
+palimpsa_status status_word(unsigned int** out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return PALIMPSA_ERR_CUDA;
+  std::lock_guard<std::mutex> lock(g_status_mu);
+  if (!g_status_ptr[dev]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_status_word) != cudaSuccess) return PALIMPSA_ERR_CUDA;
+    g_status_ptr[dev] = static_cast<unsigned int*>(p);
+  }
+  *out = g_status_ptr[dev];
+  return PALIMPSA_OK;
+}
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
+
+bool supported_dims(int d_k, int d_v) {
+  return (d_k == 64 || d_k == 128) && d_v >= 8 && d_v <= 256 && d_v % 8 == 0;
+}
+
+// Element counts must fit comfortably in 63 bits and per-head token counts in int.
+bool sizes_ok(long long B, long long H, long long T, int d_k, int d_v) {
+  if (B < 1 || H < 1 || T < 0) return false;
+  const long long lim = 1LL << 40;
+  if (B * H > lim / 256) return false;
+  if (B * H * (T > 0 ? T : 1) > lim) return false;
+  (void)d_k;
+  (void)d_v;
+  return true;
+}
+
+}  // namespace
+}  // namespace palimpsa
+
+using namespace palimpsa;
+
+extern "C" {
+
+palimpsa_status palimpsa_forward_chunked(const void* q, const void* k, const void* v, const void* beta,
+                                         const float* d_t, const float* A, const float* I_prior,
+                                         const float* mu0, const float* I0, float* y, float* mu_T,
+                                         float* I_T, int B, int H, int T, int d_k, int d_v, int chunk,
+                                         palimpsa_dtype in_dtype, void* cuda_stream) {
+  if (!A || !I_prior || !mu_T || !I_T) return PALIMPSA_ERR_NULL;
+  // With T == 0 the per-token arrays are empty and may be NULL.
+  if (T != 0 && (!q || !k || !v || !beta || !d_t || !y)) return PALIMPSA_ERR_NULL;
+  if (in_dtype != PALIMPSA_F32 && in_dtype != PALIMPSA_BF16) return PALIMPSA_ERR_DTYPE;
+  if (!sizes_ok(B, H, T, d_k, d_v)) return PALIMPSA_ERR_SHAPE;
+  if (!supported_dims(d_k, d_v)) return PALIMPSA_ERR_UNSUPPORTED;
+  if (chunk != 0 && chunk != 16 && chunk != 32 && chunk != 64) return PALIMPSA_ERR_UNSUPPORTED;
+  const void* a16[] = {q, k, v, beta, y, mu_T, I_T, mu0, I0};
+  for (const void* p : a16)
+    if (p && !aligned(p, 16)) return PALIMPSA_ERR_ALIGN;
+  const void* a4[] = {d_t, A, I_prior};
+  for (const void* p : a4)
+    if (p && !aligned(p, 4)) return PALIMPSA_ERR_ALIGN;
+  unsigned int* st = nullptr;
+  if (palimpsa_status s = status_word(&st)) return s;
+  FwdArgs a{q, k, v, beta, d_t, A, I_prior, mu0, I0, y, mu_T, I_T, B, H, T, d_k, d_v,
+            chunk == 0 ? 32 : chunk, in_dtype == PALIMPSA_BF16, st,
+            g_wait_timeout_ns.load(), g_withhold_first_copy.load()};
+  if (launch_forward_chunked(a, static_cast<cudaStream_t>(cuda_stream)) != cudaSuccess)
+    return PALIMPSA_ERR_CUDA;
+  return PALIMPSA_OK;
+}
+
+palimpsa_status palimpsa_step(const void* q, const void* k, const void* v, const void* beta,
+                              const float* d_t, const float* A, const float* I_prior, float* mu, float* I,
+                              float* y, int B, int H, int d_k, int d_v, palimpsa_dtype in_dtype,
+                              void* cuda_stream) {
+  if (!q || !k || !v || !beta || !d_t || !A || !I_prior || !mu || !I || !y) return PALIMPSA_ERR_NULL;
+  if (in_dtype != PALIMPSA_F32 && in_dtype != PALIMPSA_BF16) return PALIMPSA_ERR_DTYPE;
+  if (!sizes_ok(B, H, 1, d_k, d_v)) return PALIMPSA_ERR_SHAPE;
+  if (!supported_dims(d_k, d_v)) return PALIMPSA_ERR_UNSUPPORTED;
+  const void* a16[] = {q, k, v, beta, mu, I, y};
+  for (const void* p : a16)
+    if (!aligned(p, 16)) return PALIMPSA_ERR_ALIGN;
+  const void* a4[] = {d_t, A, I_prior};
+  for (const void* p : a4)
+    if (!aligned(p, 4)) return PALIMPSA_ERR_ALIGN;
+  unsigned int* st = nullptr;
+  if (palimpsa_status s = status_word(&st)) return s;
+  StepArgs a{q, k, v, beta, d_t, A, I_prior, mu, I, y, B, H, d_k, d_v, in_dtype == PALIMPSA_BF16, st};
+  if (launch_step(a, static_cast<cudaStream_t>(cuda_stream)) != cudaSuccess) return PALIMPSA_ERR_CUDA;
+  return PALIMPSA_OK;
+}
+
+const char* palimpsa_status_string(palimpsa_status s) {
+  switch (s) {
+    case PALIMPSA_OK: return "ok";
+    case PALIMPSA_ERR_NULL: return "a required pointer is NULL";
+    case PALIMPSA_ERR_SHAPE: return "a size is out of range";
+    case PALIMPSA_ERR_ALIGN: return "a pointer is not aligned as required";
+    case PALIMPSA_ERR_DTYPE: return "unknown input dtype";
+    case PALIMPSA_ERR_DOMAIN: return "an input broke a precondition (A, I_prior, I0 > 0; d_t, beta >= 0)";
+    case PALIMPSA_ERR_UNSUPPORTED: return "d_k, d_v or chunk not supported";
+    case PALIMPSA_ERR_CUDA: return "a CUDA runtime call failed";
+    case PALIMPSA_ERR_TIMEOUT: return "a bounded device wait gave up";
+  }
+  return "unknown status";
+}
+
+palimpsa_status palimpsa_get_device_status(void* cuda_stream) {
+  if (cudaStreamSynchronize(static_cast<cudaStream_t>(cuda_stream)) != cudaSuccess) return PALIMPSA_ERR_CUDA;
+  unsigned int* st = nullptr;
+  if (palimpsa_status s = status_word(&st)) return s;
+  unsigned int bits = 0;
+  if (cudaMemcpy(&bits, st, sizeof(bits), cudaMemcpyDeviceToHost) != cudaSuccess) return PALIMPSA_ERR_CUDA;
+  if (bits) {
+    const unsigned int zero = 0;
+    if (cudaMemcpy(st, &zero, sizeof(zero), cudaMemcpyHostToDevice) != cudaSuccess) return PALIMPSA_ERR_CUDA;
+  }
+  if (bits & kStatusTimeout) return PALIMPSA_ERR_TIMEOUT;
+  if (bits & kStatusDomain) return PALIMPSA_ERR_DOMAIN;
+  return PALIMPSA_OK;
+}
+
+int palimpsa_abi_version(void) { return PALIMPSA_ABI_VERSION; }
+
+void palimpsa_set_wait_timeout_ns(uint64_t ns) { g_wait_timeout_ns.store(ns); }
+
+void palimpsa_debug_withhold_first_copy(int on) { g_withhold_first_copy.store(on ? 1 : 0); }
+
+}  // extern "C"

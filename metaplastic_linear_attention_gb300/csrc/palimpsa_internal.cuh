@@ -1,0 +1,142 @@
+// Internal declarations shared by the kernels and the C ABI layer: launch
+// argument structs, the device status bits, and thin inline-PTX wrappers for
+// the sm_103a features the kernels use (mbarrier, bulk async copies, packed
+// fp32x2 arithmetic, the hardware reciprocal).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <cuda_bf16.h>
+#include <stdint.h>
+
+namespace palimpsa {
+
+// Bits latched into the per-device status word.
+enum : unsigned int {
+  kStatusTimeout = 1u << 0,
+  kStatusDomain = 1u << 1,
+};
+
+struct FwdArgs {
+  const void* q;
+  const void* k;
+  const void* v;
+  const void* beta;
+  const float* d_t;
+  const float* A;
+  const float* I_prior;
+  const float* mu0;  // may be null
+  const float* I0;   // may be null
+  float* y;
+  float* mu_T;
+  float* I_T;
+  int B, H, T, d_k, d_v, chunk;
+  bool bf16;
+  unsigned int* status;
+  unsigned long long wait_timeout_ns;
+  int withhold_first_copy;
+};
+
+struct StepArgs {
+  const void* q;
+  const void* k;
+  const void* v;
+  const void* beta;
+  const float* d_t;
+  const float* A;
+  const float* I_prior;
+  float* mu;
+  float* I;
+  float* y;
+  int B, H, d_k, d_v;
+  bool bf16;
+  unsigned int* status;
+};
+
+// Launchers (return the launch error, cudaSuccess on success). Arguments are
+// validated by the caller.
+cudaError_t launch_forward_chunked(const FwdArgs& a, cudaStream_t s);
+cudaError_t launch_step(const StepArgs& a, cudaStream_t s);
+
+// ------------------------------------------------------------------ device helpers
+#if defined(__CUDACC__)
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void fence_mbar_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.release.cta.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)),
+               "r"(bytes)
+               : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+__device__ __forceinline__ unsigned long long global_ns() {
+  unsigned long long t;
+  asm volatile("mov.u64 %0, %globaltimer;" : "=l"(t));
+  return t;
+}
+
+// Waits until phase `parity` of `bar` completes or `timeout_ns` elapses.
+// Returns false on timeout. Every wait in this library goes through here.
+__device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity,
+                                                  unsigned long long timeout_ns) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const unsigned long long t0 = global_ns();
+  for (;;) {
+    for (int i = 0; i < 64; ++i)
+      if (mbar_try_wait(bar, parity)) return true;
+    if (global_ns() - t0 >= timeout_ns) return mbar_try_wait(bar, parity);
+  }
+}
+
+// 1-D bulk copy global -> shared, completion counted on `bar` (bytes).
+// dst, src 16-byte aligned; bytes a multiple of 16.
+__device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+          smem_u32(dst)),
+      "l"(src), "r"(bytes), "r"(smem_u32(bar))
+      : "memory");
+}
+
+__device__ __forceinline__ float rcp_approx(float x) {
+  float r;
+  asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(x));
+  return r;
+}
+
+__device__ __forceinline__ float bf16_lo(uint32_t packed) { return __uint_as_float(packed << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t packed) { return __uint_as_float(packed & 0xffff0000u); }
+
+__device__ __forceinline__ void latch_status(unsigned int* status, unsigned int bits) {
+  atomicOr(status, bits);
+}
+
+// fp32 "is a usable positive number" / "is a usable non-negative number".
+__device__ __forceinline__ bool pos_finite(float x) { return x > 0.f && x <= 3.0e38f; }
+__device__ __forceinline__ bool nonneg_finite(float x) { return x >= 0.f && x <= 3.0e38f; }
+
+#endif  // __CUDACC__
+
+}  // namespace palimpsa

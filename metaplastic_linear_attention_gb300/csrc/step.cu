@@ -1,0 +1,132 @@
+// Recurrent (decode) step of the Palimpsa recurrence on sm_103a.
+//
+// Source: Bonnet et al., "Learning to Remember, Learn, and Forget in
+// Attention-Based Models" — slide 22 (paper App. A.13, Fig. 7): recurrent
+// inference performs the dual-state update of Eq. (5) (slide 7) and the read
+// y = mu q (slide 4, Eq. 2) once per generated token.
+//
+// The step is a stream over the state: each of the B*H*d_v*d_k elements of mu
+// and I is read once and written once (16 bytes per element), against ~1 KB of
+// per-head inputs and outputs. It is therefore bound by HBM bandwidth, and the
+// kernel is built as a copy kernel with arithmetic in the middle:
+// * one warp owns 8 value rows of one head; a lane owns 4 consecutive key
+//   columns (one 16-byte vector of mu and one of I per row, d_k = 128) or two
+//   rows are interleaved per warp instruction (d_k = 64);
+// * all 16 state loads of a lane are issued before any arithmetic, so every
+//   SM keeps well over the ~45 KB in flight that 6.8 TB/s needs at ~1 us of
+//   latency; loads and stores use the streaming (evict-first) cache policy,
+//   because the state (537 MB at B=256, H=32) is far larger than L2;
+// * q, k of the head are loaded once per warp; k^2, alpha and (1 - alpha)
+//   I_prior once per lane;
+// * y_i is a butterfly shuffle reduction over the lanes of the row.
+// The update uses the mean/precision form of Eq. (5) directly:
+//   I' = alpha I + (1 - alpha) I_prior + beta_i k_j^2
+//   mu' = (alpha I mu + beta_i v_i k_j) / I'      (IEEE division)
+#include "palimpsa_internal.cuh"
+
+namespace palimpsa {
+namespace {
+
+constexpr int kRowsPerWarp = 8;
+constexpr int kWarpsPerBlock = 8;
+
+template <bool BF16>
+__device__ __forceinline__ float4 load4(const void* base, size_t idx) {
+  if constexpr (BF16) {
+    const uint2 u = *reinterpret_cast<const uint2*>(static_cast<const __nv_bfloat16*>(base) + idx);
+    return make_float4(bf16_lo(u.x), bf16_hi(u.x), bf16_lo(u.y), bf16_hi(u.y));
+  } else {
+    return *reinterpret_cast<const float4*>(static_cast<const float*>(base) + idx);
+  }
+}
+
+template <bool BF16>
+__device__ __forceinline__ float load1(const void* base, size_t idx) {
+  if constexpr (BF16) return __bfloat162float(static_cast<const __nv_bfloat16*>(base)[idx]);
+  else return static_cast<const float*>(base)[idx];
+}
+
+template <int DK, bool BF16>
+__global__ void __launch_bounds__(kWarpsPerBlock * 32)
+palimpsa_step_kernel(StepArgs a) {
+  constexpr int LPR = DK / 4;       // lanes per row
+  constexpr int RPI = 32 / LPR;     // rows per warp instruction
+  constexpr int NIT = kRowsPerWarp / RPI;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const long total_rows = (long)a.B * a.H * a.d_v;
+  const long row_base = ((long)blockIdx.x * kWarpsPerBlock + warp) * kRowsPerWarp;
+  if (row_base >= total_rows) return;
+  const long bh = row_base / a.d_v;
+  const int h = (int)(bh % a.H);
+  const int sub = lane / LPR;
+  const int col = 4 * (lane % LPR);
+
+  // Issue the state loads first: 2 * NIT independent 16-byte loads per lane.
+  float4 mu4[NIT], I4[NIT];
+#pragma unroll
+  for (int it = 0; it < NIT; ++it) {
+    const size_t off = (size_t)(row_base + it * RPI + sub) * DK + col;
+    mu4[it] = __ldcs(reinterpret_cast<const float4*>(a.mu + off));
+    I4[it] = __ldcs(reinterpret_cast<const float4*>(a.I + off));
+  }
+
+  const float4 q4 = load4<BF16>(a.q, (size_t)bh * DK + col);
+  const float4 k4 = load4<BF16>(a.k, (size_t)bh * DK + col);
+  const float d = a.d_t[bh];
+  const float A_h = a.A[h], Ip = a.I_prior[h];
+  bool bad = !(pos_finite(A_h) && pos_finite(Ip) && nonneg_finite(d));
+  const float x = -A_h * d;
+  const float al = expf(x);
+  const float om = -expm1f(x) * Ip;  // (1 - alpha) I_prior
+  const float kj[4] = {k4.x, k4.y, k4.z, k4.w};
+  const float qj[4] = {q4.x, q4.y, q4.z, q4.w};
+  float kk[4];
+#pragma unroll
+  for (int e = 0; e < 4; ++e) kk[e] = kj[e] * kj[e];
+
+  const int i_base = (int)(row_base - bh * a.d_v);
+#pragma unroll
+  for (int it = 0; it < NIT; ++it) {
+    const long row = row_base + it * RPI + sub;
+    const size_t in_off = (size_t)bh * a.d_v + i_base + it * RPI + sub;
+    const float b = load1<BF16>(a.beta, in_off);
+    const float bv = b * load1<BF16>(a.v, in_off);
+    bad |= !nonneg_finite(b);
+    float Io[4] = {I4[it].x, I4[it].y, I4[it].z, I4[it].w};
+    float mo[4] = {mu4[it].x, mu4[it].y, mu4[it].z, mu4[it].w};
+    float In[4], mn[4];
+    float yp = 0.f;
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      bad |= !pos_finite(Io[e]);
+      In[e] = fmaf(al, Io[e], fmaf(b, kk[e], om));
+      mn[e] = fmaf(al * Io[e], mo[e], bv * kj[e]) / In[e];
+      yp = fmaf(mn[e], qj[e], yp);
+    }
+#pragma unroll
+    for (int m = 1; m < LPR; m <<= 1) yp += __shfl_xor_sync(0xffffffffu, yp, m);
+    const size_t off = (size_t)row * DK + col;
+    __stcs(reinterpret_cast<float4*>(a.mu + off), make_float4(mn[0], mn[1], mn[2], mn[3]));
+    __stcs(reinterpret_cast<float4*>(a.I + off), make_float4(In[0], In[1], In[2], In[3]));
+    if ((lane % LPR) == 0) a.y[row] = yp;
+  }
+  if (__any_sync(0xffffffffu, bad) && lane == 0) latch_status(a.status, kStatusDomain);
+}
+
+}  // namespace
+
+cudaError_t launch_step(const StepArgs& a, cudaStream_t s) {
+  const long rows = (long)a.B * a.H * a.d_v;
+  const long rows_per_block = (long)kWarpsPerBlock * kRowsPerWarp;
+  const unsigned blocks = (unsigned)((rows + rows_per_block - 1) / rows_per_block);
+  if (a.d_k == 128) {
+    if (a.bf16) palimpsa_step_kernel<128, true><<<blocks, kWarpsPerBlock * 32, 0, s>>>(a);
+    else palimpsa_step_kernel<128, false><<<blocks, kWarpsPerBlock * 32, 0, s>>>(a);
+  } else {
+    if (a.bf16) palimpsa_step_kernel<64, true><<<blocks, kWarpsPerBlock * 32, 0, s>>>(a);
+    else palimpsa_step_kernel<64, false><<<blocks, kWarpsPerBlock * 32, 0, s>>>(a);
+  }
+  return cudaGetLastError();
+}
+
+}  // namespace palimpsa

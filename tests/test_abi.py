@@ -1,0 +1,134 @@
+"""Host-side tests of the C ABI (no GPU needed): the library loads, exports every
+function declared in include/palimpsa.h, and rejects bad arguments with status
+codes before touching a device."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import metaplastic_linear_attention_gb300 as pal
+from metaplastic_linear_attention_gb300 import build_lib
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "palimpsa.h")
+
+OK, ERR_NULL, ERR_SHAPE, ERR_ALIGN, ERR_DTYPE, ERR_DOMAIN, ERR_UNSUPPORTED, ERR_CUDA, ERR_TIMEOUT = range(9)
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build_lib.build()
+    return pal.load_library()
+
+
+def _declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    names = re.findall(r"\b(palimpsa_[a-z_0-9]+)\s*\(", text)
+    return sorted(set(names))
+
+
+def test_header_declares_the_entry_points():
+    names = _declared_functions()
+    for required in ("palimpsa_forward_chunked", "palimpsa_step", "palimpsa_status_string",
+                     "palimpsa_get_device_status"):
+        assert required in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in _declared_functions():
+        assert hasattr(lib, name), f"{name} declared in palimpsa.h but not exported"
+
+
+def test_abi_version_and_status_strings(lib):
+    assert pal.palimpsa_abi_version() == 1
+    seen = set()
+    for code in range(9):
+        s = pal.palimpsa_status_string(code)
+        assert s and s not in seen
+        seen.add(s)
+    assert pal.palimpsa_status_string(99) == "unknown status"
+
+
+# Fake, well-aligned addresses: every check below fails before any pointer is used.
+P = 1 << 20
+
+
+def _fwd(lib, **over):
+    args = dict(q=P, k=P, v=P, beta=P, d_t=P, A=P, I_prior=P, mu0=None, I0=None, y=P, mu_T=P, I_T=P,
+                B=1, H=2, T=16, d_k=128, d_v=64, chunk=0, dtype=1)
+    args.update(over)
+    return lib.palimpsa_forward_chunked(
+        args["q"], args["k"], args["v"], args["beta"], args["d_t"], args["A"], args["I_prior"], args["mu0"],
+        args["I0"], args["y"], args["mu_T"], args["I_T"], args["B"], args["H"], args["T"], args["d_k"],
+        args["d_v"], args["chunk"], args["dtype"], None)
+
+
+def _step(lib, **over):
+    args = dict(q=P, k=P, v=P, beta=P, d_t=P, A=P, I_prior=P, mu=P, I=P, y=P, B=4, H=2, d_k=128, d_v=64,
+                dtype=1)
+    args.update(over)
+    return lib.palimpsa_step(args["q"], args["k"], args["v"], args["beta"], args["d_t"], args["A"],
+                             args["I_prior"], args["mu"], args["I"], args["y"], args["B"], args["H"],
+                             args["d_k"], args["d_v"], args["dtype"], None)
+
+
+@pytest.mark.parametrize("field", ["q", "k", "v", "beta", "d_t", "A", "I_prior", "y", "mu_T", "I_T"])
+def test_forward_rejects_null(lib, field):
+    assert _fwd(lib, **{field: None}) == ERR_NULL
+
+
+@pytest.mark.parametrize("field", ["A", "I_prior", "mu_T", "I_T"])
+def test_forward_empty_sequence_still_needs_state_and_gates(lib, field):
+    assert _fwd(lib, T=0, q=None, k=None, v=None, beta=None, d_t=None, y=None, **{field: None}) == ERR_NULL
+
+
+@pytest.mark.parametrize("field", ["q", "k", "v", "beta", "d_t", "A", "I_prior", "mu", "I", "y"])
+def test_step_rejects_null(lib, field):
+    assert _step(lib, **{field: None}) == ERR_NULL
+
+
+@pytest.mark.parametrize("over,code", [
+    (dict(dtype=2), ERR_DTYPE), (dict(dtype=-1), ERR_DTYPE),
+    (dict(B=0), ERR_SHAPE), (dict(H=0), ERR_SHAPE), (dict(T=-1), ERR_SHAPE), (dict(B=-3), ERR_SHAPE),
+    (dict(d_k=96), ERR_UNSUPPORTED), (dict(d_k=32), ERR_UNSUPPORTED), (dict(d_v=12), ERR_UNSUPPORTED),
+    (dict(d_v=0), ERR_UNSUPPORTED), (dict(d_v=264), ERR_UNSUPPORTED), (dict(chunk=48), ERR_UNSUPPORTED),
+    (dict(chunk=128), ERR_UNSUPPORTED),
+    (dict(q=P + 8), ERR_ALIGN), (dict(v=P + 4), ERR_ALIGN), (dict(y=P + 2), ERR_ALIGN),
+    (dict(mu0=P + 8), ERR_ALIGN), (dict(I0=P + 4), ERR_ALIGN), (dict(d_t=P + 2), ERR_ALIGN),
+])
+def test_forward_rejects_bad_arguments(lib, over, code):
+    assert _fwd(lib, **over) == code
+
+
+@pytest.mark.parametrize("over,code", [
+    (dict(dtype=7), ERR_DTYPE), (dict(B=0), ERR_SHAPE), (dict(H=-1), ERR_SHAPE),
+    (dict(d_k=256), ERR_UNSUPPORTED), (dict(d_v=7), ERR_UNSUPPORTED),
+    (dict(mu=P + 8), ERR_ALIGN), (dict(k=P + 2), ERR_ALIGN), (dict(A=P + 1), ERR_ALIGN),
+])
+def test_step_rejects_bad_arguments(lib, over, code):
+    assert _step(lib, **over) == code
+
+
+def test_binding_raises_without_fallback(tmp_path):
+    """A missing library is an error, never a silent CPU path."""
+    import metaplastic_linear_attention_gb300.binding as b
+    saved = b._lib
+    try:
+        b._lib = None
+        with pytest.raises(RuntimeError):
+            b.load_library(str(tmp_path / "libpalimpsa.so"))
+    finally:
+        b._lib = saved
+
+
+def test_product_path_does_not_import_the_oracle():
+    """The package never imports the oracle (the oracle is test infrastructure)."""
+    pkg = os.path.join(ROOT, "metaplastic_linear_attention_gb300")
+    for dirpath, _, files in os.walk(pkg):
+        for f in files:
+            if f.endswith((".py", ".cu", ".cuh", ".h", ".cpp")):
+                text = open(os.path.join(dirpath, f)).read()
+                assert "import oracle" not in text and "from oracle" not in text, f
+                assert "palimpsa_oracle" not in text, f

@@ -1,0 +1,265 @@
+"""GPU parity: the CUDA kernels, called through the C ABI, against the fp64
+oracle on the same seeded inputs (relative L2 per output tensor).
+
+Small cases run the oracle on everything; the full-size workloads run the GPU
+on the whole problem in the launch configuration the benchmark times, and the
+oracle on sampled heads (rows and heads are independent, which the oracle's own
+row-independence pin establishes)."""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import metaplastic_linear_attention_gb300 as pal
+from metaplastic_linear_attention_gb300 import synthetic as syn
+from tests._helpers import TIGHT, oracle_forward_from, pick, rel_l2, tol_for
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda"
+
+
+def _gpu(inputs):
+    return {k: v.to(DEV) for k, v in inputs.items()}
+
+
+def _fwd(gi, mu0=None, I0=None, chunk=0, **kw):
+    out = pal.palimpsa_forward_chunked(gi["q"], gi["k"], gi["v"], gi["beta"], gi["d_t"], gi["A"],
+                                       gi["I_prior"], mu0, I0, chunk=chunk, **kw)
+    assert pal.palimpsa_get_device_status() == 0
+    return out
+
+
+def _check_all(out, ref, tol, tight=None):
+    errs = [rel_l2(o.cpu().numpy(), r) for o, r in zip(out, ref)]
+    assert max(errs) <= tol, errs
+    if tight is not None:
+        assert max(errs) <= tight, errs
+    return errs
+
+
+def _random_state(B, H, dv, dk, seed, I_lo=0.5, I_hi=4.0):
+    g = torch.Generator().manual_seed(seed)
+    mu0 = torch.randn((B, H, dv, dk), generator=g)
+    I0 = I_lo + (I_hi - I_lo) * torch.rand((B, H, dv, dk), generator=g)
+    return mu0, I0
+
+
+# ----------------------------------------------------------------- small, everything checked
+
+def test_tiny_workload_all_chunks_bitwise_equal():
+    """The fp32 tiny sequence (B=1, H=2, T=256, d=64): parity with the oracle, and
+    the staging chunk size leaves the result bit-for-bit unchanged."""
+    wl = syn.WORKLOADS["tiny"]
+    inp = syn.sequence_inputs(wl)
+    ref = oracle_forward_from(inp)
+    gi = _gpu(inp)
+    outs = [_fwd(gi, chunk=c) for c in (16, 32, 64)]
+    _check_all(outs[0], ref, tol_for(inp), TIGHT)
+    for o in outs[1:]:
+        for a, b in zip(o, outs[0]):
+            assert torch.equal(a, b)
+
+
+CASES = [
+    # (B, H, T, d_k, d_v, bf16, chunk)
+    (1, 1, 1, 128, 64, True, 16),
+    (2, 3, 5, 128, 64, True, 32),
+    (1, 2, 77, 64, 8, False, 16),
+    (3, 2, 130, 128, 24, True, 64),
+    (2, 1, 200, 64, 128, True, 32),
+    (1, 3, 97, 128, 256, False, 16),
+    (4, 5, 33, 128, 64, False, 32),
+    (1, 1, 300, 64, 40, True, 64),
+]
+
+
+@pytest.mark.parametrize("B,H,T,dk,dv,bf16,chunk", CASES)
+def test_forward_ragged_and_odd_shapes(B, H, T, dk, dv, bf16, chunk):
+    wl = syn.WORKLOADS["small_layer"].with_(B=B, H=H, T=T, d_k=dk, d_v=dv, bf16=bf16, chunk=chunk)
+    inp = syn.sequence_inputs(wl, seed=1000 + T)
+    ref = oracle_forward_from(inp)
+    out = _fwd(_gpu(inp), chunk=chunk)
+    _check_all(out, ref, tol_for(inp), TIGHT)
+
+
+@pytest.mark.parametrize("bf16", [False, True])
+def test_forward_initial_state_and_in_place(bf16):
+    B, H, T, dk, dv = 2, 3, 150, 128, 64
+    wl = syn.WORKLOADS["small_layer"].with_(B=B, H=H, T=T, bf16=bf16)
+    inp = syn.sequence_inputs(wl, seed=7)
+    mu0, I0 = _random_state(B, H, dv, dk, 8)
+    ref = oracle_forward_from(inp, mu0=mu0, I0=I0)
+    gi = _gpu(inp)
+    out = _fwd(gi, mu0.to(DEV), I0.to(DEV))
+    _check_all(out, ref, tol_for(inp), TIGHT)
+    # in place: mu_T aliases mu0, I_T aliases I0
+    m, i = mu0.to(DEV), I0.to(DEV)
+    y, mT, IT = _fwd(gi, m, i, mu_T=m, I_T=i)
+    assert mT.data_ptr() == m.data_ptr() and IT.data_ptr() == i.data_ptr()
+    for a, b in zip((y, mT, IT), out):
+        assert torch.equal(a, b)
+
+
+def test_forward_empty_sequence_passes_state_through():
+    B, H, dk, dv = 2, 2, 128, 64
+    wl = syn.WORKLOADS["small_layer"].with_(B=B, H=H, T=0)
+    inp = syn.sequence_inputs(wl)
+    mu0, I0 = _random_state(B, H, dv, dk, 3)
+    gi = _gpu(inp)
+    y, mT, IT = _fwd(gi, mu0.to(DEV), I0.to(DEV))
+    assert y.numel() == 0
+    assert torch.equal(mT.cpu(), mu0) and torch.equal(IT.cpu(), I0)
+    y, mT, IT = _fwd(gi)
+    assert torch.all(mT == 0) and torch.equal(IT.cpu(), torch.ones_like(I0))
+
+
+def test_forward_continuation_matches_single_pass():
+    """Checkpoint/resume: the scan split at t = 70 and resumed from (mu_T, I_T)."""
+    wl = syn.WORKLOADS["small_layer"].with_(B=2, H=2, T=200)
+    inp = syn.sequence_inputs(wl, seed=11)
+    gi = _gpu(inp)
+    y, mT, IT = _fwd(gi)
+    s = 70
+    first = {k: (v[:, :, :s].contiguous() if v.dim() >= 3 else v) for k, v in gi.items()}
+    second = {k: (v[:, :, s:].contiguous() if v.dim() >= 3 else v) for k, v in gi.items()}
+    y1, m1, i1 = _fwd(first)
+    y2, m2, i2 = _fwd(second, m1, i1)
+    assert rel_l2(torch.cat([y1, y2], 2).cpu(), y.cpu()) < 1e-6
+    assert rel_l2(m2.cpu(), mT.cpu()) < 1e-6 and rel_l2(i2.cpu(), IT.cpu()) < 1e-7
+
+
+# ----------------------------------------------------------------- decode step
+
+STEP_CASES = [(1, 1, 128, 64, True), (3, 5, 128, 64, False), (2, 3, 64, 8, True), (4, 2, 64, 24, False),
+              (2, 2, 128, 256, True), (5, 3, 128, 40, True)]
+
+
+@pytest.mark.parametrize("B,H,dk,dv,bf16", STEP_CASES)
+def test_step_matches_oracle_over_several_tokens(B, H, dk, dv, bf16):
+    wl = syn.WORKLOADS["decode"].with_(B=B, H=H, d_k=dk, d_v=dv, bf16=bf16)
+    seq = syn.sequence_inputs(wl, T=1, seed=5)
+    steps = syn.decode_inputs(wl, 6, seed=5)
+    mu0, I0 = _random_state(B, H, dv, dk, 9)
+    mu, I = mu0.to(DEV).clone(), I0.to(DEV).clone()
+    A, Ip = seq["A"].to(DEV), seq["I_prior"].to(DEV)
+    rmu, rI = mu0.double().numpy(), I0.double().numpy()
+    import oracle
+    for s in range(6):
+        gs = {k: v[s].to(DEV) for k, v in steps.items()}
+        y = pal.palimpsa_step(gs["q"], gs["k"], gs["v"], gs["beta"], gs["d_t"], A, Ip, mu, I)
+        f = syn.as_float64_numpy
+        ry, rmu, rI = oracle.step(f(steps["q"][s]), f(steps["k"][s]), f(steps["v"][s]), f(steps["beta"][s]),
+                                  f(steps["d_t"][s]), f(seq["A"]), f(seq["I_prior"]), rmu, rI)
+        assert rel_l2(y.cpu(), ry) <= TIGHT
+    assert pal.palimpsa_get_device_status() == 0
+    assert rel_l2(mu.cpu(), rmu) <= TIGHT and rel_l2(I.cpu(), rI) <= TIGHT
+
+
+def test_step_equals_one_token_forward():
+    wl = syn.WORKLOADS["small_layer"].with_(B=3, H=4, T=1)
+    inp = _gpu(syn.sequence_inputs(wl, seed=21))
+    mu0, I0 = (t.to(DEV) for t in _random_state(3, 4, 64, 128, 22))
+    y_f, m_f, i_f = _fwd(inp, mu0, I0)
+    mu, I = mu0.clone(), I0.clone()
+    y_s = pal.palimpsa_step(inp["q"][:, :, 0].contiguous(), inp["k"][:, :, 0].contiguous(),
+                            inp["v"][:, :, 0].contiguous(), inp["beta"][:, :, 0].contiguous(),
+                            inp["d_t"][:, :, 0].contiguous(), inp["A"], inp["I_prior"], mu, I)
+    assert rel_l2(y_s.cpu(), y_f[:, :, 0].cpu()) < 1e-6
+    assert rel_l2(mu.cpu(), m_f.cpu()) < 1e-6 and torch.allclose(I, i_f, rtol=1e-6)
+
+
+# ----------------------------------------------------------------- full-size workloads
+
+def test_small_layer_full_size():
+    """B=4, H=16, T=2048, d_k=128, d_v=64, bf16: every output against the oracle."""
+    wl = syn.WORKLOADS["small_layer"]
+    inp = syn.sequence_inputs(wl)
+    out = _fwd(_gpu(inp), chunk=wl.chunk)
+    ref = oracle_forward_from(inp)
+    _check_all(out, ref, tol_for(inp), TIGHT)
+
+
+@pytest.mark.parametrize("name,heads", [
+    ("layer_760m", [(0, 0), (3, 7), (5, 23), (7, 12)]),
+    ("long_context", [(0, 0), (0, 13), (0, 31)]),
+])
+def test_large_workloads_sampled_heads(name, heads):
+    """Full-size launches; the oracle recomputes sampled heads over all T tokens."""
+    wl = syn.WORKLOADS[name]
+    inp = syn.sequence_inputs(wl)
+    y, mT, IT = _fwd(_gpu(inp), chunk=wl.chunk)
+    ref = oracle_forward_from(inp, heads=heads)
+    got = (pick(y, heads), pick(mT, heads), pick(IT, heads))
+    errs = [rel_l2(g, r) for g, r in zip(got, ref)]
+    assert max(errs) <= min(tol_for(inp), TIGHT), errs
+    assert torch.isfinite(y).all() and (IT > 0).all()
+
+
+def test_decode_workload_prefill_and_steps_sampled_heads():
+    """B=256, H=32: the 512-token prefill then decode steps in the benchmark's launch
+    configuration; sampled heads replayed by the oracle (prefill + every step)."""
+    wl = syn.WORKLOADS["decode"]
+    S = 8
+    inp = syn.sequence_inputs(wl)
+    steps = syn.decode_inputs(wl, S)
+    gi = _gpu(inp)
+    _, mu, I = _fwd(gi, chunk=wl.chunk)
+    heads = [(0, 0), (17, 5), (128, 31), (255, 16)]
+    _, rmu, rI = oracle_forward_from(inp, heads=heads)
+    import oracle
+    bs = [b for b, _ in heads]
+    hs = [h for _, h in heads]
+    f = syn.as_float64_numpy
+    for s in range(S):
+        gs = {k: v[s].to(DEV) for k, v in steps.items()}
+        y = pal.palimpsa_step(gs["q"], gs["k"], gs["v"], gs["beta"], gs["d_t"], gi["A"], gi["I_prior"], mu, I)
+        sel = {k: f(v[s])[bs, hs][None] for k, v in steps.items()}
+        ry, rmu, rI = oracle.step(sel["q"], sel["k"], sel["v"], sel["beta"], sel["d_t"],
+                                  f(inp["A"])[hs], f(inp["I_prior"])[hs], rmu, rI)
+        assert rel_l2(pick(y, heads), ry) <= TIGHT
+    assert pal.palimpsa_get_device_status() == 0
+    assert rel_l2(pick(mu, heads), rmu) <= TIGHT and rel_l2(pick(I, heads), rI) <= TIGHT
+
+
+# ----------------------------------------------------------------- failure detection (no fault)
+
+def test_domain_violation_is_reported_not_faulted():
+    wl = syn.WORKLOADS["small_layer"].with_(B=1, H=2, T=40)
+    gi = _gpu(syn.sequence_inputs(wl))
+    gi["A"] = gi["A"].clone()
+    gi["A"][1] = -1.0
+    pal.palimpsa_forward_chunked(gi["q"], gi["k"], gi["v"], gi["beta"], gi["d_t"], gi["A"], gi["I_prior"])
+    assert pal.palimpsa_get_device_status() == 5          # PALIMPSA_ERR_DOMAIN
+    assert pal.palimpsa_get_device_status() == 0          # read-and-clear
+    gi["A"][1] = 0.5
+    _fwd(gi)
+
+
+def test_withheld_copy_times_out_and_context_survives():
+    """A staged copy that never arrives: the bounded mbarrier wait gives up, the
+    kernel latches PALIMPSA_ERR_TIMEOUT and returns; later calls work."""
+    wl = syn.WORKLOADS["small_layer"].with_(B=1, H=2, T=100)
+    inp = syn.sequence_inputs(wl)
+    gi = _gpu(inp)
+    pal.palimpsa_set_wait_timeout_ns(2_000_000)
+    pal.palimpsa_debug_withhold_first_copy(True)
+    try:
+        pal.palimpsa_forward_chunked(gi["q"], gi["k"], gi["v"], gi["beta"], gi["d_t"], gi["A"],
+                                     gi["I_prior"], chunk=32)
+        assert pal.palimpsa_get_device_status() == 8       # PALIMPSA_ERR_TIMEOUT
+    finally:
+        pal.palimpsa_debug_withhold_first_copy(False)
+        pal.palimpsa_set_wait_timeout_ns(2_000_000_000)
+    out = _fwd(gi, chunk=32)
+    _check_all(out, oracle_forward_from(inp), tol_for(inp), TIGHT)
+
+
+def test_host_buffers_end_to_end():
+    """The public call with pinned host tensors copies in, computes on the GPU and copies out."""
+    wl = syn.WORKLOADS["small_layer"].with_(B=2, H=2, T=64)
+    inp = {k: v.pin_memory() for k, v in syn.sequence_inputs(wl, seed=4).items()}
+    y, mT, IT = pal.palimpsa_forward_chunked(inp["q"], inp["k"], inp["v"], inp["beta"], inp["d_t"], inp["A"],
+                                             inp["I_prior"])
+    assert y.device.type == "cpu"
+    _check_all((y, mT, IT), oracle_forward_from(inp), tol_for(inp), TIGHT)
