@@ -146,7 +146,7 @@ def run_ours(args, ws, rank, local):
         dist.init_process_group("nccl", device_id=dev)
     build_lib.build()
     pal.load_library()
-    wl = syn.WORKLOADS[args.workload]
+    wl = _workload(args)
     seed = wl.seed + 1000 * rank           # each rank an independent replica (weak scaling)
     inp = syn.sequence_inputs(wl, device=dev, seed=seed)
     B, H, T, dk, dv = wl.B, wl.H, wl.T, wl.d_k, wl.d_v
@@ -272,6 +272,14 @@ def run_ours(args, ws, rank, local):
         dist.destroy_process_group()
 
 
+def _workload(args):
+    from metaplastic_linear_attention_gb300 import synthetic as syn
+    wl = syn.WORKLOADS[args.workload]
+    over = {k: v for k, v in (("B", args.B), ("H", args.H), ("T", args.T), ("steps", args.decode_steps))
+            if v is not None}
+    return wl.with_(**over) if over else wl
+
+
 def _describe(wl):
     if wl.steps:
         return (f"{wl.name}: B={wl.B} H={wl.H} d_k={wl.d_k} d_v={wl.d_v}, {wl.T}-token chunked prefill + "
@@ -365,8 +373,7 @@ def run_reference(args, ws, rank):
     if rank != 0:
         return
     import oracle
-    from metaplastic_linear_attention_gb300 import synthetic as syn
-    wl = syn.WORKLOADS[args.workload]
+    wl = _workload(args)
     oracle.build()
     threads = oracle.max_threads()
     args1, _ = _oracle_sample(wl, 1)
@@ -404,6 +411,10 @@ def main():
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
     p.add_argument("--workload", default="decode",
                    choices=["decode", "small_layer", "layer_760m", "long_context", "tiny"])
+    p.add_argument("--B", type=int, default=None, help="override the workload's batch (profiling cases)")
+    p.add_argument("--H", type=int, default=None, help="override the workload's heads")
+    p.add_argument("--T", type=int, default=None, help="override the workload's scan length")
+    p.add_argument("--decode-steps", type=int, default=None, help="override the decode step count")
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--cpu-seconds", type=float, default=12.0, help="target oracle time for cpu_baseline")

@@ -81,6 +81,13 @@ typedef enum {
  * chunks of `chunk` tokens are staged on chip, the state is carried from one
  * chunk to the next). The result does not depend on `chunk`.
  *
+ * When B*H heads are too few to fill the GPU, the sequence is cut into
+ * segments whose summaries are scanned first (the affine carry of slide 9);
+ * that path takes temporary device memory (2 * d_v * d_k + 1 floats per head
+ * and segment boundary) from the CUDA stream-ordered allocator on
+ * `cuda_stream`. An allocation failure returns PALIMPSA_ERR_CUDA. Results
+ * match the unsplit scan up to fp32 rounding.
+ *
  *   q, k     [B, H, T, d_k]  in_dtype
  *   v, beta  [B, H, T, d_v]  in_dtype, beta >= 0 (per value channel)
  *   d_t      [B, H, T]       fp32, >= 0
@@ -153,6 +160,15 @@ int palimpsa_abi_version(void);
  */
 void palimpsa_set_wait_timeout_ns(uint64_t ns);
 void palimpsa_debug_withhold_first_copy(int on);
+
+/*
+ * palimpsa_set_forward_segments — process-wide override of the number of
+ * time segments palimpsa_forward_chunked cuts each sequence into (0 = the
+ * library chooses from the problem size and the GPU; S > 0 = S segments, as
+ * far as whole chunks allow). For tests and tuning; results change only by
+ * fp32 rounding.
+ */
+void palimpsa_set_forward_segments(int segments);
 
 #ifdef __cplusplus
 }

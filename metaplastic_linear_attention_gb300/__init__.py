@@ -20,6 +20,7 @@ from .binding import (  # noqa: F401
     palimpsa_debug_withhold_first_copy,
     palimpsa_forward_chunked,
     palimpsa_get_device_status,
+    palimpsa_set_forward_segments,
     palimpsa_set_wait_timeout_ns,
     palimpsa_status_string,
     palimpsa_step,

@@ -71,6 +71,8 @@ def load_library(path: str | None = None):
         lib.palimpsa_set_wait_timeout_ns.argtypes = [ctypes.c_uint64]
         lib.palimpsa_debug_withhold_first_copy.restype = None
         lib.palimpsa_debug_withhold_first_copy.argtypes = [i]
+        lib.palimpsa_set_forward_segments.restype = None
+        lib.palimpsa_set_forward_segments.argtypes = [i]
         _lib = lib
         return lib
 
@@ -89,6 +91,10 @@ def palimpsa_set_wait_timeout_ns(ns: int) -> None:
 
 def palimpsa_debug_withhold_first_copy(on: bool) -> None:
     load_library().palimpsa_debug_withhold_first_copy(1 if on else 0)
+
+
+def palimpsa_set_forward_segments(segments: int) -> None:
+    load_library().palimpsa_set_forward_segments(int(segments))
 
 
 def _stream_handle(stream) -> int:

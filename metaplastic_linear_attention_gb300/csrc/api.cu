@@ -4,7 +4,7 @@
 #include <cstdint>
 #include <mutex>
 
-#include "../../include/palimpsa.h"
+#include "palimpsa.h"
 #include "palimpsa_internal.cuh"
 
 namespace palimpsa {
@@ -19,6 +19,20 @@ std::mutex g_status_mu;
 unsigned int* g_status_ptr[kMaxDevices] = {};
 std::atomic<unsigned long long> g_wait_timeout_ns{2000000000ull};
 std::atomic<int> g_withhold_first_copy{0};
+std::atomic<int> g_forward_segments{0};
+
+// Scratch from the stream-ordered allocator: allocated and freed on the
+// launch stream, so it never synchronises and is reused from the device's
+// memory pool across calls.
+struct StreamOrderedScratch final : ScratchProvider {
+  cudaError_t acquire(size_t bytes, cudaStream_t s, float** p) override {
+    void* v = nullptr;
+    const cudaError_t e = cudaMallocAsync(&v, bytes, s);
+    *p = static_cast<float*>(v);
+    return e;
+  }
+  cudaError_t release(float* p, cudaStream_t s) override { return cudaFreeAsync(p, s); }
+};
 
 // Device address of the current device's status word (looked up once per
 // device with that device current).
@@ -81,8 +95,9 @@ palimpsa_status palimpsa_forward_chunked(const void* q, const void* k, const voi
   if (palimpsa_status s = status_word(&st)) return s;
   FwdArgs a{q, k, v, beta, d_t, A, I_prior, mu0, I0, y, mu_T, I_T, B, H, T, d_k, d_v,
             chunk == 0 ? 32 : chunk, in_dtype == PALIMPSA_BF16, st,
-            g_wait_timeout_ns.load(), g_withhold_first_copy.load()};
-  if (launch_forward_chunked(a, static_cast<cudaStream_t>(cuda_stream)) != cudaSuccess)
+            g_wait_timeout_ns.load(), g_withhold_first_copy.load(), g_forward_segments.load()};
+  StreamOrderedScratch scratch;
+  if (launch_forward_chunked(a, static_cast<cudaStream_t>(cuda_stream), &scratch) != cudaSuccess)
     return PALIMPSA_ERR_CUDA;
   return PALIMPSA_OK;
 }
@@ -143,5 +158,7 @@ int palimpsa_abi_version(void) { return PALIMPSA_ABI_VERSION; }
 void palimpsa_set_wait_timeout_ns(uint64_t ns) { g_wait_timeout_ns.store(ns); }
 
 void palimpsa_debug_withhold_first_copy(int on) { g_withhold_first_copy.store(on ? 1 : 0); }
+
+void palimpsa_set_forward_segments(int segments) { g_forward_segments.store(segments > 0 ? segments : 0); }
 
 }  // extern "C"

@@ -3,45 +3,54 @@
 // Source: Bonnet et al., "Learning to Remember, Learn, and Forget in
 // Attention-Based Models" — slide 7 (paper Eq. 5) for the update, slide 4
 // (Eq. 2) for the readout, slide 9 (App. A.12) for the natural parameters
-// M = I (.) mu and the chunked scan with a sequential carry between chunks.
+// M = I (.) mu, Ibar = I - I_prior and the chunked scan: chunks are processed
+// in parallel and the state is carried from one to the next.
 //
 // Design (GB300-first, not the pages' Triton kernel):
 // * The state of one value row i is 2 x d_k fp32 numbers (M_ij and I_ij). A CTA
-//   owns RG rows of one head for the whole sequence and keeps their state in
-//   registers: nothing of the state touches HBM between the first read and
-//   the final write, so there is no per-chunk state traffic at all.
-// * Thread tile: 2 rows x (d_k / 8) columns. The 8 lanes of a "row team" split
-//   the key dimension; lane cg owns the float4 column blocks 32 s + 4 cg, so a
-//   warp's shared-memory reads of k, k^2 and q are one 128-byte wavefront that
-//   every row team of the warp shares (broadcast).
-// * The inputs of a chunk of C tokens are staged by the bulk-copy (TMA) engine
-//   into a double buffer (cp.async.bulk + mbarrier with a bounded wait), then
-//   converted once per CTA into fp32 k, k^2, q, beta v, beta, alpha and
-//   (1 - alpha) I_prior, shared by all the CTA's rows.
-// * Per state element and token the arithmetic is
+//   owns RG rows of one head for a whole segment of the sequence and keeps
+//   their state in registers: nothing of the state touches HBM between the
+//   first read and the final write.
+// * Time split (few heads): the sequence is cut into S segments. Pass A writes
+//   each segment's summary (Gamma = prod alpha, and the decayed sums of the
+//   segment's writes into M and Ibar); pass B carries the true state across
+//   segment boundaries (state_{s+1} = Gamma_s state_s + summary_s, the affine
+//   scan of slide 9); pass C runs the recurrence with the readout from each
+//   segment's true initial state. With S = 1 only pass C runs.
+// * Staging: thread 0 stages each chunk of C tokens with four bulk async copies
+//   (cp.async.bulk, completion counted on an mbarrier with expect_tx) into a
+//   2-deep raw ring; all warps then convert a landed chunk, once per CTA, into
+//   fp32 operands shared by every row. Every wait is bounded.
+// * Compute thread tile (pass C): R rows x (d_k / 8) columns. The 8 lanes of a
+//   "row team" split the key dimension; lane cg owns the float4 column blocks
+//   32 s + 4 cg, so a warp's reads of k, k^2 and q are 128-byte wavefronts that
+//   all four row teams share (broadcast).
+// * Per state element and token pass C computes
 //       c = beta_i k_j^2 + (1 - alpha) I_prior      (FFMA)
 //       I = alpha I + c                             (FFMA)
 //       M = alpha M + (beta_i v_i) k_j              (FMUL + FFMA)
 //       y_i += (M * rcp(I)) q_j                     (MUFU.RCP, FMUL + FFMA)
-//   issued as packed f32x2 instructions over adjacent key columns, so the
-//   kernel is bound by the reciprocal (SFU) pipe, not by issue.
-// * y_{t,i} is reduced over the row team with three butterfly shuffles,
-//   staged per chunk in shared memory and stored with coalesced 16-byte stores.
+//   as packed f32x2 instructions over adjacent key columns; it is bound by the
+//   SFU reciprocal (16 per clock per SM on GB300). Pass A needs two FFMA per
+//   element and token (no reciprocal, no readout).
+// * y_{t,i} is reduced over the row team with three butterfly shuffles and
+//   stored straight to global memory.
+#include <algorithm>
+#include <cmath>
+
 #include "palimpsa_internal.cuh"
 
 namespace palimpsa {
 namespace {
 
-constexpr int kRowsPerThread = 2;
 constexpr int kLanesPerRow = 8;
 
 __host__ __device__ constexpr size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
 // Shared-memory carve-up for one CTA (all offsets 16-byte aligned).
 struct FwdSmem {
-  size_t raw_bytes;  // one raw buffer (q, k, v, beta of one chunk)
-  size_t raw_q, raw_k, raw_v, raw_b;  // offsets inside a raw buffer
-  size_t kf, k2f, qf, bvf, bf, alf, omf, ys, bars, flag, total;
+  size_t raw_q, raw_k, raw_v, raw_b, raw_bytes;  // one raw stage (q, k, v, beta of a chunk)
+  size_t kf, k2f, qf, bvf, bf, alf, omf, bars, flag, total;
 
   __host__ __device__ FwdSmem(int C, int DK, int DV, int RG, int es) {
     raw_q = 0;
@@ -57,7 +66,6 @@ struct FwdSmem {
     bf = o;  o = align_up(o + (size_t)C * RG * 4, 16);
     alf = o; o = align_up(o + (size_t)C * 4, 16);
     omf = o; o = align_up(o + (size_t)C * 4, 16);
-    ys = o;  o = align_up(o + (size_t)C * RG * 4, 16);
     bars = o; o += 2 * sizeof(uint64_t);
     flag = o; o += 16;
     total = align_up(o, 128);
@@ -66,14 +74,12 @@ struct FwdSmem {
 
 __device__ __forceinline__ float2 f2(float a) { return make_float2(a, a); }
 
-// Producer side (one thread): stage chunk n's q, k, v, beta into one raw
-// buffer with four bulk copies whose bytes complete on `bar`.
+// One thread: stage tokens [t0, t0 + tc) of q, k, v, beta into one raw buffer
+// with four bulk copies whose bytes complete on `bar`.
 template <int DK, int ES>
 __device__ __forceinline__ void stage_chunk(unsigned char* base, const FwdSmem& L, uint64_t* bar,
                                             const char* gq, const char* gk, const char* gv,
-                                            const char* gb, int n, int C, int T, int DV) {
-  const int t0 = n * C;
-  const int tc = min(C, T - t0);
+                                            const char* gb, int t0, int tc, int DV) {
   const uint32_t bq = (uint32_t)tc * DK * ES, bvb = (uint32_t)tc * DV * ES;
   mbar_arrive_expect_tx(bar, 2 * bq + 2 * bvb);
   bulk_g2s(base + L.raw_q, gq + (size_t)t0 * DK * ES, bq, bar);
@@ -82,28 +88,176 @@ __device__ __forceinline__ void stage_chunk(unsigned char* base, const FwdSmem& 
   bulk_g2s(base + L.raw_b, gb + (size_t)t0 * DV * ES, bvb, bar);
 }
 
-template <int DK, bool BF16, int RG>
-__global__ void __launch_bounds__(RG * 4)
-palimpsa_fwd_chunked_kernel(FwdArgs a, int C) {
-  constexpr int NV = DK / 32;          // float4 column blocks per thread
-  constexpr int NTH = RG * 4;          // threads per CTA
-  constexpr int ES = BF16 ? 2 : 4;     // input element size
+// Where a CTA works: head bh, segment seg, rows [row0, row0 + RG), tokens
+// [tb, tb + tn) of that head.
+struct Tile {
+  long bh;
+  int h, seg, row0, tb, tn;
+};
+
+__device__ __forceinline__ Tile tile_of(const FwdArgs& a, int RG, int nseg, int seg_len) {
+  const int groups = a.d_v / RG;
+  Tile t;
+  const long cta = blockIdx.x;
+  const int rg = (int)(cta % groups);
+  const long rest = cta / groups;
+  t.seg = (int)(rest % nseg);
+  t.bh = rest / nseg;
+  t.h = (int)(t.bh % a.H);
+  t.row0 = rg * RG;
+  t.tb = t.seg * seg_len;
+  t.tn = max(0, min(a.T, t.tb + seg_len) - t.tb);
+  return t;
+}
+
+// The staged-chunk pipeline shared by pass A and pass C: chunk order, the raw
+// ring, bounded waits and the timeout exit. Chunk c (0-based in processing
+// order) is segment-local chunk `reverse ? nch - 1 - c : c`.
+template <int DK, int ES>
+struct ChunkPipe {
+  const FwdSmem& L;
+  unsigned char* smem;
+  uint64_t* bars;
+  volatile int* flag;
+  const char *gq, *gk, *gv, *gb;
+  int C, tb, tn, DV, nch;
+  bool reverse;
+  // thread 0's record of copies in flight, for a clean exit after a timeout
+  bool pend0 = false, pend1 = false;
+  uint32_t par0 = 0, par1 = 0;
+
+  __device__ ChunkPipe(const FwdSmem& L_, unsigned char* s, const char* q, const char* k, const char* v,
+                       const char* b, int C_, int tb_, int tn_, int DV_, bool rev)
+      : L(L_), smem(s), bars(reinterpret_cast<uint64_t*>(s + L_.bars)),
+        flag(reinterpret_cast<volatile int*>(s + L_.flag)), gq(q), gk(k), gv(v), gb(b), C(C_), tb(tb_),
+        tn(tn_), DV(DV_), nch((tn_ + C_ - 1) / C_), reverse(rev) {}
+
+  __device__ int t0_of(int c) const { return (reverse ? nch - 1 - c : c) * C; }  // segment-local
+  __device__ int tc_of(int c) const { return min(C, tn - t0_of(c)); }
+  __device__ unsigned char* raw(int c) const { return smem + (size_t)(c & 1) * L.raw_bytes; }
+
+  __device__ void issue(int c) {  // thread 0 only
+    stage_chunk<DK, ES>(raw(c), L, &bars[c & 1], gq, gk, gv, gb, tb + t0_of(c), tc_of(c), DV);
+    const uint32_t par = (uint32_t)(c >> 1) & 1u;
+    if ((c & 1) == 0) { pend0 = true; par0 = par; } else { pend1 = true; par1 = par; }
+  }
+
+  __device__ void init(bool withhold_first) {  // all threads; thread 0 does the work
+    if (threadIdx.x == 0) {
+      mbar_init(&bars[0], 1);
+      mbar_init(&bars[1], 1);
+      *flag = 0;
+      fence_mbar_init();
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      for (int c = 0; c < 2 && c < nch; ++c) {
+        if (c == 0 && withhold_first) continue;
+        issue(c);
+      }
+    }
+  }
+
+  // All threads: wait until chunk c has landed. Returns false (for every
+  // thread, consistently) after a timeout; the caller must then return.
+  __device__ bool wait(int c, unsigned long long timeout_ns, unsigned int* status) {
+    if (!mbar_wait_bounded(&bars[c & 1], (uint32_t)(c >> 1) & 1u, timeout_ns)) *flag = 1;
+    __syncthreads();
+    if (*flag) {
+      if (threadIdx.x == 0) {
+        latch_status(status, kStatusTimeout);
+        const unsigned long long drain_ns = 1000000000ull;
+        if (pend0) mbar_wait_bounded(&bars[0], par0, drain_ns);
+        if (pend1) mbar_wait_bounded(&bars[1], par1, drain_ns);
+      }
+      __syncthreads();
+      return false;
+    }
+    if (threadIdx.x == 0) { if ((c & 1) == 0) pend0 = false; else pend1 = false; }
+    return true;
+  }
+
+  // After the CTA-wide barrier that ends the conversion of chunk c: refill its
+  // raw buffer with chunk c + 2 (thread 0).
+  __device__ void refill(int c) {
+    if (threadIdx.x == 0 && c + 2 < nch) issue(c + 2);
+  }
+};
+
+// Convert the landed raw chunk to fp32 k, k^2 (and q when WITH_Q) shared by all
+// rows. NTH threads cooperate.
+template <int DK, bool BF16, bool WITH_Q, int NTH>
+__device__ __forceinline__ void convert_keys(const unsigned char* raw, const FwdSmem& L, unsigned char* smem,
+                                             int tc) {
+  float* kf = reinterpret_cast<float*>(smem + L.kf);
+  float* k2f = reinterpret_cast<float*>(smem + L.k2f);
+  float* qf = reinterpret_cast<float*>(smem + L.qf);
+  constexpr int PER = 8;
+  const int items = tc * DK / PER;
+  for (int it = threadIdx.x; it < items; it += NTH) {
+    float kv[PER], qv[PER];
+    if constexpr (BF16) {
+      const uint4 k8 = *reinterpret_cast<const uint4*>(raw + L.raw_k + (size_t)it * 16);
+      const uint32_t kw[4] = {k8.x, k8.y, k8.z, k8.w};
+#pragma unroll
+      for (int e = 0; e < 4; ++e) { kv[2 * e] = bf16_lo(kw[e]); kv[2 * e + 1] = bf16_hi(kw[e]); }
+      if constexpr (WITH_Q) {
+        const uint4 q8 = *reinterpret_cast<const uint4*>(raw + L.raw_q + (size_t)it * 16);
+        const uint32_t qw[4] = {q8.x, q8.y, q8.z, q8.w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) { qv[2 * e] = bf16_lo(qw[e]); qv[2 * e + 1] = bf16_hi(qw[e]); }
+      }
+    } else {
+      const float4* k4 = reinterpret_cast<const float4*>(raw + L.raw_k) + 2 * it;
+      const float4 ka = k4[0], kb = k4[1];
+      kv[0] = ka.x; kv[1] = ka.y; kv[2] = ka.z; kv[3] = ka.w;
+      kv[4] = kb.x; kv[5] = kb.y; kv[6] = kb.z; kv[7] = kb.w;
+      if constexpr (WITH_Q) {
+        const float4* q4 = reinterpret_cast<const float4*>(raw + L.raw_q) + 2 * it;
+        const float4 qa = q4[0], qb = q4[1];
+        qv[0] = qa.x; qv[1] = qa.y; qv[2] = qa.z; qv[3] = qa.w;
+        qv[4] = qb.x; qv[5] = qb.y; qv[6] = qb.z; qv[7] = qb.w;
+      }
+    }
+    float4* ko = reinterpret_cast<float4*>(kf) + 2 * it;
+    float4* k2o = reinterpret_cast<float4*>(k2f) + 2 * it;
+    ko[0] = make_float4(kv[0], kv[1], kv[2], kv[3]);
+    ko[1] = make_float4(kv[4], kv[5], kv[6], kv[7]);
+    k2o[0] = make_float4(kv[0] * kv[0], kv[1] * kv[1], kv[2] * kv[2], kv[3] * kv[3]);
+    k2o[1] = make_float4(kv[4] * kv[4], kv[5] * kv[5], kv[6] * kv[6], kv[7] * kv[7]);
+    if constexpr (WITH_Q) {
+      float4* qo = reinterpret_cast<float4*>(qf) + 2 * it;
+      qo[0] = make_float4(qv[0], qv[1], qv[2], qv[3]);
+      qo[1] = make_float4(qv[4], qv[5], qv[6], qv[7]);
+    }
+  }
+}
+
+template <bool BF16>
+__device__ __forceinline__ float raw_elem(const unsigned char* base, size_t e) {
+  if constexpr (BF16) return __bfloat162float(reinterpret_cast<const __nv_bfloat16*>(base)[e]);
+  else return reinterpret_cast<const float*>(base)[e];
+}
+
+// ------------------------------------------------------------------ pass C
+// The recurrence with the readout over one segment (the whole sequence when
+// S = 1), from the segment's true initial state.
+template <int DK, bool BF16, int RG, int R>
+__global__ void __launch_bounds__(RG / (4 * R) * 32)
+palimpsa_fwd_chunked_kernel(FwdArgs a, int C, int nseg, int seg_len, const float* __restrict__ seg_state) {
+  constexpr int NV = DK / 32;                 // float4 column blocks per thread
+  constexpr int NTH = RG / (4 * R) * 32;      // threads per CTA
+  constexpr int ES = BF16 ? 2 : 4;
   extern __shared__ __align__(128) unsigned char smem[];
 
   const int DV = a.d_v, T = a.T;
-  const int groups = DV / RG;
-  const long bh = blockIdx.x / groups;
-  const int row0 = (blockIdx.x % groups) * RG;
-  const int h = (int)(bh % a.H);
-  const int tid = threadIdx.x;
-  const int lane = tid & 31, warp = tid >> 5;
+  const Tile tl = tile_of(a, RG, nseg, seg_len);
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int cg = lane & (kLanesPerRow - 1);
   const int rt = lane >> 3;
-  const int lr0 = warp * 8 + rt * kRowsPerThread;  // first local row of this thread
+  const int lr0 = (warp * 4 + rt) * R;  // first local row of this thread
 
   const FwdSmem L(C, DK, DV, RG, ES);
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L.bars);
-  volatile int* sflag = reinterpret_cast<volatile int*>(smem + L.flag);
   float* kf = reinterpret_cast<float*>(smem + L.kf);
   float* k2f = reinterpret_cast<float*>(smem + L.k2f);
   float* qf = reinterpret_cast<float*>(smem + L.qf);
@@ -111,154 +265,89 @@ palimpsa_fwd_chunked_kernel(FwdArgs a, int C) {
   float* bfv = reinterpret_cast<float*>(smem + L.bf);
   float* alf = reinterpret_cast<float*>(smem + L.alf);
   float* omf = reinterpret_cast<float*>(smem + L.omf);
-  float* ys = reinterpret_cast<float*>(smem + L.ys);
 
-  const float A_h = a.A[h];
-  const float Ip = a.I_prior[h];
+  const float A_h = a.A[tl.h];
+  const float Ip = a.I_prior[tl.h];
   bool domain_bad = !(pos_finite(A_h) && pos_finite(Ip));
 
-  const int nchunks = (T + C - 1) / C;
-  const char* gq = static_cast<const char*>(a.q) + (size_t)bh * T * DK * ES;
-  const char* gk = static_cast<const char*>(a.k) + (size_t)bh * T * DK * ES;
-  const char* gv = static_cast<const char*>(a.v) + (size_t)bh * T * DV * ES;
-  const char* gb = static_cast<const char*>(a.beta) + (size_t)bh * T * DV * ES;
-  const float* gd = a.d_t + (size_t)bh * T;
+  const size_t head_tok = (size_t)tl.bh * T;
+  ChunkPipe<DK, ES> pipe(L, smem, static_cast<const char*>(a.q) + head_tok * DK * ES,
+                         static_cast<const char*>(a.k) + head_tok * DK * ES,
+                         static_cast<const char*>(a.v) + head_tok * DV * ES,
+                         static_cast<const char*>(a.beta) + head_tok * DV * ES, C, tl.tb, tl.tn, DV, false);
+  pipe.init(a.withhold_first_copy != 0);
 
-  // Thread 0's record of copies issued but not yet consumed, per raw buffer,
-  // with the barrier phase that will signal them.
-  bool pending0 = false, pending1 = false;
-  uint32_t parity0 = 0u, parity1 = 0u;
-  if (tid == 0) {
-    mbar_init(&bars[0], 1);
-    mbar_init(&bars[1], 1);
-    *sflag = 0;
-    fence_mbar_init();
-  }
-  __syncthreads();
-  if (tid == 0) {
-    if (nchunks > 0 && !a.withhold_first_copy) {
-      stage_chunk<DK, ES>(smem, L, &bars[0], gq, gk, gv, gb, 0, C, T, DV);
-      pending0 = true; parity0 = 0u;
-    }
-    if (nchunks > 1) {
-      stage_chunk<DK, ES>(smem + L.raw_bytes, L, &bars[1], gq, gk, gv, gb, 1, C, T, DV);
-      pending1 = true; parity1 = 0u;
-    }
-  }
-
-  // ---- initial state: M = I0 (.) mu0, I = I0 (defaults mu0 = 0, I0 = I_prior)
-  float2 Ist[kRowsPerThread][2 * NV], Mst[kRowsPerThread][2 * NV];
-  const size_t state_base = ((size_t)bh * DV + row0) * DK;
+  // ---- initial state: M = I0 (.) mu0, I = I0 for the first segment (defaults
+  // mu0 = 0, I0 = I_prior); M = carried M, I = I_prior + carried Ibar otherwise.
+  float2 Ist[R][2 * NV], Mst[R][2 * NV];
+  const size_t state_base = ((size_t)tl.bh * DV + tl.row0) * DK;
+  const float* carried = nullptr;
+  if (tl.seg > 0) carried = seg_state + ((size_t)tl.bh * (nseg - 1) + (tl.seg - 1)) * 2 * DV * DK;
 #pragma unroll
-  for (int r = 0; r < kRowsPerThread; ++r) {
+  for (int r = 0; r < R; ++r) {
 #pragma unroll
     for (int s = 0; s < NV; ++s) {
-      const size_t off = state_base + (size_t)(lr0 + r) * DK + 32 * s + 4 * cg;
-      float4 i4 = a.I0 ? *reinterpret_cast<const float4*>(a.I0 + off) : make_float4(Ip, Ip, Ip, Ip);
-      float4 m4 = a.mu0 ? *reinterpret_cast<const float4*>(a.mu0 + off) : make_float4(0.f, 0.f, 0.f, 0.f);
-      domain_bad |= !(pos_finite(i4.x) && pos_finite(i4.y) && pos_finite(i4.z) && pos_finite(i4.w));
+      const size_t e = (size_t)(tl.row0 + lr0 + r) * DK + 32 * s + 4 * cg;
+      float4 i4, m4;
+      if (carried) {
+        m4 = *reinterpret_cast<const float4*>(carried + e);
+        const float4 ib = *reinterpret_cast<const float4*>(carried + (size_t)DV * DK + e);
+        i4 = make_float4(Ip + ib.x, Ip + ib.y, Ip + ib.z, Ip + ib.w);
+      } else {
+        const size_t off = state_base + (size_t)(lr0 + r) * DK + 32 * s + 4 * cg;
+        i4 = a.I0 ? *reinterpret_cast<const float4*>(a.I0 + off) : make_float4(Ip, Ip, Ip, Ip);
+        const float4 u = a.mu0 ? *reinterpret_cast<const float4*>(a.mu0 + off) : make_float4(0.f, 0.f, 0.f, 0.f);
+        domain_bad |= !(pos_finite(i4.x) && pos_finite(i4.y) && pos_finite(i4.z) && pos_finite(i4.w));
+        m4 = make_float4(i4.x * u.x, i4.y * u.y, i4.z * u.z, i4.w * u.w);
+      }
       Ist[r][2 * s] = make_float2(i4.x, i4.y);
       Ist[r][2 * s + 1] = make_float2(i4.z, i4.w);
-      Mst[r][2 * s] = make_float2(i4.x * m4.x, i4.y * m4.y);
-      Mst[r][2 * s + 1] = make_float2(i4.z * m4.z, i4.w * m4.w);
+      Mst[r][2 * s] = make_float2(m4.x, m4.y);
+      Mst[r][2 * s + 1] = make_float2(m4.z, m4.w);
     }
   }
 
-  for (int n = 0; n < nchunks; ++n) {
-    const int t0 = n * C;
-    const int tc = min(C, T - t0);
-    const int buf = n & 1;
-    if (!mbar_wait_bounded(&bars[buf], (n >> 1) & 1, a.wait_timeout_ns)) *sflag = 1;
-    __syncthreads();
-    if (*sflag) {
-      // A staged copy never arrived: report, let copies still in flight land, leave.
-      if (tid == 0) {
-        latch_status(a.status, kStatusTimeout);
-        const unsigned long long drain_ns = 1000000000ull;
-        if (pending0) mbar_wait_bounded(&bars[0], parity0, drain_ns);
-        if (pending1) mbar_wait_bounded(&bars[1], parity1, drain_ns);
-      }
-      __syncthreads();
-      return;
-    }
-
+  float* gy = a.y + (head_tok + tl.tb) * DV + tl.row0 + lr0;
+  const float* gd = a.d_t + head_tok + tl.tb;
+  for (int c = 0; c < pipe.nch; ++c) {
+    const int t0 = pipe.t0_of(c), tc = pipe.tc_of(c);
+    if (!pipe.wait(c, a.wait_timeout_ns, a.status)) return;
     // ---- convert the staged chunk to fp32 operands shared by all rows
-    const unsigned char* raw = smem + (size_t)buf * L.raw_bytes;
-    {
-      constexpr int PER = 8;  // elements per work item (16 B of bf16, 32 B of fp32)
-      const int items = tc * DK / PER;
-      for (int it = tid; it < items; it += NTH) {
-        float qv[PER], kv[PER];
-        if constexpr (BF16) {
-          const uint4 q8 = *reinterpret_cast<const uint4*>(raw + L.raw_q + (size_t)it * 16);
-          const uint4 k8 = *reinterpret_cast<const uint4*>(raw + L.raw_k + (size_t)it * 16);
-          const uint32_t qw[4] = {q8.x, q8.y, q8.z, q8.w}, kw[4] = {k8.x, k8.y, k8.z, k8.w};
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            qv[2 * e] = bf16_lo(qw[e]); qv[2 * e + 1] = bf16_hi(qw[e]);
-            kv[2 * e] = bf16_lo(kw[e]); kv[2 * e + 1] = bf16_hi(kw[e]);
-          }
-        } else {
-          const float4* q4 = reinterpret_cast<const float4*>(raw + L.raw_q) + 2 * it;
-          const float4* k4 = reinterpret_cast<const float4*>(raw + L.raw_k) + 2 * it;
-          const float4 qa = q4[0], qb = q4[1], ka = k4[0], kb = k4[1];
-          qv[0] = qa.x; qv[1] = qa.y; qv[2] = qa.z; qv[3] = qa.w;
-          qv[4] = qb.x; qv[5] = qb.y; qv[6] = qb.z; qv[7] = qb.w;
-          kv[0] = ka.x; kv[1] = ka.y; kv[2] = ka.z; kv[3] = ka.w;
-          kv[4] = kb.x; kv[5] = kb.y; kv[6] = kb.z; kv[7] = kb.w;
-        }
-        float4* qo = reinterpret_cast<float4*>(qf) + 2 * it;
-        float4* ko = reinterpret_cast<float4*>(kf) + 2 * it;
-        float4* k2o = reinterpret_cast<float4*>(k2f) + 2 * it;
-        qo[0] = make_float4(qv[0], qv[1], qv[2], qv[3]);
-        qo[1] = make_float4(qv[4], qv[5], qv[6], qv[7]);
-        ko[0] = make_float4(kv[0], kv[1], kv[2], kv[3]);
-        ko[1] = make_float4(kv[4], kv[5], kv[6], kv[7]);
-        k2o[0] = make_float4(kv[0] * kv[0], kv[1] * kv[1], kv[2] * kv[2], kv[3] * kv[3]);
-        k2o[1] = make_float4(kv[4] * kv[4], kv[5] * kv[5], kv[6] * kv[6], kv[7] * kv[7]);
-      }
-      for (int it = tid; it < tc * RG; it += NTH) {
-        const int t = it / RG, r = it % RG;
-        const size_t e = (size_t)t * DV + row0 + r;
-        float vv, bb;
-        if constexpr (BF16) {
-          vv = __bfloat162float(reinterpret_cast<const __nv_bfloat16*>(raw + L.raw_v)[e]);
-          bb = __bfloat162float(reinterpret_cast<const __nv_bfloat16*>(raw + L.raw_b)[e]);
-        } else {
-          vv = reinterpret_cast<const float*>(raw + L.raw_v)[e];
-          bb = reinterpret_cast<const float*>(raw + L.raw_b)[e];
-        }
-        domain_bad |= !nonneg_finite(bb);
-        bvf[it] = bb * vv;
-        bfv[it] = bb;
-      }
-      for (int t = tid; t < tc; t += NTH) {
-        const float d = gd[t0 + t];
-        domain_bad |= !nonneg_finite(d);
-        const float x = -A_h * d;
-        alf[t] = expf(x);
-        omf[t] = -expm1f(x) * Ip;  // (1 - alpha) I_prior without cancellation
-      }
+    const unsigned char* raw = pipe.raw(c);
+    convert_keys<DK, BF16, true, NTH>(raw, L, smem, tc);
+    for (int it = threadIdx.x; it < tc * RG; it += NTH) {
+      const int t = it / RG, r = it % RG;
+      const size_t e = (size_t)t * DV + tl.row0 + r;
+      const float vv = raw_elem<BF16>(raw + L.raw_v, e), bb = raw_elem<BF16>(raw + L.raw_b, e);
+      domain_bad |= !nonneg_finite(bb);
+      bvf[it] = bb * vv;
+      bfv[it] = bb;
+    }
+    for (int t = threadIdx.x; t < tc; t += NTH) {
+      const float d = gd[t0 + t];
+      domain_bad |= !nonneg_finite(d);
+      const float x = -A_h * d;
+      alf[t] = expf(x);
+      omf[t] = -expm1f(x) * Ip;  // (1 - alpha) I_prior without cancellation
     }
     __syncthreads();
-    // raw[buf] is consumed: refill it with chunk n + 2 while this chunk computes.
-    if (tid == 0) {
-      const bool more = n + 2 < nchunks;
-      if (more) stage_chunk<DK, ES>(smem + (size_t)buf * L.raw_bytes, L, &bars[buf], gq, gk, gv, gb, n + 2, C, T, DV);
-      const uint32_t par = (uint32_t)((n + 2) >> 1) & 1u;
-      if (buf == 0) { pending0 = more; parity0 = par; } else { pending1 = more; parity1 = par; }
-    }
+    pipe.refill(c);
 
     // ---- the recurrence over the chunk's tokens, state in registers
     for (int t = 0; t < tc; ++t) {
-      const float al = alf[t], om = omf[t];
-      const float2 a2 = f2(al), om2 = f2(om);
-      const float2 bb = *reinterpret_cast<const float2*>(bfv + t * RG + lr0);
-      const float2 bv = *reinterpret_cast<const float2*>(bvf + t * RG + lr0);
-      const float brow[2] = {bb.x, bb.y}, bvrow[2] = {bv.x, bv.y};
-      float2 acc[kRowsPerThread];
+      const float2 a2 = f2(alf[t]), om2 = f2(omf[t]);
+      float brow[R], bvrow[R];
+      if constexpr (R == 2) {
+        const float2 bb = *reinterpret_cast<const float2*>(bfv + t * RG + lr0);
+        const float2 bv = *reinterpret_cast<const float2*>(bvf + t * RG + lr0);
+        brow[0] = bb.x; brow[1] = bb.y; bvrow[0] = bv.x; bvrow[1] = bv.y;
+      } else {
 #pragma unroll
-      for (int r = 0; r < kRowsPerThread; ++r) acc[r] = make_float2(0.f, 0.f);
+        for (int r = 0; r < R; ++r) { brow[r] = bfv[t * RG + lr0 + r]; bvrow[r] = bvf[t * RG + lr0 + r]; }
+      }
+      float2 acc[R];
+#pragma unroll
+      for (int r = 0; r < R; ++r) acc[r] = make_float2(0.f, 0.f);
 #pragma unroll
       for (int s = 0; s < NV; ++s) {
         const int col = 32 * s + 4 * cg;
@@ -269,7 +358,7 @@ palimpsa_fwd_chunked_kernel(FwdArgs a, int C) {
         const float2 kkp[2] = {make_float2(kk4.x, kk4.y), make_float2(kk4.z, kk4.w)};
         const float2 qp[2] = {make_float2(q4.x, q4.y), make_float2(q4.z, q4.w)};
 #pragma unroll
-        for (int r = 0; r < kRowsPerThread; ++r) {
+        for (int r = 0; r < R; ++r) {
 #pragma unroll
           for (int p = 0; p < 2; ++p) {
             float2& I2 = Ist[r][2 * s + p];
@@ -282,102 +371,343 @@ palimpsa_fwd_chunked_kernel(FwdArgs a, int C) {
           }
         }
       }
-      float y0 = acc[0].x + acc[0].y, y1 = acc[1].x + acc[1].y;
+      float yv[R];
 #pragma unroll
-      for (int m = 1; m < kLanesPerRow; m <<= 1) {
-        y0 += __shfl_xor_sync(0xffffffffu, y0, m);
-        y1 += __shfl_xor_sync(0xffffffffu, y1, m);
+      for (int r = 0; r < R; ++r) {
+        yv[r] = acc[r].x + acc[r].y;
+#pragma unroll
+        for (int m = 1; m < kLanesPerRow; m <<= 1) yv[r] += __shfl_xor_sync(0xffffffffu, yv[r], m);
       }
-      if (cg == 0) *reinterpret_cast<float2*>(ys + t * RG + lr0) = make_float2(y0, y1);
+      if (cg == 0) {
+        if constexpr (R == 2) *reinterpret_cast<float2*>(gy + (size_t)(t0 + t) * DV) = make_float2(yv[0], yv[1]);
+        else gy[(size_t)(t0 + t) * DV] = yv[0];
+      }
     }
-    __syncthreads();
+    // (the barrier at the top of the next chunk orders these reads before the
+    // next conversion overwrites the operands)
+  }
 
-    // ---- store the chunk's y rows (RG contiguous fp32 per token)
-    {
-      float* gy = a.y + ((size_t)bh * T + t0) * DV + row0;
-      const int per_t = RG / 4;
-      for (int it = tid; it < tc * per_t; it += NTH) {
-        const int t = it / per_t, c4 = it % per_t;
-        *reinterpret_cast<float4*>(gy + (size_t)t * DV + 4 * c4) =
-            *reinterpret_cast<const float4*>(ys + t * RG + 4 * c4);
+  // ---- final state (last segment only): mu_T = M / I, I_T = I.
+  if (tl.seg == nseg - 1) {
+#pragma unroll
+    for (int r = 0; r < R; ++r) {
+#pragma unroll
+      for (int s = 0; s < NV; ++s) {
+        const size_t off = state_base + (size_t)(lr0 + r) * DK + 32 * s + 4 * cg;
+        const float2 i01 = Ist[r][2 * s], i23 = Ist[r][2 * s + 1];
+        float4 m4;
+        if (T == 0) {  // pass the initial state through unchanged
+          m4 = a.mu0 ? *reinterpret_cast<const float4*>(a.mu0 + off) : make_float4(0.f, 0.f, 0.f, 0.f);
+        } else {
+          const float2 m01 = Mst[r][2 * s], m23 = Mst[r][2 * s + 1];
+          m4 = make_float4(m01.x / i01.x, m01.y / i01.y, m23.x / i23.x, m23.y / i23.y);
+        }
+        *reinterpret_cast<float4*>(a.mu_T + off) = m4;
+        *reinterpret_cast<float4*>(a.I_T + off) = make_float4(i01.x, i01.y, i23.x, i23.y);
       }
     }
   }
-
-  // ---- final state: mu_T = M / I, I_T = I (T = 0 passes the initial state through)
-#pragma unroll
-  for (int r = 0; r < kRowsPerThread; ++r) {
-#pragma unroll
-    for (int s = 0; s < NV; ++s) {
-      const size_t off = state_base + (size_t)(lr0 + r) * DK + 32 * s + 4 * cg;
-      const float2 i01 = Ist[r][2 * s], i23 = Ist[r][2 * s + 1];
-      float4 m4;
-      if (nchunks == 0) {
-        m4 = a.mu0 ? *reinterpret_cast<const float4*>(a.mu0 + off) : make_float4(0.f, 0.f, 0.f, 0.f);
-      } else {
-        const float2 m01 = Mst[r][2 * s], m23 = Mst[r][2 * s + 1];
-        m4 = make_float4(m01.x / i01.x, m01.y / i01.y, m23.x / i23.x, m23.y / i23.y);
-      }
-      *reinterpret_cast<float4*>(a.mu_T + off) = m4;
-      *reinterpret_cast<float4*>(a.I_T + off) = make_float4(i01.x, i01.y, i23.x, i23.y);
-    }
-  }
-  if (domain_bad) latch_status(a.status, kStatusDomain);
+  if (__any_sync(0xffffffffu, domain_bad) && lane == 0) latch_status(a.status, kStatusDomain);
 }
 
+// ------------------------------------------------------------------ pass A
+// Segment summary for segments 0 .. S-2: with W_t = prod_{u > t in segment} alpha_u,
+//   dM    = sum_t W_t (beta_t v_t) (x) k_t,
+//   dIbar = sum_t W_t beta_t (x) k_t^2,
+//   Gamma = prod_{t in segment} alpha_t,
+// so that the state after the segment is Gamma * state_before + (dM, dIbar)
+// (slide 9: both natural-parameter recurrences are affine with the shared
+// scalar decay alpha). Chunks are staged and processed from the segment's end
+// backwards, so W is a running suffix product (it only ever shrinks; no
+// quotients of products).
+// Output: seg_state[(bh, seg)] = (dM, dIbar), seg_gamma[(bh, seg)] = Gamma.
+template <int DK, bool BF16, int RG, int R>
+__global__ void __launch_bounds__(RG / (4 * R) * 32)
+palimpsa_fwd_summary_kernel(FwdArgs a, int C, int nseg, int seg_len, float* __restrict__ seg_state,
+                            float* __restrict__ seg_gamma) {
+  constexpr int NV = DK / 32;
+  constexpr int NTH = RG / (4 * R) * 32;
+  constexpr int ES = BF16 ? 2 : 4;
+  extern __shared__ __align__(128) unsigned char smem[];
+
+  const int DV = a.d_v, T = a.T;
+  // the grid covers segments 0 .. nseg - 2 only
+  const Tile tl = tile_of(a, RG, nseg - 1, seg_len);
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int cg = lane & (kLanesPerRow - 1);
+  const int rt = lane >> 3;
+  const int lr0 = (warp * 4 + rt) * R;
+
+  const FwdSmem L(C, DK, DV, RG, ES);
+  const float* kf = reinterpret_cast<const float*>(smem + L.kf);
+  const float* k2f = reinterpret_cast<const float*>(smem + L.k2f);
+  float* wbvf = reinterpret_cast<float*>(smem + L.bvf);   // W_t beta_t v_t
+  float* wbf = reinterpret_cast<float*>(smem + L.bf);     // W_t beta_t
+  float* wf = reinterpret_cast<float*>(smem + L.alf);     // W_t
+  float* carry = reinterpret_cast<float*>(smem + L.omf);  // [0] = product of alpha after this chunk
+
+  const float A_h = a.A[tl.h];
+  const size_t head_tok = (size_t)tl.bh * T;
+  ChunkPipe<DK, ES> pipe(L, smem, static_cast<const char*>(a.q) + head_tok * DK * ES,
+                         static_cast<const char*>(a.k) + head_tok * DK * ES,
+                         static_cast<const char*>(a.v) + head_tok * DV * ES,
+                         static_cast<const char*>(a.beta) + head_tok * DV * ES, C, tl.tb, tl.tn, DV, true);
+  if (threadIdx.x == 0) carry[0] = 1.f;
+  pipe.init(a.withhold_first_copy != 0);
+
+  float2 dI[R][2 * NV], dM[R][2 * NV];
+#pragma unroll
+  for (int r = 0; r < R; ++r)
+#pragma unroll
+    for (int j = 0; j < 2 * NV; ++j) { dI[r][j] = make_float2(0.f, 0.f); dM[r][j] = make_float2(0.f, 0.f); }
+
+  const float* gd = a.d_t + head_tok + tl.tb;
+  for (int c = 0; c < pipe.nch; ++c) {
+    const int t0 = pipe.t0_of(c), tc = pipe.tc_of(c);
+    if (!pipe.wait(c, a.wait_timeout_ns, a.status)) return;
+    const unsigned char* raw = pipe.raw(c);
+    // suffix products inside the chunk (warp 0; at most 32 tokens per chunk):
+    // W_t = carry * prod_{t < u < tc} alpha_u
+    if (warp == 0) {
+      const float al = lane < tc ? expf(-A_h * gd[t0 + lane]) : 1.f;
+      float p = al;  // inclusive suffix product prod_{u >= lane}
+#pragma unroll
+      for (int off = 1; off < 32; off <<= 1) {
+        const float o = __shfl_down_sync(0xffffffffu, p, off);
+        if (lane + off < 32) p *= o;
+      }
+      const float excl = __shfl_down_sync(0xffffffffu, p, 1);
+      const float cin = carry[0];
+      if (lane < tc) wf[lane] = cin * (lane + 1 < tc ? excl : 1.f);
+      __syncwarp();
+      if (lane == 0) carry[0] = cin * p;  // lane 0 holds the product over the whole chunk
+    }
+    convert_keys<DK, BF16, false, NTH>(raw, L, smem, tc);
+    __syncthreads();  // W_t ready
+    for (int it = threadIdx.x; it < tc * RG; it += NTH) {
+      const int t = it / RG, r = it % RG;
+      const size_t e = (size_t)t * DV + tl.row0 + r;
+      const float vv = raw_elem<BF16>(raw + L.raw_v, e), bb = raw_elem<BF16>(raw + L.raw_b, e);
+      const float w = wf[t];
+      wbvf[it] = w * (bb * vv);
+      wbf[it] = w * bb;
+    }
+    __syncthreads();
+    pipe.refill(c);
+    for (int t = tc - 1; t >= 0; --t) {
+      float wb[R], wbv[R];
+#pragma unroll
+      for (int r = 0; r < R; ++r) { wb[r] = wbf[t * RG + lr0 + r]; wbv[r] = wbvf[t * RG + lr0 + r]; }
+#pragma unroll
+      for (int s = 0; s < NV; ++s) {
+        const int col = 32 * s + 4 * cg;
+        const float4 k4 = *reinterpret_cast<const float4*>(kf + t * DK + col);
+        const float4 kk4 = *reinterpret_cast<const float4*>(k2f + t * DK + col);
+        const float2 kp[2] = {make_float2(k4.x, k4.y), make_float2(k4.z, k4.w)};
+        const float2 kkp[2] = {make_float2(kk4.x, kk4.y), make_float2(kk4.z, kk4.w)};
+#pragma unroll
+        for (int r = 0; r < R; ++r) {
+#pragma unroll
+          for (int p = 0; p < 2; ++p) {
+            dM[r][2 * s + p] = __ffma2_rn(f2(wbv[r]), kp[p], dM[r][2 * s + p]);
+            dI[r][2 * s + p] = __ffma2_rn(f2(wb[r]), kkp[p], dI[r][2 * s + p]);
+          }
+        }
+      }
+    }
+    // (the barrier at the top of the next chunk orders these reads before the
+    // next conversion overwrites the operands)
+  }
+
+  float* out = seg_state + ((size_t)tl.bh * (nseg - 1) + tl.seg) * 2 * DV * DK;
+#pragma unroll
+  for (int r = 0; r < R; ++r) {
+#pragma unroll
+    for (int s = 0; s < NV; ++s) {
+      const size_t e = (size_t)(tl.row0 + lr0 + r) * DK + 32 * s + 4 * cg;
+      const float2 m01 = dM[r][2 * s], m23 = dM[r][2 * s + 1], i01 = dI[r][2 * s], i23 = dI[r][2 * s + 1];
+      *reinterpret_cast<float4*>(out + e) = make_float4(m01.x, m01.y, m23.x, m23.y);
+      *reinterpret_cast<float4*>(out + (size_t)DV * DK + e) = make_float4(i01.x, i01.y, i23.x, i23.y);
+    }
+  }
+  __syncthreads();  // carry[0] final (written by warp 0 in the last chunk)
+  if (threadIdx.x == 0 && tl.row0 == 0) seg_gamma[(size_t)tl.bh * (nseg - 1) + tl.seg] = carry[0];
+}
+
+// ------------------------------------------------------------------ pass B
+// Carry across segments, per state element (in place over the summaries):
+//   (M, Ibar)_0 = (I0 mu0, I0 - I_prior)   (mu0 = 0 and I0 = I_prior when absent)
+//   (M, Ibar)_{s+1} = Gamma_s (M, Ibar)_s + summary_s,   s = 0 .. S-2,
+// leaving in slot s the state at the start of segment s + 1.
+__global__ void __launch_bounds__(256)
+palimpsa_fwd_carry_kernel(FwdArgs a, int nseg, float* __restrict__ seg_state,
+                          const float* __restrict__ seg_gamma) {
+  const long per_head = (long)a.d_v * a.d_k / 4;  // float4 quads per array
+  const long q = (long)blockIdx.x * blockDim.x + threadIdx.x;
+  if (q >= (long)a.B * a.H * per_head) return;
+  const long bh = q / per_head;
+  const long e = (q % per_head) * 4;
+  const int h = (int)(bh % a.H);
+  const float Ip = a.I_prior[h];
+  const size_t DVK = (size_t)a.d_v * a.d_k;
+  const size_t off = (size_t)bh * DVK + e;
+  const float4 i0 = a.I0 ? *reinterpret_cast<const float4*>(a.I0 + off) : make_float4(Ip, Ip, Ip, Ip);
+  const float4 u = a.mu0 ? *reinterpret_cast<const float4*>(a.mu0 + off) : make_float4(0.f, 0.f, 0.f, 0.f);
+  float4 m = make_float4(i0.x * u.x, i0.y * u.y, i0.z * u.z, i0.w * u.w);
+  float4 ib = make_float4(i0.x - Ip, i0.y - Ip, i0.z - Ip, i0.w - Ip);
+  for (int s = 0; s < nseg - 1; ++s) {
+    const float g = seg_gamma[(size_t)bh * (nseg - 1) + s];
+    float* slot = seg_state + ((size_t)bh * (nseg - 1) + s) * 2 * DVK;
+    const float4 dm = *reinterpret_cast<const float4*>(slot + e);
+    const float4 di = *reinterpret_cast<const float4*>(slot + DVK + e);
+    m = make_float4(fmaf(g, m.x, dm.x), fmaf(g, m.y, dm.y), fmaf(g, m.z, dm.z), fmaf(g, m.w, dm.w));
+    ib = make_float4(fmaf(g, ib.x, di.x), fmaf(g, ib.y, di.y), fmaf(g, ib.z, di.z), fmaf(g, ib.w, di.w));
+    *reinterpret_cast<float4*>(slot + e) = m;
+    *reinterpret_cast<float4*>(slot + DVK + e) = ib;
+  }
+}
+
+// ------------------------------------------------------------------ host side
+
+constexpr int kRowsPerThread = 2;
+
 template <int DK, bool BF16, int RG>
-cudaError_t launch_t(const FwdArgs& a, int C, cudaStream_t s) {
-  const FwdSmem L(C, DK, a.d_v, RG, BF16 ? 2 : 4);
-  auto kern = palimpsa_fwd_chunked_kernel<DK, BF16, RG>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)L.total);
-  if (e != cudaSuccess) return e;
-  const long ctas = (long)a.B * a.H * (a.d_v / RG);
-  kern<<<(unsigned)ctas, RG * 4, L.total, s>>>(a, C);
-  return cudaGetLastError();
+struct Kernels {
+  static constexpr int kThreads = RG / (4 * kRowsPerThread) * 32;
+  static size_t smem(const FwdArgs& a, int C) { return FwdSmem(C, DK, a.d_v, RG, BF16 ? 2 : 4).total; }
+
+  static int ctas_per_sm(const FwdArgs& a, int C) {
+    auto kern = palimpsa_fwd_chunked_kernel<DK, BF16, RG, kRowsPerThread>;
+    const size_t sm = smem(a, C);
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm) != cudaSuccess) return 1;
+    int n = 1;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kern, kThreads, sm) != cudaSuccess || n < 1) n = 1;
+    return n;
+  }
+
+  static cudaError_t run(const FwdArgs& a, int C, int nseg, int seg_len, float* scratch, cudaStream_t s) {
+    const size_t sm = smem(a, C);
+    const long groups = a.d_v / RG;
+    const long heads = (long)a.B * a.H;
+    auto main_k = palimpsa_fwd_chunked_kernel<DK, BF16, RG, kRowsPerThread>;
+    cudaError_t e = cudaFuncSetAttribute(main_k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
+    if (e != cudaSuccess) return e;
+    float* seg_state = scratch;
+    if (nseg > 1) {
+      float* seg_gamma = scratch + (size_t)heads * (nseg - 1) * 2 * a.d_v * a.d_k;
+      auto sum_k = palimpsa_fwd_summary_kernel<DK, BF16, RG, kRowsPerThread>;
+      e = cudaFuncSetAttribute(sum_k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
+      if (e != cudaSuccess) return e;
+      sum_k<<<(unsigned)(heads * (nseg - 1) * groups), kThreads, sm, s>>>(a, C, nseg, seg_len, seg_state,
+                                                                          seg_gamma);
+      if ((e = cudaGetLastError()) != cudaSuccess) return e;
+      const long quads = heads * a.d_v * a.d_k / 4;
+      palimpsa_fwd_carry_kernel<<<(unsigned)((quads + 255) / 256), 256, 0, s>>>(a, nseg, seg_state, seg_gamma);
+      if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    }
+    main_k<<<(unsigned)(heads * nseg * groups), kThreads, sm, s>>>(a, C, nseg, seg_len, seg_state);
+    return cudaGetLastError();
+  }
+};
+
+struct Plan {
+  int RG, C, nseg, seg_len;
+};
+
+// Rows per CTA: 64 where d_v allows (the staging work per CTA is then shared
+// by the most rows), else the largest of {32, 16, 8} dividing d_v.
+int rows_per_cta(int d_v) {
+  for (int c : {64, 32, 16, 8})
+    if (d_v % c == 0) return c;
+  return 8;
+}
+
+// Segments: minimise the modelled time of pass A + pass C, where a pass takes
+// ceil(CTAs / resident CTA slots) waves of (segment length) token-steps and a
+// pass-A token-step costs a quarter of a pass-C one (2 FFMA against 6 FP32
+// operations plus the SFU reciprocal per element).
+void choose_segments(const FwdArgs& a, long units_per_seg, int slots, int C, Plan* p) {
+  const long T = a.T;
+  p->nseg = 1;
+  p->seg_len = a.T > 0 ? a.T : 1;
+  if (T <= 2L * C) return;
+  double best = 1e300;
+  const int max_seg = (int)std::min<long>(256, T / C);
+  for (int S = 1; S <= max_seg; ++S) {
+    const long len = (T + S - 1) / S;
+    const long len_c = (len + C - 1) / C * C;  // whole chunks per segment
+    const long nseg = (T + len_c - 1) / len_c;
+    if (nseg != S) continue;
+    const double wC = std::ceil((double)units_per_seg * nseg / slots);
+    const double wA = nseg > 1 ? std::ceil((double)units_per_seg * (nseg - 1) / slots) : 0.0;
+    const double cost = (wC + 0.25 * wA) * (double)len_c + (nseg > 1 ? 64.0 : 0.0);
+    if (cost < best * 0.98) {
+      best = cost;
+      p->nseg = (int)nseg;
+      p->seg_len = (int)len_c;
+    }
+  }
 }
 
 template <int DK, bool BF16>
-cudaError_t launch_rg(const FwdArgs& a, int RG, int C, cudaStream_t s) {
-  switch (RG) {
-    case 64: return launch_t<DK, BF16, 64>(a, C, s);
-    case 32: return launch_t<DK, BF16, 32>(a, C, s);
-    case 16: return launch_t<DK, BF16, 16>(a, C, s);
-    default: return launch_t<DK, BF16, 8>(a, C, s);
+cudaError_t plan_and_run(const FwdArgs& a, Plan p, cudaStream_t s, ScratchProvider* sp) {
+  int dev = 0, num_sms = 152;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&num_sms, cudaDevAttrMultiProcessorCount, dev);
+  int per_sm = 1;
+  switch (p.RG) {
+    case 64: per_sm = Kernels<DK, BF16, 64>::ctas_per_sm(a, p.C); break;
+    case 32: per_sm = Kernels<DK, BF16, 32>::ctas_per_sm(a, p.C); break;
+    case 16: per_sm = Kernels<DK, BF16, 16>::ctas_per_sm(a, p.C); break;
+    default: per_sm = Kernels<DK, BF16, 8>::ctas_per_sm(a, p.C); break;
   }
+  const long heads = (long)a.B * a.H;
+  const long units = heads * (a.d_v / p.RG);
+  if (a.force_segments > 0 && a.T > 0) {
+    const long len = ((long)a.T + a.force_segments - 1) / a.force_segments;
+    p.seg_len = (int)((len + p.C - 1) / p.C * p.C);
+    p.nseg = (int)(((long)a.T + p.seg_len - 1) / p.seg_len);
+  } else {
+    choose_segments(a, units, num_sms * per_sm, p.C, &p);
+  }
+  float* scratch = nullptr;
+  if (p.nseg > 1) {
+    const size_t bytes = (size_t)heads * (p.nseg - 1) * (2 * (size_t)a.d_v * a.d_k + 1) * sizeof(float);
+    cudaError_t e = sp->acquire(bytes, s, &scratch);
+    if (e != cudaSuccess) return e;
+  }
+  cudaError_t e;
+  switch (p.RG) {
+    case 64: e = Kernels<DK, BF16, 64>::run(a, p.C, p.nseg, p.seg_len, scratch, s); break;
+    case 32: e = Kernels<DK, BF16, 32>::run(a, p.C, p.nseg, p.seg_len, scratch, s); break;
+    case 16: e = Kernels<DK, BF16, 16>::run(a, p.C, p.nseg, p.seg_len, scratch, s); break;
+    default: e = Kernels<DK, BF16, 8>::run(a, p.C, p.nseg, p.seg_len, scratch, s); break;
+  }
+  if (scratch) {
+    const cudaError_t e2 = sp->release(scratch, s);
+    if (e == cudaSuccess) e = e2;
+  }
+  return e;
 }
 
 }  // namespace
 
-// Rows per CTA: the largest of {64, 32, 16, 8} that divides d_v while the grid
-// still fills every SM about twice; smaller groups trade duplicated staging
-// work for a better balance of CTAs over the 152 SMs.
-static int choose_rows_per_cta(const FwdArgs& a, int num_sms) {
-  const long heads = (long)a.B * a.H;
-  const int cands[4] = {64, 32, 16, 8};
-  for (int c : cands) {
-    if (a.d_v % c) continue;
-    if (heads * (a.d_v / c) >= 2L * num_sms || c == 8) return c;
-  }
-  return 8;
-}
-
-static size_t fwd_smem_bytes(int C, int DK, int DV, int RG, int es) {
-  return FwdSmem(C, DK, DV, RG, es).total;
-}
-
-cudaError_t launch_forward_chunked(const FwdArgs& a, cudaStream_t s) {
-  int dev = 0, num_sms = 152, max_smem = 227 * 1024;
+cudaError_t launch_forward_chunked(const FwdArgs& a, cudaStream_t s, ScratchProvider* sp) {
+  int dev = 0, max_smem = 227 * 1024;
   cudaGetDevice(&dev);
-  cudaDeviceGetAttribute(&num_sms, cudaDevAttrMultiProcessorCount, dev);
   cudaDeviceGetAttribute(&max_smem, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
-  int RG = choose_rows_per_cta(a, num_sms);
+  Plan p;
+  p.RG = rows_per_cta(a.d_v);
   const int es = a.bf16 ? 2 : 4;
-  int C = a.chunk;
-  while (C > 16 && fwd_smem_bytes(C, a.d_k, a.d_v, RG, es) > (size_t)max_smem) C /= 2;
-  while (RG > 8 && fwd_smem_bytes(C, a.d_k, a.d_v, RG, es) > (size_t)max_smem) RG /= 2;
-  if (fwd_smem_bytes(C, a.d_k, a.d_v, RG, es) > (size_t)max_smem) return cudaErrorInvalidConfiguration;
-  if (a.d_k == 128) return a.bf16 ? launch_rg<128, true>(a, RG, C, s) : launch_rg<128, false>(a, RG, C, s);
-  return a.bf16 ? launch_rg<64, true>(a, RG, C, s) : launch_rg<64, false>(a, RG, C, s);
+  // Chunk: at most 32 tokens (pass A computes a chunk's suffix products in one
+  // warp), shrunk until three CTAs' staging fits an SM.
+  p.C = std::min(a.chunk, 32);
+  while (p.C > 16 && FwdSmem(p.C, a.d_k, a.d_v, p.RG, es).total > (size_t)max_smem / 3) p.C /= 2;
+  if (FwdSmem(p.C, a.d_k, a.d_v, p.RG, es).total > (size_t)max_smem) return cudaErrorInvalidConfiguration;
+  p.nseg = 1;
+  p.seg_len = a.T;
+  if (a.d_k == 128) return a.bf16 ? plan_and_run<128, true>(a, p, s, sp) : plan_and_run<128, false>(a, p, s, sp);
+  return a.bf16 ? plan_and_run<64, true>(a, p, s, sp) : plan_and_run<64, false>(a, p, s, sp);
 }
 
 }  // namespace palimpsa

@@ -34,6 +34,7 @@ struct FwdArgs {
   unsigned int* status;
   unsigned long long wait_timeout_ns;
   int withhold_first_copy;
+  int force_segments;  // 0: the library chooses the time split
 };
 
 struct StepArgs {
@@ -52,9 +53,17 @@ struct StepArgs {
   unsigned int* status;
 };
 
+// Source of temporary device memory for a launch that needs scratch (the time
+// split of the forward). acquire/release are stream-ordered on `s`.
+struct ScratchProvider {
+  virtual cudaError_t acquire(size_t bytes, cudaStream_t s, float** p) = 0;
+  virtual cudaError_t release(float* p, cudaStream_t s) = 0;
+  virtual ~ScratchProvider() = default;
+};
+
 // Launchers (return the launch error, cudaSuccess on success). Arguments are
 // validated by the caller.
-cudaError_t launch_forward_chunked(const FwdArgs& a, cudaStream_t s);
+cudaError_t launch_forward_chunked(const FwdArgs& a, cudaStream_t s, ScratchProvider* sp);
 cudaError_t launch_step(const StepArgs& a, cudaStream_t s);
 
 // ------------------------------------------------------------------ device helpers

@@ -54,7 +54,12 @@ def test_tiny_workload_all_chunks_bitwise_equal():
     inp = syn.sequence_inputs(wl)
     ref = oracle_forward_from(inp)
     gi = _gpu(inp)
-    outs = [_fwd(gi, chunk=c) for c in (16, 32, 64)]
+    _check_all(_fwd(gi, chunk=wl.chunk), ref, tol_for(inp), TIGHT)   # automatic time split
+    pal.palimpsa_set_forward_segments(1)                               # one segment: chunk is staging only
+    try:
+        outs = [_fwd(gi, chunk=c) for c in (16, 32, 64)]
+    finally:
+        pal.palimpsa_set_forward_segments(0)
     _check_all(outs[0], ref, tol_for(inp), TIGHT)
     for o in outs[1:]:
         for a, b in zip(o, outs[0]):
@@ -263,3 +268,52 @@ def test_host_buffers_end_to_end():
                                              inp["I_prior"])
     assert y.device.type == "cpu"
     _check_all((y, mT, IT), oracle_forward_from(inp), tol_for(inp), TIGHT)
+
+
+# ----------------------------------------------------------------- time split (segments)
+
+SPLIT_CASES = [
+    # (B, H, T, d_k, d_v, bf16, segments)
+    (1, 2, 100, 128, 64, True, 2),
+    (2, 1, 333, 128, 64, True, 3),
+    (1, 3, 257, 64, 8, False, 7),
+    (1, 1, 1000, 128, 24, True, 16),
+    (2, 2, 64, 128, 128, False, 4),
+    (1, 2, 17, 128, 64, True, 5),      # more segments requested than whole chunks exist
+]
+
+
+@pytest.mark.parametrize("B,H,T,dk,dv,bf16,S", SPLIT_CASES)
+def test_time_split_matches_oracle(B, H, T, dk, dv, bf16, S):
+    """Segment summaries + carry + per-segment recurrence equal the sequential scan."""
+    wl = syn.WORKLOADS["small_layer"].with_(B=B, H=H, T=T, d_k=dk, d_v=dv, bf16=bf16)
+    inp = syn.sequence_inputs(wl, seed=3000 + T)
+    mu0, I0 = _random_state(B, H, dv, dk, 31)
+    ref = oracle_forward_from(inp, mu0=mu0, I0=I0)
+    gi = _gpu(inp)
+    pal.palimpsa_set_forward_segments(S)
+    try:
+        out = _fwd(gi, mu0.to(DEV), I0.to(DEV), chunk=16)
+    finally:
+        pal.palimpsa_set_forward_segments(0)
+    _check_all(out, ref, tol_for(inp), TIGHT)
+    unsplit = _fwd(gi, mu0.to(DEV), I0.to(DEV), chunk=16)
+    for a, b in zip(out, unsplit):
+        assert rel_l2(a.cpu(), b.cpu()) < 1e-6
+
+
+def test_time_split_with_default_state_and_in_place():
+    wl = syn.WORKLOADS["small_layer"].with_(B=1, H=2, T=300)
+    inp = syn.sequence_inputs(wl, seed=77)
+    gi = _gpu(inp)
+    ref = oracle_forward_from(inp)
+    pal.palimpsa_set_forward_segments(6)
+    try:
+        out = _fwd(gi, chunk=32)
+        _check_all(out, ref, tol_for(inp), TIGHT)
+        mu0, I0 = _random_state(1, 2, 64, 128, 78)
+        m, i = mu0.to(DEV), I0.to(DEV)
+        y, mT, IT = _fwd(gi, m, i, mu_T=m, I_T=i, chunk=32)
+        _check_all((y, mT, IT), oracle_forward_from(inp, mu0=mu0, I0=I0), tol_for(inp), TIGHT)
+    finally:
+        pal.palimpsa_set_forward_segments(0)
