@@ -70,7 +70,9 @@ typedef enum {
   PALIMPSA_ERR_DOMAIN = 5,      /* (device status) an input broke a precondition      */
   PALIMPSA_ERR_UNSUPPORTED = 6, /* d_k, d_v or chunk not supported by this build      */
   PALIMPSA_ERR_CUDA = 7,        /* a CUDA runtime call failed                         */
-  PALIMPSA_ERR_TIMEOUT = 8      /* (device status) a bounded device wait gave up      */
+  PALIMPSA_ERR_TIMEOUT = 8,     /* (device status) a bounded device wait gave up      */
+  PALIMPSA_ERR_SCRATCH_LIMIT = 9 /* palimpsa_forward_chunked_noalloc: its fixed scratch
+                                    buffer is too small for this call                 */
 } palimpsa_status;
 
 /*
@@ -104,6 +106,50 @@ typedef enum {
  *   chunk    0 (library default) or one of {16, 32, 64}.
  */
 palimpsa_status palimpsa_forward_chunked(
+    const void* q, const void* k, const void* v, const void* beta,
+    const float* d_t, const float* A, const float* I_prior,
+    const float* mu0, const float* I0,
+    float* y, float* mu_T, float* I_T,
+    int B, int H, int T, int d_k, int d_v, int chunk,
+    palimpsa_dtype in_dtype, void* cuda_stream);
+
+/*
+ * palimpsa_forward_chunked_noalloc — palimpsa_forward_chunked for callers that
+ * must not allocate device memory. (The paper has no counterpart: this is a
+ * deployment variant of the same computation.)
+ *
+ * Who needs it: code that runs where a CUDA allocation is not allowed or not
+ * safe — a serving process that reserves all device memory at start-up and
+ * forbids allocations while requests are in flight (an allocation there can
+ * fail with out-of-memory or stall behind a device-wide synchronisation), a
+ * plugin inside a host framework that owns the device heap and does not let
+ * guests call the CUDA allocator, or a latency-critical loop that cannot pay
+ * for an allocator call. palimpsa_forward_chunked takes its time-split
+ * scratch from the stream-ordered allocator; this entry point instead uses a
+ * fixed 16 MiB array compiled into the library (every GPU that loads the
+ * library holds it until the process exits). It calls no cudaMalloc,
+ * cudaFree or other allocating routine.
+ *
+ * Arguments, layouts, results and errors are those of
+ * palimpsa_forward_chunked, plus one error: when the launch plan needs more
+ * than 16 MiB of scratch it returns PALIMPSA_ERR_SCRATCH_LIMIT and launches
+ * nothing. The plan needs 4 * (2 * d_v * d_k + 1) bytes per head and segment
+ * boundary (about 64 KiB at d_v = 64, d_k = 128, so 255 head-boundaries fit);
+ * palimpsa_set_forward_segments(1) makes any call fit (one segment needs no
+ * scratch), smaller segment counts make larger calls fit.
+ *
+ * Sharing: all calls on a device use the same array, which keeps the last
+ * call's contents; nothing in it has to start at zero, because every scratch
+ * element a call reads was written earlier in that same call. Calls that
+ * overlap on the GPU (issued on different streams, or from several threads
+ * without ordering) race on the array and corrupt each other's results:
+ * order them on one stream.
+ *
+ * Set-up: the first call on each device looks up the array's device address
+ * (cudaGetSymbolAddress) with that device current; make that first call
+ * before any stream capture.
+ */
+palimpsa_status palimpsa_forward_chunked_noalloc(
     const void* q, const void* k, const void* v, const void* beta,
     const float* d_t, const float* A, const float* I_prior,
     const float* mu0, const float* I0,

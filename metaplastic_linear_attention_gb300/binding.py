@@ -25,7 +25,7 @@ PALIMPSA_BF16 = 1
 STATUS_NAMES = {
     0: "PALIMPSA_OK", 1: "PALIMPSA_ERR_NULL", 2: "PALIMPSA_ERR_SHAPE", 3: "PALIMPSA_ERR_ALIGN",
     4: "PALIMPSA_ERR_DTYPE", 5: "PALIMPSA_ERR_DOMAIN", 6: "PALIMPSA_ERR_UNSUPPORTED",
-    7: "PALIMPSA_ERR_CUDA", 8: "PALIMPSA_ERR_TIMEOUT",
+    7: "PALIMPSA_ERR_CUDA", 8: "PALIMPSA_ERR_TIMEOUT", 9: "PALIMPSA_ERR_SCRATCH_LIMIT",
 }
 
 _lib = None
@@ -59,6 +59,9 @@ def load_library(path: str | None = None):
         lib.palimpsa_forward_chunked.restype = i
         lib.palimpsa_forward_chunked.argtypes = [vp, vp, vp, vp, fp, fp, fp, fp, fp, fp, fp, fp,
                                                  i, i, i, i, i, i, i, vp]
+        lib.palimpsa_forward_chunked_noalloc.restype = i
+        lib.palimpsa_forward_chunked_noalloc.argtypes = [vp, vp, vp, vp, fp, fp, fp, fp, fp, fp, fp, fp,
+                                                         i, i, i, i, i, i, i, vp]
         lib.palimpsa_step.restype = i
         lib.palimpsa_step.argtypes = [vp, vp, vp, vp, fp, fp, fp, fp, fp, fp, i, i, i, i, i, vp]
         lib.palimpsa_status_string.restype = ctypes.c_char_p

@@ -134,6 +134,7 @@ const char* palimpsa_status_string(palimpsa_status s) {
     case PALIMPSA_ERR_UNSUPPORTED: return "d_k, d_v or chunk not supported";
     case PALIMPSA_ERR_CUDA: return "a CUDA runtime call failed";
     case PALIMPSA_ERR_TIMEOUT: return "a bounded device wait gave up";
+    case PALIMPSA_ERR_SCRATCH_LIMIT: return "the call needs more scratch than the fixed no-allocation buffer holds";
   }
   return "unknown status";
 }
@@ -162,3 +163,83 @@ void palimpsa_debug_withhold_first_copy(int on) { g_withhold_first_copy.store(on
 void palimpsa_set_forward_segments(int segments) { g_forward_segments.store(segments > 0 ? segments : 0); }
 
 }  // extern "C"
+
+// ---------------------------------------------------------------------------
+// palimpsa_forward_chunked_noalloc: the chunked forward for callers that must
+// not allocate device memory. Its time-split scratch lives in one fixed,
+// file-scope device array instead of coming from the stream-ordered
+// allocator.
+namespace palimpsa {
+namespace {
+
+constexpr size_t kNoAllocScratchBytes = 16u << 20;  // 16 MiB per device, held until the process exits
+
+// The shared scratch. Device code never names it directly: the host looks up
+// its device address (once per device) and passes that pointer to the kernels.
+static __device__ __align__(256) float g_noalloc_scratch[kNoAllocScratchBytes / sizeof(float)];
+
+std::mutex g_noalloc_mu;
+float* g_noalloc_ptr[kMaxDevices] = {};
+
+// Device address of the current device's scratch array. The first call on a
+// device does the lookup with that device current.
+palimpsa_status noalloc_scratch(float** out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return PALIMPSA_ERR_CUDA;
+  std::lock_guard<std::mutex> lock(g_noalloc_mu);
+  if (!g_noalloc_ptr[dev]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || !p) return PALIMPSA_ERR_CUDA;
+    g_noalloc_ptr[dev] = static_cast<float*>(p);
+  }
+  *out = g_noalloc_ptr[dev];
+  return PALIMPSA_OK;
+}
+
+// Hands out the fixed array; a request larger than the array is refused before
+// any kernel is launched. Nothing is allocated and nothing is freed.
+struct FixedScratch final : ScratchProvider {
+  float* base = nullptr;
+  bool too_large = false;
+  cudaError_t acquire(size_t bytes, cudaStream_t, float** p) override {
+    if (bytes > kNoAllocScratchBytes) {
+      too_large = true;
+      return cudaErrorMemoryAllocation;
+    }
+    *p = base;
+    return cudaSuccess;
+  }
+  cudaError_t release(float*, cudaStream_t) override { return cudaSuccess; }
+};
+
+}  // namespace
+}  // namespace palimpsa
+
+extern "C" palimpsa_status palimpsa_forward_chunked_noalloc(
+    const void* q, const void* k, const void* v, const void* beta, const float* d_t, const float* A,
+    const float* I_prior, const float* mu0, const float* I0, float* y, float* mu_T, float* I_T, int B, int H,
+    int T, int d_k, int d_v, int chunk, palimpsa_dtype in_dtype, void* cuda_stream) {
+  if (!A || !I_prior || !mu_T || !I_T) return PALIMPSA_ERR_NULL;
+  if (T != 0 && (!q || !k || !v || !beta || !d_t || !y)) return PALIMPSA_ERR_NULL;
+  if (in_dtype != PALIMPSA_F32 && in_dtype != PALIMPSA_BF16) return PALIMPSA_ERR_DTYPE;
+  if (!sizes_ok(B, H, T, d_k, d_v)) return PALIMPSA_ERR_SHAPE;
+  if (!supported_dims(d_k, d_v)) return PALIMPSA_ERR_UNSUPPORTED;
+  if (chunk != 0 && chunk != 16 && chunk != 32 && chunk != 64) return PALIMPSA_ERR_UNSUPPORTED;
+  const void* a16[] = {q, k, v, beta, y, mu_T, I_T, mu0, I0};
+  for (const void* p : a16)
+    if (p && !aligned(p, 16)) return PALIMPSA_ERR_ALIGN;
+  const void* a4[] = {d_t, A, I_prior};
+  for (const void* p : a4)
+    if (p && !aligned(p, 4)) return PALIMPSA_ERR_ALIGN;
+  unsigned int* st = nullptr;
+  if (palimpsa_status s = status_word(&st)) return s;
+  FixedScratch scratch;
+  if (palimpsa_status s = noalloc_scratch(&scratch.base)) return s;
+  FwdArgs a{q, k, v, beta, d_t, A, I_prior, mu0, I0, y, mu_T, I_T, B, H, T, d_k, d_v,
+            chunk == 0 ? 32 : chunk, in_dtype == PALIMPSA_BF16, st,
+            g_wait_timeout_ns.load(), g_withhold_first_copy.load(), g_forward_segments.load()};
+  const cudaError_t e = launch_forward_chunked(a, static_cast<cudaStream_t>(cuda_stream), &scratch);
+  if (scratch.too_large) return PALIMPSA_ERR_SCRATCH_LIMIT;
+  if (e != cudaSuccess) return PALIMPSA_ERR_CUDA;
+  return PALIMPSA_OK;
+}

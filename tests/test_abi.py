@@ -13,7 +13,8 @@ from metaplastic_linear_attention_gb300 import build_lib
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 HEADER = os.path.join(ROOT, "include", "palimpsa.h")
 
-OK, ERR_NULL, ERR_SHAPE, ERR_ALIGN, ERR_DTYPE, ERR_DOMAIN, ERR_UNSUPPORTED, ERR_CUDA, ERR_TIMEOUT = range(9)
+(OK, ERR_NULL, ERR_SHAPE, ERR_ALIGN, ERR_DTYPE, ERR_DOMAIN, ERR_UNSUPPORTED, ERR_CUDA, ERR_TIMEOUT,
+ ERR_SCRATCH_LIMIT) = range(10)
 
 
 @pytest.fixture(scope="module")
@@ -44,7 +45,7 @@ def test_library_exports_every_declared_symbol(lib):
 def test_abi_version_and_status_strings(lib):
     assert pal.palimpsa_abi_version() == 1
     seen = set()
-    for code in range(9):
+    for code in range(10):
         s = pal.palimpsa_status_string(code)
         assert s and s not in seen
         seen.add(s)
@@ -132,3 +133,18 @@ def test_product_path_does_not_import_the_oracle():
                 text = open(os.path.join(dirpath, f)).read()
                 assert "import oracle" not in text and "from oracle" not in text, f
                 assert "palimpsa_oracle" not in text, f
+
+
+@pytest.mark.parametrize("entry", ["palimpsa_forward_chunked", "palimpsa_forward_chunked_noalloc"])
+@pytest.mark.parametrize("over,code", [
+    (dict(q=None), ERR_NULL), (dict(I_T=None), ERR_NULL), (dict(dtype=3), ERR_DTYPE), (dict(H=0), ERR_SHAPE),
+    (dict(d_k=96), ERR_UNSUPPORTED), (dict(mu_T=P + 4), ERR_ALIGN),
+])
+def test_both_forward_entry_points_validate_alike(lib, entry, over, code):
+    args = dict(q=P, k=P, v=P, beta=P, d_t=P, A=P, I_prior=P, mu0=None, I0=None, y=P, mu_T=P, I_T=P,
+                B=1, H=2, T=16, d_k=128, d_v=64, chunk=0, dtype=1)
+    args.update(over)
+    fn = getattr(lib, entry)
+    assert fn(args["q"], args["k"], args["v"], args["beta"], args["d_t"], args["A"], args["I_prior"], args["mu0"],
+              args["I0"], args["y"], args["mu_T"], args["I_T"], args["B"], args["H"], args["T"], args["d_k"],
+              args["d_v"], args["chunk"], args["dtype"], None) == code
