@@ -86,9 +86,11 @@ typedef enum {
  * When B*H heads are too few to fill the GPU, the sequence is cut into
  * segments whose summaries are scanned first (the affine carry of slide 9);
  * that path takes temporary device memory (2 * d_v * d_k + 1 floats per head
- * and segment boundary) from the CUDA stream-ordered allocator on
- * `cuda_stream`. An allocation failure returns PALIMPSA_ERR_CUDA. Results
- * match the unsplit scan up to fp32 rounding.
+ * and segment boundary) in stream order on `cuda_stream`, from a memory pool
+ * the library creates per device and that keeps what it has reserved (at most
+ * the largest scratch one call needed) until the process exits. An allocation
+ * failure returns PALIMPSA_ERR_CUDA. Results match the unsplit scan up to
+ * fp32 rounding.
  *
  *   q, k     [B, H, T, d_k]  in_dtype
  *   v, beta  [B, H, T, d_v]  in_dtype, beta >= 0 (per value channel)

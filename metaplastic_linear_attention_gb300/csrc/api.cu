@@ -21,13 +21,46 @@ std::atomic<unsigned long long> g_wait_timeout_ns{2000000000ull};
 std::atomic<int> g_withhold_first_copy{0};
 std::atomic<int> g_forward_segments{0};
 
-// Scratch from the stream-ordered allocator: allocated and freed on the
-// launch stream, so it never synchronises and is reused from the device's
-// memory pool across calls.
+// The library's own stream-ordered memory pool on the current device, created
+// on first use. Its release threshold is unbounded, so memory freed by one
+// call stays mapped for the next instead of being returned to the driver at
+// every synchronisation (re-mapping fresh pages costs the time-split passes a
+// few percent); the pool holds at most the largest scratch any call needed.
+cudaError_t scratch_pool(cudaMemPool_t* out) {
+  static std::mutex mu;
+  static cudaMemPool_t pools[kMaxDevices] = {};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+  std::lock_guard<std::mutex> lock(mu);
+  if (!pools[dev]) {
+    cudaMemPoolProps props = {};
+    props.allocType = cudaMemAllocationTypePinned;
+    props.location.type = cudaMemLocationTypeDevice;
+    props.location.id = dev;
+    cudaMemPool_t pool = nullptr;
+    if ((e = cudaMemPoolCreate(&pool, &props)) != cudaSuccess) return e;
+    unsigned long long keep = ~0ull;
+    if ((e = cudaMemPoolSetAttribute(pool, cudaMemPoolAttrReleaseThreshold, &keep)) != cudaSuccess) {
+      cudaMemPoolDestroy(pool);
+      return e;
+    }
+    pools[dev] = pool;
+  }
+  *out = pools[dev];
+  return cudaSuccess;
+}
+
+// Scratch from that pool, allocated and freed in stream order on the launch
+// stream: no synchronisation, and reuse across calls.
 struct StreamOrderedScratch final : ScratchProvider {
   cudaError_t acquire(size_t bytes, cudaStream_t s, float** p) override {
+    cudaMemPool_t pool = nullptr;
+    cudaError_t e = scratch_pool(&pool);
+    if (e != cudaSuccess) return e;
     void* v = nullptr;
-    const cudaError_t e = cudaMallocAsync(&v, bytes, s);
+    e = cudaMallocFromPoolAsync(&v, bytes, pool, s);
     *p = static_cast<float*>(v);
     return e;
   }

@@ -622,15 +622,20 @@ int rows_per_cta(int d_v) {
   return 8;
 }
 
-// Segments: minimise the modelled time of pass A + pass C, where a pass takes
-// ceil(CTAs / resident CTA slots) waves of (segment length) token-steps and a
-// pass-A token-step costs a quarter of a pass-C one (2 FFMA against 6 FP32
-// operations plus the SFU reciprocal per element).
+// Segments: minimise a cost model of the whole forward, in units of one pass-C
+// token-step of one wave of resident CTAs. Constants were measured on GB300
+// (two 256-thread CTAs per SM): a pass-A token-step costs 0.46 of a pass-C one;
+// each wave of either pass pays ~3 units of fill and drain; the carry kernel
+// streams (read + write) 16 d_v d_k bytes per head and segment boundary at
+// ~6.3 TB/s (2.24e-7 units per byte); the two extra launches cost ~15 units.
+// A pass over U CTAs on `slots` resident CTA slots takes ceil(U / slots) waves.
 void choose_segments(const FwdArgs& a, long units_per_seg, int slots, int C, Plan* p) {
+  constexpr double kPassA = 0.46, kWave = 3.0, kCarryPerByte = 2.24e-7, kSplitFixed = 15.0;
   const long T = a.T;
   p->nseg = 1;
   p->seg_len = a.T > 0 ? a.T : 1;
   if (T <= 2L * C) return;
+  const double carry_bytes_per_boundary = 16.0 * a.d_v * a.d_k * ((double)a.B * a.H);
   double best = 1e300;
   const int max_seg = (int)std::min<long>(256, T / C);
   for (int S = 1; S <= max_seg; ++S) {
@@ -639,9 +644,13 @@ void choose_segments(const FwdArgs& a, long units_per_seg, int slots, int C, Pla
     const long nseg = (T + len_c - 1) / len_c;
     if (nseg != S) continue;
     const double wC = std::ceil((double)units_per_seg * nseg / slots);
-    const double wA = nseg > 1 ? std::ceil((double)units_per_seg * (nseg - 1) / slots) : 0.0;
-    const double cost = (wC + 0.25 * wA) * (double)len_c + (nseg > 1 ? 64.0 : 0.0);
-    if (cost < best * 0.98) {
+    double cost = wC * ((double)len_c + kWave);
+    if (nseg > 1) {
+      const double wA = std::ceil((double)units_per_seg * (nseg - 1) / slots);
+      cost += wA * (kPassA * (double)len_c + kWave) + kCarryPerByte * carry_bytes_per_boundary * (nseg - 1) +
+              kSplitFixed;
+    }
+    if (cost < best) {
       best = cost;
       p->nseg = (int)nseg;
       p->seg_len = (int)len_c;
