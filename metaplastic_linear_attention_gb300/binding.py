@@ -168,17 +168,7 @@ def palimpsa_forward_chunked(q, k, v, beta, d_t, A, I_prior, mu0=None, I0=None, 
     allocated when not given; mu_T / I_T may be mu0 / I0 (in place).
     """
     if q.device.type == "cpu":
-        # Host inputs: copy them in, compute on the device, and deliver each output
-        # where the caller's tensor lives (a host output is copied back; a CUDA
-        # output, e.g. a resident decode state, is written in place).
-        dev = _compute_device(y, mu_T, I_T, mu0, I0)
-        dq = _to_device([q, k, v, beta, d_t, A, I_prior, mu0, I0], dev)
-        dev_out = [o if (o is not None and o.is_cuda) else None for o in (y, mu_T, I_T)]
-        res = palimpsa_forward_chunked(*dq, y=dev_out[0], mu_T=dev_out[1], I_T=dev_out[2], chunk=chunk,
-                                       stream=stream)
-        outs = [_deliver(dst, src) for dst, src in zip((y, mu_T, I_T), res)]
-        (stream or torch.cuda.current_stream()).synchronize()
-        return tuple(outs)
+        return _forward_from_host(q, k, v, beta, d_t, A, I_prior, mu0, I0, y, mu_T, I_T, chunk, stream)
 
     B, H, T, d_k = q.shape
     d_v = v.shape[-1]
@@ -214,7 +204,14 @@ def palimpsa_forward_chunked(q, k, v, beta, d_t, A, I_prior, mu0=None, I0=None, 
 
 
 def palimpsa_step(q, k, v, beta, d_t, A, I_prior, mu, I, *, y=None, stream=None):
-    """One decode token (see palimpsa.h): updates mu, I in place and returns y [B,H,d_v]."""
+    """Decode tokens (see palimpsa.h): updates mu, I in place and returns y.
+
+    One token: q, k [B,H,d_k], v, beta [B,H,d_v], d_t [B,H] -> y [B,H,d_v].
+    A sequence of S tokens: a leading steps dimension on q, k, v, beta, d_t
+    -> y [S,B,H,d_v]; each token is one palimpsa_step call, in order.
+    """
+    if q.dim() == 4:
+        return _step_sequence(q, k, v, beta, d_t, A, I_prior, mu, I, y, stream)
     if q.device.type == "cpu":
         # Host inputs: the state stays where it is when it is on the device (the
         # resident decode state); host state is copied in and back.
@@ -253,4 +250,164 @@ def palimpsa_step(q, k, v, beta, d_t, A, I_prior, mu, I, *, y=None, stream=None)
                                ctypes.c_void_p(_stream_handle(stream)))
     if rc != 0:
         raise PalimpsaError(rc, "palimpsa_step")
+    return y
+
+
+# ---------------------------------------------------------------- host-buffer pipelines
+#
+# Callers with host (ideally pinned) buffers: the work is cut into blocks that
+# move through three CUDA streams - host-to-device copies, the library's
+# kernels on the caller's stream, device-to-host copies - two device buffers
+# deep, so the copies of one block overlap the computation of its neighbours.
+# Only copies and stream/event ordering happen here; all arithmetic runs in
+# the library's kernels. The call returns when every result is in place.
+
+HOST_BLOCK_BYTES = 256 << 20   # host input bytes per pipelined block
+
+
+def _blocks(n, per_item_bytes, target=None):
+    target = HOST_BLOCK_BYTES if target is None else target
+    size = max(1, min(n, target // max(1, per_item_bytes)))
+    return [(i, min(n, i + size)) for i in range(0, n, size)], size
+
+
+def _nbytes(t):
+    return 0 if t is None else t.numel() * t.element_size()
+
+
+class _Pipe:
+    def __init__(self, dev, stream):
+        self.dev = dev
+        self.comp = stream or torch.cuda.current_stream(dev)
+        self.h2d = torch.cuda.Stream(dev)
+        self.d2h = torch.cuda.Stream(dev)
+        self.in_free = [None, None]    # compute finished reading slot s
+        self.out_free = [None, None]   # device-to-host copy finished reading slot s
+
+    def load(self, slot, pairs):
+        """Copy (device_dst, host_src) pairs on the h2d stream into slot `slot`."""
+        if self.in_free[slot] is not None:
+            self.h2d.wait_event(self.in_free[slot])
+        with torch.cuda.stream(self.h2d):
+            for dst, src in pairs:
+                dst.copy_(src, non_blocking=True)
+        ev = torch.cuda.Event()
+        ev.record(self.h2d)
+        self.comp.wait_event(ev)
+        if self.out_free[slot] is not None:
+            self.comp.wait_event(self.out_free[slot])
+
+    def computed(self, slot):
+        ev = torch.cuda.Event()
+        ev.record(self.comp)
+        self.in_free[slot] = ev
+        return ev
+
+    def store(self, slot, after, pairs):
+        """Copy (host_dst, device_src) pairs on the d2h stream once `after` has fired."""
+        self.d2h.wait_event(after)
+        with torch.cuda.stream(self.d2h):
+            for dst, src in pairs:
+                dst.copy_(src, non_blocking=True)
+        ev = torch.cuda.Event()
+        ev.record(self.d2h)
+        self.out_free[slot] = ev
+
+    def finish(self):
+        self.d2h.synchronize()
+        self.h2d.synchronize()
+        self.comp.synchronize()
+
+
+def _host_out(t, shape, dtype):
+    return t if t is not None else torch.empty(shape, dtype=dtype, pin_memory=True)
+
+
+def _forward_from_host(q, k, v, beta, d_t, A, I_prior, mu0, I0, y, mu_T, I_T, chunk, stream):
+    """palimpsa_forward_chunked with host inputs: pipelined over batch blocks
+    (heads of different batch entries are independent)."""
+    dev = _compute_device(y, mu_T, I_T, mu0, I0)
+    B, H, T, d_k = q.shape
+    d_v = v.shape[-1]
+    f32 = torch.float32
+    per_b = sum(_nbytes(t) // max(1, B) for t in (q, k, v, beta, d_t, mu0, I0))
+    blocks, nb = _blocks(B, per_b)
+    outs = []
+    for t, shape in ((y, (B, H, T, d_v)), (mu_T, (B, H, d_v, d_k)), (I_T, (B, H, d_v, d_k))):
+        outs.append(t if (t is not None and t.is_cuda) else _host_out(t, shape, f32))
+    with torch.cuda.device(dev):
+        p = _Pipe(dev, stream)
+        with torch.cuda.stream(p.comp):
+            A_d = A.to(dev, non_blocking=True) if not A.is_cuda else A
+            Ip_d = I_prior.to(dev, non_blocking=True) if not I_prior.is_cuda else I_prior
+        ins = [q, k, v, beta, d_t, mu0, I0]
+        slots = [[None if t is None else torch.empty((nb,) + tuple(t.shape[1:]), dtype=t.dtype, device=dev)
+                  for t in ins] for _ in range(min(2, len(blocks)))]
+        oslots = [[None if o.is_cuda else torch.empty((nb,) + tuple(o.shape[1:]), dtype=f32, device=dev)
+                   for o in outs] for _ in range(min(2, len(blocks)))]
+        for i, (b0, b1) in enumerate(blocks):
+            s, n = i % 2, b1 - b0
+            src = [None if t is None else (t[b0:b1] if t.is_cuda else None) for t in ins]
+            pairs = []
+            dq = []
+            for j, t in enumerate(ins):
+                if t is None:
+                    dq.append(None)
+                elif t.is_cuda:
+                    dq.append(src[j])
+                else:
+                    dq.append(slots[s][j][:n])
+                    pairs.append((dq[-1], t[b0:b1]))
+            p.load(s, pairs)
+            od = [o[b0:b1] if o.is_cuda else oslots[s][j][:n] for j, o in enumerate(outs)]
+            palimpsa_forward_chunked(dq[0], dq[1], dq[2], dq[3], dq[4], A_d, Ip_d, dq[5], dq[6], y=od[0],
+                                     mu_T=od[1], I_T=od[2], chunk=chunk, stream=p.comp)
+            ev = p.computed(s)
+            p.store(s, ev, [(o[b0:b1], od[j]) for j, o in enumerate(outs) if not o.is_cuda])
+        p.finish()
+    return tuple(outs)
+
+
+def _step_sequence(q, k, v, beta, d_t, A, I_prior, mu, I, y, stream):
+    """S decode tokens in order; host inputs are pipelined over blocks of tokens
+    while the state stays resident on the device."""
+    S, B, H, d_k = q.shape
+    d_v = v.shape[-1]
+    f32 = torch.float32
+    if q.device.type != "cpu":
+        y = torch.empty((S, B, H, d_v), dtype=f32, device=q.device) if y is None else y
+        for t in range(S):
+            palimpsa_step(q[t], k[t], v[t], beta[t], d_t[t], A, I_prior, mu, I, y=y[t], stream=stream)
+        return y
+    dev = _compute_device(mu, I, y)
+    per_step = sum(_nbytes(t) // max(1, S) for t in (q, k, v, beta, d_t))
+    blocks, ns = _blocks(S, per_step)
+    y_dev_direct = y is not None and y.is_cuda
+    y = y if y is not None else torch.empty((S, B, H, d_v), dtype=f32, pin_memory=True)
+    with torch.cuda.device(dev):
+        p = _Pipe(dev, stream)
+        with torch.cuda.stream(p.comp):
+            A_d = A.to(dev, non_blocking=True) if not A.is_cuda else A
+            Ip_d = I_prior.to(dev, non_blocking=True) if not I_prior.is_cuda else I_prior
+            mu_d = mu if mu.is_cuda else mu.to(dev, non_blocking=True)
+            I_d = I if I.is_cuda else I.to(dev, non_blocking=True)
+        ins = [q, k, v, beta, d_t]
+        slots = [[torch.empty((ns,) + tuple(t.shape[1:]), dtype=t.dtype, device=dev) for t in ins]
+                 for _ in range(min(2, len(blocks)))]
+        yslots = [torch.empty((ns, B, H, d_v), dtype=f32, device=dev) for _ in range(min(2, len(blocks)))]
+        for i, (s0, s1) in enumerate(blocks):
+            s, n = i % 2, s1 - s0
+            p.load(s, [(slots[s][j][:n], t[s0:s1]) for j, t in enumerate(ins)])
+            yd = y[s0:s1] if y_dev_direct else yslots[s][:n]
+            for t in range(n):
+                palimpsa_step(slots[s][0][t], slots[s][1][t], slots[s][2][t], slots[s][3][t], slots[s][4][t],
+                              A_d, Ip_d, mu_d, I_d, y=yd[t], stream=p.comp)
+            ev = p.computed(s)
+            if not y_dev_direct:
+                p.store(s, ev, [(y[s0:s1], yd)])
+        if not mu.is_cuda:
+            with torch.cuda.stream(p.comp):
+                mu.copy_(mu_d, non_blocking=True)
+                I.copy_(I_d, non_blocking=True)
+        p.finish()
     return y

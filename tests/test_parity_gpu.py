@@ -317,3 +317,54 @@ def test_time_split_with_default_state_and_in_place():
         _check_all((y, mT, IT), oracle_forward_from(inp, mu0=mu0, I0=I0), tol_for(inp), TIGHT)
     finally:
         pal.palimpsa_set_forward_segments(0)
+
+
+# ----------------------------------------------------------------- host buffers, pipelined
+
+def test_host_forward_pipeline_matches_device_path(monkeypatch):
+    """Pinned host inputs streamed in several batch blocks give the device path's results."""
+    import metaplastic_linear_attention_gb300.binding as b
+    wl = syn.WORKLOADS["small_layer"].with_(B=5, H=3, T=96)
+    inp = syn.sequence_inputs(wl, seed=61)
+    g = torch.Generator().manual_seed(62)
+    mu0 = torch.randn((5, 3, 64, 128), generator=g)
+    I0 = 0.5 + torch.rand((5, 3, 64, 128), generator=g)
+    ref = _fwd(_gpu(inp), mu0.to(DEV), I0.to(DEV))
+    monkeypatch.setattr(b, "HOST_BLOCK_BYTES", 1)          # one batch entry per block: 5 blocks
+    host = {k: v.pin_memory() for k, v in inp.items()}
+    y, mT, IT = pal.palimpsa_forward_chunked(host["q"], host["k"], host["v"], host["beta"], host["d_t"], host["A"],
+                                             host["I_prior"], mu0.pin_memory(), I0.pin_memory())
+    assert y.device.type == "cpu" and mT.device.type == "cpu"
+    for a_, r_ in zip((y, mT, IT), ref):
+        assert rel_l2(a_, r_.cpu()) < 1e-6
+    # state outputs on the device, y to the host
+    m_d, i_d = torch.empty_like(mu0, device=DEV), torch.empty_like(I0, device=DEV)
+    y2, m2, i2 = pal.palimpsa_forward_chunked(host["q"], host["k"], host["v"], host["beta"], host["d_t"], host["A"],
+                                              host["I_prior"], y=torch.empty_like(y).pin_memory(), mu_T=m_d, I_T=i_d)
+    assert m2.data_ptr() == m_d.data_ptr() and y2.device.type == "cpu"
+    ref_default = _fwd(_gpu(inp))
+    assert rel_l2(y2, ref_default[0].cpu()) < 1e-6 and rel_l2(m2.cpu(), ref_default[1].cpu()) < 1e-6
+
+
+def test_step_sequence_host_pipeline_matches_token_by_token(monkeypatch):
+    import metaplastic_linear_attention_gb300.binding as b
+    wl = syn.WORKLOADS["decode"].with_(B=4, H=3)
+    seq = syn.sequence_inputs(wl, T=1, seed=71)
+    steps = syn.decode_inputs(wl, 11, seed=71)
+    mu0, I0 = _random_state(4, 3, 64, 128, 72)
+    A, Ip = seq["A"].to(DEV), seq["I_prior"].to(DEV)
+    mu, I = mu0.to(DEV), I0.to(DEV)
+    ys = [pal.palimpsa_step(*(steps[n][t].to(DEV) for n in ("q", "k", "v", "beta", "d_t")), A, Ip, mu, I).cpu()
+          for t in range(11)]
+    monkeypatch.setattr(b, "HOST_BLOCK_BYTES", 1)          # one token per block: 11 blocks
+    mu2, I2 = mu0.to(DEV), I0.to(DEV)
+    host = {k: v.pin_memory() for k, v in steps.items()}
+    y = pal.palimpsa_step(host["q"], host["k"], host["v"], host["beta"], host["d_t"], seq["A"], seq["I_prior"],
+                          mu2, I2)
+    assert y.shape == (11, 4, 3, 64) and y.device.type == "cpu"
+    assert torch.equal(y, torch.stack(ys))
+    assert torch.equal(mu2, mu) and torch.equal(I2, I)
+    # device-resident sequence
+    mu3, I3 = mu0.to(DEV), I0.to(DEV)
+    y3 = pal.palimpsa_step(*(steps[n].to(DEV) for n in ("q", "k", "v", "beta", "d_t")), A, Ip, mu3, I3)
+    assert torch.equal(y3.cpu(), y) and torch.equal(mu3, mu)
