@@ -289,6 +289,27 @@ def run_ours(args, ws, rank, local):
                     "unit": "G element-updates/s", "frac": a["frac"], "traffic": args.traffic,
                     "peak_source": f"{SM_COUNT_GB300} SMs x {MUFU_RCP_PER_CLK_PER_SM} rcp/clk x {sm_max:.0f} MHz"}
 
+    # The "without Meta" comparator (importance frozen at I_prior) on the same scan
+    # inputs, timed outside the timed region: what metaplasticity costs here.
+    def _nometa():
+        pal.palimpsa_forward_without_meta(inp["q"], inp["k"], inp["v"], inp["beta"], inp["d_t"], inp["A"],
+                                          inp["I_prior"], y=y_pre, mu_T=mu, chunk=wl.chunk)
+    for _ in range(2):
+        _nometa()
+    c0, c1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    reps = 5
+    c0.record(stream)
+    for _ in range(reps):
+        _nometa()
+    c1.record(stream)
+    torch.cuda.synchronize()
+    nometa_ms = c0.elapsed_time(c1) / reps
+    kernels["without_meta_comparator"] = {
+        "avg_ms": nometa_ms, "head_tokens_per_s": B * H * T / (nometa_ms / 1e3),
+        "palimpsa_forward_over_comparator": fwd_avg_ms / nometa_ms,
+        "note": "same scan inputs with the importance frozen at I_prior (Mamba2 / scalar-decay form), "
+                "no time split; timed after the timed region"}
+
     e2e = None
     if not args.no_e2e:
         e2e = run_e2e(args, wl, inp, dec, dev, pal, ws)

@@ -181,6 +181,28 @@ palimpsa_status palimpsa_step(
     int B, int H, int d_k, int d_v,
     palimpsa_dtype in_dtype, void* cuda_stream);
 
+/*
+ * palimpsa_forward_without_meta — the "without Meta" comparator: the same
+ * recurrence with the importance frozen at its prior (I_t = I_prior), i.e. the
+ * Mamba2 limit of Eq. (5) (slide 11; slide 10 names Mamba2 as Palimpsa-M's
+ * "without Meta" model):
+ *
+ *   mu_t = alpha_t mu_{t-1} + ((beta_t (.) v_t) / I_prior) (x) k_t,   y_t = mu_t q_t.
+ *
+ * It exists to measure what metaplasticity costs on this GPU (slide 22 compares
+ * Palimpsa's kernel with a Simple GLA kernel of this scalar-decay form).
+ * Arguments and conventions are those of palimpsa_forward_chunked without the
+ * precision state: mu0 [B,H,d_v,d_k] or NULL (= 0), y [B,H,T,d_v],
+ * mu_T [B,H,d_v,d_k] (may alias mu0). No time split: one CTA per (head, row
+ * group) runs the whole sequence.
+ */
+palimpsa_status palimpsa_forward_without_meta(
+    const void* q, const void* k, const void* v, const void* beta,
+    const float* d_t, const float* A, const float* I_prior,
+    const float* mu0, float* y, float* mu_T,
+    int B, int H, int T, int d_k, int d_v, int chunk,
+    palimpsa_dtype in_dtype, void* cuda_stream);
+
 /* Static English text for a status code (never NULL). */
 const char* palimpsa_status_string(palimpsa_status s);
 

@@ -19,6 +19,7 @@ from .binding import (  # noqa: F401
     palimpsa_abi_version,
     palimpsa_debug_withhold_first_copy,
     palimpsa_forward_chunked,
+    palimpsa_forward_without_meta,
     palimpsa_get_device_status,
     palimpsa_set_forward_segments,
     palimpsa_set_wait_timeout_ns,

@@ -62,6 +62,9 @@ def load_library(path: str | None = None):
         lib.palimpsa_forward_chunked_noalloc.restype = i
         lib.palimpsa_forward_chunked_noalloc.argtypes = [vp, vp, vp, vp, fp, fp, fp, fp, fp, fp, fp, fp,
                                                          i, i, i, i, i, i, i, vp]
+        lib.palimpsa_forward_without_meta.restype = i
+        lib.palimpsa_forward_without_meta.argtypes = [vp, vp, vp, vp, fp, fp, fp, fp, fp, fp,
+                                                      i, i, i, i, i, i, i, vp]
         lib.palimpsa_step.restype = i
         lib.palimpsa_step.argtypes = [vp, vp, vp, vp, fp, fp, fp, fp, fp, fp, i, i, i, i, i, vp]
         lib.palimpsa_status_string.restype = ctypes.c_char_p
@@ -201,6 +204,36 @@ def palimpsa_forward_chunked(q, k, v, beta, d_t, A, I_prior, mu0=None, I0=None, 
     if rc != 0:
         raise PalimpsaError(rc, "palimpsa_forward_chunked")
     return y, mu_T, I_T
+
+
+def palimpsa_forward_without_meta(q, k, v, beta, d_t, A, I_prior, mu0=None, *, y=None, mu_T=None, chunk: int = 0,
+                                  stream=None):
+    """The "without Meta" comparator (see palimpsa.h): importance frozen at I_prior.
+    Device tensors only. Returns (y, mu_T)."""
+    B, H, T, d_k = q.shape
+    d_v = v.shape[-1]
+    dev = q.device
+    f32 = torch.float32
+    _check(k, "k", q.shape, q.dtype, dev)
+    _check(v, "v", (B, H, T, d_v), q.dtype, dev)
+    _check(beta, "beta", (B, H, T, d_v), q.dtype, dev)
+    _check(q, "q", q.shape, None, dev)
+    _check(d_t, "d_t", (B, H, T), f32, dev)
+    _check(A, "A", (H,), f32, dev)
+    _check(I_prior, "I_prior", (H,), f32, dev)
+    _check(mu0, "mu0", (B, H, d_v, d_k), f32, dev)
+    y = torch.empty((B, H, T, d_v), dtype=f32, device=dev) if y is None else y
+    mu_T = torch.empty((B, H, d_v, d_k), dtype=f32, device=dev) if mu_T is None else mu_T
+    _check(y, "y", (B, H, T, d_v), f32, dev)
+    _check(mu_T, "mu_T", (B, H, d_v, d_k), f32, dev)
+    lib = load_library()
+    with torch.cuda.device(dev):
+        rc = lib.palimpsa_forward_without_meta(
+            _ptr(q), _ptr(k), _ptr(v), _ptr(beta), _ptr(d_t), _ptr(A), _ptr(I_prior), _ptr(mu0), _ptr(y),
+            _ptr(mu_T), B, H, T, d_k, d_v, int(chunk), _in_dtype(q), ctypes.c_void_p(_stream_handle(stream)))
+    if rc != 0:
+        raise PalimpsaError(rc, "palimpsa_forward_without_meta")
+    return y, mu_T
 
 
 def palimpsa_step(q, k, v, beta, d_t, A, I_prior, mu, I, *, y=None, stream=None):

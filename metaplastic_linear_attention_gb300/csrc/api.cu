@@ -135,6 +135,33 @@ palimpsa_status palimpsa_forward_chunked(const void* q, const void* k, const voi
   return PALIMPSA_OK;
 }
 
+palimpsa_status palimpsa_forward_without_meta(const void* q, const void* k, const void* v, const void* beta,
+                                              const float* d_t, const float* A, const float* I_prior,
+                                              const float* mu0, float* y, float* mu_T, int B, int H, int T,
+                                              int d_k, int d_v, int chunk, palimpsa_dtype in_dtype,
+                                              void* cuda_stream) {
+  if (!A || !I_prior || !mu_T) return PALIMPSA_ERR_NULL;
+  if (T != 0 && (!q || !k || !v || !beta || !d_t || !y)) return PALIMPSA_ERR_NULL;
+  if (in_dtype != PALIMPSA_F32 && in_dtype != PALIMPSA_BF16) return PALIMPSA_ERR_DTYPE;
+  if (!sizes_ok(B, H, T, d_k, d_v)) return PALIMPSA_ERR_SHAPE;
+  if (!supported_dims(d_k, d_v)) return PALIMPSA_ERR_UNSUPPORTED;
+  if (chunk != 0 && chunk != 16 && chunk != 32 && chunk != 64) return PALIMPSA_ERR_UNSUPPORTED;
+  const void* a16[] = {q, k, v, beta, y, mu_T, mu0};
+  for (const void* p : a16)
+    if (p && !aligned(p, 16)) return PALIMPSA_ERR_ALIGN;
+  const void* a4[] = {d_t, A, I_prior};
+  for (const void* p : a4)
+    if (p && !aligned(p, 4)) return PALIMPSA_ERR_ALIGN;
+  unsigned int* st = nullptr;
+  if (palimpsa_status s = status_word(&st)) return s;
+  FwdArgs a{q, k, v, beta, d_t, A, I_prior, mu0, nullptr, y, mu_T, nullptr, B, H, T, d_k, d_v,
+            chunk == 0 ? 32 : chunk, in_dtype == PALIMPSA_BF16, st,
+            g_wait_timeout_ns.load(), g_withhold_first_copy.load(), 1};
+  if (launch_forward_without_meta(a, static_cast<cudaStream_t>(cuda_stream)) != cudaSuccess)
+    return PALIMPSA_ERR_CUDA;
+  return PALIMPSA_OK;
+}
+
 palimpsa_status palimpsa_step(const void* q, const void* k, const void* v, const void* beta,
                               const float* d_t, const float* A, const float* I_prior, float* mu, float* I,
                               float* y, int B, int H, int d_k, int d_v, palimpsa_dtype in_dtype,

@@ -65,6 +65,9 @@ struct ScratchProvider {
 // validated by the caller.
 cudaError_t launch_forward_chunked(const FwdArgs& a, cudaStream_t s, ScratchProvider* sp);
 cudaError_t launch_step(const StepArgs& a, cudaStream_t s);
+// The "without Meta" comparator (importance frozen at I_prior); uses a.mu0,
+// a.y, a.mu_T and ignores a.I0, a.I_T.
+cudaError_t launch_forward_without_meta(const FwdArgs& a, cudaStream_t s);
 
 // ------------------------------------------------------------------ device helpers
 #if defined(__CUDACC__)

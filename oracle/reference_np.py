@@ -14,6 +14,9 @@ Attention-Based Models" — its slide deck and its Chinese reading notes.
   token's (M_t, Ibar_t) is written in closed form as a decayed sum over the
   chunk's writes (the "parallel scan within the chunk"), and the end state is
   carried to the next chunk in sequence.
+* ``forward_without_meta``: the same recurrence with the importance frozen at
+  I_prior (slide 10's "without Meta" ablation; slide 11's Mamba2 limit),
+  token by token.
 * ``forward_full_gaussian``: the coupled Gaussian posterior that Eq. (5)
   approximates (slide 25, App. A.3-A.5; reading notes section 2.5), with a full
   dk x dk precision matrix per value row. Used only on tiny inputs.
@@ -150,3 +153,21 @@ def forward_full_gaussian(q, k, v, beta, d_t, A, I_prior, P0=None, mu0=None):
                     P[b, h, i] = Pn
                 y[b, h, t] = mu[b, h] @ q[b, h, t]
     return y, mu, P
+
+
+def forward_without_meta(q, k, v, beta, d_t, A, I_prior, mu0=None):
+    """Importance frozen at the prior (slide 11): mu_t = alpha_t mu_{t-1}
+    + ((beta_t v_t) / I_prior) (x) k_t, y_t = mu_t q_t. I_prior is per head [H].
+    Returns (y, mu_T)."""
+    q, k, v, beta, d_t = (np.asarray(a, dtype=np.float64) for a in (q, k, v, beta, d_t))
+    B, H, T, dk = q.shape
+    dv = v.shape[-1]
+    Ip = np.asarray(I_prior, dtype=np.float64)[None, :, None, None]
+    mu = np.zeros((B, H, dv, dk)) if mu0 is None else np.array(mu0, dtype=np.float64)
+    A = np.asarray(A, dtype=np.float64)
+    y = np.zeros((B, H, T, dv))
+    for t in range(T):
+        alpha = np.exp(-A[None, :] * d_t[:, :, t])[:, :, None, None]
+        mu = alpha * mu + ((beta[:, :, t, :, None] * v[:, :, t, :, None]) / Ip) * k[:, :, t, None, :]
+        y[:, :, t, :] = np.einsum("bhij,bhj->bhi", mu, q[:, :, t, :])
+    return y, mu

@@ -297,3 +297,26 @@ def test_prior_scale_invariance():
     np.testing.assert_allclose(yc, y, rtol=1e-11, atol=1e-13)
     np.testing.assert_allclose(muc, muT, rtol=1e-11, atol=1e-13)
     np.testing.assert_allclose(Ic, c * IT, rtol=1e-12)
+
+
+def test_without_meta_matches_the_explicit_decayed_sum_and_the_limit():
+    """The frozen-importance oracle (slide 10 / slide 11) equals the separately written
+    scalar-decay sum, and Palimpsa's oracle approaches it in the Mamba2 limit."""
+    rng = _rng(23)
+    B, H, T, dk, dv = 1, 2, 30, 5, 3
+    q, k, v, beta, d_t, A, I_prior = _random_problem(rng, B, H, T, dk, dv)
+    y, muT = rnp.forward_without_meta(q, k, v, beta, d_t, A, I_prior)
+    y_sum = _scalar_decay_readout(q, k, beta * v, d_t, A, I_prior)
+    np.testing.assert_allclose(y, y_sum, rtol=1e-11, atol=1e-13)
+    eps = 1e-6
+    y_lim, _, _ = oracle.forward(q, k, beta * v / eps, np.full_like(beta, eps), d_t, A, I_prior)
+    assert np.linalg.norm(y_lim - y) / np.linalg.norm(y) < 1e-4
+    # continuation from a nonzero mean
+    mu0 = rng.standard_normal((B, H, dv, dk))
+    y1, m1 = rnp.forward_without_meta(q[:, :, :11], k[:, :, :11], v[:, :, :11], beta[:, :, :11], d_t[:, :, :11], A,
+                                      I_prior, mu0)
+    y2, m2 = rnp.forward_without_meta(q[:, :, 11:], k[:, :, 11:], v[:, :, 11:], beta[:, :, 11:], d_t[:, :, 11:], A,
+                                      I_prior, m1)
+    yf, mf = rnp.forward_without_meta(q, k, v, beta, d_t, A, I_prior, mu0)
+    np.testing.assert_allclose(np.concatenate([y1, y2], 2), yf, rtol=1e-12, atol=1e-14)
+    np.testing.assert_allclose(m2, mf, rtol=1e-12, atol=1e-14)

@@ -368,3 +368,40 @@ def test_step_sequence_host_pipeline_matches_token_by_token(monkeypatch):
     mu3, I3 = mu0.to(DEV), I0.to(DEV)
     y3 = pal.palimpsa_step(*(steps[n].to(DEV) for n in ("q", "k", "v", "beta", "d_t")), A, Ip, mu3, I3)
     assert torch.equal(y3.cpu(), y) and torch.equal(mu3, mu)
+
+
+# ----------------------------------------------------------------- "without Meta" comparator
+
+@pytest.mark.parametrize("B,H,T,dk,dv,bf16", [(1, 2, 1, 128, 64, True), (2, 3, 77, 128, 64, True),
+                                              (1, 2, 130, 64, 24, False), (3, 1, 200, 128, 128, False)])
+def test_without_meta_matches_oracle(B, H, T, dk, dv, bf16):
+    from oracle import reference_np as rnp
+    wl = syn.WORKLOADS["small_layer"].with_(B=B, H=H, T=T, d_k=dk, d_v=dv, bf16=bf16)
+    inp = syn.sequence_inputs(wl, seed=900 + T)
+    g = torch.Generator().manual_seed(901)
+    mu0 = torch.randn((B, H, dv, dk), generator=g)
+    f = syn.as_float64_numpy
+    ry, rmu = rnp.forward_without_meta(*(f(inp[n]) for n in ("q", "k", "v", "beta", "d_t", "A", "I_prior")),
+                                       mu0=f(mu0))
+    gi = _gpu(inp)
+    m = mu0.to(DEV)
+    y, mT = pal.palimpsa_forward_without_meta(gi["q"], gi["k"], gi["v"], gi["beta"], gi["d_t"], gi["A"],
+                                              gi["I_prior"], m, mu_T=m)       # in place
+    assert pal.palimpsa_get_device_status() == 0
+    assert rel_l2(y.cpu(), ry) <= TIGHT and rel_l2(mT.cpu(), rmu) <= TIGHT
+
+
+def test_without_meta_full_size_sampled_heads():
+    from oracle import reference_np as rnp
+    wl = syn.WORKLOADS["layer_760m"]
+    inp = syn.sequence_inputs(wl)
+    gi = _gpu(inp)
+    y, mT = pal.palimpsa_forward_without_meta(gi["q"], gi["k"], gi["v"], gi["beta"], gi["d_t"], gi["A"],
+                                              gi["I_prior"])
+    assert pal.palimpsa_get_device_status() == 0
+    heads = [(0, 0), (6, 19)]
+    bs, hs = [b for b, _ in heads], [h for _, h in heads]
+    f = syn.as_float64_numpy
+    sel = [f(inp[n])[bs, hs][None] for n in ("q", "k", "v", "beta", "d_t")]
+    ry, rmu = rnp.forward_without_meta(*sel, f(inp["A"])[hs], f(inp["I_prior"])[hs])
+    assert rel_l2(pick(y, heads), ry) <= TIGHT and rel_l2(pick(mT, heads), rmu) <= TIGHT
