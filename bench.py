@@ -310,6 +310,26 @@ def run_ours(args, ws, rank, local):
         "note": "same scan inputs with the importance frozen at I_prior (Mamba2 / scalar-decay form), "
                 "no time split; timed after the timed region"}
 
+    # The backward through the scan (gradients of <dy, y> for every input), timed
+    # outside the timed region on the same inputs.
+    if not S:
+        dy = torch.randn((B, H, T, dv), dtype=f32, device=dev)
+        def _bwd():
+            pal.palimpsa_backward(inp["q"], inp["k"], inp["v"], inp["beta"], inp["d_t"], inp["A"], inp["I_prior"],
+                                  None, None, dy, want_state_grads=False)
+        _bwd()
+        b0, b1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        b0.record(stream)
+        for _ in range(3):
+            _bwd()
+        b1.record(stream)
+        torch.cuda.synchronize()
+        bwd_ms = b0.elapsed_time(b1) / 3
+        kernels["palimpsa_backward"] = {"avg_ms": bwd_ms, "head_tokens_per_s": B * H * T / (bwd_ms / 1e3),
+                                        "over_forward": bwd_ms / fwd_avg_ms,
+                                        "note": "gradients of <dy, y> w.r.t. q, k, v, beta, d_t, A, I_prior; "
+                                                "timed after the timed region"}
+
     e2e = None
     if not args.no_e2e:
         e2e = run_e2e(args, wl, inp, dec, dev, pal, ws)

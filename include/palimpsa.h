@@ -203,6 +203,39 @@ palimpsa_status palimpsa_forward_without_meta(
     int B, int H, int T, int d_k, int d_v, int chunk,
     palimpsa_dtype in_dtype, void* cuda_stream);
 
+/*
+ * palimpsa_backward — gradients of a scalar loss L through
+ * palimpsa_forward_chunked (the same recurrence: slide 7 / Eq. (5), slide 4 /
+ * Eq. (2); the pages train the projections and gates that feed it by
+ * backpropagating through it, slide 4 and slide 9).
+ *
+ *   inputs   q, k, v, beta, d_t, A, I_prior, mu0, I0 exactly as given to the
+ *            forward (mu0 / I0 may be NULL for the defaults);
+ *            dy [B,H,T,d_v] fp32 = dL/dy; dmu_T, dI_T [B,H,d_v,d_k] fp32 =
+ *            dL/dmu_T, dL/dI_T, or NULL for zero.
+ *   outputs  (fp32, whatever in_dtype is) dq, dk [B,H,T,d_k]; dv, dbeta
+ *            [B,H,T,d_v]; dd_t [B,H,T]; dA, dI_prior [H] (summed over the
+ *            batch); dmu0, dI0 [B,H,d_v,d_k] or NULL when not wanted. When I0
+ *            is NULL the initial precision is I_prior itself and its gradient
+ *            is included in dI_prior.
+ *
+ * The forward states are recomputed, never stored by the forward: one sweep
+ * keeps a checkpoint every 64 tokens in stream-ordered scratch from the
+ * library's pool (B * H * ceil(T / 64) * 8 * d_v * d_k bytes). All states used
+ * come from forward-direction steps. dq, dk, dd_t, dA and dI_prior are
+ * accumulated with fp32 atomics (the library zeroes them first), so their last
+ * bits may differ between runs; everything else is deterministic.
+ */
+palimpsa_status palimpsa_backward(
+    const void* q, const void* k, const void* v, const void* beta,
+    const float* d_t, const float* A, const float* I_prior,
+    const float* mu0, const float* I0,
+    const float* dy, const float* dmu_T, const float* dI_T,
+    float* dq, float* dk, float* dv, float* dbeta, float* dd_t,
+    float* dA, float* dI_prior, float* dmu0, float* dI0,
+    int B, int H, int T, int d_k, int d_v,
+    palimpsa_dtype in_dtype, void* cuda_stream);
+
 /* Static English text for a status code (never NULL). */
 const char* palimpsa_status_string(palimpsa_status s);
 

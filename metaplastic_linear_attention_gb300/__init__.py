@@ -17,6 +17,7 @@ from .binding import (  # noqa: F401
     library_path,
     load_library,
     palimpsa_abi_version,
+    palimpsa_backward,
     palimpsa_debug_withhold_first_copy,
     palimpsa_forward_chunked,
     palimpsa_forward_without_meta,

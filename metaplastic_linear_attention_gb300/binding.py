@@ -65,6 +65,9 @@ def load_library(path: str | None = None):
         lib.palimpsa_forward_without_meta.restype = i
         lib.palimpsa_forward_without_meta.argtypes = [vp, vp, vp, vp, fp, fp, fp, fp, fp, fp,
                                                       i, i, i, i, i, i, i, vp]
+        lib.palimpsa_backward.restype = i
+        lib.palimpsa_backward.argtypes = [vp, vp, vp, vp, fp, fp, fp, fp, fp, fp, fp, fp, fp, fp, fp, fp, fp, fp,
+                                          fp, fp, fp, i, i, i, i, i, i, vp]
         lib.palimpsa_step.restype = i
         lib.palimpsa_step.argtypes = [vp, vp, vp, vp, fp, fp, fp, fp, fp, fp, i, i, i, i, i, vp]
         lib.palimpsa_status_string.restype = ctypes.c_char_p
@@ -234,6 +237,44 @@ def palimpsa_forward_without_meta(q, k, v, beta, d_t, A, I_prior, mu0=None, *, y
     if rc != 0:
         raise PalimpsaError(rc, "palimpsa_forward_without_meta")
     return y, mu_T
+
+
+def palimpsa_backward(q, k, v, beta, d_t, A, I_prior, mu0, I0, dy, dmu_T=None, dI_T=None, *, want_state_grads=True,
+                      stream=None):
+    """Gradients through palimpsa_forward_chunked (see palimpsa.h). Device tensors.
+
+    Returns a dict: dq, dk, dv, dbeta, dd_t, dA, dI_prior, and dmu0 / dI0 when
+    want_state_grads (fp32 throughout)."""
+    B, H, T, d_k = q.shape
+    d_v = v.shape[-1]
+    dev = q.device
+    f32 = torch.float32
+    _check(k, "k", q.shape, q.dtype, dev)
+    _check(v, "v", (B, H, T, d_v), q.dtype, dev)
+    _check(beta, "beta", (B, H, T, d_v), q.dtype, dev)
+    _check(q, "q", q.shape, None, dev)
+    _check(d_t, "d_t", (B, H, T), f32, dev)
+    _check(A, "A", (H,), f32, dev)
+    _check(I_prior, "I_prior", (H,), f32, dev)
+    for name, t in (("mu0", mu0), ("I0", I0), ("dmu_T", dmu_T), ("dI_T", dI_T)):
+        _check(t, name, (B, H, d_v, d_k), f32, dev)
+    _check(dy, "dy", (B, H, T, d_v), f32, dev)
+    e = lambda *shape: torch.empty(shape, dtype=f32, device=dev)
+    g = {"dq": e(B, H, T, d_k), "dk": e(B, H, T, d_k), "dv": e(B, H, T, d_v), "dbeta": e(B, H, T, d_v),
+         "dd_t": e(B, H, T), "dA": e(H), "dI_prior": e(H)}
+    if want_state_grads:
+        g["dmu0"] = e(B, H, d_v, d_k)
+        g["dI0"] = e(B, H, d_v, d_k)
+    lib = load_library()
+    with torch.cuda.device(dev):
+        rc = lib.palimpsa_backward(
+            _ptr(q), _ptr(k), _ptr(v), _ptr(beta), _ptr(d_t), _ptr(A), _ptr(I_prior), _ptr(mu0), _ptr(I0), _ptr(dy),
+            _ptr(dmu_T), _ptr(dI_T), _ptr(g["dq"]), _ptr(g["dk"]), _ptr(g["dv"]), _ptr(g["dbeta"]), _ptr(g["dd_t"]),
+            _ptr(g["dA"]), _ptr(g["dI_prior"]), _ptr(g.get("dmu0")), _ptr(g.get("dI0")), B, H, T, d_k, d_v,
+            _in_dtype(q), ctypes.c_void_p(_stream_handle(stream)))
+    if rc != 0:
+        raise PalimpsaError(rc, "palimpsa_backward")
+    return g
 
 
 def palimpsa_step(q, k, v, beta, d_t, A, I_prior, mu, I, *, y=None, stream=None):

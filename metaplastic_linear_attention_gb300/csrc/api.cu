@@ -162,6 +162,46 @@ palimpsa_status palimpsa_forward_without_meta(const void* q, const void* k, cons
   return PALIMPSA_OK;
 }
 
+palimpsa_status palimpsa_backward(const void* q, const void* k, const void* v, const void* beta, const float* d_t,
+                                  const float* A, const float* I_prior, const float* mu0, const float* I0,
+                                  const float* dy, const float* dmu_T, const float* dI_T, float* dq, float* dk,
+                                  float* dv, float* dbeta, float* dd_t, float* dA, float* dI_prior, float* dmu0,
+                                  float* dI0, int B, int H, int T, int d_k, int d_v, palimpsa_dtype in_dtype,
+                                  void* cuda_stream) {
+  if (!A || !I_prior || !dA || !dI_prior) return PALIMPSA_ERR_NULL;
+  if (T != 0 && (!q || !k || !v || !beta || !d_t || !dy || !dq || !dk || !dv || !dbeta || !dd_t))
+    return PALIMPSA_ERR_NULL;
+  if (in_dtype != PALIMPSA_F32 && in_dtype != PALIMPSA_BF16) return PALIMPSA_ERR_DTYPE;
+  if (!sizes_ok(B, H, T, d_k, d_v)) return PALIMPSA_ERR_SHAPE;
+  if (!supported_dims(d_k, d_v)) return PALIMPSA_ERR_UNSUPPORTED;
+  const void* a16[] = {q, k, v, beta, mu0, I0, dy, dmu_T, dI_T, dq, dk, dv, dbeta, dmu0, dI0};
+  for (const void* p : a16)
+    if (p && !aligned(p, 16)) return PALIMPSA_ERR_ALIGN;
+  const void* a4[] = {d_t, A, I_prior, dd_t, dA, dI_prior};
+  for (const void* p : a4)
+    if (p && !aligned(p, 4)) return PALIMPSA_ERR_ALIGN;
+  cudaStream_t s = static_cast<cudaStream_t>(cuda_stream);
+  BwdArgs a{q, k, v, beta, d_t, A, I_prior, mu0, I0, dy, dmu_T, dI_T, dq, dk, dv, dbeta, dd_t, dA, dI_prior,
+            dmu0, dI0, B, H, T, d_k, d_v, in_dtype == PALIMPSA_BF16};
+  const size_t tok = (size_t)B * H * T;
+  // outputs that the kernel accumulates into start at zero
+  if (T != 0 && (cudaMemsetAsync(dq, 0, tok * d_k * sizeof(float), s) != cudaSuccess ||
+                 cudaMemsetAsync(dk, 0, tok * d_k * sizeof(float), s) != cudaSuccess ||
+                 cudaMemsetAsync(dd_t, 0, tok * sizeof(float), s) != cudaSuccess))
+    return PALIMPSA_ERR_CUDA;
+  if (cudaMemsetAsync(dA, 0, (size_t)H * sizeof(float), s) != cudaSuccess ||
+      cudaMemsetAsync(dI_prior, 0, (size_t)H * sizeof(float), s) != cudaSuccess)
+    return PALIMPSA_ERR_CUDA;
+  StreamOrderedScratch scratch;
+  float* ck = nullptr;
+  const size_t bytes = backward_scratch_bytes(a);
+  if (bytes && scratch.acquire(bytes, s, &ck) != cudaSuccess) return PALIMPSA_ERR_CUDA;
+  const cudaError_t e = launch_backward(a, ck, s);
+  const cudaError_t e2 = ck ? scratch.release(ck, s) : cudaSuccess;
+  if (e != cudaSuccess || e2 != cudaSuccess) return PALIMPSA_ERR_CUDA;
+  return PALIMPSA_OK;
+}
+
 palimpsa_status palimpsa_step(const void* q, const void* k, const void* v, const void* beta,
                               const float* d_t, const float* A, const float* I_prior, float* mu, float* I,
                               float* y, int B, int H, int d_k, int d_v, palimpsa_dtype in_dtype,

@@ -53,6 +53,32 @@ struct StepArgs {
   unsigned int* status;
 };
 
+struct BwdArgs {
+  const void* q;
+  const void* k;
+  const void* v;
+  const void* beta;
+  const float* d_t;
+  const float* A;
+  const float* I_prior;
+  const float* mu0;    // may be null
+  const float* I0;     // may be null
+  const float* dy;
+  const float* dmu_T;  // may be null
+  const float* dI_T;   // may be null
+  float* dq;           // zeroed by the caller of the launcher (accumulated)
+  float* dk;           // zeroed (accumulated)
+  float* dv;
+  float* dbeta;
+  float* dd_t;         // zeroed (accumulated)
+  float* dA;           // zeroed (accumulated)
+  float* dI_prior;     // zeroed (accumulated)
+  float* dmu0;         // may be null
+  float* dI0;          // may be null
+  int B, H, T, d_k, d_v;
+  bool bf16;
+};
+
 // Source of temporary device memory for a launch that needs scratch (the time
 // split of the forward). acquire/release are stream-ordered on `s`.
 struct ScratchProvider {
@@ -68,6 +94,9 @@ cudaError_t launch_step(const StepArgs& a, cudaStream_t s);
 // The "without Meta" comparator (importance frozen at I_prior); uses a.mu0,
 // a.y, a.mu_T and ignores a.I0, a.I_T.
 cudaError_t launch_forward_without_meta(const FwdArgs& a, cudaStream_t s);
+// Backward: scratch of backward_scratch_bytes(a) bytes holds the checkpoints.
+size_t backward_scratch_bytes(const BwdArgs& a);
+cudaError_t launch_backward(const BwdArgs& a, float* scratch, cudaStream_t s);
 
 // ------------------------------------------------------------------ device helpers
 #if defined(__CUDACC__)

@@ -320,3 +320,54 @@ def test_without_meta_matches_the_explicit_decayed_sum_and_the_limit():
     yf, mf = rnp.forward_without_meta(q, k, v, beta, d_t, A, I_prior, mu0)
     np.testing.assert_allclose(np.concatenate([y1, y2], 2), yf, rtol=1e-12, atol=1e-14)
     np.testing.assert_allclose(m2, mf, rtol=1e-12, atol=1e-14)
+
+
+def test_autograd_oracle_forward_equals_the_c_oracle():
+    from oracle import autograd as ag
+    import torch
+    rng = _rng(81)
+    q, k, v, beta, d_t, A, I_prior = _random_problem(rng, 2, 2, 20, 5, 3)
+    mu0 = rng.standard_normal((2, 2, 3, 5))
+    I0 = rng.uniform(0.5, 3.0, (2, 2, 3, 5))
+    y, muT, IT = oracle.forward(q, k, v, beta, d_t, A, I_prior, mu0=mu0, I0=I0)
+    tt = [torch.tensor(x) for x in (q, k, v, beta, d_t, A, I_prior, mu0, I0)]
+    y2, mu2, I2 = ag.forward_torch(*tt)
+    np.testing.assert_allclose(y2.numpy(), y, rtol=1e-12, atol=1e-14)
+    np.testing.assert_allclose(mu2.numpy(), muT, rtol=1e-12, atol=1e-14)
+    np.testing.assert_allclose(I2.numpy(), IT, rtol=1e-13)
+
+
+@pytest.mark.parametrize("with_state", [False, True])
+def test_autograd_gradients_equal_finite_differences_of_the_c_oracle(with_state):
+    """The gradient oracle is pinned to central differences of a different
+    implementation (the C oracle), on a tiny problem, for every input."""
+    from oracle import autograd as ag
+    rng = _rng(82 + with_state)
+    B, H, T, dk, dv = 1, 2, 6, 3, 2
+    q, k, v, beta, d_t, A, I_prior = _random_problem(rng, B, H, T, dk, dv, unit_keys=False)
+    inp = dict(q=q, k=k, v=v, beta=beta, d_t=d_t, A=A, I_prior=I_prior, mu0=None, I0=None)
+    if with_state:
+        inp["mu0"] = rng.standard_normal((B, H, dv, dk))
+        inp["I0"] = rng.uniform(0.5, 2.0, (B, H, dv, dk))
+    dy = rng.standard_normal((B, H, T, dv))
+    dmu = rng.standard_normal((B, H, dv, dk))
+    dI = rng.standard_normal((B, H, dv, dk))
+    g = ag.gradients(inp, dy, dmu, dI)
+
+    def loss(d):
+        y, muT, IT = oracle.forward(d["q"], d["k"], d["v"], d["beta"], d["d_t"], d["A"], d["I_prior"],
+                                    mu0=d["mu0"], I0=d["I0"])
+        return float(np.sum(y * dy) + np.sum(muT * dmu) + np.sum(IT * dI))
+
+    h = 1e-6
+    for name, arr in inp.items():
+        if arr is None:
+            continue
+        fd = np.zeros(arr.shape)
+        for idx in np.ndindex(arr.shape):
+            dp = {n: (None if a_ is None else np.array(a_, dtype=np.float64)) for n, a_ in inp.items()}
+            dm = {n: (None if a_ is None else np.array(a_, dtype=np.float64)) for n, a_ in inp.items()}
+            dp[name][idx] += h
+            dm[name][idx] -= h
+            fd[idx] = (loss(dp) - loss(dm)) / (2 * h)
+        np.testing.assert_allclose(g[name], fd, rtol=2e-6, atol=2e-7, err_msg=name)

@@ -405,3 +405,55 @@ def test_without_meta_full_size_sampled_heads():
     sel = [f(inp[n])[bs, hs][None] for n in ("q", "k", "v", "beta", "d_t")]
     ry, rmu = rnp.forward_without_meta(*sel, f(inp["A"])[hs], f(inp["I_prior"])[hs])
     assert rel_l2(pick(y, heads), ry) <= TIGHT and rel_l2(pick(mT, heads), rmu) <= TIGHT
+
+
+# ----------------------------------------------------------------- backward
+
+BWD_CASES = [
+    # (B, H, T, d_k, d_v, bf16, with_state, with_final_grads)
+    (1, 2, 100, 128, 64, False, True, True),
+    (2, 1, 70, 128, 64, True, False, False),
+    (1, 2, 9, 64, 8, False, True, False),
+    (1, 1, 1, 128, 16, True, False, True),
+    (1, 1, 200, 128, 64, True, True, True),
+]
+
+
+def _bwd_case(B, H, T, dk, dv, bf16, with_state, with_final, seed):
+    from oracle import autograd as ag
+    wl = syn.WORKLOADS["small_layer"].with_(B=B, H=H, T=T, d_k=dk, d_v=dv, bf16=bf16)
+    inp = syn.sequence_inputs(wl, seed=seed)
+    g = torch.Generator().manual_seed(seed + 1)
+    mu0 = torch.randn((B, H, dv, dk), generator=g) if with_state else None
+    I0 = (0.5 + 2.0 * torch.rand((B, H, dv, dk), generator=g)) if with_state else None
+    dy = torch.randn((B, H, T, dv), generator=g)
+    dmu = torch.randn((B, H, dv, dk), generator=g) if with_final else None
+    dI = torch.randn((B, H, dv, dk), generator=g) if with_final else None
+    f = syn.as_float64_numpy
+    ref = ag.gradients({n: (None if t is None else f(t)) for n, t in
+                        dict(q=inp["q"], k=inp["k"], v=inp["v"], beta=inp["beta"], d_t=inp["d_t"], A=inp["A"],
+                             I_prior=inp["I_prior"], mu0=mu0, I0=I0).items()},
+                       f(dy), None if dmu is None else f(dmu), None if dI is None else f(dI))
+    d = lambda t: None if t is None else t.to(DEV)
+    gi = _gpu(inp)
+    out = pal.palimpsa_backward(gi["q"], gi["k"], gi["v"], gi["beta"], gi["d_t"], gi["A"], gi["I_prior"], d(mu0),
+                                d(I0), d(dy), d(dmu), d(dI))
+    assert pal.palimpsa_get_device_status() == 0
+    return out, ref, with_state
+
+
+@pytest.mark.parametrize("B,H,T,dk,dv,bf16,with_state,with_final", BWD_CASES)
+def test_backward_matches_fp64_autograd(B, H, T, dk, dv, bf16, with_state, with_final):
+    out, ref, with_state = _bwd_case(B, H, T, dk, dv, bf16, with_state, with_final, seed=4000 + T)
+    pairs = [("dq", "q"), ("dk", "k"), ("dv", "v"), ("dbeta", "beta"), ("dd_t", "d_t"), ("dA", "A"),
+             ("dI_prior", "I_prior")]
+    if with_state:
+        pairs += [("dmu0", "mu0"), ("dI0", "I0")]
+    errs = {n: rel_l2(out[n].cpu(), ref[m]) for n, m in pairs}
+    assert max(errs.values()) <= TIGHT, errs
+
+
+def test_backward_empty_sequence():
+    out, ref, _ = _bwd_case(1, 2, 0, 128, 64, False, True, True, seed=4500)
+    assert rel_l2(out["dmu0"].cpu(), ref["mu0"]) <= 1e-6 and rel_l2(out["dI0"].cpu(), ref["I0"]) <= 1e-6
+    assert rel_l2(out["dI_prior"].cpu(), ref["I_prior"]) <= 1e-6 or float(abs(out["dI_prior"]).max()) == 0.0
