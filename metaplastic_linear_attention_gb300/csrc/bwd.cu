@@ -74,17 +74,31 @@ struct TokRow {
   float alpha, om, b, v, bv;
 };
 
+// alpha_t and (1 - alpha_t) I_prior come from the segment's table in shared
+// memory (index t - ts), computed once per CTA.
 template <bool BF16>
-__device__ __forceinline__ TokRow tok_row(const BwdArgs& a, size_t head_tok, int t, size_t row_idx, float A_h,
-                                          float Ip) {
+__device__ __forceinline__ TokRow tok_row(const BwdArgs& a, size_t head_tok, int t, size_t row_idx,
+                                          const float* seg_al, const float* seg_om, int ts) {
   TokRow r;
-  const float x = -A_h * a.d_t[head_tok + t];
-  r.alpha = expf(x);
-  r.om = -expm1f(x) * Ip;
+  r.alpha = seg_al[t - ts];
+  r.om = seg_om[t - ts];
   r.b = load1<BF16>(a.beta, (head_tok + t) * a.d_v + row_idx);
   r.v = load1<BF16>(a.v, (head_tok + t) * a.d_v + row_idx);
   r.bv = r.b * r.v;
   return r;
+}
+
+// All threads: the gate of tokens [ts, te) into the segment tables; ends with a
+// CTA barrier (callers must reach it together).
+__device__ __forceinline__ void fill_gates(const float* d_t, size_t head_tok, int ts, int te, float A_h, float Ip,
+                                           float* seg_al, float* seg_om) {
+  __syncthreads();  // previous users of the tables are done
+  for (int u = threadIdx.x; u < te - ts; u += blockDim.x) {
+    const float x = -A_h * d_t[head_tok + ts + u];
+    seg_al[u] = expf(x);
+    seg_om[u] = -expm1f(x) * Ip;  // (1 - alpha) I_prior without cancellation
+  }
+  __syncthreads();
 }
 
 // One forward step of a lane's NC state elements (the forward kernel's update).
@@ -109,6 +123,8 @@ palimpsa_bwd_kernel(BwdArgs a, float* __restrict__ ckpt) {
   auto win_I = reinterpret_cast<float (*)[NW][DK]>(bsm + kRowsPerCta * NW * DK);
   auto red = reinterpret_cast<float (*)[2][kRowsPerCta][DK]>(bsm + 2 * kRowsPerCta * NW * DK);
   auto red_a = reinterpret_cast<float (*)[kRowsPerCta]>(bsm + 2 * kRowsPerCta * NW * DK + 4 * kRowsPerCta * DK);
+  float* seg_al = bsm + 2 * kRowsPerCta * NW * DK + 4 * kRowsPerCta * DK + 2 * kRowsPerCta;
+  float* seg_om = seg_al + kSeg;
 
   const int DV = a.d_v, T = a.T;
   const int groups = DV / kRowsPerCta;
@@ -140,10 +156,11 @@ palimpsa_bwd_kernel(BwdArgs a, float* __restrict__ ckpt) {
 #pragma unroll
     for (int e = 0; e < NC; ++e) { cp[c0 + e] = M[e]; cp[DK + c0 + e] = I[e]; }
     const int t_end = min(T, (s + 1) * kSeg);
+    fill_gates(a.d_t, head_tok, s * kSeg, t_end, A_h, Ip, seg_al, seg_om);
     for (int t = s * kSeg; t < t_end; ++t) {
       float k[NC];
       load_cols<BF16, NC>(a.k, (head_tok + t) * DK + c0, k);
-      fwd_step<NC>(M, I, k, tok_row<BF16>(a, head_tok, t, i, A_h, Ip));
+      fwd_step<NC>(M, I, k, tok_row<BF16>(a, head_tok, t, i, seg_al, seg_om, s * kSeg));
     }
   }
 
@@ -163,6 +180,7 @@ palimpsa_bwd_kernel(BwdArgs a, float* __restrict__ ckpt) {
   // ---- phase 2: segments in reverse
   for (int s = nseg - 1; s >= 0; --s) {
     const int ts = s * kSeg, te = min(T, ts + kSeg);
+    fill_gates(a.d_t, head_tok, ts, te, A_h, Ip, seg_al, seg_om);
     const float* cp = my_ckpt + ((size_t)s * kRowsPerCta + w) * DK * 2;
 #pragma unroll
     for (int e = 0; e < NC; ++e) { M[e] = cp[c0 + e]; I[e] = cp[DK + c0 + e]; }
@@ -175,7 +193,7 @@ palimpsa_bwd_kernel(BwdArgs a, float* __restrict__ ckpt) {
       }
       float k[NC];
       load_cols<BF16, NC>(a.k, (head_tok + t) * DK + c0, k);
-      fwd_step<NC>(M, I, k, tok_row<BF16>(a, head_tok, t, i, A_h, Ip));
+      fwd_step<NC>(M, I, k, tok_row<BF16>(a, head_tok, t, i, seg_al, seg_om, ts));
     }
     __syncwarp();
     const int nwin = (te - ts + kWin - 1) / kWin;
@@ -190,7 +208,7 @@ palimpsa_bwd_kernel(BwdArgs a, float* __restrict__ ckpt) {
         if (u < n) {
           float k[NC];
           load_cols<BF16, NC>(a.k, (head_tok + tw + u) * DK + c0, k);
-          const TokRow tr = tok_row<BF16>(a, head_tok, tw + u, i, A_h, Ip);
+          const TokRow tr = tok_row<BF16>(a, head_tok, tw + u, i, seg_al, seg_om, ts);
 #pragma unroll
           for (int e = 0; e < NC; ++e) {
             Is[u + 1][e] = fmaf(tr.alpha, Is[u][e], fmaf(tr.b, k[e] * k[e], tr.om));
@@ -206,13 +224,14 @@ palimpsa_bwd_kernel(BwdArgs a, float* __restrict__ ckpt) {
           float k[NC], q[NC];
           load_cols<BF16, NC>(a.k, (head_tok + t) * DK + c0, k);
           load_cols<BF16, NC>(a.q, (head_tok + t) * DK + c0, q);
-          const TokRow tr = tok_row<BF16>(a, head_tok, t, i, A_h, Ip);
+          const TokRow tr = tok_row<BF16>(a, head_tok, t, i, seg_al, seg_om, ts);
           const float dyi = a.dy[(head_tok + t) * DV + i];
           float s_bv = 0.f, s_b = 0.f, s_al = 0.f, s_gi = 0.f;
+          const float om_w = tr.om / Ip;  // 1 - alpha_t
           float dq_p[NC], dk_p[NC];
 #pragma unroll
           for (int e = 0; e < NC; ++e) {
-            const float r = 1.f / Is[u + 1][e];
+            const float r = rcp_approx(Is[u + 1][e]);
             const float mu = Ms[u + 1][e] * r;
             const float dmu = dyi * q[e];
             gM[e] = fmaf(dmu, r, gM[e]);
@@ -227,13 +246,12 @@ palimpsa_bwd_kernel(BwdArgs a, float* __restrict__ ckpt) {
           s_bv = warp_sum(s_bv);
           s_b = warp_sum(s_b);
           s_al = warp_sum(s_al);
-          s_gi = warp_sum(s_gi);
+          dIp_acc = fmaf(om_w, s_gi, dIp_acc);  // per lane; reduced over the warp at the end
           if (lane == 0) {
             const size_t o = (head_tok + t) * DV + i;
             a.dv[o] = s_bv * tr.b;
             a.dbeta[o] = fmaf(s_bv, tr.v, s_b);
             red_a[par][w] = s_al;
-            dIp_acc = fmaf(-expm1f(-A_h * a.d_t[head_tok + t]), s_gi, dIp_acc);
           }
 #pragma unroll
           for (int e = 0; e < NC; ++e) { red[par][0][w][c0 + e] = dq_p[e]; red[par][1][w][c0 + e] = dk_p[e]; }
@@ -273,10 +291,8 @@ palimpsa_bwd_kernel(BwdArgs a, float* __restrict__ ckpt) {
     s_ip0 += dI0;
   }
   // With I0 absent the initial precision is I_prior itself.
-  if (!a.I0) {
-    s_ip0 = warp_sum(s_ip0);
-    if (lane == 0) dIp_acc += s_ip0;
-  }
+  if (!a.I0) dIp_acc += s_ip0;
+  dIp_acc = warp_sum(dIp_acc);
   if (lane == 0) atomicAdd(a.dI_prior + h, dIp_acc);
   if (threadIdx.x == 0) atomicAdd(a.dA + h, dA_acc);
 }
@@ -292,7 +308,8 @@ size_t backward_scratch_bytes(const BwdArgs& a) {
 template <int DK, bool BF16>
 cudaError_t launch_t(const BwdArgs& a, float* scratch, cudaStream_t s) {
   const unsigned ctas = (unsigned)((long)a.B * a.H * (a.d_v / kRowsPerCta));
-  const size_t smem = (2 * kRowsPerCta * (kSeg / kWin) * DK + 4 * kRowsPerCta * DK + 2 * kRowsPerCta) * sizeof(float);
+  const size_t smem =
+      (2 * kRowsPerCta * (kSeg / kWin) * DK + 4 * kRowsPerCta * DK + 2 * kRowsPerCta + 2 * kSeg) * sizeof(float);
   auto kern = palimpsa_bwd_kernel<DK, BF16>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
