@@ -10,6 +10,8 @@ the CUDA path.
 Contents:
 * ``palimpsa_oracle.c`` — the sequential token-by-token recurrence in fp64
   (OpenMP over independent value rows only), loaded here through ctypes.
+* ``prologue`` — the fused layer prologue in fp64: per-token L2 norm of q and
+  k, d_t = softplus(raw), beta = b_scale * sigmoid(raw), and the v* input.
 * ``reference_np`` — independent NumPy statements: the mean/precision form, the
   chunked natural-parameter form and the full-Gaussian posterior it
   approximates.
@@ -59,6 +61,12 @@ def _load():
         lib.oracle_forward.restype = ctypes.c_int
         lib.oracle_forward.argtypes = [dp, dp, dp, dp, dp, dp, dp, ctypes.c_int, dp, dp,
                                        dp, dp, dp, L, L, L, L, L, ctypes.c_int]
+        lib.oracle_forward_ex.restype = ctypes.c_int
+        lib.oracle_forward_ex.argtypes = [dp, dp, dp, dp, dp, dp, dp, ctypes.c_int, ctypes.c_int, dp, dp,
+                                          dp, dp, dp, L, L, L, L, L, ctypes.c_int]
+        lib.oracle_step_ex.restype = ctypes.c_int
+        lib.oracle_step_ex.argtypes = [dp, dp, dp, dp, dp, dp, dp, ctypes.c_int, ctypes.c_int, dp, dp, dp,
+                                       L, L, L, L, ctypes.c_int]
         lib.oracle_step.restype = ctypes.c_int
         lib.oracle_step.argtypes = [dp, dp, dp, dp, dp, dp, dp, ctypes.c_int, dp, dp, dp,
                                     L, L, L, L, ctypes.c_int]
@@ -81,11 +89,12 @@ def max_threads() -> int:
     return int(_load().oracle_max_threads())
 
 
-def forward(q, k, v, beta, d_t, A, I_prior, mu0=None, I0=None, nthreads: int = 0):
+def forward(q, k, v, beta, d_t, A, I_prior, mu0=None, I0=None, nthreads: int = 0, v_star: bool = False):
     """Sequential Eq. (5) over T tokens for every (b, h, value row).
 
     q, k [B,H,T,dk]; v, beta [B,H,T,dv]; d_t [B,H,T]; A [H]; I_prior [H] or
     [H,dv,dk]; mu0, I0 [B,H,dv,dk] or None (mu0 = 0, I0 = I_prior).
+    With v_star, v holds v* = beta (.) v and is written as is (slide 11).
     Returns (y [B,H,T,dv], mu_T, I_T) in fp64.
     """
     q, k, v, beta, d_t, A, Ip = (_f64(x) for x in (q, k, v, beta, d_t, A, I_prior))
@@ -101,16 +110,17 @@ def forward(q, k, v, beta, d_t, A, I_prior, mu0=None, I0=None, nthreads: int = 0
     y = np.zeros((B, H, T, dv))
     muT = np.zeros((B, H, dv, dk))
     IT = np.zeros((B, H, dv, dk))
-    rc = _load().oracle_forward(_ptr(q), _ptr(k), _ptr(v), _ptr(beta), _ptr(d_t), _ptr(A), _ptr(Ip),
-                                prior_full, _ptr(m0), _ptr(i0), _ptr(y), _ptr(muT), _ptr(IT),
-                                B, H, T, dk, dv, int(nthreads))
+    rc = _load().oracle_forward_ex(_ptr(q), _ptr(k), _ptr(v), _ptr(beta), _ptr(d_t), _ptr(A), _ptr(Ip),
+                                   prior_full, int(bool(v_star)), _ptr(m0), _ptr(i0), _ptr(y), _ptr(muT),
+                                   _ptr(IT), B, H, T, dk, dv, int(nthreads))
     if rc != 0:
         raise RuntimeError(f"oracle_forward failed with code {rc}")
     return y, muT, IT
 
 
-def step(q, k, v, beta, d_t, A, I_prior, mu, I, nthreads: int = 0):
-    """One recurrent token: q, k [B,H,dk]; v, beta [B,H,dv]; d_t [B,H].
+def step(q, k, v, beta, d_t, A, I_prior, mu, I, nthreads: int = 0, v_star: bool = False):
+    """One recurrent token: q, k [B,H,dk]; v, beta [B,H,dv]; d_t [B,H]
+    (v holds v* when v_star, as in ``forward``).
 
     Returns (y [B,H,dv], mu', I') without modifying the arguments.
     """
@@ -121,8 +131,9 @@ def step(q, k, v, beta, d_t, A, I_prior, mu, I, nthreads: int = 0):
     mu_o = _f64(mu).copy()
     I_o = _f64(I).copy()
     y = np.zeros((B, H, dv))
-    rc = _load().oracle_step(_ptr(q), _ptr(k), _ptr(v), _ptr(beta), _ptr(d_t), _ptr(A), _ptr(Ip),
-                             prior_full, _ptr(mu_o), _ptr(I_o), _ptr(y), B, H, dk, dv, int(nthreads))
+    rc = _load().oracle_step_ex(_ptr(q), _ptr(k), _ptr(v), _ptr(beta), _ptr(d_t), _ptr(A), _ptr(Ip),
+                                prior_full, int(bool(v_star)), _ptr(mu_o), _ptr(I_o), _ptr(y), B, H, dk, dv,
+                                int(nthreads))
     if rc != 0:
         raise RuntimeError(f"oracle_step failed with code {rc}")
     return y, mu_o, I_o
