@@ -310,6 +310,49 @@ def run_ours(args, ws, rank, local):
         "note": "same scan inputs with the importance frozen at I_prior (Mamba2 / scalar-decay form), "
                 "no time split; timed after the timed region"}
 
+    # The fused prologue (palimpsa_forward_fused / palimpsa_step_fused): the same
+    # workload from raw projections with the Palimpsa-D q/k norm and the v* input,
+    # timed outside the timed region against the unfused kernels above.
+    raw = syn.sequence_inputs(wl, device=dev, seed=seed, raw=True)
+
+    def _fused():
+        pal.palimpsa_forward_fused(raw["q"], raw["k"], raw["v"], raw["beta_raw"], raw["d_raw"], raw["A"],
+                                   raw["I_prior"], raw["b_scale"], qk_norm=True, v_star=True, y=y_pre, mu_T=mu,
+                                   I_T=I, chunk=wl.chunk)
+    for _ in range(2):
+        _fused()
+    c0.record(stream)
+    for _ in range(reps):
+        _fused()
+    c1.record(stream)
+    torch.cuda.synchronize()
+    fused_ms = c0.elapsed_time(c1) / reps
+    kernels["palimpsa_fwd_fused"] = {
+        "avg_ms": fused_ms, "head_tokens_per_s": B * H * T / (fused_ms / 1e3), "over_unfused": fused_ms / fwd_avg_ms,
+        "note": "raw q, k, v*, beta_raw, d_raw in; softplus, b_scale * sigmoid and the q/k L2 norm applied while "
+                "staging; timed after the timed region"}
+    if S:
+        SF = min(S, 64)
+        rdec = syn.decode_inputs(wl, SF, device=dev, seed=seed, raw=True)
+
+        def _fused_steps():
+            for s in range(SF):
+                pal.palimpsa_step_fused(rdec["q"][s], rdec["k"][s], rdec["v"][s], rdec["beta_raw"][s],
+                                        rdec["d_raw"][s], raw["A"], raw["I_prior"], mu, I, raw["b_scale"],
+                                        qk_norm=True, v_star=True, y=y_dec[s])
+        _fused_steps()
+        c0.record(stream)
+        _fused_steps()
+        c1.record(stream)
+        torch.cuda.synchronize()
+        fstep_ms = c0.elapsed_time(c1) / SF
+        db = decode_step_bytes(B, H, dk, dv, in_bytes)
+        kernels["palimpsa_step_fused"] = {
+            "avg_ms": fstep_ms, "hbm_gbs": db / (fstep_ms / 1e3) / 1e9,
+            "frac_of_hbm_peak": db / (fstep_ms / 1e3) / 1e9 / hbm_peak,
+            "over_unfused": fstep_ms / kernels["palimpsa_step"]["avg_ms"],
+            "note": f"{SF} fused steps from raw inputs; timed after the timed region"}
+
     # The backward through the scan (gradients of <dy, y> for every input), timed
     # outside the timed region on the same inputs.
     if not S:

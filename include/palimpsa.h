@@ -182,6 +182,65 @@ palimpsa_status palimpsa_step(
     palimpsa_dtype in_dtype, void* cuda_stream);
 
 /*
+ * Options of the fused entry points (bit flags; combine with |).
+ *   PALIMPSA_FUSE_QK_NORM  divide q_t and k_t by their L2 norm over d_k
+ *                          (x / max(||x||_2, 1e-12)), as the Palimpsa-D block
+ *                          does (slide 10);
+ *   PALIMPSA_FUSE_V_STAR   v holds v* = beta (.) v, the kernel input of slide 11:
+ *                          the content write is v*_i k_j, and beta (activated)
+ *                          enters only the precision.
+ */
+typedef enum {
+  PALIMPSA_FUSE_QK_NORM = 1,
+  PALIMPSA_FUSE_V_STAR = 2
+} palimpsa_fuse_flags;
+
+/*
+ * palimpsa_forward_fused — palimpsa_forward_chunked with the layer's prologue
+ * applied in the kernels as each chunk is staged, so that raw projections go
+ * in without extra passes over HBM:
+ *
+ *   d_t  = softplus(d_raw)                        (so d_t >= 0, slide 5)
+ *   beta = b_scale[h] * sigmoid(beta_raw)         (so beta >= 0; per-head
+ *                                                  b_scale, slide 11)
+ *   q, k L2-normalised per token                  (PALIMPSA_FUSE_QK_NORM)
+ *   write v* as given instead of beta (.) v       (PALIMPSA_FUSE_V_STAR)
+ *
+ * The pages do not print the two activations; they are the ones that map any
+ * real input into the recurrence's domain, as in the workload recipes.
+ *
+ *   q, k      [B, H, T, d_k] in_dtype (raw)
+ *   v         [B, H, T, d_v] in_dtype: v, or v* with PALIMPSA_FUSE_V_STAR
+ *   beta_raw  [B, H, T, d_v] in_dtype (pre-activation)
+ *   d_raw     [B, H, T]      fp32 (pre-activation)
+ *   b_scale   [H] fp32 >= 0, or NULL for 1
+ *   flags     palimpsa_fuse_flags; unknown bits give PALIMPSA_ERR_UNSUPPORTED
+ *   all other arguments, the time split and the errors are those of
+ *   palimpsa_forward_chunked. A negative or non-finite b_scale, or a
+ *   non-finite raw gate, latches PALIMPSA_ERR_DOMAIN in the device status.
+ */
+palimpsa_status palimpsa_forward_fused(
+    const void* q, const void* k, const void* v, const void* beta_raw,
+    const float* d_raw, const float* A, const float* I_prior,
+    const float* b_scale, const float* mu0, const float* I0,
+    float* y, float* mu_T, float* I_T,
+    int B, int H, int T, int d_k, int d_v, int chunk, unsigned int flags,
+    palimpsa_dtype in_dtype, void* cuda_stream);
+
+/*
+ * palimpsa_step_fused — palimpsa_step with the same prologue on the token's
+ * raw inputs: q, k [B,H,d_k], v and beta_raw [B,H,d_v] in in_dtype, d_raw [B,H]
+ * fp32, b_scale [H] or NULL, flags as for palimpsa_forward_fused. State, y and
+ * errors as for palimpsa_step.
+ */
+palimpsa_status palimpsa_step_fused(
+    const void* q, const void* k, const void* v, const void* beta_raw,
+    const float* d_raw, const float* A, const float* I_prior,
+    const float* b_scale, float* mu, float* I, float* y,
+    int B, int H, int d_k, int d_v, unsigned int flags,
+    palimpsa_dtype in_dtype, void* cuda_stream);
+
+/*
  * palimpsa_forward_without_meta — the "without Meta" comparator: the same
  * recurrence with the importance frozen at its prior (I_t = I_prior), i.e. the
  * Mamba2 limit of Eq. (5) (slide 11; slide 10 names Mamba2 as Palimpsa-M's

@@ -13,6 +13,8 @@ plus the seeded synthetic-input generator.
 from .binding import (  # noqa: F401
     PALIMPSA_BF16,
     PALIMPSA_F32,
+    PALIMPSA_FUSE_QK_NORM,
+    PALIMPSA_FUSE_V_STAR,
     PalimpsaError,
     library_path,
     load_library,
@@ -20,10 +22,12 @@ from .binding import (  # noqa: F401
     palimpsa_backward,
     palimpsa_debug_withhold_first_copy,
     palimpsa_forward_chunked,
+    palimpsa_forward_fused,
     palimpsa_forward_without_meta,
     palimpsa_get_device_status,
     palimpsa_set_forward_segments,
     palimpsa_set_wait_timeout_ns,
     palimpsa_status_string,
     palimpsa_step,
+    palimpsa_step_fused,
 )

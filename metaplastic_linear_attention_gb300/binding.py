@@ -22,6 +22,8 @@ from . import build_lib
 
 PALIMPSA_F32 = 0
 PALIMPSA_BF16 = 1
+PALIMPSA_FUSE_QK_NORM = 1   # palimpsa_fuse_flags
+PALIMPSA_FUSE_V_STAR = 2
 STATUS_NAMES = {
     0: "PALIMPSA_OK", 1: "PALIMPSA_ERR_NULL", 2: "PALIMPSA_ERR_SHAPE", 3: "PALIMPSA_ERR_ALIGN",
     4: "PALIMPSA_ERR_DTYPE", 5: "PALIMPSA_ERR_DOMAIN", 6: "PALIMPSA_ERR_UNSUPPORTED",
@@ -68,6 +70,12 @@ def load_library(path: str | None = None):
         lib.palimpsa_backward.restype = i
         lib.palimpsa_backward.argtypes = [vp, vp, vp, vp, fp, fp, fp, fp, fp, fp, fp, fp, fp, fp, fp, fp, fp, fp,
                                           fp, fp, fp, i, i, i, i, i, i, vp]
+        u = ctypes.c_uint
+        lib.palimpsa_forward_fused.restype = i
+        lib.palimpsa_forward_fused.argtypes = [vp, vp, vp, vp, fp, fp, fp, fp, fp, fp, fp, fp, fp,
+                                               i, i, i, i, i, i, u, i, vp]
+        lib.palimpsa_step_fused.restype = i
+        lib.palimpsa_step_fused.argtypes = [vp, vp, vp, vp, fp, fp, fp, fp, fp, fp, fp, i, i, i, i, u, i, vp]
         lib.palimpsa_step.restype = i
         lib.palimpsa_step.argtypes = [vp, vp, vp, vp, fp, fp, fp, fp, fp, fp, i, i, i, i, i, vp]
         lib.palimpsa_status_string.restype = ctypes.c_char_p
@@ -175,29 +183,8 @@ def palimpsa_forward_chunked(q, k, v, beta, d_t, A, I_prior, mu0=None, I0=None, 
     """
     if q.device.type == "cpu":
         return _forward_from_host(q, k, v, beta, d_t, A, I_prior, mu0, I0, y, mu_T, I_T, chunk, stream)
-
-    B, H, T, d_k = q.shape
-    d_v = v.shape[-1]
-    dev = q.device
-    f32 = torch.float32
-    _check(k, "k", q.shape, q.dtype, dev)
-    _check(v, "v", (B, H, T, d_v), q.dtype, dev)
-    _check(beta, "beta", (B, H, T, d_v), q.dtype, dev)
-    _check(q, "q", q.shape, None, dev)
-    _check(d_t, "d_t", (B, H, T), f32, dev)
-    _check(A, "A", (H,), f32, dev)
-    _check(I_prior, "I_prior", (H,), f32, dev)
-    _check(mu0, "mu0", (B, H, d_v, d_k), f32, dev)
-    _check(I0, "I0", (B, H, d_v, d_k), f32, dev)
-    if y is None:
-        y = torch.empty((B, H, T, d_v), dtype=f32, device=dev)
-    if mu_T is None:
-        mu_T = torch.empty((B, H, d_v, d_k), dtype=f32, device=dev)
-    if I_T is None:
-        I_T = torch.empty((B, H, d_v, d_k), dtype=f32, device=dev)
-    _check(y, "y", (B, H, T, d_v), f32, dev)
-    _check(mu_T, "mu_T", (B, H, d_v, d_k), f32, dev)
-    _check(I_T, "I_T", (B, H, d_v, d_k), f32, dev)
+    B, H, T, d_k, d_v, dev = _check_forward_inputs(q, k, v, beta, d_t, A, I_prior, mu0, I0, ("beta", "d_t"))
+    y, mu_T, I_T = _forward_outputs(B, H, T, d_k, d_v, dev, y, mu_T, I_T)
     lib = load_library()
     with torch.cuda.device(dev):
         rc = lib.palimpsa_forward_chunked(
@@ -207,6 +194,100 @@ def palimpsa_forward_chunked(q, k, v, beta, d_t, A, I_prior, mu0=None, I0=None, 
     if rc != 0:
         raise PalimpsaError(rc, "palimpsa_forward_chunked")
     return y, mu_T, I_T
+
+
+def _check_forward_inputs(q, k, v, beta, d_t, A, I_prior, mu0, I0, names):
+    """Shapes, dtypes and placement of a forward's inputs (device tensors);
+    returns (B, H, T, d_k, d_v, device)."""
+    if q.device.type != "cuda":
+        raise ValueError("this entry point takes device tensors")
+    B, H, T, d_k = q.shape
+    d_v = v.shape[-1]
+    dev = q.device
+    f32 = torch.float32
+    _check(k, "k", q.shape, q.dtype, dev)
+    _check(v, "v", (B, H, T, d_v), q.dtype, dev)
+    _check(beta, names[0], (B, H, T, d_v), q.dtype, dev)
+    _check(q, "q", q.shape, None, dev)
+    _check(d_t, names[1], (B, H, T), f32, dev)
+    _check(A, "A", (H,), f32, dev)
+    _check(I_prior, "I_prior", (H,), f32, dev)
+    _check(mu0, "mu0", (B, H, d_v, d_k), f32, dev)
+    _check(I0, "I0", (B, H, d_v, d_k), f32, dev)
+    return B, H, T, d_k, d_v, dev
+
+
+def _forward_outputs(B, H, T, d_k, d_v, dev, y, mu_T, I_T):
+    f32 = torch.float32
+    if y is None:
+        y = torch.empty((B, H, T, d_v), dtype=f32, device=dev)
+    if mu_T is None:
+        mu_T = torch.empty((B, H, d_v, d_k), dtype=f32, device=dev)
+    if I_T is None:
+        I_T = torch.empty((B, H, d_v, d_k), dtype=f32, device=dev)
+    _check(y, "y", (B, H, T, d_v), f32, dev)
+    _check(mu_T, "mu_T", (B, H, d_v, d_k), f32, dev)
+    _check(I_T, "I_T", (B, H, d_v, d_k), f32, dev)
+    return y, mu_T, I_T
+
+
+def _fuse_flags(qk_norm, v_star):
+    return (PALIMPSA_FUSE_QK_NORM if qk_norm else 0) | (PALIMPSA_FUSE_V_STAR if v_star else 0)
+
+
+def palimpsa_forward_fused(q, k, v, beta_raw, d_raw, A, I_prior, b_scale=None, mu0=None, I0=None, *,
+                           qk_norm=False, v_star=False, y=None, mu_T=None, I_T=None, chunk: int = 0, stream=None):
+    """The forward with the layer prologue fused in (see palimpsa.h): d_t =
+    softplus(d_raw), beta = b_scale * sigmoid(beta_raw), q/k L2-normalised per
+    token when qk_norm, v taken as v* = beta v when v_star. Device tensors;
+    b_scale [H] fp32 or None. Returns (y, mu_T, I_T)."""
+    B, H, T, d_k, d_v, dev = _check_forward_inputs(q, k, v, beta_raw, d_raw, A, I_prior, mu0, I0,
+                                                   ("beta_raw", "d_raw"))
+    _check(b_scale, "b_scale", (H,), torch.float32, dev)
+    y, mu_T, I_T = _forward_outputs(B, H, T, d_k, d_v, dev, y, mu_T, I_T)
+    lib = load_library()
+    with torch.cuda.device(dev):
+        rc = lib.palimpsa_forward_fused(
+            _ptr(q), _ptr(k), _ptr(v), _ptr(beta_raw), _ptr(d_raw), _ptr(A), _ptr(I_prior), _ptr(b_scale), _ptr(mu0),
+            _ptr(I0), _ptr(y), _ptr(mu_T), _ptr(I_T), B, H, T, d_k, d_v, int(chunk), _fuse_flags(qk_norm, v_star),
+            _in_dtype(q), ctypes.c_void_p(_stream_handle(stream)))
+    if rc != 0:
+        raise PalimpsaError(rc, "palimpsa_forward_fused")
+    return y, mu_T, I_T
+
+
+def palimpsa_step_fused(q, k, v, beta_raw, d_raw, A, I_prior, mu, I, b_scale=None, *, qk_norm=False, v_star=False,
+                        y=None, stream=None):
+    """One decode token from raw inputs (see palimpsa.h): q, k [B,H,d_k], v and
+    beta_raw [B,H,d_v], d_raw [B,H]; mu, I updated in place. Device tensors.
+    Returns y [B,H,d_v]."""
+    if q.device.type != "cuda":
+        raise ValueError("palimpsa_step_fused takes device tensors")
+    B, H, d_k = q.shape
+    d_v = v.shape[-1]
+    dev = q.device
+    f32 = torch.float32
+    _check(k, "k", q.shape, q.dtype, dev)
+    _check(q, "q", q.shape, None, dev)
+    _check(v, "v", (B, H, d_v), q.dtype, dev)
+    _check(beta_raw, "beta_raw", (B, H, d_v), q.dtype, dev)
+    _check(d_raw, "d_raw", (B, H), f32, dev)
+    _check(A, "A", (H,), f32, dev)
+    _check(I_prior, "I_prior", (H,), f32, dev)
+    _check(b_scale, "b_scale", (H,), f32, dev)
+    _check(mu, "mu", (B, H, d_v, d_k), f32, dev)
+    _check(I, "I", (B, H, d_v, d_k), f32, dev)
+    y = torch.empty((B, H, d_v), dtype=f32, device=dev) if y is None else y
+    _check(y, "y", (B, H, d_v), f32, dev)
+    lib = load_library()
+    with torch.cuda.device(dev):
+        rc = lib.palimpsa_step_fused(_ptr(q), _ptr(k), _ptr(v), _ptr(beta_raw), _ptr(d_raw), _ptr(A), _ptr(I_prior),
+                                     _ptr(b_scale), _ptr(mu), _ptr(I), _ptr(y), B, H, d_k, d_v,
+                                     _fuse_flags(qk_norm, v_star), _in_dtype(q),
+                                     ctypes.c_void_p(_stream_handle(stream)))
+    if rc != 0:
+        raise PalimpsaError(rc, "palimpsa_step_fused")
+    return y
 
 
 def palimpsa_forward_without_meta(q, k, v, beta, d_t, A, I_prior, mu0=None, *, y=None, mu_T=None, chunk: int = 0,

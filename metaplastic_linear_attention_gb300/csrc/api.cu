@@ -99,18 +99,12 @@ bool sizes_ok(long long B, long long H, long long T, int d_k, int d_v) {
   return true;
 }
 
-}  // namespace
-}  // namespace palimpsa
-
-using namespace palimpsa;
-
-extern "C" {
-
-palimpsa_status palimpsa_forward_chunked(const void* q, const void* k, const void* v, const void* beta,
-                                         const float* d_t, const float* A, const float* I_prior,
-                                         const float* mu0, const float* I0, float* y, float* mu_T,
-                                         float* I_T, int B, int H, int T, int d_k, int d_v, int chunk,
-                                         palimpsa_dtype in_dtype, void* cuda_stream) {
+// Validation and launch shared by palimpsa_forward_chunked and
+// palimpsa_forward_fused (pro.on only for the latter).
+palimpsa_status forward_impl(const void* q, const void* k, const void* v, const void* beta, const float* d_t,
+                             const float* A, const float* I_prior, const float* mu0, const float* I0, float* y,
+                             float* mu_T, float* I_T, int B, int H, int T, int d_k, int d_v, int chunk,
+                             palimpsa_dtype in_dtype, void* cuda_stream, const Prologue& pro) {
   if (!A || !I_prior || !mu_T || !I_T) return PALIMPSA_ERR_NULL;
   // With T == 0 the per-token arrays are empty and may be NULL.
   if (T != 0 && (!q || !k || !v || !beta || !d_t || !y)) return PALIMPSA_ERR_NULL;
@@ -128,11 +122,79 @@ palimpsa_status palimpsa_forward_chunked(const void* q, const void* k, const voi
   if (palimpsa_status s = status_word(&st)) return s;
   FwdArgs a{q, k, v, beta, d_t, A, I_prior, mu0, I0, y, mu_T, I_T, B, H, T, d_k, d_v,
             chunk == 0 ? 32 : chunk, in_dtype == PALIMPSA_BF16, st,
-            g_wait_timeout_ns.load(), g_withhold_first_copy.load(), g_forward_segments.load()};
+            g_wait_timeout_ns.load(), g_withhold_first_copy.load(), g_forward_segments.load(), pro};
   StreamOrderedScratch scratch;
   if (launch_forward_chunked(a, static_cast<cudaStream_t>(cuda_stream), &scratch) != cudaSuccess)
     return PALIMPSA_ERR_CUDA;
   return PALIMPSA_OK;
+}
+
+// Validation and launch shared by palimpsa_step and palimpsa_step_fused.
+palimpsa_status step_impl(const void* q, const void* k, const void* v, const void* beta, const float* d_t,
+                          const float* A, const float* I_prior, float* mu, float* I, float* y, int B, int H,
+                          int d_k, int d_v, palimpsa_dtype in_dtype, void* cuda_stream, const Prologue& pro) {
+  if (!q || !k || !v || !beta || !d_t || !A || !I_prior || !mu || !I || !y) return PALIMPSA_ERR_NULL;
+  if (in_dtype != PALIMPSA_F32 && in_dtype != PALIMPSA_BF16) return PALIMPSA_ERR_DTYPE;
+  if (!sizes_ok(B, H, 1, d_k, d_v)) return PALIMPSA_ERR_SHAPE;
+  if (!supported_dims(d_k, d_v)) return PALIMPSA_ERR_UNSUPPORTED;
+  const void* a16[] = {q, k, v, beta, mu, I, y};
+  for (const void* p : a16)
+    if (!aligned(p, 16)) return PALIMPSA_ERR_ALIGN;
+  const void* a4[] = {d_t, A, I_prior, pro.b_scale};
+  for (const void* p : a4)
+    if (p && !aligned(p, 4)) return PALIMPSA_ERR_ALIGN;
+  unsigned int* st = nullptr;
+  if (palimpsa_status s = status_word(&st)) return s;
+  StepArgs a{q, k, v, beta, d_t, A, I_prior, mu, I, y, B, H, d_k, d_v, in_dtype == PALIMPSA_BF16, st, pro};
+  if (launch_step(a, static_cast<cudaStream_t>(cuda_stream)) != cudaSuccess) return PALIMPSA_ERR_CUDA;
+  return PALIMPSA_OK;
+}
+
+constexpr unsigned int kKnownFuseFlags = PALIMPSA_FUSE_QK_NORM | PALIMPSA_FUSE_V_STAR;
+
+Prologue fused_prologue(const float* b_scale, unsigned int flags) {
+  Prologue p;
+  p.on = true;
+  p.qk_norm = (flags & PALIMPSA_FUSE_QK_NORM) != 0;
+  p.v_star = (flags & PALIMPSA_FUSE_V_STAR) != 0;
+  p.b_scale = b_scale;
+  return p;
+}
+
+}  // namespace
+}  // namespace palimpsa
+
+using namespace palimpsa;
+
+extern "C" {
+
+palimpsa_status palimpsa_forward_chunked(const void* q, const void* k, const void* v, const void* beta,
+                                         const float* d_t, const float* A, const float* I_prior,
+                                         const float* mu0, const float* I0, float* y, float* mu_T,
+                                         float* I_T, int B, int H, int T, int d_k, int d_v, int chunk,
+                                         palimpsa_dtype in_dtype, void* cuda_stream) {
+  return forward_impl(q, k, v, beta, d_t, A, I_prior, mu0, I0, y, mu_T, I_T, B, H, T, d_k, d_v, chunk, in_dtype,
+                      cuda_stream, Prologue{});
+}
+
+palimpsa_status palimpsa_forward_fused(const void* q, const void* k, const void* v, const void* beta_raw,
+                                       const float* d_raw, const float* A, const float* I_prior,
+                                       const float* b_scale, const float* mu0, const float* I0, float* y,
+                                       float* mu_T, float* I_T, int B, int H, int T, int d_k, int d_v, int chunk,
+                                       unsigned int flags, palimpsa_dtype in_dtype, void* cuda_stream) {
+  if (flags & ~kKnownFuseFlags) return PALIMPSA_ERR_UNSUPPORTED;
+  if (b_scale && !aligned(b_scale, 4)) return PALIMPSA_ERR_ALIGN;
+  return forward_impl(q, k, v, beta_raw, d_raw, A, I_prior, mu0, I0, y, mu_T, I_T, B, H, T, d_k, d_v, chunk,
+                      in_dtype, cuda_stream, fused_prologue(b_scale, flags));
+}
+
+palimpsa_status palimpsa_step_fused(const void* q, const void* k, const void* v, const void* beta_raw,
+                                    const float* d_raw, const float* A, const float* I_prior, const float* b_scale,
+                                    float* mu, float* I, float* y, int B, int H, int d_k, int d_v,
+                                    unsigned int flags, palimpsa_dtype in_dtype, void* cuda_stream) {
+  if (flags & ~kKnownFuseFlags) return PALIMPSA_ERR_UNSUPPORTED;
+  return step_impl(q, k, v, beta_raw, d_raw, A, I_prior, mu, I, y, B, H, d_k, d_v, in_dtype, cuda_stream,
+                   fused_prologue(b_scale, flags));
 }
 
 palimpsa_status palimpsa_forward_without_meta(const void* q, const void* k, const void* v, const void* beta,
@@ -206,21 +268,7 @@ palimpsa_status palimpsa_step(const void* q, const void* k, const void* v, const
                               const float* d_t, const float* A, const float* I_prior, float* mu, float* I,
                               float* y, int B, int H, int d_k, int d_v, palimpsa_dtype in_dtype,
                               void* cuda_stream) {
-  if (!q || !k || !v || !beta || !d_t || !A || !I_prior || !mu || !I || !y) return PALIMPSA_ERR_NULL;
-  if (in_dtype != PALIMPSA_F32 && in_dtype != PALIMPSA_BF16) return PALIMPSA_ERR_DTYPE;
-  if (!sizes_ok(B, H, 1, d_k, d_v)) return PALIMPSA_ERR_SHAPE;
-  if (!supported_dims(d_k, d_v)) return PALIMPSA_ERR_UNSUPPORTED;
-  const void* a16[] = {q, k, v, beta, mu, I, y};
-  for (const void* p : a16)
-    if (!aligned(p, 16)) return PALIMPSA_ERR_ALIGN;
-  const void* a4[] = {d_t, A, I_prior};
-  for (const void* p : a4)
-    if (!aligned(p, 4)) return PALIMPSA_ERR_ALIGN;
-  unsigned int* st = nullptr;
-  if (palimpsa_status s = status_word(&st)) return s;
-  StepArgs a{q, k, v, beta, d_t, A, I_prior, mu, I, y, B, H, d_k, d_v, in_dtype == PALIMPSA_BF16, st};
-  if (launch_step(a, static_cast<cudaStream_t>(cuda_stream)) != cudaSuccess) return PALIMPSA_ERR_CUDA;
-  return PALIMPSA_OK;
+  return step_impl(q, k, v, beta, d_t, A, I_prior, mu, I, y, B, H, d_k, d_v, in_dtype, cuda_stream, Prologue{});
 }
 
 const char* palimpsa_status_string(palimpsa_status s) {

@@ -35,6 +35,11 @@
 //   element and token (no reciprocal, no readout).
 // * y_{t,i} is reduced over the row team with three butterfly shuffles and
 //   stored straight to global memory.
+// * Fused prologue (palimpsa_forward_fused): the conversion stage of passes A
+//   and C also applies the layer's activations - softplus to the gate input,
+//   b_scale * sigmoid to beta, the per-token L2 norm of q and k (Palimpsa-D,
+//   slide 10) - and, in the v* mode of slide 11, writes v as given instead of
+//   beta v. It runs once per chunk and CTA, outside the token loop.
 #include <algorithm>
 #include <cmath>
 
@@ -74,6 +79,7 @@ palimpsa_fwd_chunked_kernel(FwdArgs a, int C, int nseg, int seg_len, const float
 
   const float A_h = a.A[tl.h];
   const float Ip = a.I_prior[tl.h];
+  const float bsc = a.pro.b_scale ? a.pro.b_scale[tl.h] : 1.f;
   bool domain_bad = !(pos_finite(A_h) && pos_finite(Ip));
 
   const size_t head_tok = (size_t)tl.bh * T;
@@ -120,17 +126,20 @@ palimpsa_fwd_chunked_kernel(FwdArgs a, int C, int nseg, int seg_len, const float
     if (!pipe.wait(c, a.wait_timeout_ns, a.status)) return;
     // ---- convert the staged chunk to fp32 operands shared by all rows
     const unsigned char* raw = pipe.raw(c);
-    convert_keys<DK, BF16, true, NTH>(raw, L, smem, tc);
+    convert_keys<DK, BF16, true, NTH>(raw, L, smem, tc, a.pro.qk_norm);
     for (int it = threadIdx.x; it < tc * RG; it += NTH) {
       const int t = it / RG, r = it % RG;
       const size_t e = (size_t)t * DV + tl.row0 + r;
-      const float vv = raw_elem<BF16>(raw + L.raw_v, e), bb = raw_elem<BF16>(raw + L.raw_b, e);
+      const float vv = raw_elem<BF16>(raw + L.raw_v, e);
+      float bb = raw_elem<BF16>(raw + L.raw_b, e);
+      if (a.pro.on) bb = bsc * sigmoid_f(bb);
       domain_bad |= !nonneg_finite(bb);
-      bvf[it] = bb * vv;
+      bvf[it] = a.pro.v_star ? vv : bb * vv;
       bfv[it] = bb;
     }
     for (int t = threadIdx.x; t < tc; t += NTH) {
-      const float d = gd[t0 + t];
+      float d = gd[t0 + t];
+      if (a.pro.on) d = softplus_f(d);
       domain_bad |= !nonneg_finite(d);
       const float x = -A_h * d;
       alf[t] = expf(x);
@@ -253,6 +262,7 @@ palimpsa_fwd_summary_kernel(FwdArgs a, int C, int nseg, int seg_len, float* __re
   float* carry = reinterpret_cast<float*>(smem + L.omf);  // [0] = product of alpha after this chunk
 
   const float A_h = a.A[tl.h];
+  const float bsc = a.pro.b_scale ? a.pro.b_scale[tl.h] : 1.f;
   const size_t head_tok = (size_t)tl.bh * T;
   ChunkPipe<DK, ES> pipe(L, smem, static_cast<const char*>(a.q) + head_tok * DK * ES,
                          static_cast<const char*>(a.k) + head_tok * DK * ES,
@@ -275,7 +285,9 @@ palimpsa_fwd_summary_kernel(FwdArgs a, int C, int nseg, int seg_len, float* __re
     // suffix products inside the chunk (warp 0; at most 32 tokens per chunk):
     // W_t = carry * prod_{t < u < tc} alpha_u
     if (warp == 0) {
-      const float al = lane < tc ? expf(-A_h * gd[t0 + lane]) : 1.f;
+      float d = lane < tc ? gd[t0 + lane] : 0.f;
+      if (a.pro.on) d = softplus_f(d);
+      const float al = lane < tc ? expf(-A_h * d) : 1.f;
       float p = al;  // inclusive suffix product prod_{u >= lane}
 #pragma unroll
       for (int off = 1; off < 32; off <<= 1) {
@@ -288,14 +300,16 @@ palimpsa_fwd_summary_kernel(FwdArgs a, int C, int nseg, int seg_len, float* __re
       __syncwarp();
       if (lane == 0) carry[0] = cin * p;  // lane 0 holds the product over the whole chunk
     }
-    convert_keys<DK, BF16, false, NTH>(raw, L, smem, tc);
+    convert_keys<DK, BF16, false, NTH>(raw, L, smem, tc, a.pro.qk_norm);
     __syncthreads();  // W_t ready
     for (int it = threadIdx.x; it < tc * RG; it += NTH) {
       const int t = it / RG, r = it % RG;
       const size_t e = (size_t)t * DV + tl.row0 + r;
-      const float vv = raw_elem<BF16>(raw + L.raw_v, e), bb = raw_elem<BF16>(raw + L.raw_b, e);
+      const float vv = raw_elem<BF16>(raw + L.raw_v, e);
+      float bb = raw_elem<BF16>(raw + L.raw_b, e);
+      if (a.pro.on) bb = bsc * sigmoid_f(bb);
       const float w = wf[t];
-      wbvf[it] = w * (bb * vv);
+      wbvf[it] = w * (a.pro.v_star ? vv : bb * vv);
       wbf[it] = w * bb;
     }
     __syncthreads();

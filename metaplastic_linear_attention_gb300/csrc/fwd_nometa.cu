@@ -76,7 +76,7 @@ palimpsa_fwd_nometa_kernel(FwdArgs a, int C) {
     const int t0 = pipe.t0_of(c), tc = pipe.tc_of(c);
     if (!pipe.wait(c, a.wait_timeout_ns, a.status)) return;
     const unsigned char* raw = pipe.raw(c);
-    convert_keys<DK, BF16, true, NTH>(raw, L, smem, tc);
+    convert_keys<DK, BF16, true, NTH>(raw, L, smem, tc, false);
     for (int it = threadIdx.x; it < tc * RG; it += NTH) {
       const int t = it / RG, r = it % RG;
       const size_t e = (size_t)t * DV + tl.row0 + r;

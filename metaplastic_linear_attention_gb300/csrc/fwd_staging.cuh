@@ -150,14 +150,19 @@ struct ChunkPipe {
 };
 
 // Convert the landed raw chunk to fp32 k, k^2 (and q when WITH_Q) shared by all
-// rows. NTH threads cooperate.
+// rows. NTH threads cooperate. With `norm` (uniform over the CTA) each token's
+// k and q are divided by their L2 norm first: the G = d_k / 8 items of a token
+// sit on G consecutive, G-aligned lanes of one warp (NTH is a multiple of 32),
+// which sum their squares with a butterfly inside that lane group.
 template <int DK, bool BF16, bool WITH_Q, int NTH>
 __device__ __forceinline__ void convert_keys(const unsigned char* raw, const FwdSmem& L, unsigned char* smem,
-                                             int tc) {
+                                             int tc, bool norm) {
   float* kf = reinterpret_cast<float*>(smem + L.kf);
   float* k2f = reinterpret_cast<float*>(smem + L.k2f);
   float* qf = reinterpret_cast<float*>(smem + L.qf);
   constexpr int PER = 8;
+  constexpr int G = DK / PER;  // items (lanes) per token
+  static_assert(32 % G == 0 && NTH % 32 == 0, "a token's items must fill aligned lane groups");
   const int items = tc * DK / PER;
   for (int it = threadIdx.x; it < items; it += NTH) {
     float kv[PER], qv[PER];
@@ -182,6 +187,29 @@ __device__ __forceinline__ void convert_keys(const unsigned char* raw, const Fwd
         const float4 qa = q4[0], qb = q4[1];
         qv[0] = qa.x; qv[1] = qa.y; qv[2] = qa.z; qv[3] = qa.w;
         qv[4] = qb.x; qv[5] = qb.y; qv[6] = qb.z; qv[7] = qb.w;
+      }
+    }
+    if (norm) {
+      const unsigned lane = threadIdx.x & 31u;
+      const unsigned gmask = G == 32 ? 0xffffffffu : ((1u << G) - 1u) << (lane & ~(unsigned)(G - 1));
+      float sk = 0.f, sq = 0.f;
+#pragma unroll
+      for (int e = 0; e < PER; ++e) {
+        sk = fmaf(kv[e], kv[e], sk);
+        if constexpr (WITH_Q) sq = fmaf(qv[e], qv[e], sq);
+      }
+#pragma unroll
+      for (int m = 1; m < G; m <<= 1) {
+        sk += __shfl_xor_sync(gmask, sk, m);
+        if constexpr (WITH_Q) sq += __shfl_xor_sync(gmask, sq, m);
+      }
+      const float ik = rsqrtf(fmaxf(sk, kNormFloorSq));
+#pragma unroll
+      for (int e = 0; e < PER; ++e) kv[e] *= ik;
+      if constexpr (WITH_Q) {
+        const float iq = rsqrtf(fmaxf(sq, kNormFloorSq));
+#pragma unroll
+        for (int e = 0; e < PER; ++e) qv[e] *= iq;
       }
     }
     float4* ko = reinterpret_cast<float4*>(kf) + 2 * it;

@@ -16,6 +16,15 @@ enum : unsigned int {
   kStatusDomain = 1u << 1,
 };
 
+// The fused layer prologue (palimpsa_forward_fused / palimpsa_step_fused):
+// raw projections are turned into the recurrence's inputs as they are staged.
+struct Prologue {
+  bool on = false;                 // d_t = softplus(raw), beta = b_scale[h] * sigmoid(raw)
+  bool qk_norm = false;            // q, k divided by their L2 norm per token
+  bool v_star = false;             // v holds v* = beta (.) v: the content write takes it as is
+  const float* b_scale = nullptr;  // [H]; NULL means 1
+};
+
 struct FwdArgs {
   const void* q;
   const void* k;
@@ -35,6 +44,7 @@ struct FwdArgs {
   unsigned long long wait_timeout_ns;
   int withhold_first_copy;
   int force_segments;  // 0: the library chooses the time split
+  Prologue pro{};
 };
 
 struct StepArgs {
@@ -51,6 +61,7 @@ struct StepArgs {
   int B, H, d_k, d_v;
   bool bf16;
   unsigned int* status;
+  Prologue pro{};
 };
 
 struct BwdArgs {
@@ -177,6 +188,15 @@ __device__ __forceinline__ void latch_status(unsigned int* status, unsigned int 
 // fp32 "is a usable positive number" / "is a usable non-negative number".
 __device__ __forceinline__ bool pos_finite(float x) { return x > 0.f && x <= 3.0e38f; }
 __device__ __forceinline__ bool nonneg_finite(float x) { return x >= 0.f && x <= 3.0e38f; }
+
+// Prologue activations. softplus(x) = log(1 + e^x) as max(x, 0) + log1p(e^-|x|)
+// (no overflow for large x, no lost tail for very negative x); sigmoid(x) =
+// 1 / (1 + e^-x), which tends to 0 when e^-x overflows.
+__device__ __forceinline__ float softplus_f(float x) { return fmaxf(x, 0.f) + log1pf(expf(-fabsf(x))); }
+__device__ __forceinline__ float sigmoid_f(float x) { return 1.f / (1.f + expf(-x)); }
+
+// Squared-norm floor of the q/k L2 norm: x / max(||x||, 1e-12).
+constexpr float kNormFloorSq = 1e-24f;
 
 #endif  // __CUDACC__
 

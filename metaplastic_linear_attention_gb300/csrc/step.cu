@@ -22,6 +22,10 @@
 // The update uses the mean/precision form of Eq. (5) directly:
 //   I' = alpha I + (1 - alpha) I_prior + beta_i k_j^2
 //   mu' = (alpha I mu + beta_i v_i k_j) / I'      (IEEE division)
+// The fused variant (PRO, palimpsa_step_fused) first applies the layer's
+// prologue to the token's raw inputs: softplus to the gate input, b_scale *
+// sigmoid to beta, optionally the L2 norm of q and k (one more butterfly over
+// the row's lanes) and the v* write of slide 11.
 #include "palimpsa_internal.cuh"
 
 namespace palimpsa {
@@ -46,7 +50,7 @@ __device__ __forceinline__ float load1(const void* base, size_t idx) {
   else return static_cast<const float*>(base)[idx];
 }
 
-template <int DK, bool BF16>
+template <int DK, bool BF16, bool PRO>
 __global__ void __launch_bounds__(kWarpsPerBlock * 32)
 palimpsa_step_kernel(StepArgs a) {
   constexpr int LPR = DK / 4;       // lanes per row
@@ -70,9 +74,26 @@ palimpsa_step_kernel(StepArgs a) {
     I4[it] = __ldcs(reinterpret_cast<const float4*>(a.I + off));
   }
 
-  const float4 q4 = load4<BF16>(a.q, (size_t)bh * DK + col);
-  const float4 k4 = load4<BF16>(a.k, (size_t)bh * DK + col);
-  const float d = a.d_t[bh];
+  float4 q4 = load4<BF16>(a.q, (size_t)bh * DK + col);
+  float4 k4 = load4<BF16>(a.k, (size_t)bh * DK + col);
+  float d = a.d_t[bh];
+  float bsc = 1.f;
+  if constexpr (PRO) {
+    d = softplus_f(d);
+    if (a.pro.b_scale) bsc = a.pro.b_scale[h];
+    if (a.pro.qk_norm) {  // the LPR lanes of a row hold the whole q and k of the head
+      float sq = q4.x * q4.x + q4.y * q4.y + q4.z * q4.z + q4.w * q4.w;
+      float sk = k4.x * k4.x + k4.y * k4.y + k4.z * k4.z + k4.w * k4.w;
+#pragma unroll
+      for (int m = 1; m < LPR; m <<= 1) {
+        sq += __shfl_xor_sync(0xffffffffu, sq, m);
+        sk += __shfl_xor_sync(0xffffffffu, sk, m);
+      }
+      const float iq = rsqrtf(fmaxf(sq, kNormFloorSq)), ik = rsqrtf(fmaxf(sk, kNormFloorSq));
+      q4 = make_float4(q4.x * iq, q4.y * iq, q4.z * iq, q4.w * iq);
+      k4 = make_float4(k4.x * ik, k4.y * ik, k4.z * ik, k4.w * ik);
+    }
+  }
   const float A_h = a.A[h], Ip = a.I_prior[h];
   bool bad = !(pos_finite(A_h) && pos_finite(Ip) && nonneg_finite(d));
   const float x = -A_h * d;
@@ -89,8 +110,10 @@ palimpsa_step_kernel(StepArgs a) {
   for (int it = 0; it < NIT; ++it) {
     const long row = row_base + it * RPI + sub;
     const size_t in_off = (size_t)bh * a.d_v + i_base + it * RPI + sub;
-    const float b = load1<BF16>(a.beta, in_off);
-    const float bv = b * load1<BF16>(a.v, in_off);
+    float b = load1<BF16>(a.beta, in_off);
+    const float vi = load1<BF16>(a.v, in_off);
+    if constexpr (PRO) b = bsc * sigmoid_f(b);
+    const float bv = (PRO && a.pro.v_star) ? vi : b * vi;
     bad |= !nonneg_finite(b);
     float Io[4] = {I4[it].x, I4[it].y, I4[it].z, I4[it].w};
     float mo[4] = {mu4[it].x, mu4[it].y, mu4[it].z, mu4[it].w};
@@ -119,12 +142,21 @@ cudaError_t launch_step(const StepArgs& a, cudaStream_t s) {
   const long rows = (long)a.B * a.H * a.d_v;
   const long rows_per_block = (long)kWarpsPerBlock * kRowsPerWarp;
   const unsigned blocks = (unsigned)((rows + rows_per_block - 1) / rows_per_block);
-  if (a.d_k == 128) {
-    if (a.bf16) palimpsa_step_kernel<128, true><<<blocks, kWarpsPerBlock * 32, 0, s>>>(a);
-    else palimpsa_step_kernel<128, false><<<blocks, kWarpsPerBlock * 32, 0, s>>>(a);
+  const dim3 g(blocks), b(kWarpsPerBlock * 32);
+  if (a.pro.on) {
+    if (a.d_k == 128) {
+      if (a.bf16) palimpsa_step_kernel<128, true, true><<<g, b, 0, s>>>(a);
+      else palimpsa_step_kernel<128, false, true><<<g, b, 0, s>>>(a);
+    } else {
+      if (a.bf16) palimpsa_step_kernel<64, true, true><<<g, b, 0, s>>>(a);
+      else palimpsa_step_kernel<64, false, true><<<g, b, 0, s>>>(a);
+    }
+  } else if (a.d_k == 128) {
+    if (a.bf16) palimpsa_step_kernel<128, true, false><<<g, b, 0, s>>>(a);
+    else palimpsa_step_kernel<128, false, false><<<g, b, 0, s>>>(a);
   } else {
-    if (a.bf16) palimpsa_step_kernel<64, true><<<blocks, kWarpsPerBlock * 32, 0, s>>>(a);
-    else palimpsa_step_kernel<64, false><<<blocks, kWarpsPerBlock * 32, 0, s>>>(a);
+    if (a.bf16) palimpsa_step_kernel<64, true, false><<<g, b, 0, s>>>(a);
+    else palimpsa_step_kernel<64, false, false><<<g, b, 0, s>>>(a);
   }
   return cudaGetLastError();
 }

@@ -15,6 +15,12 @@ A, key pool, d_t, q, k, v, beta from one torch Generator seeded per workload):
 * d_t = softplus(N(m, s)) per head-token (alpha = exp(-A d_t), slide 5).
 * A = 0.5 for ``tiny``, else U(0.1, 1) per head; I_prior = 1 per head;
   mu0 = 0 and I0 = I_prior.
+
+``raw=True`` returns the same draws before any activation, for the fused
+prologue: q and k as drawn (pooled keys with their jitter, not renormalised),
+beta_raw ~ N(0, 1), d_raw ~ N(m, s), v as drawn (read as v* in the v* mode),
+plus a per-head b_scale ~ U(0.1, 1) (slide 11's fine-tuning range) drawn after
+everything else, so the other tensors equal the activated recipe's draws.
 """
 from __future__ import annotations
 
@@ -75,28 +81,31 @@ def _unit(x):
     return x / torch.linalg.vector_norm(x, dim=-1, keepdim=True)
 
 
-def _draw(wl: Workload, lead: tuple, H: int, g, device, pool=None):
-    """Draw q, k, v, beta, d_t with leading shape `lead` (ending in H)."""
+def _draw(wl: Workload, lead: tuple, H: int, g, device, pool=None, raw=False):
+    """Draw q, k, v, beta, d_t with leading shape `lead` (ending in H); with
+    `raw`, the pre-activation values (q, k, v, beta_raw, d_raw)."""
     dk, dv = wl.d_k, wl.d_v
     f32 = torch.float32
-    d_t = F.softplus(wl.dt_mean + wl.dt_std * torch.randn(lead, generator=g, device=device, dtype=f32))
-    q = _unit(torch.randn(lead + (dk,), generator=g, device=device, dtype=f32))
+    act = (lambda f, x: x) if raw else (lambda f, x: f(x))
+    d_t = act(F.softplus, wl.dt_mean + wl.dt_std * torch.randn(lead, generator=g, device=device, dtype=f32))
+    q = act(_unit, torch.randn(lead + (dk,), generator=g, device=device, dtype=f32))
     if wl.key_pool:
         idx = torch.randint(0, wl.key_pool, lead, generator=g, device=device)
         eps = torch.randn(lead + (dk,), generator=g, device=device, dtype=f32) * (wl.key_jitter / dk ** 0.5)
-        k = _unit(pool[idx] + eps)
+        k = act(_unit, pool[idx] + eps)
     else:
-        k = _unit(torch.randn(lead + (dk,), generator=g, device=device, dtype=f32))
+        k = act(_unit, torch.randn(lead + (dk,), generator=g, device=device, dtype=f32))
     v = torch.randn(lead + (dv,), generator=g, device=device, dtype=f32)
-    beta = torch.sigmoid(torch.randn(lead + (dv,), generator=g, device=device, dtype=f32))
+    beta = act(torch.sigmoid, torch.randn(lead + (dv,), generator=g, device=device, dtype=f32))
     if wl.bf16:
         q, k, v, beta = (x.to(torch.bfloat16) for x in (q, k, v, beta))
     return q, k, v, beta, d_t
 
 
-def sequence_inputs(wl: Workload, *, B=None, H=None, T=None, device="cpu", seed=None):
+def sequence_inputs(wl: Workload, *, B=None, H=None, T=None, device="cpu", seed=None, raw=False):
     """Inputs of one scan: q, k [B,H,T,d_k]; v, beta [B,H,T,d_v]; d_t [B,H,T];
-    A, I_prior [H]. Returns a dict of contiguous tensors on `device`."""
+    A, I_prior [H]. Returns a dict of contiguous tensors on `device`. With
+    `raw`, the keys are q, k, v, beta_raw, d_raw, A, I_prior, b_scale."""
     B = wl.B if B is None else B
     H = wl.H if H is None else H
     T = wl.T if T is None else T
@@ -109,22 +118,28 @@ def sequence_inputs(wl: Workload, *, B=None, H=None, T=None, device="cpu", seed=
     pool = None
     if wl.key_pool:
         pool = _unit(torch.randn((wl.key_pool, wl.d_k), generator=g, device=device, dtype=f32))
-    q, k, v, beta, d_t = _draw(wl, (B, H, T), H, g, device, pool)
+    q, k, v, beta, d_t = _draw(wl, (B, H, T), H, g, device, pool, raw)
     I_prior = torch.ones((H,), dtype=f32, device=device)
+    if raw:
+        b_scale = 0.1 + 0.9 * torch.rand((H,), generator=g, device=device, dtype=f32)
+        return {"q": q.contiguous(), "k": k.contiguous(), "v": v.contiguous(), "beta_raw": beta.contiguous(),
+                "d_raw": d_t.contiguous(), "A": A, "I_prior": I_prior, "b_scale": b_scale}
     return {"q": q.contiguous(), "k": k.contiguous(), "v": v.contiguous(), "beta": beta.contiguous(),
             "d_t": d_t.contiguous(), "A": A, "I_prior": I_prior}
 
 
-def decode_inputs(wl: Workload, steps: int, *, B=None, H=None, device="cpu", seed=None):
+def decode_inputs(wl: Workload, steps: int, *, B=None, H=None, device="cpu", seed=None, raw=False):
     """Per-step decode inputs stacked over steps: q, k [S,B,H,d_k]; v, beta
     [S,B,H,d_v]; d_t [S,B,H] (the same statistics as the scan). A and I_prior
-    are those of the prefill (same seed), so pass ``sequence_inputs``' A."""
+    are those of the prefill (same seed), so pass ``sequence_inputs``' A.
+    With `raw`: q, k, v, beta_raw, d_raw before activation."""
     B = wl.B if B is None else B
     H = wl.H if H is None else H
     g = _gen(device, (wl.seed if seed is None else seed) * 7919 + 1)
-    q, k, v, beta, d_t = _draw(wl, (steps, B, H), H, g, device)
-    return {"q": q.contiguous(), "k": k.contiguous(), "v": v.contiguous(), "beta": beta.contiguous(),
-            "d_t": d_t.contiguous()}
+    q, k, v, beta, d_t = _draw(wl, (steps, B, H), H, g, device, raw=raw)
+    names = ("beta_raw", "d_raw") if raw else ("beta", "d_t")
+    return {"q": q.contiguous(), "k": k.contiguous(), "v": v.contiguous(), names[0]: beta.contiguous(),
+            names[1]: d_t.contiguous()}
 
 
 def as_float64_numpy(t: torch.Tensor):

@@ -148,3 +148,42 @@ def test_both_forward_entry_points_validate_alike(lib, entry, over, code):
     assert fn(args["q"], args["k"], args["v"], args["beta"], args["d_t"], args["A"], args["I_prior"], args["mu0"],
               args["I0"], args["y"], args["mu_T"], args["I_T"], args["B"], args["H"], args["T"], args["d_k"],
               args["d_v"], args["chunk"], args["dtype"], None) == code
+
+
+def _fused(lib, **over):
+    args = dict(q=P, k=P, v=P, b=P, d=P, A=P, I_prior=P, b_scale=None, mu0=None, I0=None, y=P, mu_T=P, I_T=P,
+                B=1, H=2, T=16, d_k=128, d_v=64, chunk=0, flags=3, dtype=1)
+    args.update(over)
+    return lib.palimpsa_forward_fused(
+        args["q"], args["k"], args["v"], args["b"], args["d"], args["A"], args["I_prior"], args["b_scale"],
+        args["mu0"], args["I0"], args["y"], args["mu_T"], args["I_T"], args["B"], args["H"], args["T"],
+        args["d_k"], args["d_v"], args["chunk"], args["flags"], args["dtype"], None)
+
+
+def _step_fused(lib, **over):
+    args = dict(q=P, k=P, v=P, b=P, d=P, A=P, I_prior=P, b_scale=None, mu=P, I=P, y=P, B=4, H=2, d_k=128, d_v=64,
+                flags=1, dtype=1)
+    args.update(over)
+    return lib.palimpsa_step_fused(args["q"], args["k"], args["v"], args["b"], args["d"], args["A"],
+                                   args["I_prior"], args["b_scale"], args["mu"], args["I"], args["y"], args["B"],
+                                   args["H"], args["d_k"], args["d_v"], args["flags"], args["dtype"], None)
+
+
+@pytest.mark.parametrize("over,code", [
+    (dict(flags=4), ERR_UNSUPPORTED), (dict(flags=0x80000000), ERR_UNSUPPORTED),
+    (dict(b_scale=P + 2), ERR_ALIGN), (dict(q=None), ERR_NULL), (dict(d=None), ERR_NULL),
+    (dict(I_T=None), ERR_NULL), (dict(dtype=5), ERR_DTYPE), (dict(T=-1), ERR_SHAPE),
+    (dict(d_k=96), ERR_UNSUPPORTED), (dict(chunk=24), ERR_UNSUPPORTED), (dict(v=P + 8), ERR_ALIGN),
+    (dict(d=P + 1), ERR_ALIGN),
+])
+def test_forward_fused_rejects_bad_arguments(lib, over, code):
+    assert _fused(lib, **over) == code
+
+
+@pytest.mark.parametrize("over,code", [
+    (dict(flags=8), ERR_UNSUPPORTED), (dict(b_scale=P + 1), ERR_ALIGN), (dict(b=None), ERR_NULL),
+    (dict(mu=None), ERR_NULL), (dict(dtype=-2), ERR_DTYPE), (dict(B=0), ERR_SHAPE), (dict(d_v=20), ERR_UNSUPPORTED),
+    (dict(I=P + 4), ERR_ALIGN),
+])
+def test_step_fused_rejects_bad_arguments(lib, over, code):
+    assert _step_fused(lib, **over) == code
