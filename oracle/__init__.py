@@ -12,6 +12,7 @@ Contents:
   (OpenMP over independent value rows only), loaded here through ctypes.
 * ``prologue`` — the fused layer prologue in fp64: per-token L2 norm of q and
   k, d_t = softplus(raw), beta = b_scale * sigmoid(raw), and the v* input.
+* ``varlen`` — packed variable-length batches: one ``forward`` per sequence.
 * ``reference_np`` — independent NumPy statements: the mean/precision form, the
   chunked natural-parameter form and the full-Gaussian posterior it
   approximates.

@@ -1,0 +1,84 @@
+"""Pins for the oracle's packed variable-length forward (``oracle/varlen.py``).
+
+Source: Bonnet et al., "Learning to Remember, Learn, and Forget in
+Attention-Based Models" — slide 7 / Eq. (5) per sequence, slide 9 (the state
+carried along one sequence). Each pin ties the packed layout to the dense,
+already pinned oracle in a way a wrong offset, a swapped state index or a
+leaked state between sequences would break."""
+import numpy as np
+
+import oracle
+from oracle import varlen as ovl
+
+
+def _packed(rng, H, lengths, dk, dv, gap=0):
+    total = sum(lengths) + gap
+    q = rng.standard_normal((H, total, dk))
+    k = rng.standard_normal((H, total, dk))
+    q /= np.linalg.norm(q, axis=-1, keepdims=True)
+    k /= np.linalg.norm(k, axis=-1, keepdims=True)
+    v = rng.standard_normal((H, total, dv))
+    beta = 1.0 / (1.0 + np.exp(-rng.standard_normal((H, total, dv))))
+    d_t = np.log1p(np.exp(rng.standard_normal((H, total))))
+    A = rng.uniform(0.1, 1.0, H)
+    Ip = rng.uniform(0.5, 2.0, H)
+    cu = np.concatenate([[0], np.cumsum(lengths)]).astype(np.int64)
+    return q, k, v, beta, d_t, A, Ip, cu
+
+
+def test_equal_lengths_equal_the_dense_batch():
+    rng = np.random.default_rng(1)
+    B, H, T, dk, dv = 3, 2, 17, 6, 4
+    q, k, v, beta, d_t, A, Ip, cu = _packed(rng, H, [T] * B, dk, dv)
+    y, muT, IT = ovl.forward(q, k, v, beta, d_t, A, Ip, cu)
+    dense = lambda x: x.reshape((H, B, T) + x.shape[2:]).swapaxes(0, 1)   # [H, B*T, .] -> [B, H, T, .]
+    yd, mud, Id = oracle.forward(dense(q), dense(k), dense(v), dense(beta), dense(d_t), A, Ip)
+    np.testing.assert_array_equal(dense(y), yd)
+    np.testing.assert_array_equal(muT, mud)
+    np.testing.assert_array_equal(IT, Id)
+
+
+def test_state_handed_across_sequences_equals_one_long_run():
+    rng = np.random.default_rng(2)
+    H, dk, dv = 2, 5, 3
+    lengths = [9, 1, 30, 14]
+    q, k, v, beta, d_t, A, Ip, cu = _packed(rng, H, lengths, dk, dv)
+    y_long, mu_long, I_long = oracle.forward(q[None], k[None], v[None], beta[None], d_t[None], A, Ip)
+    mu0 = np.zeros((1, H, dv, dk))
+    I0 = np.broadcast_to(Ip[None, :, None, None], (1, H, dv, dk)).copy()
+    for n in range(len(lengths)):
+        y, mu, I = ovl.forward(q, k, v, beta, d_t, A, Ip, cu[n:n + 2], mu0=mu0, I0=I0)
+        s0, s1 = cu[n], cu[n + 1]
+        np.testing.assert_allclose(y[:, s0:s1], y_long[0, :, s0:s1], rtol=1e-12, atol=1e-14)
+        mu0, I0 = mu, I
+    np.testing.assert_allclose(mu0[0], mu_long[0], rtol=1e-12, atol=1e-14)
+    np.testing.assert_allclose(I0[0], I_long[0], rtol=1e-12)
+
+
+def test_empty_sequences_and_unused_tokens():
+    rng = np.random.default_rng(3)
+    H, dk, dv = 2, 4, 3
+    lengths = [0, 12, 0, 5]
+    q, k, v, beta, d_t, A, Ip, cu = _packed(rng, H, lengths, dk, dv, gap=6)
+    N = len(lengths)
+    mu0 = rng.standard_normal((N, H, dv, dk))
+    I0 = rng.uniform(0.5, 3.0, (N, H, dv, dk))
+    y, muT, IT = ovl.forward(q, k, v, beta, d_t, A, Ip, cu, mu0=mu0, I0=I0)
+    for n in (0, 2):
+        np.testing.assert_array_equal(muT[n], mu0[n])
+        np.testing.assert_array_equal(IT[n], I0[n])
+    assert np.all(y[:, cu[-1]:] == 0.0)
+    # the unused tail is never read
+    q2, k2 = q.copy(), k.copy()
+    q2[:, cu[-1]:] = np.nan
+    k2[:, cu[-1]:] = np.nan
+    y2, mu2, I2 = ovl.forward(q2, k2, v, beta, d_t, A, Ip, cu, mu0=mu0, I0=I0)
+    np.testing.assert_array_equal(y2[:, :cu[-1]], y[:, :cu[-1]])
+    np.testing.assert_array_equal(mu2, muT)
+    # a sequence does not see its neighbours: perturbing sequence 3 leaves sequence 1 alone
+    v3 = v.copy()
+    v3[:, cu[3]:cu[4]] += 1.0
+    y3, mu3, _ = ovl.forward(q, k, v3, beta, d_t, A, Ip, cu, mu0=mu0, I0=I0)
+    np.testing.assert_array_equal(y3[:, cu[1]:cu[2]], y[:, cu[1]:cu[2]])
+    np.testing.assert_array_equal(mu3[1], muT[1])
+    assert not np.allclose(mu3[3], muT[3])
