@@ -160,6 +160,46 @@ palimpsa_status palimpsa_forward_chunked_noalloc(
     palimpsa_dtype in_dtype, void* cuda_stream);
 
 /*
+ * palimpsa_forward_varlen — palimpsa_forward_chunked over a packed batch of N
+ * independent sequences of different lengths (each with its own initial and
+ * final state), without padding. Each sequence runs the recurrence from its
+ * own initial state (slide 7 / Eq. (5), carried along the sequence as in
+ * slide 9), exactly as if it were the only one.
+ *
+ * Layout: the dense layout with B = 1 and the sequences concatenated along T.
+ *   q, k      [H, total_T, d_k] in_dtype
+ *   v, beta   [H, total_T, d_v] in_dtype, beta >= 0
+ *   d_t       [H, total_T]      fp32, >= 0
+ *   y         [H, total_T, d_v] fp32; rows of tokens outside every sequence
+ *             are not written
+ *   cu_seqlens [N + 1] int32 in DEVICE memory: sequence n is tokens
+ *             [cu_seqlens[n], cu_seqlens[n+1]) of every head; the offsets must
+ *             be non-decreasing, within [0, total_T], and no sequence longer
+ *             than max_seqlen (empty sequences are allowed and pass their state
+ *             through)
+ *   max_seqlen the longest sequence's length (host value, used to plan the
+ *             launch; a tighter value is faster, a smaller one is an error)
+ *   mu0, I0   [N, H, d_v, d_k] fp32 or NULL (defaults as for the forward)
+ *   mu_T, I_T [N, H, d_v, d_k] fp32
+ *   A, I_prior, d_k, d_v, chunk, in_dtype, cuda_stream as for the forward.
+ *
+ * The offsets live on the device, so the host cannot check them: every CTA
+ * checks its own sequence's offsets before it reads anything, and a sequence
+ * whose offsets break the rules above is skipped (its outputs are left as
+ * they were) and latches PALIMPSA_ERR_DOMAIN in the device status. Long
+ * sequences are cut into segments as in palimpsa_forward_chunked, planned
+ * from max_seqlen, with scratch for 2 * d_v * d_k + 1 floats per sequence,
+ * head and segment boundary.
+ */
+palimpsa_status palimpsa_forward_varlen(
+    const void* q, const void* k, const void* v, const void* beta,
+    const float* d_t, const float* A, const float* I_prior,
+    const float* mu0, const float* I0,
+    float* y, float* mu_T, float* I_T,
+    const int* cu_seqlens, int N, int H, int total_T, int max_seqlen,
+    int d_k, int d_v, int chunk, palimpsa_dtype in_dtype, void* cuda_stream);
+
+/*
  * palimpsa_step — one recurrent (decode) token for B x H heads, in place.
  *
  * The recurrent inference update of slide 22 / paper App. A.13 (Fig. 7):

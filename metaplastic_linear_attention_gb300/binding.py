@@ -74,6 +74,9 @@ def load_library(path: str | None = None):
         lib.palimpsa_forward_fused.restype = i
         lib.palimpsa_forward_fused.argtypes = [vp, vp, vp, vp, fp, fp, fp, fp, fp, fp, fp, fp, fp,
                                                i, i, i, i, i, i, u, i, vp]
+        lib.palimpsa_forward_varlen.restype = i
+        lib.palimpsa_forward_varlen.argtypes = [vp, vp, vp, vp, fp, fp, fp, fp, fp, fp, fp, fp, vp,
+                                                i, i, i, i, i, i, i, i, vp]
         lib.palimpsa_step_fused.restype = i
         lib.palimpsa_step_fused.argtypes = [vp, vp, vp, vp, fp, fp, fp, fp, fp, fp, fp, i, i, i, i, u, i, vp]
         lib.palimpsa_step.restype = i
@@ -233,6 +236,56 @@ def _forward_outputs(B, H, T, d_k, d_v, dev, y, mu_T, I_T):
 
 def _fuse_flags(qk_norm, v_star):
     return (PALIMPSA_FUSE_QK_NORM if qk_norm else 0) | (PALIMPSA_FUSE_V_STAR if v_star else 0)
+
+
+def palimpsa_forward_varlen(q, k, v, beta, d_t, A, I_prior, cu_seqlens, mu0=None, I0=None, *, max_seqlen=None,
+                            y=None, mu_T=None, I_T=None, chunk: int = 0, stream=None):
+    """The forward over a packed batch of N sequences (see palimpsa.h).
+
+    q, k [H, total_T, d_k] and v, beta [H, total_T, d_v] (one dtype), d_t
+    [H, total_T] fp32; cu_seqlens [N + 1] int32 (sequence n = tokens
+    [cu[n], cu[n+1])), on the device or the host (then copied); mu0, I0 [N, H,
+    d_v, d_k] or None. max_seqlen: the longest sequence (read from cu_seqlens
+    when not given, which synchronises). Device tensors otherwise. Returns
+    (y [H, total_T, d_v], mu_T [N, H, d_v, d_k], I_T)."""
+    if q.device.type != "cuda":
+        raise ValueError("palimpsa_forward_varlen takes device tensors")
+    H, total_T, d_k = q.shape
+    d_v = v.shape[-1]
+    dev = q.device
+    f32 = torch.float32
+    if cu_seqlens.dtype != torch.int32 or cu_seqlens.dim() != 1 or cu_seqlens.numel() < 2:
+        raise ValueError("cu_seqlens must be a 1-D int32 tensor of N + 1 offsets")
+    N = cu_seqlens.numel() - 1
+    if max_seqlen is None:
+        host = cu_seqlens.cpu()
+        max_seqlen = int((host[1:] - host[:-1]).max())
+    cu_d = cu_seqlens if cu_seqlens.is_cuda else cu_seqlens.to(dev)
+    _check(cu_d, "cu_seqlens", (N + 1,), torch.int32, dev)
+    _check(k, "k", q.shape, q.dtype, dev)
+    _check(q, "q", q.shape, None, dev)
+    _check(v, "v", (H, total_T, d_v), q.dtype, dev)
+    _check(beta, "beta", (H, total_T, d_v), q.dtype, dev)
+    _check(d_t, "d_t", (H, total_T), f32, dev)
+    _check(A, "A", (H,), f32, dev)
+    _check(I_prior, "I_prior", (H,), f32, dev)
+    _check(mu0, "mu0", (N, H, d_v, d_k), f32, dev)
+    _check(I0, "I0", (N, H, d_v, d_k), f32, dev)
+    y = torch.zeros((H, total_T, d_v), dtype=f32, device=dev) if y is None else y
+    mu_T = torch.empty((N, H, d_v, d_k), dtype=f32, device=dev) if mu_T is None else mu_T
+    I_T = torch.empty((N, H, d_v, d_k), dtype=f32, device=dev) if I_T is None else I_T
+    _check(y, "y", (H, total_T, d_v), f32, dev)
+    _check(mu_T, "mu_T", (N, H, d_v, d_k), f32, dev)
+    _check(I_T, "I_T", (N, H, d_v, d_k), f32, dev)
+    lib = load_library()
+    with torch.cuda.device(dev):
+        rc = lib.palimpsa_forward_varlen(
+            _ptr(q), _ptr(k), _ptr(v), _ptr(beta), _ptr(d_t), _ptr(A), _ptr(I_prior), _ptr(mu0), _ptr(I0), _ptr(y),
+            _ptr(mu_T), _ptr(I_T), _ptr(cu_d), N, H, total_T, int(max_seqlen), d_k, d_v, int(chunk), _in_dtype(q),
+            ctypes.c_void_p(_stream_handle(stream)))
+    if rc != 0:
+        raise PalimpsaError(rc, "palimpsa_forward_varlen")
+    return y, mu_T, I_T
 
 
 def palimpsa_forward_fused(q, k, v, beta_raw, d_raw, A, I_prior, b_scale=None, mu0=None, I0=None, *,

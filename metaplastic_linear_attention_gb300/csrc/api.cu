@@ -177,6 +177,37 @@ palimpsa_status palimpsa_forward_chunked(const void* q, const void* k, const voi
                       cuda_stream, Prologue{});
 }
 
+palimpsa_status palimpsa_forward_varlen(const void* q, const void* k, const void* v, const void* beta,
+                                        const float* d_t, const float* A, const float* I_prior, const float* mu0,
+                                        const float* I0, float* y, float* mu_T, float* I_T, const int* cu_seqlens,
+                                        int N, int H, int total_T, int max_seqlen, int d_k, int d_v, int chunk,
+                                        palimpsa_dtype in_dtype, void* cuda_stream) {
+  if (!A || !I_prior || !mu_T || !I_T || !cu_seqlens) return PALIMPSA_ERR_NULL;
+  if (total_T != 0 && (!q || !k || !v || !beta || !d_t || !y)) return PALIMPSA_ERR_NULL;
+  if (in_dtype != PALIMPSA_F32 && in_dtype != PALIMPSA_BF16) return PALIMPSA_ERR_DTYPE;
+  if (total_T < 0 || max_seqlen < 0 || max_seqlen > total_T) return PALIMPSA_ERR_SHAPE;
+  if (!sizes_ok(N, H, max_seqlen, d_k, d_v) || !sizes_ok(1, H, total_T, d_k, d_v)) return PALIMPSA_ERR_SHAPE;
+  if (!supported_dims(d_k, d_v)) return PALIMPSA_ERR_UNSUPPORTED;
+  if (chunk != 0 && chunk != 16 && chunk != 32 && chunk != 64) return PALIMPSA_ERR_UNSUPPORTED;
+  const void* a16[] = {q, k, v, beta, y, mu_T, I_T, mu0, I0};
+  for (const void* p : a16)
+    if (p && !aligned(p, 16)) return PALIMPSA_ERR_ALIGN;
+  const void* a4[] = {d_t, A, I_prior, cu_seqlens};
+  for (const void* p : a4)
+    if (p && !aligned(p, 4)) return PALIMPSA_ERR_ALIGN;
+  unsigned int* st = nullptr;
+  if (palimpsa_status s = status_word(&st)) return s;
+  FwdArgs a{q, k, v, beta, d_t, A, I_prior, mu0, I0, y, mu_T, I_T, N, H, max_seqlen, d_k, d_v,
+            chunk == 0 ? 32 : chunk, in_dtype == PALIMPSA_BF16, st,
+            g_wait_timeout_ns.load(), g_withhold_first_copy.load(), g_forward_segments.load(), Prologue{}};
+  a.cu_seqlens = cu_seqlens;
+  a.total_T = total_T;
+  StreamOrderedScratch scratch;
+  if (launch_forward_chunked(a, static_cast<cudaStream_t>(cuda_stream), &scratch) != cudaSuccess)
+    return PALIMPSA_ERR_CUDA;
+  return PALIMPSA_OK;
+}
+
 palimpsa_status palimpsa_forward_fused(const void* q, const void* k, const void* v, const void* beta_raw,
                                        const float* d_raw, const float* A, const float* I_prior,
                                        const float* b_scale, const float* mu0, const float* I0, float* y,

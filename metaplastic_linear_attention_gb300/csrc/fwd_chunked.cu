@@ -61,8 +61,13 @@ palimpsa_fwd_chunked_kernel(FwdArgs a, int C, int nseg, int seg_len, const float
   constexpr int ES = BF16 ? 2 : 4;
   extern __shared__ __align__(128) unsigned char smem[];
 
-  const int DV = a.d_v, T = a.T;
+  const int DV = a.d_v;
   const Tile tl = tile_of(a, RG, nseg, seg_len);
+  if (tl.bad) {  // packed offsets out of order or range: touch nothing
+    if (threadIdx.x == 0) latch_status(a.status, kStatusDomain);
+    return;
+  }
+  if (tl.seg > tl.last_seg) return;  // past the end of a shorter packed sequence
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int cg = lane & (kLanesPerRow - 1);
   const int rt = lane >> 3;
@@ -82,7 +87,7 @@ palimpsa_fwd_chunked_kernel(FwdArgs a, int C, int nseg, int seg_len, const float
   const float bsc = a.pro.b_scale ? a.pro.b_scale[tl.h] : 1.f;
   bool domain_bad = !(pos_finite(A_h) && pos_finite(Ip));
 
-  const size_t head_tok = (size_t)tl.bh * T;
+  const size_t head_tok = tl.head_tok;
   ChunkPipe<DK, ES> pipe(L, smem, static_cast<const char*>(a.q) + head_tok * DK * ES,
                          static_cast<const char*>(a.k) + head_tok * DK * ES,
                          static_cast<const char*>(a.v) + head_tok * DV * ES,
@@ -202,8 +207,8 @@ palimpsa_fwd_chunked_kernel(FwdArgs a, int C, int nseg, int seg_len, const float
     // next conversion overwrites the operands)
   }
 
-  // ---- final state (last segment only): mu_T = M / I, I_T = I.
-  if (tl.seg == nseg - 1) {
+  // ---- final state (the sequence's last segment only): mu_T = M / I, I_T = I.
+  if (tl.seg == tl.last_seg) {
 #pragma unroll
     for (int r = 0; r < R; ++r) {
 #pragma unroll
@@ -211,7 +216,7 @@ palimpsa_fwd_chunked_kernel(FwdArgs a, int C, int nseg, int seg_len, const float
         const size_t off = state_base + (size_t)(lr0 + r) * DK + 32 * s + 4 * cg;
         const float2 i01 = Ist[r][2 * s], i23 = Ist[r][2 * s + 1];
         float4 m4;
-        if (T == 0) {  // pass the initial state through unchanged
+        if (tl.L == 0) {  // pass the initial state through unchanged
           m4 = a.mu0 ? *reinterpret_cast<const float4*>(a.mu0 + off) : make_float4(0.f, 0.f, 0.f, 0.f);
         } else {
           const float2 m01 = Mst[r][2 * s], m23 = Mst[r][2 * s + 1];
@@ -245,9 +250,11 @@ palimpsa_fwd_summary_kernel(FwdArgs a, int C, int nseg, int seg_len, float* __re
   constexpr int ES = BF16 ? 2 : 4;
   extern __shared__ __align__(128) unsigned char smem[];
 
-  const int DV = a.d_v, T = a.T;
-  // the grid covers segments 0 .. nseg - 2 only
+  const int DV = a.d_v;
+  // the grid covers segments 0 .. nseg - 2 only; a sequence needs the summaries
+  // of the segments before its last one (a bad packed sequence is reported by pass C)
   const Tile tl = tile_of(a, RG, nseg - 1, seg_len);
+  if (tl.bad || tl.seg >= tl.last_seg) return;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int cg = lane & (kLanesPerRow - 1);
   const int rt = lane >> 3;
@@ -263,7 +270,7 @@ palimpsa_fwd_summary_kernel(FwdArgs a, int C, int nseg, int seg_len, float* __re
 
   const float A_h = a.A[tl.h];
   const float bsc = a.pro.b_scale ? a.pro.b_scale[tl.h] : 1.f;
-  const size_t head_tok = (size_t)tl.bh * T;
+  const size_t head_tok = tl.head_tok;
   ChunkPipe<DK, ES> pipe(L, smem, static_cast<const char*>(a.q) + head_tok * DK * ES,
                          static_cast<const char*>(a.k) + head_tok * DK * ES,
                          static_cast<const char*>(a.v) + head_tok * DV * ES,
@@ -360,7 +367,7 @@ palimpsa_fwd_summary_kernel(FwdArgs a, int C, int nseg, int seg_len, float* __re
 //   (M, Ibar)_{s+1} = Gamma_s (M, Ibar)_s + summary_s,   s = 0 .. S-2,
 // leaving in slot s the state at the start of segment s + 1.
 __global__ void __launch_bounds__(256)
-palimpsa_fwd_carry_kernel(FwdArgs a, int nseg, float* __restrict__ seg_state,
+palimpsa_fwd_carry_kernel(FwdArgs a, int nseg, int seg_len, float* __restrict__ seg_state,
                           const float* __restrict__ seg_gamma) {
   const long per_head = (long)a.d_v * a.d_k / 4;  // float4 quads per array
   const long q = (long)blockIdx.x * blockDim.x + threadIdx.x;
@@ -368,6 +375,11 @@ palimpsa_fwd_carry_kernel(FwdArgs a, int nseg, float* __restrict__ seg_state,
   const long bh = q / per_head;
   const long e = (q % per_head) * 4;
   const int h = (int)(bh % a.H);
+  int L = 0;
+  size_t first_tok = 0;
+  if (!seq_extent(a, bh, &L, &first_tok)) return;  // reported by pass C
+  // boundaries this sequence uses: those before its last segment
+  const int nb = min(nseg - 1, L > 0 ? (L - 1) / seg_len : 0);
   const float Ip = a.I_prior[h];
   const size_t DVK = (size_t)a.d_v * a.d_k;
   const size_t off = (size_t)bh * DVK + e;
@@ -375,7 +387,7 @@ palimpsa_fwd_carry_kernel(FwdArgs a, int nseg, float* __restrict__ seg_state,
   const float4 u = a.mu0 ? *reinterpret_cast<const float4*>(a.mu0 + off) : make_float4(0.f, 0.f, 0.f, 0.f);
   float4 m = make_float4(i0.x * u.x, i0.y * u.y, i0.z * u.z, i0.w * u.w);
   float4 ib = make_float4(i0.x - Ip, i0.y - Ip, i0.z - Ip, i0.w - Ip);
-  for (int s = 0; s < nseg - 1; ++s) {
+  for (int s = 0; s < nb; ++s) {
     const float g = seg_gamma[(size_t)bh * (nseg - 1) + s];
     float* slot = seg_state + ((size_t)bh * (nseg - 1) + s) * 2 * DVK;
     const float4 dm = *reinterpret_cast<const float4*>(slot + e);
@@ -422,7 +434,8 @@ struct Kernels {
                                                                           seg_gamma);
       if ((e = cudaGetLastError()) != cudaSuccess) return e;
       const long quads = heads * a.d_v * a.d_k / 4;
-      palimpsa_fwd_carry_kernel<<<(unsigned)((quads + 255) / 256), 256, 0, s>>>(a, nseg, seg_state, seg_gamma);
+      palimpsa_fwd_carry_kernel<<<(unsigned)((quads + 255) / 256), 256, 0, s>>>(a, nseg, seg_len, seg_state,
+                                                                                 seg_gamma);
       if ((e = cudaGetLastError()) != cudaSuccess) return e;
     }
     main_k<<<(unsigned)(heads * nseg * groups), kThreads, sm, s>>>(a, C, nseg, seg_len, seg_state);

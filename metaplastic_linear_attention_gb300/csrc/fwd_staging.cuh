@@ -53,12 +53,35 @@ __device__ __forceinline__ void stage_chunk(unsigned char* base, const FwdSmem& 
   bulk_g2s(base + L.raw_b, gb + (size_t)t0 * DV * ES, bvb, bar);
 }
 
-// Where a CTA works: head bh, segment seg, rows [row0, row0 + RG), tokens
-// [tb, tb + tn) of that head.
+// Where a CTA works: head bh (sequence n = bh / H of a packed batch), segment
+// seg, rows [row0, row0 + RG), tokens [tb, tb + tn) of that sequence, whose
+// first token is head_tok in the token-major input arrays and whose length is
+// L; last_seg is the sequence's final segment. A packed sequence whose offsets
+// are out of order or out of range is `bad`: the CTA must touch nothing.
 struct Tile {
   long bh;
-  int h, seg, row0, tb, tn;
+  int h, seg, row0, tb, tn, L, last_seg;
+  size_t head_tok;
+  bool bad;
 };
+
+// Length and first token (in the token-major input arrays) of head bh's
+// sequence. Returns false, with L = 0, when packed offsets are out of order or
+// out of range; nothing of that sequence may then be touched.
+__device__ __forceinline__ bool seq_extent(const FwdArgs& a, long bh, int* L, size_t* head_tok) {
+  if (!a.cu_seqlens) {
+    *L = a.T;
+    *head_tok = (size_t)bh * a.T;
+    return true;
+  }
+  const long n = bh / a.H;
+  const int h = (int)(bh % a.H);
+  const int s0 = a.cu_seqlens[n], s1 = a.cu_seqlens[n + 1];
+  const bool ok = s0 >= 0 && s1 >= s0 && (long long)s1 <= a.total_T && s1 - s0 <= a.T;
+  *L = ok ? s1 - s0 : 0;
+  *head_tok = ok ? (size_t)h * (size_t)a.total_T + (size_t)s0 : 0;
+  return ok;
+}
 
 __device__ __forceinline__ Tile tile_of(const FwdArgs& a, int RG, int nseg, int seg_len) {
   const int groups = a.d_v / RG;
@@ -70,8 +93,10 @@ __device__ __forceinline__ Tile tile_of(const FwdArgs& a, int RG, int nseg, int 
   t.bh = rest / nseg;
   t.h = (int)(t.bh % a.H);
   t.row0 = rg * RG;
+  t.bad = !seq_extent(a, t.bh, &t.L, &t.head_tok);
   t.tb = t.seg * seg_len;
-  t.tn = max(0, min(a.T, t.tb + seg_len) - t.tb);
+  t.tn = max(0, min(t.L, t.tb + seg_len) - t.tb);
+  t.last_seg = t.L > 0 ? (t.L - 1) / seg_len : 0;
   return t;
 }
 

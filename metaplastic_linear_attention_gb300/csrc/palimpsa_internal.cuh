@@ -45,6 +45,11 @@ struct FwdArgs {
   int withhold_first_copy;
   int force_segments;  // 0: the library chooses the time split
   Prologue pro{};
+  // Packed variable-length batch (palimpsa_forward_varlen): B counts sequences,
+  // T is the longest sequence, and sequence n is tokens [cu[n], cu[n+1]) of each
+  // head's total_T tokens. NULL for the dense [B, H, T] layout.
+  const int* cu_seqlens = nullptr;
+  long long total_T = 0;
 };
 
 struct StepArgs {

@@ -145,3 +145,28 @@ def decode_inputs(wl: Workload, steps: int, *, B=None, H=None, device="cpu", see
 def as_float64_numpy(t: torch.Tensor):
     """Exact upcast of (possibly bf16-rounded) inputs for the fp64 oracle."""
     return t.detach().to("cpu").to(torch.float64).numpy()
+
+
+def varlen_lengths(total: int, n: int, seed: int):
+    """n sequence lengths summing to `total`: a seeded uniform mix, each at least 1
+    (requires n <= total). Only draws numbers; the packing is the caller's."""
+    g = torch.Generator().manual_seed(int(seed))
+    w = 0.05 + torch.rand((n,), generator=g, dtype=torch.float64)
+    raw = (w / w.sum() * (total - n)).floor().to(torch.int64) + 1
+    raw[-1] += total - int(raw.sum())
+    return [int(x) for x in raw]
+
+
+def packed_inputs(wl: Workload, lengths, *, H=None, device="cpu", seed=None):
+    """A packed variable-length batch with the workload's recipe: q, k
+    [H, total_T, d_k]; v, beta [H, total_T, d_v]; d_t [H, total_T]; A, I_prior
+    [H]; cu_seqlens [N + 1] int32 with sequence n = tokens [cu[n], cu[n+1])."""
+    H = wl.H if H is None else H
+    total = int(sum(lengths))
+    inp = sequence_inputs(wl, B=1, H=H, T=total, device=device, seed=seed)
+    out = {k: (v[0].contiguous() if v.dim() >= 3 else v) for k, v in inp.items()}
+    cu = [0]
+    for n in lengths:
+        cu.append(cu[-1] + int(n))
+    out["cu_seqlens"] = torch.tensor(cu, dtype=torch.int32, device=device)
+    return out

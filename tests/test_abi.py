@@ -187,3 +187,30 @@ def test_forward_fused_rejects_bad_arguments(lib, over, code):
 ])
 def test_step_fused_rejects_bad_arguments(lib, over, code):
     assert _step_fused(lib, **over) == code
+
+
+def _varlen(lib, **over):
+    args = dict(q=P, k=P, v=P, beta=P, d=P, A=P, I_prior=P, mu0=None, I0=None, y=P, mu_T=P, I_T=P, cu=P, N=3, H=2,
+                total_T=100, max_seqlen=50, d_k=128, d_v=64, chunk=0, dtype=1)
+    args.update(over)
+    return lib.palimpsa_forward_varlen(
+        args["q"], args["k"], args["v"], args["beta"], args["d"], args["A"], args["I_prior"], args["mu0"],
+        args["I0"], args["y"], args["mu_T"], args["I_T"], args["cu"], args["N"], args["H"], args["total_T"],
+        args["max_seqlen"], args["d_k"], args["d_v"], args["chunk"], args["dtype"], None)
+
+
+@pytest.mark.parametrize("over,code", [
+    (dict(cu=None), ERR_NULL), (dict(q=None), ERR_NULL), (dict(mu_T=None), ERR_NULL),
+    (dict(cu=P + 2), ERR_ALIGN), (dict(y=P + 8), ERR_ALIGN), (dict(N=0), ERR_SHAPE), (dict(H=0), ERR_SHAPE),
+    (dict(total_T=-1), ERR_SHAPE), (dict(max_seqlen=-1), ERR_SHAPE), (dict(max_seqlen=101), ERR_SHAPE),
+    (dict(dtype=9), ERR_DTYPE), (dict(d_v=4), ERR_UNSUPPORTED), (dict(chunk=8), ERR_UNSUPPORTED),
+])
+def test_forward_varlen_rejects_bad_arguments(lib, over, code):
+    assert _varlen(lib, **over) == code
+
+
+def test_forward_varlen_empty_tokens_need_no_token_arrays(lib):
+    # total_T = 0: every sequence is empty; the token arrays are not read and may be
+    # NULL, but the state arrays and offsets are still required
+    assert _varlen(lib, total_T=0, max_seqlen=0, q=None, k=None, v=None, beta=None, d=None, y=None,
+                   mu_T=None) == ERR_NULL

@@ -1,0 +1,126 @@
+"""GPU parity of the packed variable-length forward (palimpsa_forward_varlen)
+against the fp64 oracle, which runs each sequence on its own.
+
+Source: Bonnet et al., "Learning to Remember, Learn, and Forget in
+Attention-Based Models" — slide 7 / Eq. (5) per sequence, slide 9 (the state
+carried along a sequence, and across segments by the affine scan)."""
+import pytest
+import torch
+
+import metaplastic_linear_attention_gb300 as pal
+from metaplastic_linear_attention_gb300 import synthetic as syn
+from metaplastic_linear_attention_gb300.synthetic import as_float64_numpy as f64
+from oracle import varlen as ovl
+from tests._helpers import TIGHT, rel_l2
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda"
+
+
+def _inputs(lengths, H, dk, dv, bf16, seed):
+    wl = syn.WORKLOADS["small_layer"].with_(d_k=dk, d_v=dv, bf16=bf16, seed=seed)
+    return syn.packed_inputs(wl, lengths, H=H)
+
+
+def _oracle(inp, mu0=None, I0=None):
+    return ovl.forward(f64(inp["q"]), f64(inp["k"]), f64(inp["v"]), f64(inp["beta"]), f64(inp["d_t"]),
+                       f64(inp["A"]), f64(inp["I_prior"]), inp["cu_seqlens"].tolist(),
+                       mu0=None if mu0 is None else f64(mu0), I0=None if I0 is None else f64(I0))
+
+
+def _gpu(inp, mu0=None, I0=None, chunk=0, **kw):
+    g = {k: v.to(DEV) for k, v in inp.items()}
+    out = pal.palimpsa_forward_varlen(g["q"], g["k"], g["v"], g["beta"], g["d_t"], g["A"], g["I_prior"],
+                                      g["cu_seqlens"], None if mu0 is None else mu0.to(DEV),
+                                      None if I0 is None else I0.to(DEV), chunk=chunk, **kw)
+    assert pal.palimpsa_get_device_status() == 0
+    return out
+
+
+def _check(out, ref):
+    errs = [rel_l2(o.cpu().numpy(), r) for o, r in zip(out, ref)]
+    assert max(errs) <= TIGHT, errs
+
+
+CASES = [
+    # (lengths, H, d_k, d_v, bf16, chunk, segments)
+    ([1], 2, 128, 64, True, 16, 0),
+    ([5, 0, 17, 1, 64], 3, 128, 64, True, 32, 0),
+    ([130, 7, 0, 0, 61], 2, 64, 40, False, 16, 0),
+    ([300, 45, 1, 199], 2, 128, 64, True, 32, 3),   # forced time split on a ragged mix
+    ([0, 257, 96], 1, 64, 128, False, 16, 4),
+    ([700, 3], 2, 128, 256, False, 32, 0),
+]
+
+
+@pytest.mark.parametrize("lengths,H,dk,dv,bf16,chunk,S", CASES)
+def test_varlen_matches_oracle(lengths, H, dk, dv, bf16, chunk, S):
+    inp = _inputs(lengths, H, dk, dv, bf16, seed=len(lengths) * 31 + dk + dv)
+    ref = _oracle(inp)
+    pal.palimpsa_set_forward_segments(S)
+    try:
+        out = _gpu(inp, chunk=chunk)
+    finally:
+        pal.palimpsa_set_forward_segments(0)
+    _check(out, ref)
+
+
+@pytest.mark.parametrize("S", [1, 3])
+def test_varlen_initial_state_and_in_place(S):
+    lengths = [40, 0, 211, 9]
+    N, H, dk, dv = len(lengths), 2, 128, 64
+    inp = _inputs(lengths, H, dk, dv, True, seed=8)
+    g = torch.Generator().manual_seed(3)
+    mu0 = torch.randn((N, H, dv, dk), generator=g)
+    I0 = 0.5 + 3.0 * torch.rand((N, H, dv, dk), generator=g)
+    ref = _oracle(inp, mu0, I0)
+    gi = {k: v.to(DEV) for k, v in inp.items()}
+    mu, I = mu0.to(DEV), I0.to(DEV)
+    pal.palimpsa_set_forward_segments(S)
+    try:
+        y, _, _ = pal.palimpsa_forward_varlen(gi["q"], gi["k"], gi["v"], gi["beta"], gi["d_t"], gi["A"],
+                                              gi["I_prior"], gi["cu_seqlens"], mu, I, mu_T=mu, I_T=I)
+    finally:
+        pal.palimpsa_set_forward_segments(0)
+    assert pal.palimpsa_get_device_status() == 0
+    _check((y, mu, I), ref)
+
+
+def test_varlen_equal_lengths_equal_the_dense_forward_bitwise():
+    """Same plan, same kernels: N equal sequences give the dense batch's bits."""
+    N, H, T = 3, 2, 150
+    inp = _inputs([T] * N, H, 128, 64, True, seed=12)
+    yv, mv, Iv = _gpu(inp)
+    dense = lambda x: x.reshape((H, N, T) + x.shape[2:]).transpose(0, 1).contiguous()
+    g = {k: dense(inp[k]).to(DEV) for k in ("q", "k", "v", "beta", "d_t")}
+    yd, md, Id = pal.palimpsa_forward_chunked(g["q"], g["k"], g["v"], g["beta"], g["d_t"], inp["A"].to(DEV),
+                                              inp["I_prior"].to(DEV))
+    assert torch.equal(dense(yv.cpu()), yd.cpu())
+    assert torch.equal(mv, md) and torch.equal(Iv, Id)
+
+
+def test_varlen_long_and_short_mix_uses_the_time_split():
+    """A few heads, one long sequence and short ones: the planner splits time."""
+    lengths = [4000, 13, 250, 1]
+    inp = _inputs(lengths, 2, 128, 64, True, seed=21)
+    _check(_gpu(inp), _oracle(inp))
+
+
+def test_bad_offsets_are_reported_not_faulted():
+    """Offsets out of order, past total_T or longer than max_seqlen: the CTAs of
+    that sequence read nothing, the call latches a domain error, and the other
+    sequences and the context are unaffected."""
+    lengths = [20, 30, 10]
+    inp = _inputs(lengths, 2, 128, 64, True, seed=5)
+    ref = _oracle(inp)
+    g = {k: v.to(DEV) for k, v in inp.items()}
+    total = sum(lengths)
+    for cu in ([0, 20, 15, 60], [0, 20, 50, total + 40], [0, 20, 50, 60]):
+        cu_d = torch.tensor(cu, dtype=torch.int32, device=DEV)
+        y, mu, I = pal.palimpsa_forward_varlen(g["q"], g["k"], g["v"], g["beta"], g["d_t"], g["A"], g["I_prior"],
+                                               cu_d, max_seqlen=25)
+        assert pal.palimpsa_get_device_status() == 5  # PALIMPSA_ERR_DOMAIN
+        # sequence 0 ([0, 20), within max_seqlen) is still right
+        assert rel_l2(y[:, :20].cpu().numpy(), ref[0][:, :20]) <= TIGHT
+        assert rel_l2(mu[0].cpu().numpy(), ref[1][0]) <= TIGHT
+    _check(_gpu(inp), ref)
