@@ -200,6 +200,52 @@ palimpsa_status palimpsa_forward_varlen(
     int d_k, int d_v, int chunk, palimpsa_dtype in_dtype, void* cuda_stream);
 
 /*
+ * Time-sharded sequences (one exchange). Both natural-parameter recurrences are
+ * affine in the state with the shared scalar decay alpha (slide 9 / App.
+ * A.12), so a stretch of tokens acts on the state as
+ *     (M, Ibar) -> Gamma (M, Ibar) + (dM, dIbar),   M = I (.) mu, Ibar = I - I_prior,
+ * with Gamma the product of its alphas and (dM, dIbar) the state it produces
+ * from zero. When the T tokens of each sequence are split into R consecutive
+ * shards (one per GPU), shard r: (1) computes its summary with
+ * palimpsa_segment_summary, (2) gathers the summaries of all shards (the one
+ * exchange), (3) folds the summaries of shards 0 .. r-1 into the initial state
+ * with palimpsa_state_combine, and (4) runs palimpsa_forward_chunked on its
+ * own tokens from that state. The result equals the unsharded forward up to
+ * fp32 rounding.
+ *
+ * palimpsa_segment_summary — the summary of each head's T tokens.
+ *   q, k, v, beta, d_t, A, I_prior, B, H, T, d_k, d_v, chunk, in_dtype as for
+ *   palimpsa_forward_chunked (T = 0 gives Gamma = 1 and a zero summary).
+ *   summary  [B, H, 2, d_v, d_k] fp32 out: [..., 0, :, :] = dM, [..., 1, :, :] = dIbar
+ *   gamma    [B, H] fp32 out
+ * Long ranges are cut into segments as in the forward (scratch from the same
+ * pool: 2 * d_v * d_k + 1 floats per head and segment).
+ */
+palimpsa_status palimpsa_segment_summary(
+    const void* q, const void* k, const void* v, const void* beta,
+    const float* d_t, const float* A, const float* I_prior,
+    float* summary, float* gamma,
+    int B, int H, int T, int d_k, int d_v, int chunk,
+    palimpsa_dtype in_dtype, void* cuda_stream);
+
+/*
+ * palimpsa_state_combine — the state after R stretches, in order, from an
+ * initial state:
+ *   summaries [R, B, H, 2, d_v, d_k] fp32 (as written by palimpsa_segment_summary)
+ *   gammas    [R, B, H] fp32
+ *   I_prior   [H] fp32; mu0, I0 [B, H, d_v, d_k] fp32 or NULL (defaults as for
+ *             the forward)
+ *   mu_out, I_out [B, H, d_v, d_k] fp32: the state as (mu, I), ready to pass as
+ *             mu0 / I0 to palimpsa_forward_chunked. They may alias mu0 / I0.
+ * R = 0 copies the initial state. Summaries and gammas may be NULL when R = 0.
+ */
+palimpsa_status palimpsa_state_combine(
+    const float* summaries, const float* gammas, int R,
+    const float* I_prior, const float* mu0, const float* I0,
+    float* mu_out, float* I_out,
+    int B, int H, int d_k, int d_v, void* cuda_stream);
+
+/*
  * palimpsa_step — one recurrent (decode) token for B x H heads, in place.
  *
  * The recurrent inference update of slide 22 / paper App. A.13 (Fig. 7):

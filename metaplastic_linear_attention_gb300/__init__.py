@@ -26,8 +26,10 @@ from .binding import (  # noqa: F401
     palimpsa_forward_varlen,
     palimpsa_forward_without_meta,
     palimpsa_get_device_status,
+    palimpsa_segment_summary,
     palimpsa_set_forward_segments,
     palimpsa_set_wait_timeout_ns,
+    palimpsa_state_combine,
     palimpsa_status_string,
     palimpsa_step,
     palimpsa_step_fused,

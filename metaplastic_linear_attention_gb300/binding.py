@@ -77,6 +77,10 @@ def load_library(path: str | None = None):
         lib.palimpsa_forward_varlen.restype = i
         lib.palimpsa_forward_varlen.argtypes = [vp, vp, vp, vp, fp, fp, fp, fp, fp, fp, fp, fp, vp,
                                                 i, i, i, i, i, i, i, i, vp]
+        lib.palimpsa_segment_summary.restype = i
+        lib.palimpsa_segment_summary.argtypes = [vp, vp, vp, vp, fp, fp, fp, fp, fp, i, i, i, i, i, i, i, vp]
+        lib.palimpsa_state_combine.restype = i
+        lib.palimpsa_state_combine.argtypes = [fp, fp, i, fp, fp, fp, fp, fp, i, i, i, i, vp]
         lib.palimpsa_step_fused.restype = i
         lib.palimpsa_step_fused.argtypes = [vp, vp, vp, vp, fp, fp, fp, fp, fp, fp, fp, i, i, i, i, u, i, vp]
         lib.palimpsa_step.restype = i
@@ -286,6 +290,54 @@ def palimpsa_forward_varlen(q, k, v, beta, d_t, A, I_prior, cu_seqlens, mu0=None
     if rc != 0:
         raise PalimpsaError(rc, "palimpsa_forward_varlen")
     return y, mu_T, I_T
+
+
+def palimpsa_segment_summary(q, k, v, beta, d_t, A, I_prior, *, summary=None, gamma=None, chunk: int = 0,
+                             stream=None):
+    """Summary of each head's T tokens from a zero state (see palimpsa.h):
+    returns (summary [B,H,2,d_v,d_k] = (dM, dIbar), gamma [B,H] = prod alpha).
+    Device tensors laid out as for palimpsa_forward_chunked."""
+    B, H, T, d_k, d_v, dev = _check_forward_inputs(q, k, v, beta, d_t, A, I_prior, None, None, ("beta", "d_t"))
+    f32 = torch.float32
+    summary = torch.empty((B, H, 2, d_v, d_k), dtype=f32, device=dev) if summary is None else summary
+    gamma = torch.empty((B, H), dtype=f32, device=dev) if gamma is None else gamma
+    _check(summary, "summary", (B, H, 2, d_v, d_k), f32, dev)
+    _check(gamma, "gamma", (B, H), f32, dev)
+    lib = load_library()
+    with torch.cuda.device(dev):
+        rc = lib.palimpsa_segment_summary(_ptr(q), _ptr(k), _ptr(v), _ptr(beta), _ptr(d_t), _ptr(A), _ptr(I_prior),
+                                          _ptr(summary), _ptr(gamma), B, H, T, d_k, d_v, int(chunk), _in_dtype(q),
+                                          ctypes.c_void_p(_stream_handle(stream)))
+    if rc != 0:
+        raise PalimpsaError(rc, "palimpsa_segment_summary")
+    return summary, gamma
+
+
+def palimpsa_state_combine(summaries, gammas, I_prior, mu0=None, I0=None, *, mu_out=None, I_out=None, stream=None):
+    """The state after R stretches, in order, from (mu0, I0) (see palimpsa.h):
+    summaries [R,B,H,2,d_v,d_k], gammas [R,B,H] -> (mu [B,H,d_v,d_k], I)."""
+    R, B, H, _, d_v, d_k = summaries.shape
+    dev = summaries.device
+    f32 = torch.float32
+    if dev.type != "cuda":
+        raise ValueError("palimpsa_state_combine takes device tensors")
+    _check(summaries, "summaries", (R, B, H, 2, d_v, d_k), f32, dev)
+    _check(gammas, "gammas", (R, B, H), f32, dev)
+    _check(I_prior, "I_prior", (H,), f32, dev)
+    _check(mu0, "mu0", (B, H, d_v, d_k), f32, dev)
+    _check(I0, "I0", (B, H, d_v, d_k), f32, dev)
+    mu_out = torch.empty((B, H, d_v, d_k), dtype=f32, device=dev) if mu_out is None else mu_out
+    I_out = torch.empty((B, H, d_v, d_k), dtype=f32, device=dev) if I_out is None else I_out
+    _check(mu_out, "mu_out", (B, H, d_v, d_k), f32, dev)
+    _check(I_out, "I_out", (B, H, d_v, d_k), f32, dev)
+    lib = load_library()
+    with torch.cuda.device(dev):
+        rc = lib.palimpsa_state_combine(_ptr(summaries) if R else None, _ptr(gammas) if R else None, R,
+                                        _ptr(I_prior), _ptr(mu0), _ptr(I0), _ptr(mu_out), _ptr(I_out), B, H, d_k,
+                                        d_v, ctypes.c_void_p(_stream_handle(stream)))
+    if rc != 0:
+        raise PalimpsaError(rc, "palimpsa_state_combine")
+    return mu_out, I_out
 
 
 def palimpsa_forward_fused(q, k, v, beta_raw, d_raw, A, I_prior, b_scale=None, mu0=None, I0=None, *,

@@ -208,6 +208,53 @@ palimpsa_status palimpsa_forward_varlen(const void* q, const void* k, const void
   return PALIMPSA_OK;
 }
 
+palimpsa_status palimpsa_segment_summary(const void* q, const void* k, const void* v, const void* beta,
+                                         const float* d_t, const float* A, const float* I_prior, float* summary,
+                                         float* gamma, int B, int H, int T, int d_k, int d_v, int chunk,
+                                         palimpsa_dtype in_dtype, void* cuda_stream) {
+  if (!A || !I_prior || !summary || !gamma) return PALIMPSA_ERR_NULL;
+  if (T != 0 && (!q || !k || !v || !beta || !d_t)) return PALIMPSA_ERR_NULL;
+  if (in_dtype != PALIMPSA_F32 && in_dtype != PALIMPSA_BF16) return PALIMPSA_ERR_DTYPE;
+  if (!sizes_ok(B, H, T, d_k, d_v)) return PALIMPSA_ERR_SHAPE;
+  if (!supported_dims(d_k, d_v)) return PALIMPSA_ERR_UNSUPPORTED;
+  if (chunk != 0 && chunk != 16 && chunk != 32 && chunk != 64) return PALIMPSA_ERR_UNSUPPORTED;
+  const void* a16[] = {q, k, v, beta, summary};
+  for (const void* p : a16)
+    if (p && !aligned(p, 16)) return PALIMPSA_ERR_ALIGN;
+  const void* a4[] = {d_t, A, I_prior, gamma};
+  for (const void* p : a4)
+    if (p && !aligned(p, 4)) return PALIMPSA_ERR_ALIGN;
+  unsigned int* st = nullptr;
+  if (palimpsa_status s = status_word(&st)) return s;
+  FwdArgs a{q, k, v, beta, d_t, A, I_prior, nullptr, nullptr, nullptr, nullptr, nullptr, B, H, T, d_k, d_v,
+            chunk == 0 ? 32 : chunk, in_dtype == PALIMPSA_BF16, st,
+            g_wait_timeout_ns.load(), g_withhold_first_copy.load(), g_forward_segments.load(), Prologue{}};
+  StreamOrderedScratch scratch;
+  if (launch_segment_summary(a, summary, gamma, static_cast<cudaStream_t>(cuda_stream), &scratch) != cudaSuccess)
+    return PALIMPSA_ERR_CUDA;
+  return PALIMPSA_OK;
+}
+
+palimpsa_status palimpsa_state_combine(const float* summaries, const float* gammas, int R, const float* I_prior,
+                                       const float* mu0, const float* I0, float* mu_out, float* I_out, int B, int H,
+                                       int d_k, int d_v, void* cuda_stream) {
+  if (!I_prior || !mu_out || !I_out) return PALIMPSA_ERR_NULL;
+  if (R > 0 && (!summaries || !gammas)) return PALIMPSA_ERR_NULL;
+  if (R < 0 || !sizes_ok(B, H, R > 0 ? R : 1, d_k, d_v)) return PALIMPSA_ERR_SHAPE;
+  if (!supported_dims(d_k, d_v)) return PALIMPSA_ERR_UNSUPPORTED;
+  const void* a16[] = {summaries, mu0, I0, mu_out, I_out};
+  for (const void* p : a16)
+    if (p && !aligned(p, 16)) return PALIMPSA_ERR_ALIGN;
+  const void* a4[] = {gammas, I_prior};
+  for (const void* p : a4)
+    if (p && !aligned(p, 4)) return PALIMPSA_ERR_ALIGN;
+  const long long heads = (long long)B * H, DVK = (long long)d_v * d_k;
+  const FoldArgs f{summaries, gammas, heads * 2 * DVK, 2 * DVK, heads, 1, R, heads, H, (int)DVK, true, I_prior,
+                   mu0, I0, mu_out, I_out, nullptr, DVK};
+  if (launch_fold(f, static_cast<cudaStream_t>(cuda_stream)) != cudaSuccess) return PALIMPSA_ERR_CUDA;
+  return PALIMPSA_OK;
+}
+
 palimpsa_status palimpsa_forward_fused(const void* q, const void* k, const void* v, const void* beta_raw,
                                        const float* d_raw, const float* A, const float* I_prior,
                                        const float* b_scale, const float* mu0, const float* I0, float* y,

@@ -251,10 +251,11 @@ palimpsa_fwd_summary_kernel(FwdArgs a, int C, int nseg, int seg_len, float* __re
   extern __shared__ __align__(128) unsigned char smem[];
 
   const int DV = a.d_v;
-  // the grid covers segments 0 .. nseg - 2 only; a sequence needs the summaries
-  // of the segments before its last one (a bad packed sequence is reported by pass C)
+  // the grid covers segments 0 .. nseg - 2; a packed sequence needs only the
+  // summaries of the segments before its own last one (a bad packed sequence
+  // is reported by pass C)
   const Tile tl = tile_of(a, RG, nseg - 1, seg_len);
-  if (tl.bad || tl.seg >= tl.last_seg) return;
+  if (tl.bad || (a.cu_seqlens && tl.seg >= tl.last_seg)) return;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int cg = lane & (kLanesPerRow - 1);
   const int rt = lane >> 3;
@@ -441,6 +442,18 @@ struct Kernels {
     main_k<<<(unsigned)(heads * nseg * groups), kThreads, sm, s>>>(a, C, nseg, seg_len, seg_state);
     return cudaGetLastError();
   }
+
+  // Pass A over all `nseg` segments of every head (summary slots [bh][seg]).
+  static cudaError_t summaries(const FwdArgs& a, int C, int nseg, int seg_len, float* st, float* gm,
+                               cudaStream_t s) {
+    const size_t sm = smem(a, C);
+    auto sum_k = palimpsa_fwd_summary_kernel<DK, BF16, RG, kRowsPerThread>;
+    cudaError_t e = cudaFuncSetAttribute(sum_k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
+    if (e != cudaSuccess) return e;
+    const long units = (long)a.B * a.H * nseg * (a.d_v / RG);
+    sum_k<<<(unsigned)units, kThreads, sm, s>>>(a, C, nseg + 1, seg_len, st, gm);
+    return cudaGetLastError();
+  }
 };
 
 struct Plan {
@@ -492,7 +505,7 @@ void choose_segments(const FwdArgs& a, long units_per_seg, int slots, int C, Pla
 }
 
 template <int DK, bool BF16>
-cudaError_t plan_and_run(const FwdArgs& a, Plan p, cudaStream_t s, ScratchProvider* sp) {
+Plan plan_segments(const FwdArgs& a, Plan p) {
   int dev = 0, num_sms = 152;
   cudaGetDevice(&dev);
   cudaDeviceGetAttribute(&num_sms, cudaDevAttrMultiProcessorCount, dev);
@@ -512,6 +525,13 @@ cudaError_t plan_and_run(const FwdArgs& a, Plan p, cudaStream_t s, ScratchProvid
   } else {
     choose_segments(a, units, num_sms * per_sm, p.C, &p);
   }
+  return p;
+}
+
+template <int DK, bool BF16>
+cudaError_t plan_and_run(const FwdArgs& a, Plan p, cudaStream_t s, ScratchProvider* sp) {
+  p = plan_segments<DK, BF16>(a, p);
+  const long heads = (long)a.B * a.H;
   float* scratch = nullptr;
   if (p.nseg > 1) {
     const size_t bytes = (size_t)heads * (p.nseg - 1) * (2 * (size_t)a.d_v * a.d_k + 1) * sizeof(float);
@@ -532,12 +552,40 @@ cudaError_t plan_and_run(const FwdArgs& a, Plan p, cudaStream_t s, ScratchProvid
   return e;
 }
 
-}  // namespace
+// The summary of each head's whole range: pass A over the planned segments
+// straight into (summary, gamma) when there is one segment, else into scratch
+// and then folded.
+template <int DK, bool BF16>
+cudaError_t summary_plan_and_run(const FwdArgs& a, Plan p, float* summary, float* gamma, cudaStream_t s,
+                                 ScratchProvider* sp) {
+  p = plan_segments<DK, BF16>(a, p);
+  auto pass_a = [&](float* st, float* gm) -> cudaError_t {
+    switch (p.RG) {
+      case 64: return Kernels<DK, BF16, 64>::summaries(a, p.C, p.nseg, p.seg_len, st, gm, s);
+      case 32: return Kernels<DK, BF16, 32>::summaries(a, p.C, p.nseg, p.seg_len, st, gm, s);
+      case 16: return Kernels<DK, BF16, 16>::summaries(a, p.C, p.nseg, p.seg_len, st, gm, s);
+      default: return Kernels<DK, BF16, 8>::summaries(a, p.C, p.nseg, p.seg_len, st, gm, s);
+    }
+  };
+  if (p.nseg == 1) return pass_a(summary, gamma);
+  const long heads = (long)a.B * a.H;
+  const long long DVK = (long long)a.d_v * a.d_k;
+  float* scratch = nullptr;
+  cudaError_t e = sp->acquire((size_t)heads * p.nseg * (2 * DVK + 1) * sizeof(float), s, &scratch);
+  if (e != cudaSuccess) return e;
+  float* gm = scratch + (size_t)heads * p.nseg * 2 * DVK;
+  e = pass_a(scratch, gm);
+  if (e == cudaSuccess) {
+    // slot (bh, seg) of the scratch: states at (bh * nseg + seg) * 2 DVK, gammas at bh * nseg + seg
+    const FoldArgs f{scratch, gm, 2 * DVK, (long long)p.nseg * 2 * DVK, 1, p.nseg, p.nseg, heads, a.H,
+                     (int)DVK, false, a.I_prior, nullptr, nullptr, summary, summary + DVK, gamma, 2 * DVK};
+    e = launch_fold(f, s);
+  }
+  const cudaError_t e2 = sp->release(scratch, s);
+  return e != cudaSuccess ? e : e2;
+}
 
-cudaError_t launch_forward_chunked(const FwdArgs& a, cudaStream_t s, ScratchProvider* sp) {
-  int dev = 0, max_smem = 227 * 1024;
-  cudaGetDevice(&dev);
-  cudaDeviceGetAttribute(&max_smem, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+Plan base_plan(const FwdArgs& a, int max_smem, bool* ok) {
   Plan p;
   p.RG = rows_per_cta(a.d_v);
   const int es = a.bf16 ? 2 : 4;
@@ -545,11 +593,39 @@ cudaError_t launch_forward_chunked(const FwdArgs& a, cudaStream_t s, ScratchProv
   // warp), shrunk until three CTAs' staging fits an SM.
   p.C = std::min(a.chunk, 32);
   while (p.C > 16 && FwdSmem(p.C, a.d_k, a.d_v, p.RG, es).total > (size_t)max_smem / 3) p.C /= 2;
-  if (FwdSmem(p.C, a.d_k, a.d_v, p.RG, es).total > (size_t)max_smem) return cudaErrorInvalidConfiguration;
+  *ok = FwdSmem(p.C, a.d_k, a.d_v, p.RG, es).total <= (size_t)max_smem;
   p.nseg = 1;
   p.seg_len = a.T;
+  return p;
+}
+
+int max_smem_optin() {
+  int dev = 0, max_smem = 227 * 1024;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&max_smem, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+  return max_smem;
+}
+
+}  // namespace
+
+cudaError_t launch_forward_chunked(const FwdArgs& a, cudaStream_t s, ScratchProvider* sp) {
+  bool ok = false;
+  const Plan p = base_plan(a, max_smem_optin(), &ok);
+  if (!ok) return cudaErrorInvalidConfiguration;
   if (a.d_k == 128) return a.bf16 ? plan_and_run<128, true>(a, p, s, sp) : plan_and_run<128, false>(a, p, s, sp);
   return a.bf16 ? plan_and_run<64, true>(a, p, s, sp) : plan_and_run<64, false>(a, p, s, sp);
+}
+
+cudaError_t launch_segment_summary(const FwdArgs& a, float* summary, float* gamma, cudaStream_t s,
+                                   ScratchProvider* sp) {
+  bool ok = false;
+  const Plan p = base_plan(a, max_smem_optin(), &ok);
+  if (!ok) return cudaErrorInvalidConfiguration;
+  if (a.d_k == 128)
+    return a.bf16 ? summary_plan_and_run<128, true>(a, p, summary, gamma, s, sp)
+                  : summary_plan_and_run<128, false>(a, p, summary, gamma, s, sp);
+  return a.bf16 ? summary_plan_and_run<64, true>(a, p, summary, gamma, s, sp)
+                : summary_plan_and_run<64, false>(a, p, summary, gamma, s, sp);
 }
 
 }  // namespace palimpsa

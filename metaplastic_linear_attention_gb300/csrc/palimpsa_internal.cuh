@@ -107,6 +107,37 @@ struct ScratchProvider {
 // validated by the caller.
 cudaError_t launch_forward_chunked(const FwdArgs& a, cudaStream_t s, ScratchProvider* sp);
 cudaError_t launch_step(const StepArgs& a, cudaStream_t s);
+// Summary of the whole token range of each head from a zero state (pass A over
+// the planned segments, then folded): summary [B,H,2,d_v,d_k] = (dM, dIbar),
+// gamma [B,H] = prod alpha.
+cudaError_t launch_segment_summary(const FwdArgs& a, float* summary, float* gamma, cudaStream_t s,
+                                   ScratchProvider* sp);
+
+// Affine fold of R segment summaries, in order (fold.cu):
+//   (M, Ibar) <- Gamma_s (M, Ibar) + (dM_s, dIbar_s),   s = 0 .. R-1.
+// Summary element (s, bh, part, e) is at sum[s*sum_ss + bh*sum_sh + part*DVK + e],
+// gamma (s, bh) at gam[s*gam_ss + bh*gam_sh]. With to_state the fold starts
+// from (I0 mu0, I0 - I_prior) (defaults mu0 = 0, I0 = I_prior) and writes the
+// state as (mu, I) to out_a, out_b; otherwise it starts from zero and writes
+// (dM, dIbar) to out_a, out_b and prod Gamma to out_gamma [heads]. Output
+// element (bh, e) is at out_*[bh*out_sh + e]; mu0 and I0 are [heads, DVK].
+struct FoldArgs {
+  const float* sum;
+  const float* gam;
+  long long sum_ss, sum_sh, gam_ss, gam_sh;
+  int R;
+  long long heads;
+  int H, DVK;
+  bool to_state;
+  const float* I_prior;
+  const float* mu0;
+  const float* I0;
+  float* out_a;
+  float* out_b;
+  float* out_gamma;
+  long long out_sh;
+};
+cudaError_t launch_fold(const FoldArgs& f, cudaStream_t s);
 // The "without Meta" comparator (importance frozen at I_prior); uses a.mu0,
 // a.y, a.mu_T and ignores a.I0, a.I_T.
 cudaError_t launch_forward_without_meta(const FwdArgs& a, cudaStream_t s);

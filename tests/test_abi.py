@@ -214,3 +214,31 @@ def test_forward_varlen_empty_tokens_need_no_token_arrays(lib):
     # NULL, but the state arrays and offsets are still required
     assert _varlen(lib, total_T=0, max_seqlen=0, q=None, k=None, v=None, beta=None, d=None, y=None,
                    mu_T=None) == ERR_NULL
+
+
+@pytest.mark.parametrize("over,code", [
+    (dict(summary=None), ERR_NULL), (dict(gamma=None), ERR_NULL), (dict(q=None), ERR_NULL),
+    (dict(summary=P + 4), ERR_ALIGN), (dict(gamma=P + 2), ERR_ALIGN), (dict(T=-2), ERR_SHAPE),
+    (dict(d_k=32), ERR_UNSUPPORTED), (dict(dtype=3), ERR_DTYPE),
+])
+def test_segment_summary_rejects_bad_arguments(lib, over, code):
+    args = dict(q=P, k=P, v=P, beta=P, d=P, A=P, I_prior=P, summary=P, gamma=P, B=1, H=2, T=16, d_k=128, d_v=64,
+                chunk=0, dtype=1)
+    args.update(over)
+    assert lib.palimpsa_segment_summary(args["q"], args["k"], args["v"], args["beta"], args["d"], args["A"],
+                                        args["I_prior"], args["summary"], args["gamma"], args["B"], args["H"],
+                                        args["T"], args["d_k"], args["d_v"], args["chunk"], args["dtype"],
+                                        None) == code
+
+
+@pytest.mark.parametrize("over,code", [
+    (dict(S=None), ERR_NULL), (dict(G=None), ERR_NULL), (dict(I_prior=None), ERR_NULL), (dict(mu=None), ERR_NULL),
+    (dict(R=-1), ERR_SHAPE), (dict(B=0), ERR_SHAPE), (dict(S=P + 8), ERR_ALIGN), (dict(I=P + 4), ERR_ALIGN),
+    (dict(G=P + 1), ERR_ALIGN), (dict(d_v=12), ERR_UNSUPPORTED),
+])
+def test_state_combine_rejects_bad_arguments(lib, over, code):
+    args = dict(S=P, G=P, R=3, I_prior=P, mu0=None, I0=None, mu=P, I=P, B=1, H=2, d_k=128, d_v=64)
+    args.update(over)
+    assert lib.palimpsa_state_combine(args["S"], args["G"], args["R"], args["I_prior"], args["mu0"], args["I0"],
+                                      args["mu"], args["I"], args["B"], args["H"], args["d_k"], args["d_v"],
+                                      None) == code
