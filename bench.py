@@ -37,8 +37,8 @@ MUFU_RCP_PER_CLK_PER_SM = 16     # SFU reciprocal issue rate per SM (one per ele
 # capture at the bench's full size (profiles/launches_decode_B256_H32.md), valid only while the
 # kernel's source file is byte-identical to the one captured (sha256 below); otherwise null.
 NCU_TRAFFIC = {
-    "palimpsa_step": {"bytes_per_launch": 1019186000, "source": "csrc/step.cu",
-                      "sha256": "53d6c7c222739b7622af430fe64b3b1f73fbd99ec674074022d53584303334af"},
+    "palimpsa_step": {"bytes_per_launch": 1019104171, "source": "csrc/step.cu",
+                      "sha256": "a6071dc649bba97d682ba9c5b9511c1cad7feedc2cb5726ae9b569ec3fbcc0c0"},
 }
 
 
