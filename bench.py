@@ -353,6 +353,32 @@ def run_ours(args, ws, rank, local):
             "over_unfused": fstep_ms / kernels["palimpsa_step"]["avg_ms"],
             "note": f"{SF} fused steps from raw inputs; timed after the timed region"}
 
+    # Variable-length batch: the same tokens per head packed as 4 B ragged
+    # sequences (seeded uniform length mix), timed against the dense forward.
+    if not S:
+        lengths = syn.varlen_lengths(B * T, 4 * B, seed)
+        pk = syn.packed_inputs(wl, lengths, H=H, device=dev, seed=seed)
+        mx = max(lengths)
+        yv = torch.empty((H, B * T, dv), dtype=f32, device=dev)
+        mv = torch.empty((len(lengths), H, dv, dk), dtype=f32, device=dev)
+        Iv = torch.empty_like(mv)
+
+        def _varlen():
+            pal.palimpsa_forward_varlen(pk["q"], pk["k"], pk["v"], pk["beta"], pk["d_t"], pk["A"], pk["I_prior"],
+                                        pk["cu_seqlens"], max_seqlen=mx, y=yv, mu_T=mv, I_T=Iv, chunk=wl.chunk)
+        for _ in range(2):
+            _varlen()
+        c0.record(stream)
+        for _ in range(reps):
+            _varlen()
+        c1.record(stream)
+        torch.cuda.synchronize()
+        var_ms = c0.elapsed_time(c1) / reps
+        kernels["palimpsa_fwd_varlen"] = {
+            "avg_ms": var_ms, "head_tokens_per_s": B * H * T / (var_ms / 1e3), "over_dense": var_ms / fwd_avg_ms,
+            "sequences": len(lengths), "max_seqlen": mx,
+            "note": "the dense workload's tokens per head packed as ragged sequences; timed after the timed region"}
+
     # The backward through the scan (gradients of <dy, y> for every input), timed
     # outside the timed region on the same inputs.
     if not S:

@@ -365,8 +365,8 @@ palimpsa_status palimpsa_forward_without_meta(
  *            is included in dI_prior.
  *
  * The forward states are recomputed, never stored by the forward: one sweep
- * keeps a checkpoint every 64 tokens in stream-ordered scratch from the
- * library's pool (B * H * ceil(T / 64) * 8 * d_v * d_k bytes). All states used
+ * keeps a checkpoint every 32 tokens in stream-ordered scratch from the
+ * library's pool (B * H * ceil(T / 32) * 8 * d_v * d_k bytes). All states used
  * come from forward-direction steps. dq, dk, dd_t, dA and dI_prior are
  * accumulated with fp32 atomics (the library zeroes them first), so their last
  * bits may differ between runs; everything else is deterministic.
