@@ -44,7 +44,8 @@ namespace palimpsa {
 namespace {
 
 constexpr int kRowsPerCta = 8;     // one warp per value row
-constexpr int kThreads = kRowsPerCta * 32;
+constexpr int kWarps = 8;
+constexpr int kThreads = kWarps * 32;
 constexpr int kSeg = 32;           // checkpoint spacing and staging unit (tokens)
 constexpr int kWin = 8;            // window re-run into registers (tokens)
 constexpr int kNW = kSeg / kWin;   // windows per segment
@@ -54,7 +55,7 @@ __host__ __device__ constexpr size_t al16(size_t x) { return (x + 15) / 16 * 16;
 // Shared-memory carve-up (byte offsets; every piece 16-byte aligned).
 struct BwdSmem {
   size_t k, q, v, b, dy, dt, stage;   // one staged segment (offsets inside a stage)
-  size_t win, red, red_a, al, om, total;
+  size_t win, rowp, al, om, total;
 
   __host__ __device__ BwdSmem(int DK, int ES) {
     size_t o = 0;
@@ -67,8 +68,7 @@ struct BwdSmem {
     stage = (o + 127) / 128 * 128;
     o = 2 * stage;
     win = o;   o += (size_t)2 * kRowsPerCta * kNW * DK * 4;   // window starts [M | I][row][window][col]
-    red = o;   o += (size_t)2 * 2 * kRowsPerCta * DK * 4;     // [parity][dq | dk][row][col]
-    red_a = o; o += (size_t)2 * kRowsPerCta * 4;              // [parity][row] dalpha
+    rowp = o;  o += (size_t)kWarps * kWin * kRowsPerCta * 3 * 4;  // row-sum partials [warp][token][row][3]
     al = o;    o += (size_t)kSeg * 4;                         // alpha of the segment's tokens
     om = o;    o += (size_t)kSeg * 4;                         // (1 - alpha) I_prior
     total = (o + 127) / 128 * 128;
@@ -154,6 +154,17 @@ __device__ __forceinline__ float warp_sum(float x) {
   return x;
 }
 
+__device__ __forceinline__ float2 f2(float x) { return make_float2(x, x); }
+
+// This lane's NC key columns of token u of a staged q or k, as NC / 2 pairs.
+template <bool BF16, int NC>
+__device__ __forceinline__ void col_pairs(const unsigned char* base, int DK, int u, int c0, float2 (&x)[NC / 2]) {
+  float c[NC];
+  cols<BF16, NC>(base, DK, u, c0, c);
+#pragma unroll
+  for (int p = 0; p < NC / 2; ++p) x[p] = make_float2(c[2 * p], c[2 * p + 1]);
+}
+
 // Per-token scalars of the forward update for one value row.
 struct TokRow {
   float alpha, om, b, v, bv;
@@ -161,24 +172,55 @@ struct TokRow {
 
 template <bool BF16>
 __device__ __forceinline__ TokRow tok_row(const unsigned char* st, const BwdSmem& L, const float* al,
-                                          const float* om, int u, int w) {
-  TokRow r;
-  r.alpha = al[u];
-  r.om = om[u];
-  r.b = row_val<BF16>(st + L.b, u, w);
-  r.v = row_val<BF16>(st + L.v, u, w);
-  r.bv = r.b * r.v;
-  return r;
+                                          const float* om, int u, int r) {
+  TokRow t;
+  t.alpha = al[u];
+  t.om = om[u];
+  t.b = row_val<BF16>(st + L.b, u, r);
+  t.v = row_val<BF16>(st + L.v, u, r);
+  t.bv = t.b * t.v;
+  return t;
 }
 
-// One forward step of a lane's NC state elements (the forward kernel's update).
-template <int NC>
-__device__ __forceinline__ void fwd_step(float (&M)[NC], float (&I)[NC], const float (&k)[NC], const TokRow& tr) {
+// One forward step of a lane's state pairs (the forward kernel's update, packed):
+//   I = alpha I + (beta_i k_j^2 + (1 - alpha) I_prior),  M = alpha M + (beta_i v_i) k_j.
+template <int NP>
+__device__ __forceinline__ void fwd_step(float2 (&M)[NP], float2 (&I)[NP], const float2 (&k)[NP], const TokRow& t) {
+  const float2 a2 = f2(t.alpha), om2 = f2(t.om), b2 = f2(t.b), bv2 = f2(t.bv);
 #pragma unroll
-  for (int e = 0; e < NC; ++e) {
-    I[e] = fmaf(tr.alpha, I[e], fmaf(tr.b, k[e] * k[e], tr.om));
-    M[e] = fmaf(tr.alpha, M[e], tr.bv * k[e]);
+  for (int p = 0; p < NP; ++p) {
+    I[p] = __ffma2_rn(a2, I[p], __ffma2_rn(b2, __fmul2_rn(k[p], k[p]), om2));
+    M[p] = __ffma2_rn(a2, M[p], __fmul2_rn(bv2, k[p]));
   }
+}
+
+// Reduce-scatter of V = 2 NC column partials over the 8 lanes that share this
+// lane's columns (lane bits 4, 3, 2, i.e. the 8 rows): each level halves the
+// values a lane keeps and adds its partner's half. Returns the lane's finished
+// value; its index is (lane >> 2) & 7 for V = 8 and (lane >> 3) & 3 for V = 4
+// (the last level then only completes the sum, on both partners).
+template <int V>
+__device__ __forceinline__ float reduce_scatter_rows(float (&x)[V], int lane) {
+  int n = V;
+#pragma unroll
+  for (int m = 16; m >= 4; m >>= 1) {
+    const bool hi = (lane & m) != 0;
+    if (n >= 2) {
+      const int half = n / 2;
+#pragma unroll
+      for (int v = 0; v < V / 2; ++v) {
+        if (v < half) {
+          const float send = hi ? x[v] : x[v + half];
+          const float keep = hi ? x[v + half] : x[v];
+          x[v] = keep + __shfl_xor_sync(0xffffffffu, send, m);
+        }
+      }
+      n = half;
+    } else {
+      x[0] += __shfl_xor_sync(0xffffffffu, x[0], m);
+    }
+  }
+  return x[0];
 }
 
 // All threads: alpha and (1 - alpha) I_prior of the staged segment's tokens into
@@ -196,14 +238,15 @@ __device__ __forceinline__ void fill_gates(const unsigned char* st, const BwdSme
 template <int DK, bool BF16>
 __global__ void __launch_bounds__(kThreads)
 palimpsa_bwd_kernel(BwdArgs a, float* __restrict__ ckpt) {
-  constexpr int NC = DK / 32;
+  constexpr int NC = DK / 32;       // key columns per lane
+  constexpr int NP = NC / 2;        // packed pairs per lane
+  constexpr int CW = DK / kWarps;   // key columns per warp
   constexpr int ES = BF16 ? 2 : 4;
   extern __shared__ __align__(128) unsigned char bsm[];
   const BwdSmem L(DK, ES);
   auto win_M = reinterpret_cast<float (*)[kNW][DK]>(bsm + L.win);
   auto win_I = reinterpret_cast<float (*)[kNW][DK]>(bsm + L.win + (size_t)kRowsPerCta * kNW * DK * 4);
-  auto red = reinterpret_cast<float (*)[2][kRowsPerCta][DK]>(bsm + L.red);
-  auto red_a = reinterpret_cast<float (*)[kRowsPerCta]>(bsm + L.red_a);
+  auto rowp = reinterpret_cast<float (*)[kWin][kRowsPerCta][3]>(bsm + L.rowp);
   float* al = reinterpret_cast<float*>(bsm + L.al);
   float* om = reinterpret_cast<float*>(bsm + L.om);
 
@@ -213,22 +256,23 @@ palimpsa_bwd_kernel(BwdArgs a, float* __restrict__ ckpt) {
   const int row0 = (blockIdx.x % groups) * kRowsPerCta;
   const int h = (int)(bh % a.H);
   const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
-  const int i = row0 + w;             // this warp's value row
-  const int c0 = lane * NC;           // this lane's first key column
+  const int rl = lane >> 2;                 // this lane's row within the CTA
+  const int i = row0 + rl;                  // ... and within the head
+  const int c0 = w * CW + (lane & 3) * NC;  // this lane's first key column
   const size_t head_tok = (size_t)bh * T;
   const float A_h = a.A[h], Ip = a.I_prior[h];
   const int nseg = (T + kSeg - 1) / kSeg;
   float* my_ckpt = ckpt + (size_t)blockIdx.x * nseg * kRowsPerCta * DK * 2;
 
   // ---- initial state
-  float M[NC], I[NC], mu0v[NC], I0v[NC];
+  float2 M[NP], I[NP], mu0v[NP], I0v[NP];
   const size_t soff = ((size_t)bh * DV + i) * DK + c0;
 #pragma unroll
-  for (int e = 0; e < NC; ++e) {
-    I0v[e] = a.I0 ? a.I0[soff + e] : Ip;
-    mu0v[e] = a.mu0 ? a.mu0[soff + e] : 0.f;
-    I[e] = I0v[e];
-    M[e] = I0v[e] * mu0v[e];
+  for (int p = 0; p < NP; ++p) {
+    I0v[p] = a.I0 ? *reinterpret_cast<const float2*>(a.I0 + soff + 2 * p) : f2(Ip);
+    mu0v[p] = a.mu0 ? *reinterpret_cast<const float2*>(a.mu0 + soff + 2 * p) : f2(0.f);
+    I[p] = I0v[p];
+    M[p] = __fmul2_rn(I0v[p], mu0v[p]);
   }
 
   // ---- phase 1: forward sweep, checkpoint at every segment start; segment
@@ -245,30 +289,32 @@ palimpsa_bwd_kernel(BwdArgs a, float* __restrict__ ckpt) {
     __syncthreads();  // segment s staged by every thread
     const unsigned char* st = bsm + (size_t)(s & 1) * L.stage;
     fill_gates(st, L, tn, A_h, Ip, al, om);
-    float* cp = my_ckpt + ((size_t)s * kRowsPerCta + w) * DK * 2;
+    float* cp = my_ckpt + ((size_t)s * kRowsPerCta + rl) * DK * 2;
 #pragma unroll
-    for (int e = 0; e < NC; ++e) { cp[c0 + e] = M[e]; cp[DK + c0 + e] = I[e]; }
+    for (int p = 0; p < NP; ++p) {
+      *reinterpret_cast<float2*>(cp + c0 + 2 * p) = M[p];
+      *reinterpret_cast<float2*>(cp + DK + c0 + 2 * p) = I[p];
+    }
     __syncthreads();  // gates ready
     for (int u = 0; u < tn; ++u) {
-      float k[NC];
-      cols<BF16, NC>(st + L.k, DK, u, c0, k);
-      fwd_step<NC>(M, I, k, tok_row<BF16>(st, L, al, om, u, w));
+      float2 k[NP];
+      col_pairs<BF16, NC>(st + L.k, DK, u, c0, k);
+      fwd_step<NP>(M, I, k, tok_row<BF16>(st, L, al, om, u, rl));
     }
     __syncthreads();  // this stage and the gate tables are free again
   }
 
   // ---- adjoints at t = T from the final-state gradients
-  float gM[NC], gI[NC];
+  float2 gM[NP], gI[NP];
 #pragma unroll
-  for (int e = 0; e < NC; ++e) {
-    const float dmu = a.dmu_T ? a.dmu_T[soff + e] : 0.f;
-    const float dI = a.dI_T ? a.dI_T[soff + e] : 0.f;
-    const float r = 1.f / I[e];
-    gM[e] = dmu * r;
-    gI[e] = dI - dmu * (M[e] * r) * r;
+  for (int p = 0; p < NP; ++p) {
+    const float2 dmu = a.dmu_T ? *reinterpret_cast<const float2*>(a.dmu_T + soff + 2 * p) : f2(0.f);
+    const float2 dI = a.dI_T ? *reinterpret_cast<const float2*>(a.dI_T + soff + 2 * p) : f2(0.f);
+    const float2 r = make_float2(1.f / I[p].x, 1.f / I[p].y);
+    gM[p] = __fmul2_rn(dmu, r);
+    gI[p] = make_float2(dI.x - dmu.x * (M[p].x * r.x) * r.x, dI.y - dmu.y * (M[p].y * r.y) * r.y);
   }
   float dIp_acc = 0.f, dA_acc = 0.f;
-  int par = 0;
 
   // ---- phase 2: segments in reverse; segment s - 1 is being copied in while
   // segment s computes (the last segment is still staged from phase 1).
@@ -282,101 +328,126 @@ palimpsa_bwd_kernel(BwdArgs a, float* __restrict__ ckpt) {
     const float* dts = reinterpret_cast<const float*>(st + L.dt);
     const float* dys = reinterpret_cast<const float*>(st + L.dy);
     fill_gates(st, L, tn, A_h, Ip, al, om);
-    const float* cp = my_ckpt + ((size_t)s * kRowsPerCta + w) * DK * 2;
+    const float* cp = my_ckpt + ((size_t)s * kRowsPerCta + rl) * DK * 2;
 #pragma unroll
-    for (int e = 0; e < NC; ++e) { M[e] = cp[c0 + e]; I[e] = cp[DK + c0 + e]; }
+    for (int p = 0; p < NP; ++p) {
+      M[p] = *reinterpret_cast<const float2*>(cp + c0 + 2 * p);
+      I[p] = *reinterpret_cast<const float2*>(cp + DK + c0 + 2 * p);
+    }
     __syncthreads();  // gates ready
-    // re-run the segment, keeping the state at each window start (this warp's row only)
+    // re-run the segment, keeping the state at each window start (this lane's elements only)
     for (int u = 0; u < tn; ++u) {
       if (u % kWin == 0) {
 #pragma unroll
-        for (int e = 0; e < NC; ++e) { win_M[w][u / kWin][c0 + e] = M[e]; win_I[w][u / kWin][c0 + e] = I[e]; }
+        for (int p = 0; p < NP; ++p) {
+          *reinterpret_cast<float2*>(&win_M[rl][u / kWin][c0 + 2 * p]) = M[p];
+          *reinterpret_cast<float2*>(&win_I[rl][u / kWin][c0 + 2 * p]) = I[p];
+        }
       }
-      float k[NC];
-      cols<BF16, NC>(st + L.k, DK, u, c0, k);
-      fwd_step<NC>(M, I, k, tok_row<BF16>(st, L, al, om, u, w));
+      float2 k[NP];
+      col_pairs<BF16, NC>(st + L.k, DK, u, c0, k);
+      fwd_step<NP>(M, I, k, tok_row<BF16>(st, L, al, om, u, rl));
     }
-    __syncwarp();
     const int nwin = (tn + kWin - 1) / kWin;
     for (int wi = nwin - 1; wi >= 0; --wi) {
       const int uw = wi * kWin, n = min(kWin, tn - uw);
       // re-run the window into registers: state before token uw + uu is (Ms[uu], Is[uu])
-      float Ms[kWin + 1][NC], Is[kWin + 1][NC];
+      float2 Ms[kWin + 1][NP], Is[kWin + 1][NP];
 #pragma unroll
-      for (int e = 0; e < NC; ++e) { Ms[0][e] = win_M[w][wi][c0 + e]; Is[0][e] = win_I[w][wi][c0 + e]; }
+      for (int p = 0; p < NP; ++p) {
+        Ms[0][p] = *reinterpret_cast<const float2*>(&win_M[rl][wi][c0 + 2 * p]);
+        Is[0][p] = *reinterpret_cast<const float2*>(&win_I[rl][wi][c0 + 2 * p]);
+      }
 #pragma unroll
       for (int uu = 0; uu < kWin; ++uu) {
         if (uu < n) {
-          float k[NC];
-          cols<BF16, NC>(st + L.k, DK, uw + uu, c0, k);
-          const TokRow tr = tok_row<BF16>(st, L, al, om, uw + uu, w);
+          float2 k[NP];
+          col_pairs<BF16, NC>(st + L.k, DK, uw + uu, c0, k);
+          const TokRow tr = tok_row<BF16>(st, L, al, om, uw + uu, rl);
 #pragma unroll
-          for (int e = 0; e < NC; ++e) {
-            Is[uu + 1][e] = fmaf(tr.alpha, Is[uu][e], fmaf(tr.b, k[e] * k[e], tr.om));
-            Ms[uu + 1][e] = fmaf(tr.alpha, Ms[uu][e], tr.bv * k[e]);
-          }
+          for (int p = 0; p < NP; ++p) { Ms[uu + 1][p] = Ms[uu][p]; Is[uu + 1][p] = Is[uu][p]; }
+          fwd_step<NP>(Ms[uu + 1], Is[uu + 1], k, tr);
         }
       }
       // sweep the window backwards
 #pragma unroll
       for (int uu = kWin - 1; uu >= 0; --uu) {
         if (uu < n) {
-          const int u = uw + uu, t = ts + u;
-          float k[NC], q[NC];
-          cols<BF16, NC>(st + L.k, DK, u, c0, k);
-          cols<BF16, NC>(st + L.q, DK, u, c0, q);
-          const TokRow tr = tok_row<BF16>(st, L, al, om, u, w);
-          const float dyi = dys[u * kRowsPerCta + w];
-          float s_bv = 0.f, s_b = 0.f, s_al = 0.f, s_gi = 0.f;
-          const float om_w = tr.om / Ip;  // 1 - alpha_t
-          float dq_p[NC], dk_p[NC];
+          const int u = uw + uu;
+          float2 k[NP], q[NP];
+          col_pairs<BF16, NC>(st + L.k, DK, u, c0, k);
+          col_pairs<BF16, NC>(st + L.q, DK, u, c0, q);
+          const TokRow tr = tok_row<BF16>(st, L, al, om, u, rl);
+          const float dyi = dys[u * kRowsPerCta + rl];
+          const float2 dy2 = f2(dyi), ndy2 = f2(-dyi), bv2 = f2(tr.bv), tb2 = f2(2.f * tr.b), nIp2 = f2(-Ip);
+          float2 sbv = f2(0.f), sb = f2(0.f), sal = f2(0.f), sgi = f2(0.f);
+          float cs[2 * NC];  // column partials: dq then dk
 #pragma unroll
-          for (int e = 0; e < NC; ++e) {
-            const float r = rcp_approx(Is[uu + 1][e]);
-            const float mu = Ms[uu + 1][e] * r;
-            const float dmu = dyi * q[e];
-            gM[e] = fmaf(dmu, r, gM[e]);
-            gI[e] = fmaf(-dmu * mu, r, gI[e]);
-            dq_p[e] = dyi * mu;
-            s_bv = fmaf(gM[e], k[e], s_bv);
-            s_b = fmaf(gI[e], k[e] * k[e], s_b);
-            dk_p[e] = fmaf(gM[e], tr.bv, 2.f * gI[e] * tr.b * k[e]);
-            s_al = fmaf(gM[e], Ms[uu][e], fmaf(gI[e], Is[uu][e] - Ip, s_al));
-            s_gi += gI[e];
+          for (int p = 0; p < NP; ++p) {
+            const float2 Ic = Is[uu + 1][p];
+            const float2 r = make_float2(rcp_approx(Ic.x), rcp_approx(Ic.y));
+            const float2 mu = __fmul2_rn(Ms[uu + 1][p], r);
+            gM[p] = __ffma2_rn(__fmul2_rn(dy2, q[p]), r, gM[p]);
+            gI[p] = __ffma2_rn(__fmul2_rn(__fmul2_rn(ndy2, q[p]), mu), r, gI[p]);
+            const float2 dq2 = __fmul2_rn(dy2, mu);
+            sbv = __ffma2_rn(gM[p], k[p], sbv);
+            sb = __ffma2_rn(gI[p], __fmul2_rn(k[p], k[p]), sb);
+            const float2 dk2 = __ffma2_rn(gM[p], bv2, __fmul2_rn(gI[p], __fmul2_rn(tb2, k[p])));
+            sal = __ffma2_rn(gM[p], Ms[uu][p], __ffma2_rn(gI[p], __fadd2_rn(Is[uu][p], nIp2), sal));
+            sgi = __fadd2_rn(sgi, gI[p]);
+            cs[2 * p] = dq2.x; cs[2 * p + 1] = dq2.y;
+            cs[NC + 2 * p] = dk2.x; cs[NC + 2 * p + 1] = dk2.y;
           }
-          s_bv = warp_sum(s_bv);
-          s_b = warp_sum(s_b);
-          s_al = warp_sum(s_al);
-          dIp_acc = fmaf(om_w, s_gi, dIp_acc);  // per lane; reduced over the warp at the end
-          if (lane == 0) {
-            const size_t o = (head_tok + t) * DV + i;
-            a.dv[o] = s_bv * tr.b;
-            a.dbeta[o] = fmaf(s_bv, tr.v, s_b);
-            red_a[par][w] = s_al;
+          // columns: finished over the 8 rows inside the warp, one global atomic per lane
+          const float cv = reduce_scatter_rows<2 * NC>(cs, lane);
+          {
+            const int t = ts + u;
+            const int v = NC == 4 ? rl : (rl >> 1);
+            if (NC == 4 || (lane & 4) == 0)
+              atomicAdd((v < NC ? a.dq : a.dk) + (head_tok + t) * DK + c0 + (v % NC), cv);
           }
+          // rows: over this warp's columns (the row's 4 lanes), then per warp into shared memory
+          float r_bv = sbv.x + sbv.y, r_b = sb.x + sb.y, r_al = sal.x + sal.y;
 #pragma unroll
-          for (int e = 0; e < NC; ++e) { red[par][0][w][c0 + e] = dq_p[e]; red[par][1][w][c0 + e] = dk_p[e]; }
-          __syncthreads();
-          for (int it = threadIdx.x; it < 2 * DK; it += kThreads) {
-            const int which = it / DK, j = it % DK;
-            float sum = 0.f;
-#pragma unroll
-            for (int rr = 0; rr < kRowsPerCta; ++rr) sum += red[par][which][rr][j];
-            atomicAdd((which ? a.dk : a.dq) + (head_tok + t) * DK + j, sum);
+          for (int m = 1; m <= 2; m <<= 1) {
+            r_bv += __shfl_xor_sync(0xffffffffu, r_bv, m);
+            r_b += __shfl_xor_sync(0xffffffffu, r_b, m);
+            r_al += __shfl_xor_sync(0xffffffffu, r_al, m);
           }
-          if (threadIdx.x == 0) {
-            float dal = 0.f;
-#pragma unroll
-            for (int rr = 0; rr < kRowsPerCta; ++rr) dal += red_a[par][rr];
-            atomicAdd(a.dd_t + head_tok + t, -A_h * tr.alpha * dal);
-            dA_acc = fmaf(-dts[u] * tr.alpha, dal, dA_acc);
+          if ((lane & 3) == 0) {
+            rowp[w][uu][rl][0] = r_bv;
+            rowp[w][uu][rl][1] = r_b;
+            rowp[w][uu][rl][2] = r_al;
           }
-          par ^= 1;
+          dIp_acc = fmaf(tr.om / Ip, sgi.x + sgi.y, dIp_acc);  // (1 - alpha_t) sum gI; reduced at the end
           // carry the adjoints to t - 1
+          const float2 a2 = f2(tr.alpha);
 #pragma unroll
-          for (int e = 0; e < NC; ++e) { gM[e] *= tr.alpha; gI[e] *= tr.alpha; }
+          for (int p = 0; p < NP; ++p) { gM[p] = __fmul2_rn(gM[p], a2); gI[p] = __fmul2_rn(gI[p], a2); }
         }
       }
+      // the window's row sums: dv, dbeta per (token, row); dalpha per token
+      __syncthreads();
+      for (int x = threadIdx.x; x < n * kRowsPerCta; x += kThreads) {
+        const int uu = x / kRowsPerCta, r = x % kRowsPerCta, u = uw + uu;
+        float s_bv = 0.f, s_b = 0.f;
+#pragma unroll
+        for (int ww = 0; ww < kWarps; ++ww) { s_bv += rowp[ww][uu][r][0]; s_b += rowp[ww][uu][r][1]; }
+        const size_t o = (head_tok + ts + u) * DV + row0 + r;
+        a.dv[o] = s_bv * row_val<BF16>(st + L.b, u, r);
+        a.dbeta[o] = fmaf(s_bv, row_val<BF16>(st + L.v, u, r), s_b);
+      }
+      if (threadIdx.x < n) {
+        const int uu = threadIdx.x, u = uw + uu;
+        float dal = 0.f;
+#pragma unroll
+        for (int ww = 0; ww < kWarps; ++ww)
+#pragma unroll
+          for (int r = 0; r < kRowsPerCta; ++r) dal += rowp[ww][uu][r][2];
+        atomicAdd(a.dd_t + head_tok + ts + u, -A_h * al[u] * dal);
+        dA_acc = fmaf(-dts[u] * al[u], dal, dA_acc);
+      }
+      __syncthreads();  // the row partials are free for the next window
     }
     __syncthreads();  // this stage, the window starts and the gate tables are free again
   }
@@ -385,17 +456,20 @@ palimpsa_bwd_kernel(BwdArgs a, float* __restrict__ ckpt) {
   // ---- initial-state gradients: M_0 = I0 (.) mu0, I_0 = I0
   float s_ip0 = 0.f;
 #pragma unroll
-  for (int e = 0; e < NC; ++e) {
-    const float dI0 = gI[e] + gM[e] * mu0v[e];
-    if (a.dmu0) a.dmu0[soff + e] = gM[e] * I0v[e];
-    if (a.dI0) a.dI0[soff + e] = dI0;
-    s_ip0 += dI0;
+  for (int p = 0; p < NP; ++p) {
+    const float2 dI0 = __ffma2_rn(gM[p], mu0v[p], gI[p]);
+    if (a.dmu0) *reinterpret_cast<float2*>(a.dmu0 + soff + 2 * p) = __fmul2_rn(gM[p], I0v[p]);
+    if (a.dI0) *reinterpret_cast<float2*>(a.dI0 + soff + 2 * p) = dI0;
+    s_ip0 += dI0.x + dI0.y;
   }
   // With I0 absent the initial precision is I_prior itself.
   if (!a.I0) dIp_acc += s_ip0;
   dIp_acc = warp_sum(dIp_acc);
   if (lane == 0) atomicAdd(a.dI_prior + h, dIp_acc);
-  if (threadIdx.x == 0) atomicAdd(a.dA + h, dA_acc);
+  if (w == 0) {  // threads 0 .. kWin - 1 hold the dA partials of their token slots
+    dA_acc = warp_sum(dA_acc);
+    if (lane == 0) atomicAdd(a.dA + h, dA_acc);
+  }
 }
 
 }  // namespace
