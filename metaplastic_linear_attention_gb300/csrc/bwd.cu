@@ -55,7 +55,7 @@ __host__ __device__ constexpr size_t al16(size_t x) { return (x + 15) / 16 * 16;
 // Shared-memory carve-up (byte offsets; every piece 16-byte aligned).
 struct BwdSmem {
   size_t k, q, v, b, dy, dt, stage;   // one staged segment (offsets inside a stage)
-  size_t win, rowp, al, om, total;
+  size_t kf, qf, win, rowp, rb, rbv, al, om, oma, total;
 
   __host__ __device__ BwdSmem(int DK, int ES) {
     size_t o = 0;
@@ -67,10 +67,16 @@ struct BwdSmem {
     dt = o; o = al16(o + (size_t)kSeg * 4);
     stage = (o + 127) / 128 * 128;
     o = 2 * stage;
-    win = o;   o += (size_t)2 * kRowsPerCta * kNW * DK * 4;   // window starts [M | I][row][window][col]
+    // fp32 copies of the current segment's k and q (bf16 inputs; fp32 inputs are read in place)
+    kf = o;    o += ES == 2 ? (size_t)kSeg * DK * 4 : 0;
+    qf = o;    o += ES == 2 ? (size_t)kSeg * DK * 4 : 0;
+    win = o;   o += (size_t)2 * kRowsPerCta * kNW * DK * 4;   // window starts [M | I][window][pair][thread]
     rowp = o;  o += (size_t)kWarps * kWin * kRowsPerCta * 3 * 4;  // row-sum partials [warp][token][row][3]
+    rb = o;    o += (size_t)kSeg * kRowsPerCta * 4;           // beta_i of the segment's tokens [token][row]
+    rbv = o;   o += (size_t)kSeg * kRowsPerCta * 4;           // beta_i v_i
     al = o;    o += (size_t)kSeg * 4;                         // alpha of the segment's tokens
     om = o;    o += (size_t)kSeg * 4;                         // (1 - alpha) I_prior
+    oma = o;   o += (size_t)kSeg * 4;                         // 1 - alpha
     total = (o + 127) / 128 * 128;
   }
 };
@@ -117,30 +123,6 @@ __device__ __forceinline__ void stage_segment(unsigned char* st, const BwdSmem& 
   for (int i = threadIdx.x; i < tn; i += kThreads) cp_async4(st + L.dt + 4 * (size_t)i, a.d_t + tok0 + i);
 }
 
-// This lane's NC key columns of token u of a staged q or k.
-template <bool BF16, int NC>
-__device__ __forceinline__ void cols(const unsigned char* base, int DK, int u, int c0, float (&x)[NC]) {
-  if constexpr (BF16) {
-    const __nv_bfloat16* p = reinterpret_cast<const __nv_bfloat16*>(base) + (size_t)u * DK + c0;
-    if constexpr (NC == 4) {
-      const uint2 w = *reinterpret_cast<const uint2*>(p);
-      x[0] = bf16_lo(w.x); x[1] = bf16_hi(w.x); x[2] = bf16_lo(w.y); x[3] = bf16_hi(w.y);
-    } else {
-      const uint32_t w = *reinterpret_cast<const uint32_t*>(p);
-      x[0] = bf16_lo(w); x[1] = bf16_hi(w);
-    }
-  } else {
-    const float* p = reinterpret_cast<const float*>(base) + (size_t)u * DK + c0;
-    if constexpr (NC == 4) {
-      const float4 w = *reinterpret_cast<const float4*>(p);
-      x[0] = w.x; x[1] = w.y; x[2] = w.z; x[3] = w.w;
-    } else {
-      const float2 w = *reinterpret_cast<const float2*>(p);
-      x[0] = w.x; x[1] = w.y;
-    }
-  }
-}
-
 // Row w's value of token u of a staged v or beta (all lanes read one word).
 template <bool BF16>
 __device__ __forceinline__ float row_val(const unsigned char* base, int u, int w) {
@@ -155,44 +137,6 @@ __device__ __forceinline__ float warp_sum(float x) {
 }
 
 __device__ __forceinline__ float2 f2(float x) { return make_float2(x, x); }
-
-// This lane's NC key columns of token u of a staged q or k, as NC / 2 pairs.
-template <bool BF16, int NC>
-__device__ __forceinline__ void col_pairs(const unsigned char* base, int DK, int u, int c0, float2 (&x)[NC / 2]) {
-  float c[NC];
-  cols<BF16, NC>(base, DK, u, c0, c);
-#pragma unroll
-  for (int p = 0; p < NC / 2; ++p) x[p] = make_float2(c[2 * p], c[2 * p + 1]);
-}
-
-// Per-token scalars of the forward update for one value row.
-struct TokRow {
-  float alpha, om, b, v, bv;
-};
-
-template <bool BF16>
-__device__ __forceinline__ TokRow tok_row(const unsigned char* st, const BwdSmem& L, const float* al,
-                                          const float* om, int u, int r) {
-  TokRow t;
-  t.alpha = al[u];
-  t.om = om[u];
-  t.b = row_val<BF16>(st + L.b, u, r);
-  t.v = row_val<BF16>(st + L.v, u, r);
-  t.bv = t.b * t.v;
-  return t;
-}
-
-// One forward step of a lane's state pairs (the forward kernel's update, packed):
-//   I = alpha I + (beta_i k_j^2 + (1 - alpha) I_prior),  M = alpha M + (beta_i v_i) k_j.
-template <int NP>
-__device__ __forceinline__ void fwd_step(float2 (&M)[NP], float2 (&I)[NP], const float2 (&k)[NP], const TokRow& t) {
-  const float2 a2 = f2(t.alpha), om2 = f2(t.om), b2 = f2(t.b), bv2 = f2(t.bv);
-#pragma unroll
-  for (int p = 0; p < NP; ++p) {
-    I[p] = __ffma2_rn(a2, I[p], __ffma2_rn(b2, __fmul2_rn(k[p], k[p]), om2));
-    M[p] = __ffma2_rn(a2, M[p], __fmul2_rn(bv2, k[p]));
-  }
-}
 
 // Reduce-scatter of V = 2 NC column partials over the 8 lanes that share this
 // lane's columns (lane bits 4, 3, 2, i.e. the 8 rows): each level halves the
@@ -223,15 +167,82 @@ __device__ __forceinline__ float reduce_scatter_rows(float (&x)[V], int lane) {
   return x[0];
 }
 
-// All threads: alpha and (1 - alpha) I_prior of the staged segment's tokens into
-// the gate tables (callers order this with barriers on both sides).
-__device__ __forceinline__ void fill_gates(const unsigned char* st, const BwdSmem& L, int tn, float A_h, float Ip,
-                                           float* al, float* om) {
+// All threads, once per staged segment: the gate tables (alpha, (1 - alpha)
+// I_prior, 1 - alpha), the row tables (beta_i, beta_i v_i of the CTA's 8 rows)
+// and, for bf16 inputs, fp32 copies of k and q. Callers order this with
+// barriers on both sides.
+template <int DK, bool BF16>
+__device__ __forceinline__ void prepare_segment(const unsigned char* st, unsigned char* bsm, const BwdSmem& L, int tn,
+                                                float A_h, float Ip) {
   const float* dt = reinterpret_cast<const float*>(st + L.dt);
+  float* al = reinterpret_cast<float*>(bsm + L.al);
+  float* om = reinterpret_cast<float*>(bsm + L.om);
+  float* oma = reinterpret_cast<float*>(bsm + L.oma);
   for (int u = threadIdx.x; u < tn; u += kThreads) {
     const float x = -A_h * dt[u];
     al[u] = expf(x);
-    om[u] = -expm1f(x) * Ip;  // (1 - alpha) I_prior without cancellation
+    const float one_minus = -expm1f(x);  // 1 - alpha without cancellation
+    oma[u] = one_minus;
+    om[u] = one_minus * Ip;
+  }
+  float* rb = reinterpret_cast<float*>(bsm + L.rb);
+  float* rbv = reinterpret_cast<float*>(bsm + L.rbv);
+  for (int x = threadIdx.x; x < tn * kRowsPerCta; x += kThreads) {
+    const float b = row_val<BF16>(st + L.b, x / kRowsPerCta, x % kRowsPerCta);
+    rb[x] = b;
+    rbv[x] = b * row_val<BF16>(st + L.v, x / kRowsPerCta, x % kRowsPerCta);
+  }
+  if constexpr (BF16) {
+    const int n8 = tn * DK / 8;  // 8 bf16 values = 16 bytes per item
+    for (int x = threadIdx.x; x < n8; x += kThreads) {
+#pragma unroll
+      for (int which = 0; which < 2; ++which) {
+        const uint4 w = reinterpret_cast<const uint4*>(st + (which ? L.q : L.k))[x];
+        float4* o = reinterpret_cast<float4*>(bsm + (which ? L.qf : L.kf)) + 2 * x;
+        o[0] = make_float4(bf16_lo(w.x), bf16_hi(w.x), bf16_lo(w.y), bf16_hi(w.y));
+        o[1] = make_float4(bf16_lo(w.z), bf16_hi(w.z), bf16_lo(w.w), bf16_hi(w.w));
+      }
+    }
+  }
+}
+
+// This lane's NC key columns of token u of the fp32 k or q, as NC / 2 pairs.
+template <int NC>
+__device__ __forceinline__ void f32_pairs(const float* base, int DK, int u, int c0, float2 (&x)[NC / 2]) {
+  const float* p = base + (size_t)u * DK + c0;
+  if constexpr (NC == 4) {
+    const float4 w = *reinterpret_cast<const float4*>(p);
+    x[0] = make_float2(w.x, w.y);
+    x[1] = make_float2(w.z, w.w);
+  } else {
+    x[0] = *reinterpret_cast<const float2*>(p);
+  }
+}
+
+// Per-token scalars of the forward update for one value row, from the tables.
+struct Tok {
+  float alpha, om, oma, b, bv;
+};
+
+__device__ __forceinline__ Tok tok(const unsigned char* bsm, const BwdSmem& L, int u, int r) {
+  Tok t;
+  t.alpha = reinterpret_cast<const float*>(bsm + L.al)[u];
+  t.om = reinterpret_cast<const float*>(bsm + L.om)[u];
+  t.oma = reinterpret_cast<const float*>(bsm + L.oma)[u];
+  t.b = reinterpret_cast<const float*>(bsm + L.rb)[u * kRowsPerCta + r];
+  t.bv = reinterpret_cast<const float*>(bsm + L.rbv)[u * kRowsPerCta + r];
+  return t;
+}
+
+// One forward step of a lane's state pairs (the forward kernel's update, packed):
+//   I = alpha I + (beta_i k_j^2 + (1 - alpha) I_prior),  M = alpha M + (beta_i v_i) k_j.
+template <int NP>
+__device__ __forceinline__ void step_pairs(float2 (&M)[NP], float2 (&I)[NP], const float2 (&k)[NP], const Tok& t) {
+  const float2 a2 = f2(t.alpha), om2 = f2(t.om), b2 = f2(t.b), bv2 = f2(t.bv);
+#pragma unroll
+  for (int p = 0; p < NP; ++p) {
+    I[p] = __ffma2_rn(a2, I[p], __ffma2_rn(b2, __fmul2_rn(k[p], k[p]), om2));
+    M[p] = __ffma2_rn(a2, M[p], __fmul2_rn(bv2, k[p]));
   }
 }
 
@@ -244,11 +255,11 @@ palimpsa_bwd_kernel(BwdArgs a, float* __restrict__ ckpt) {
   constexpr int ES = BF16 ? 2 : 4;
   extern __shared__ __align__(128) unsigned char bsm[];
   const BwdSmem L(DK, ES);
-  auto win_M = reinterpret_cast<float (*)[kNW][DK]>(bsm + L.win);
-  auto win_I = reinterpret_cast<float (*)[kNW][DK]>(bsm + L.win + (size_t)kRowsPerCta * kNW * DK * 4);
+  // window starts, lane-linear (only the owning lane reads them back): [window][pair][thread]
+  float2* winM = reinterpret_cast<float2*>(bsm + L.win);
+  float2* winI = winM + kNW * NP * kThreads;
   auto rowp = reinterpret_cast<float (*)[kWin][kRowsPerCta][3]>(bsm + L.rowp);
-  float* al = reinterpret_cast<float*>(bsm + L.al);
-  float* om = reinterpret_cast<float*>(bsm + L.om);
+  const float* al = reinterpret_cast<const float*>(bsm + L.al);
 
   const int DV = a.d_v, T = a.T;
   const int groups = DV / kRowsPerCta;
@@ -288,7 +299,8 @@ palimpsa_bwd_kernel(BwdArgs a, float* __restrict__ ckpt) {
     cp_async_wait_1();
     __syncthreads();  // segment s staged by every thread
     const unsigned char* st = bsm + (size_t)(s & 1) * L.stage;
-    fill_gates(st, L, tn, A_h, Ip, al, om);
+    prepare_segment<DK, BF16>(st, bsm, L, tn, A_h, Ip);
+    const float* kf = reinterpret_cast<const float*>(BF16 ? bsm + L.kf : st + L.k);
     float* cp = my_ckpt + ((size_t)s * kRowsPerCta + rl) * DK * 2;
 #pragma unroll
     for (int p = 0; p < NP; ++p) {
@@ -298,10 +310,10 @@ palimpsa_bwd_kernel(BwdArgs a, float* __restrict__ ckpt) {
     __syncthreads();  // gates ready
     for (int u = 0; u < tn; ++u) {
       float2 k[NP];
-      col_pairs<BF16, NC>(st + L.k, DK, u, c0, k);
-      fwd_step<NP>(M, I, k, tok_row<BF16>(st, L, al, om, u, rl));
+      f32_pairs<NC>(kf, DK, u, c0, k);
+      step_pairs<NP>(M, I, k, tok(bsm, L, u, rl));
     }
-    __syncthreads();  // this stage and the gate tables are free again
+    __syncthreads();  // this stage and the tables are free again
   }
 
   // ---- adjoints at t = T from the final-state gradients
@@ -327,7 +339,9 @@ palimpsa_bwd_kernel(BwdArgs a, float* __restrict__ ckpt) {
     const unsigned char* st = bsm + (size_t)(s & 1) * L.stage;
     const float* dts = reinterpret_cast<const float*>(st + L.dt);
     const float* dys = reinterpret_cast<const float*>(st + L.dy);
-    fill_gates(st, L, tn, A_h, Ip, al, om);
+    prepare_segment<DK, BF16>(st, bsm, L, tn, A_h, Ip);
+    const float* kf = reinterpret_cast<const float*>(BF16 ? bsm + L.kf : st + L.k);
+    const float* qf = reinterpret_cast<const float*>(BF16 ? bsm + L.qf : st + L.q);
     const float* cp = my_ckpt + ((size_t)s * kRowsPerCta + rl) * DK * 2;
 #pragma unroll
     for (int p = 0; p < NP; ++p) {
@@ -340,13 +354,13 @@ palimpsa_bwd_kernel(BwdArgs a, float* __restrict__ ckpt) {
       if (u % kWin == 0) {
 #pragma unroll
         for (int p = 0; p < NP; ++p) {
-          *reinterpret_cast<float2*>(&win_M[rl][u / kWin][c0 + 2 * p]) = M[p];
-          *reinterpret_cast<float2*>(&win_I[rl][u / kWin][c0 + 2 * p]) = I[p];
+          winM[((u / kWin) * NP + p) * kThreads + threadIdx.x] = M[p];
+          winI[((u / kWin) * NP + p) * kThreads + threadIdx.x] = I[p];
         }
       }
       float2 k[NP];
-      col_pairs<BF16, NC>(st + L.k, DK, u, c0, k);
-      fwd_step<NP>(M, I, k, tok_row<BF16>(st, L, al, om, u, rl));
+      f32_pairs<NC>(kf, DK, u, c0, k);
+      step_pairs<NP>(M, I, k, tok(bsm, L, u, rl));
     }
     const int nwin = (tn + kWin - 1) / kWin;
     for (int wi = nwin - 1; wi >= 0; --wi) {
@@ -355,18 +369,17 @@ palimpsa_bwd_kernel(BwdArgs a, float* __restrict__ ckpt) {
       float2 Ms[kWin + 1][NP], Is[kWin + 1][NP];
 #pragma unroll
       for (int p = 0; p < NP; ++p) {
-        Ms[0][p] = *reinterpret_cast<const float2*>(&win_M[rl][wi][c0 + 2 * p]);
-        Is[0][p] = *reinterpret_cast<const float2*>(&win_I[rl][wi][c0 + 2 * p]);
+        Ms[0][p] = winM[(wi * NP + p) * kThreads + threadIdx.x];
+        Is[0][p] = winI[(wi * NP + p) * kThreads + threadIdx.x];
       }
 #pragma unroll
       for (int uu = 0; uu < kWin; ++uu) {
         if (uu < n) {
           float2 k[NP];
-          col_pairs<BF16, NC>(st + L.k, DK, uw + uu, c0, k);
-          const TokRow tr = tok_row<BF16>(st, L, al, om, uw + uu, rl);
+          f32_pairs<NC>(kf, DK, uw + uu, c0, k);
 #pragma unroll
           for (int p = 0; p < NP; ++p) { Ms[uu + 1][p] = Ms[uu][p]; Is[uu + 1][p] = Is[uu][p]; }
-          fwd_step<NP>(Ms[uu + 1], Is[uu + 1], k, tr);
+          step_pairs<NP>(Ms[uu + 1], Is[uu + 1], k, tok(bsm, L, uw + uu, rl));
         }
       }
       // sweep the window backwards
@@ -375,9 +388,9 @@ palimpsa_bwd_kernel(BwdArgs a, float* __restrict__ ckpt) {
         if (uu < n) {
           const int u = uw + uu;
           float2 k[NP], q[NP];
-          col_pairs<BF16, NC>(st + L.k, DK, u, c0, k);
-          col_pairs<BF16, NC>(st + L.q, DK, u, c0, q);
-          const TokRow tr = tok_row<BF16>(st, L, al, om, u, rl);
+          f32_pairs<NC>(kf, DK, u, c0, k);
+          f32_pairs<NC>(qf, DK, u, c0, q);
+          const Tok tr = tok(bsm, L, u, rl);
           const float dyi = dys[u * kRowsPerCta + rl];
           const float2 dy2 = f2(dyi), ndy2 = f2(-dyi), bv2 = f2(tr.bv), tb2 = f2(2.f * tr.b), nIp2 = f2(-Ip);
           float2 sbv = f2(0.f), sb = f2(0.f), sal = f2(0.f), sgi = f2(0.f);
@@ -419,7 +432,7 @@ palimpsa_bwd_kernel(BwdArgs a, float* __restrict__ ckpt) {
             rowp[w][uu][rl][1] = r_b;
             rowp[w][uu][rl][2] = r_al;
           }
-          dIp_acc = fmaf(tr.om / Ip, sgi.x + sgi.y, dIp_acc);  // (1 - alpha_t) sum gI; reduced at the end
+          dIp_acc = fmaf(tr.oma, sgi.x + sgi.y, dIp_acc);  // (1 - alpha_t) sum gI; reduced at the end
           // carry the adjoints to t - 1
           const float2 a2 = f2(tr.alpha);
 #pragma unroll
