@@ -428,12 +428,7 @@ struct Kernels {
     float* seg_state = scratch;
     if (nseg > 1) {
       float* seg_gamma = scratch + (size_t)heads * (nseg - 1) * 2 * a.d_v * a.d_k;
-      auto sum_k = palimpsa_fwd_summary_kernel<DK, BF16, RG, kRowsPerThread>;
-      e = cudaFuncSetAttribute(sum_k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
-      if (e != cudaSuccess) return e;
-      sum_k<<<(unsigned)(heads * (nseg - 1) * groups), kThreads, sm, s>>>(a, C, nseg, seg_len, seg_state,
-                                                                          seg_gamma);
-      if ((e = cudaGetLastError()) != cudaSuccess) return e;
+      if ((e = summaries(a, C, nseg - 1, seg_len, seg_state, seg_gamma, s)) != cudaSuccess) return e;
       const long quads = heads * a.d_v * a.d_k / 4;
       palimpsa_fwd_carry_kernel<<<(unsigned)((quads + 255) / 256), 256, 0, s>>>(a, nseg, seg_len, seg_state,
                                                                                  seg_gamma);
@@ -443,9 +438,11 @@ struct Kernels {
     return cudaGetLastError();
   }
 
-  // Pass A over all `nseg` segments of every head (summary slots [bh][seg]).
+  // Pass A over segments 0 .. nseg - 1 of every head (summary slots [bh][seg]):
+  // on the tensor cores where the inputs allow, else with FFMA.
   static cudaError_t summaries(const FwdArgs& a, int C, int nseg, int seg_len, float* st, float* gm,
                                cudaStream_t s) {
+    if (summary_tc_eligible(a)) return launch_summary_tc(a, nseg, seg_len, st, gm, s);
     const size_t sm = smem(a, C);
     auto sum_k = palimpsa_fwd_summary_kernel<DK, BF16, RG, kRowsPerThread>;
     cudaError_t e = cudaFuncSetAttribute(sum_k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);

@@ -113,6 +113,13 @@ cudaError_t launch_step(const StepArgs& a, cudaStream_t s);
 cudaError_t launch_segment_summary(const FwdArgs& a, float* summary, float* gamma, cudaStream_t s,
                                    ScratchProvider* sp);
 
+// Pass A on the tensor cores (fwd_summary_tc.cu): bf16 inputs, d_k = 128,
+// d_v a multiple of 32 up to 128. Summaries of segments 0 ..
+// nslot - 1 of every head, laid out as the FFMA pass A writes them.
+bool summary_tc_eligible(const FwdArgs& a);
+cudaError_t launch_summary_tc(const FwdArgs& a, int nslot, int seg_len, float* seg_state, float* seg_gamma,
+                              cudaStream_t s);
+
 // Affine fold of R segment summaries, in order (fold.cu):
 //   (M, Ibar) <- Gamma_s (M, Ibar) + (dM_s, dIbar_s),   s = 0 .. R-1.
 // Summary element (s, bh, part, e) is at sum[s*sum_ss + bh*sum_sh + part*DVK + e],
