@@ -253,6 +253,8 @@ def run_ours(args, ws, rank, local):
         raise RuntimeError(f"device status after timing: {pal.palimpsa_status_string(st)}")
 
     ms_step = ms_total / args.steps
+    # kernel launches of one forward call: 1, or 3 when the planner splits time
+    fwd_launches = pal.palimpsa_forward_plan(B, H, T, dk, dv, chunk=wl.chunk, bf16=wl.bf16)["launches"]
     head_tokens = B * H * (T + S)
     value = whole_job_rate(head_tokens, ws, ms_step / 1e3)
 
@@ -418,7 +420,7 @@ def run_ours(args, ws, rank, local):
                        "l2": "inputs larger than L2 (state alone is %.0f MB)" % (B * H * dv * dk * 8 / 1e6),
                        "parallelism": f"replicas x{ws}" if ws > 1 else "single GPU"},
             "roofline": roofline, "kernels": kernels, "cpu_baseline": cpu, "e2e": e2e,
-            "gpu_launches": (1 + S) * args.steps, "clocks": clocks,
+            "gpu_launches": (fwd_launches + S) * args.steps, "clocks": clocks,
         }
         print(json.dumps(line), flush=True)
     if ws > 1:

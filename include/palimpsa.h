@@ -116,6 +116,24 @@ palimpsa_status palimpsa_forward_chunked(
     palimpsa_dtype in_dtype, void* cuda_stream);
 
 /*
+ * palimpsa_forward_plan — the launch plan palimpsa_forward_chunked (and the
+ * fused, varlen and no-allocation variants) would use for these sizes on the
+ * current device, computed by the same planner; nothing is launched or
+ * allocated. Outputs (host pointers, all required):
+ *   segments      time segments per sequence (1 = no time split)
+ *   segment_len   tokens per segment (a multiple of the staging chunk)
+ *   launches      kernel launches of one forward call: 1, or 3 with a time
+ *                 split (summaries, carry, recurrence)
+ *   scratch_bytes temporary device memory the call takes from the pool
+ * For a packed batch pass N as B and max_seqlen as T. Honours
+ * palimpsa_set_forward_segments. Errors as for palimpsa_forward_chunked;
+ * PALIMPSA_ERR_CUDA when the device cannot be queried.
+ */
+palimpsa_status palimpsa_forward_plan(
+    int B, int H, int T, int d_k, int d_v, int chunk, palimpsa_dtype in_dtype,
+    int* segments, int* segment_len, int* launches, size_t* scratch_bytes);
+
+/*
  * palimpsa_forward_chunked_noalloc — palimpsa_forward_chunked for callers that
  * must not allocate device memory. (The paper has no counterpart: this is a
  * deployment variant of the same computation.)

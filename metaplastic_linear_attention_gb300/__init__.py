@@ -23,6 +23,7 @@ from .binding import (  # noqa: F401
     palimpsa_debug_withhold_first_copy,
     palimpsa_forward_chunked,
     palimpsa_forward_fused,
+    palimpsa_forward_plan,
     palimpsa_forward_varlen,
     palimpsa_forward_without_meta,
     palimpsa_get_device_status,

@@ -81,6 +81,10 @@ def load_library(path: str | None = None):
         lib.palimpsa_segment_summary.argtypes = [vp, vp, vp, vp, fp, fp, fp, fp, fp, i, i, i, i, i, i, i, vp]
         lib.palimpsa_state_combine.restype = i
         lib.palimpsa_state_combine.argtypes = [fp, fp, i, fp, fp, fp, fp, fp, i, i, i, i, vp]
+        lib.palimpsa_forward_plan.restype = i
+        lib.palimpsa_forward_plan.argtypes = [i, i, i, i, i, i, i, ctypes.POINTER(ctypes.c_int),
+                                              ctypes.POINTER(ctypes.c_int), ctypes.POINTER(ctypes.c_int),
+                                              ctypes.POINTER(ctypes.c_size_t)]
         lib.palimpsa_step_fused.restype = i
         lib.palimpsa_step_fused.argtypes = [vp, vp, vp, vp, fp, fp, fp, fp, fp, fp, fp, i, i, i, i, u, i, vp]
         lib.palimpsa_step.restype = i
@@ -99,6 +103,18 @@ def load_library(path: str | None = None):
         lib.palimpsa_set_forward_segments.argtypes = [i]
         _lib = lib
         return lib
+
+
+def palimpsa_forward_plan(B, H, T, d_k, d_v, *, chunk: int = 0, bf16: bool = True):
+    """The forward's launch plan on the current device (see palimpsa.h): a dict
+    with segments, segment_len, launches and scratch_bytes."""
+    seg, sl, ln, sb = ctypes.c_int(), ctypes.c_int(), ctypes.c_int(), ctypes.c_size_t()
+    rc = load_library().palimpsa_forward_plan(int(B), int(H), int(T), int(d_k), int(d_v), int(chunk),
+                                              PALIMPSA_BF16 if bf16 else PALIMPSA_F32, ctypes.byref(seg),
+                                              ctypes.byref(sl), ctypes.byref(ln), ctypes.byref(sb))
+    if rc != 0:
+        raise PalimpsaError(rc, "palimpsa_forward_plan")
+    return {"segments": seg.value, "segment_len": sl.value, "launches": ln.value, "scratch_bytes": sb.value}
 
 
 def palimpsa_status_string(code: int) -> str:

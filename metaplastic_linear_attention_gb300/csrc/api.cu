@@ -177,6 +177,25 @@ palimpsa_status palimpsa_forward_chunked(const void* q, const void* k, const voi
                       cuda_stream, Prologue{});
 }
 
+palimpsa_status palimpsa_forward_plan(int B, int H, int T, int d_k, int d_v, int chunk, palimpsa_dtype in_dtype,
+                                      int* segments, int* segment_len, int* launches, size_t* scratch_bytes) {
+  if (!segments || !segment_len || !launches || !scratch_bytes) return PALIMPSA_ERR_NULL;
+  if (in_dtype != PALIMPSA_F32 && in_dtype != PALIMPSA_BF16) return PALIMPSA_ERR_DTYPE;
+  if (!sizes_ok(B, H, T, d_k, d_v)) return PALIMPSA_ERR_SHAPE;
+  if (!supported_dims(d_k, d_v)) return PALIMPSA_ERR_UNSUPPORTED;
+  if (chunk != 0 && chunk != 16 && chunk != 32 && chunk != 64) return PALIMPSA_ERR_UNSUPPORTED;
+  FwdArgs a{nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr,
+            nullptr, B, H, T, d_k, d_v, chunk == 0 ? 32 : chunk, in_dtype == PALIMPSA_BF16, nullptr, 0, 0,
+            g_forward_segments.load(), Prologue{}};
+  int nseg = 1, seg_len = 0;
+  if (plan_forward(a, &nseg, &seg_len) != cudaSuccess) return PALIMPSA_ERR_CUDA;
+  *segments = nseg;
+  *segment_len = seg_len;
+  *launches = nseg > 1 ? 3 : 1;
+  *scratch_bytes = nseg > 1 ? (size_t)B * H * (nseg - 1) * (2 * (size_t)d_v * d_k + 1) * sizeof(float) : 0;
+  return PALIMPSA_OK;
+}
+
 palimpsa_status palimpsa_forward_varlen(const void* q, const void* k, const void* v, const void* beta,
                                         const float* d_t, const float* A, const float* I_prior, const float* mu0,
                                         const float* I0, float* y, float* mu_T, float* I_T, const int* cu_seqlens,

@@ -613,6 +613,17 @@ cudaError_t launch_forward_chunked(const FwdArgs& a, cudaStream_t s, ScratchProv
   return a.bf16 ? plan_and_run<64, true>(a, p, s, sp) : plan_and_run<64, false>(a, p, s, sp);
 }
 
+cudaError_t plan_forward(const FwdArgs& a, int* nseg, int* seg_len) {
+  bool ok = false;
+  Plan p = base_plan(a, max_smem_optin(), &ok);
+  if (!ok) return cudaErrorInvalidConfiguration;
+  if (a.d_k == 128) p = a.bf16 ? plan_segments<128, true>(a, p) : plan_segments<128, false>(a, p);
+  else p = a.bf16 ? plan_segments<64, true>(a, p) : plan_segments<64, false>(a, p);
+  *nseg = p.nseg;
+  *seg_len = p.seg_len;
+  return cudaGetLastError();
+}
+
 cudaError_t launch_segment_summary(const FwdArgs& a, float* summary, float* gamma, cudaStream_t s,
                                    ScratchProvider* sp) {
   bool ok = false;

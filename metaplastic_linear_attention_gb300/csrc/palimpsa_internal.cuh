@@ -106,6 +106,8 @@ struct ScratchProvider {
 // Launchers (return the launch error, cudaSuccess on success). Arguments are
 // validated by the caller.
 cudaError_t launch_forward_chunked(const FwdArgs& a, cudaStream_t s, ScratchProvider* sp);
+// The time-split plan launch_forward_chunked would use (queries the device; launches nothing).
+cudaError_t plan_forward(const FwdArgs& a, int* nseg, int* seg_len);
 cudaError_t launch_step(const StepArgs& a, cudaStream_t s);
 // Summary of the whole token range of each head from a zero state (pass A over
 // the planned segments, then folded): summary [B,H,2,d_v,d_k] = (dM, dIbar),

@@ -242,3 +242,17 @@ def test_state_combine_rejects_bad_arguments(lib, over, code):
     assert lib.palimpsa_state_combine(args["S"], args["G"], args["R"], args["I_prior"], args["mu0"], args["I0"],
                                       args["mu"], args["I"], args["B"], args["H"], args["d_k"], args["d_v"],
                                       None) == code
+
+
+@pytest.mark.parametrize("over,code", [
+    (dict(segments=None), ERR_NULL), (dict(scratch=None), ERR_NULL), (dict(dtype=4), ERR_DTYPE),
+    (dict(B=0), ERR_SHAPE), (dict(T=-1), ERR_SHAPE), (dict(d_k=96), ERR_UNSUPPORTED), (dict(chunk=48), ERR_UNSUPPORTED),
+])
+def test_forward_plan_rejects_bad_arguments(lib, over, code):
+    seg, sl, ln, sb = ctypes.c_int(), ctypes.c_int(), ctypes.c_int(), ctypes.c_size_t()
+    args = dict(B=4, H=16, T=2048, d_k=128, d_v=64, chunk=0, dtype=1, segments=ctypes.byref(seg),
+                seg_len=ctypes.byref(sl), launches=ctypes.byref(ln), scratch=ctypes.byref(sb))
+    args.update(over)
+    assert lib.palimpsa_forward_plan(args["B"], args["H"], args["T"], args["d_k"], args["d_v"], args["chunk"],
+                                     args["dtype"], args["segments"], args["seg_len"], args["launches"],
+                                     args["scratch"]) == code

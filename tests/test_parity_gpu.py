@@ -460,3 +460,20 @@ def test_backward_empty_sequence():
     out, ref, _ = _bwd_case(1, 2, 0, 128, 64, False, True, True, seed=4500)
     assert rel_l2(out["dmu0"].cpu(), ref["mu0"]) <= 1e-6 and rel_l2(out["dI0"].cpu(), ref["I0"]) <= 1e-6
     assert rel_l2(out["dI_prior"].cpu(), ref["I_prior"]) <= 1e-6 or float(abs(out["dI_prior"]).max()) == 0.0
+
+
+def test_forward_plan_reports_the_split():
+    """palimpsa_forward_plan: many heads run unsplit in one launch; few long heads are
+    split into segments (three launches) with scratch per boundary; a forced count is
+    honoured."""
+    wide = pal.palimpsa_forward_plan(256, 32, 512, 128, 64)
+    assert wide["segments"] == 1 and wide["launches"] == 1 and wide["scratch_bytes"] == 0
+    few = pal.palimpsa_forward_plan(1, 32, 32768, 128, 64)
+    assert few["segments"] > 1 and few["launches"] == 3
+    assert few["scratch_bytes"] == 32 * (few["segments"] - 1) * (2 * 64 * 128 + 1) * 4
+    assert few["segment_len"] * few["segments"] >= 32768 > few["segment_len"] * (few["segments"] - 1)
+    pal.palimpsa_set_forward_segments(4)
+    try:
+        assert pal.palimpsa_forward_plan(2, 3, 1000, 128, 64)["segments"] == 4
+    finally:
+        pal.palimpsa_set_forward_segments(0)
