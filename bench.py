@@ -310,7 +310,7 @@ def run_ours(args, ws, rank, local):
         "avg_ms": nometa_ms, "head_tokens_per_s": B * H * T / (nometa_ms / 1e3),
         "palimpsa_forward_over_comparator": fwd_avg_ms / nometa_ms,
         "note": "same scan inputs with the importance frozen at I_prior (Mamba2 / scalar-decay form), "
-                "no time split; timed after the timed region"}
+                "same time-split plan as the forward; timed after the timed region"}
 
     # The fused prologue (palimpsa_forward_fused / palimpsa_step_fused): the same
     # workload from raw projections with the Palimpsa-D q/k norm and the v* input,

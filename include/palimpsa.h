@@ -86,7 +86,9 @@ typedef enum {
  * When B*H heads are too few to fill the GPU, the sequence is cut into
  * segments whose summaries are scanned first (the affine carry of slide 9);
  * that path takes temporary device memory (2 * d_v * d_k + 1 floats per head
- * and segment boundary) in stream order on `cuda_stream`, from a memory pool
+ * and segment boundary, plus 2 * d_v * d_k floats per head for a copy of the
+ * initial state, so that mu_T / I_T may alias mu0 / I0 even when time is split)
+ * in stream order on `cuda_stream`, from a memory pool
  * the library creates per device and that keeps what it has reserved (at most
  * the largest scratch one call needed) until the process exits. An allocation
  * failure returns PALIMPSA_ERR_CUDA. Results match the unsplit scan up to
@@ -153,8 +155,9 @@ palimpsa_status palimpsa_forward_plan(
  * Arguments, layouts, results and errors are those of
  * palimpsa_forward_chunked, plus one error: when the launch plan needs more
  * than 16 MiB of scratch it returns PALIMPSA_ERR_SCRATCH_LIMIT and launches
- * nothing. The plan needs 4 * (2 * d_v * d_k + 1) bytes per head and segment
- * boundary (about 64 KiB at d_v = 64, d_k = 128, so 255 head-boundaries fit);
+ * nothing. The plan needs about 8 * d_v * d_k bytes per head and segment
+ * (64 KiB at d_v = 64, d_k = 128, so about 255 head-segments fit; the exact
+ * figure is the scratch_bytes of palimpsa_forward_plan);
  * palimpsa_set_forward_segments(1) makes any call fit (one segment needs no
  * scratch), smaller segment counts make larger calls fit.
  *
@@ -206,8 +209,7 @@ palimpsa_status palimpsa_forward_chunked_noalloc(
  * whose offsets break the rules above is skipped (its outputs are left as
  * they were) and latches PALIMPSA_ERR_DOMAIN in the device status. Long
  * sequences are cut into segments as in palimpsa_forward_chunked, planned
- * from max_seqlen, with scratch for 2 * d_v * d_k + 1 floats per sequence,
- * head and segment boundary.
+ * from max_seqlen, with scratch as for the forward (per sequence and head).
  */
 palimpsa_status palimpsa_forward_varlen(
     const void* q, const void* k, const void* v, const void* beta,
@@ -237,7 +239,7 @@ palimpsa_status palimpsa_forward_varlen(
  *   summary  [B, H, 2, d_v, d_k] fp32 out: [..., 0, :, :] = dM, [..., 1, :, :] = dIbar
  *   gamma    [B, H] fp32 out
  * Long ranges are cut into segments as in the forward (scratch from the same
- * pool: 2 * d_v * d_k + 1 floats per head and segment).
+ * pool: 2 * d_v * d_k + 1 floats per head and segment, when split).
  */
 palimpsa_status palimpsa_segment_summary(
     const void* q, const void* k, const void* v, const void* beta,
@@ -356,8 +358,10 @@ palimpsa_status palimpsa_step_fused(
  * Palimpsa's kernel with a Simple GLA kernel of this scalar-decay form).
  * Arguments and conventions are those of palimpsa_forward_chunked without the
  * precision state: mu0 [B,H,d_v,d_k] or NULL (= 0), y [B,H,T,d_v],
- * mu_T [B,H,d_v,d_k] (may alias mu0). No time split: one CTA per (head, row
- * group) runs the whole sequence.
+ * mu_T [B,H,d_v,d_k] (may alias mu0). Few long sequences are cut into time
+ * segments exactly as palimpsa_forward_chunked plans them (its state
+ * m = I_prior mu follows Palimpsa's M recurrence, so the same summaries and
+ * carry apply), with the same scratch from the library's pool.
  */
 palimpsa_status palimpsa_forward_without_meta(
     const void* q, const void* k, const void* v, const void* beta,

@@ -192,7 +192,7 @@ palimpsa_status palimpsa_forward_plan(int B, int H, int T, int d_k, int d_v, int
   *segments = nseg;
   *segment_len = seg_len;
   *launches = nseg > 1 ? 3 : 1;
-  *scratch_bytes = nseg > 1 ? (size_t)B * H * (nseg - 1) * (2 * (size_t)d_v * d_k + 1) * sizeof(float) : 0;
+  *scratch_bytes = nseg > 1 ? SplitScratch((long long)B * H, nseg, (long long)d_v * d_k).total * sizeof(float) : 0;
   return PALIMPSA_OK;
 }
 
@@ -315,8 +315,9 @@ palimpsa_status palimpsa_forward_without_meta(const void* q, const void* k, cons
   if (palimpsa_status s = status_word(&st)) return s;
   FwdArgs a{q, k, v, beta, d_t, A, I_prior, mu0, nullptr, y, mu_T, nullptr, B, H, T, d_k, d_v,
             chunk == 0 ? 32 : chunk, in_dtype == PALIMPSA_BF16, st,
-            g_wait_timeout_ns.load(), g_withhold_first_copy.load(), 1};
-  if (launch_forward_without_meta(a, static_cast<cudaStream_t>(cuda_stream)) != cudaSuccess)
+            g_wait_timeout_ns.load(), g_withhold_first_copy.load(), g_forward_segments.load()};
+  StreamOrderedScratch scratch;
+  if (launch_forward_without_meta(a, static_cast<cudaStream_t>(cuda_stream), &scratch) != cudaSuccess)
     return PALIMPSA_ERR_CUDA;
   return PALIMPSA_OK;
 }

@@ -99,7 +99,10 @@ palimpsa_fwd_chunked_kernel(FwdArgs a, int C, int nseg, int seg_len, const float
   float2 Ist[R][2 * NV], Mst[R][2 * NV];
   const size_t state_base = ((size_t)tl.bh * DV + tl.row0) * DK;
   const float* carried = nullptr;
+  const float* init = nullptr;  // the first segment of a split reads the carry's copy of (M_0, I_0)
   if (tl.seg > 0) carried = seg_state + ((size_t)tl.bh * (nseg - 1) + (tl.seg - 1)) * 2 * DV * DK;
+  else if (nseg > 1)
+    init = seg_state + SplitScratch((long long)a.B * a.H, nseg, (long long)DV * DK).init + (size_t)tl.bh * 2 * DV * DK;
 #pragma unroll
   for (int r = 0; r < R; ++r) {
 #pragma unroll
@@ -110,6 +113,10 @@ palimpsa_fwd_chunked_kernel(FwdArgs a, int C, int nseg, int seg_len, const float
         m4 = *reinterpret_cast<const float4*>(carried + e);
         const float4 ib = *reinterpret_cast<const float4*>(carried + (size_t)DV * DK + e);
         i4 = make_float4(Ip + ib.x, Ip + ib.y, Ip + ib.z, Ip + ib.w);
+      } else if (init) {
+        m4 = *reinterpret_cast<const float4*>(init + e);
+        i4 = *reinterpret_cast<const float4*>(init + (size_t)DV * DK + e);
+        domain_bad |= !(pos_finite(i4.x) && pos_finite(i4.y) && pos_finite(i4.z) && pos_finite(i4.w));
       } else {
         const size_t off = state_base + (size_t)(lr0 + r) * DK + 32 * s + 4 * cg;
         i4 = a.I0 ? *reinterpret_cast<const float4*>(a.I0 + off) : make_float4(Ip, Ip, Ip, Ip);
@@ -388,6 +395,9 @@ palimpsa_fwd_carry_kernel(FwdArgs a, int nseg, int seg_len, float* __restrict__ 
   const float4 u = a.mu0 ? *reinterpret_cast<const float4*>(a.mu0 + off) : make_float4(0.f, 0.f, 0.f, 0.f);
   float4 m = make_float4(i0.x * u.x, i0.y * u.y, i0.z * u.z, i0.w * u.w);
   float4 ib = make_float4(i0.x - Ip, i0.y - Ip, i0.z - Ip, i0.w - Ip);
+  float* init = seg_state + SplitScratch((long long)a.B * a.H, nseg, (long long)DVK).init + (size_t)bh * 2 * DVK;
+  *reinterpret_cast<float4*>(init + e) = m;
+  *reinterpret_cast<float4*>(init + DVK + e) = i0;
   for (int s = 0; s < nb; ++s) {
     const float g = seg_gamma[(size_t)bh * (nseg - 1) + s];
     float* slot = seg_state + ((size_t)bh * (nseg - 1) + s) * 2 * DVK;
@@ -425,16 +435,20 @@ struct Kernels {
     auto main_k = palimpsa_fwd_chunked_kernel<DK, BF16, RG, kRowsPerThread>;
     cudaError_t e = cudaFuncSetAttribute(main_k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
     if (e != cudaSuccess) return e;
-    float* seg_state = scratch;
-    if (nseg > 1) {
-      float* seg_gamma = scratch + (size_t)heads * (nseg - 1) * 2 * a.d_v * a.d_k;
-      if ((e = summaries(a, C, nseg - 1, seg_len, seg_state, seg_gamma, s)) != cudaSuccess) return e;
-      const long quads = heads * a.d_v * a.d_k / 4;
-      palimpsa_fwd_carry_kernel<<<(unsigned)((quads + 255) / 256), 256, 0, s>>>(a, nseg, seg_len, seg_state,
-                                                                                 seg_gamma);
-      if ((e = cudaGetLastError()) != cudaSuccess) return e;
-    }
-    main_k<<<(unsigned)(heads * nseg * groups), kThreads, sm, s>>>(a, C, nseg, seg_len, seg_state);
+    if (nseg > 1 && (e = prefix(a, C, nseg, seg_len, scratch, s)) != cudaSuccess) return e;
+    main_k<<<(unsigned)(heads * nseg * groups), kThreads, sm, s>>>(a, C, nseg, seg_len, scratch);
+    return cudaGetLastError();
+  }
+
+  // Passes A and B: the state at the start of segments 1 .. nseg - 1 of every
+  // head into scratch[(bh, seg - 1)] as (M, Ibar).
+  static cudaError_t prefix(const FwdArgs& a, int C, int nseg, int seg_len, float* scratch, cudaStream_t s) {
+    const long heads = (long)a.B * a.H;
+    float* seg_gamma = scratch + SplitScratch(heads, nseg, (long long)a.d_v * a.d_k).gammas;
+    cudaError_t e = summaries(a, C, nseg - 1, seg_len, scratch, seg_gamma, s);
+    if (e != cudaSuccess) return e;
+    const long quads = heads * a.d_v * a.d_k / 4;
+    palimpsa_fwd_carry_kernel<<<(unsigned)((quads + 255) / 256), 256, 0, s>>>(a, nseg, seg_len, scratch, seg_gamma);
     return cudaGetLastError();
   }
 
@@ -531,7 +545,7 @@ cudaError_t plan_and_run(const FwdArgs& a, Plan p, cudaStream_t s, ScratchProvid
   const long heads = (long)a.B * a.H;
   float* scratch = nullptr;
   if (p.nseg > 1) {
-    const size_t bytes = (size_t)heads * (p.nseg - 1) * (2 * (size_t)a.d_v * a.d_k + 1) * sizeof(float);
+    const size_t bytes = SplitScratch(heads, p.nseg, (long long)a.d_v * a.d_k).total * sizeof(float);
     cudaError_t e = sp->acquire(bytes, s, &scratch);
     if (e != cudaSuccess) return e;
   }
@@ -611,6 +625,46 @@ cudaError_t launch_forward_chunked(const FwdArgs& a, cudaStream_t s, ScratchProv
   if (!ok) return cudaErrorInvalidConfiguration;
   if (a.d_k == 128) return a.bf16 ? plan_and_run<128, true>(a, p, s, sp) : plan_and_run<128, false>(a, p, s, sp);
   return a.bf16 ? plan_and_run<64, true>(a, p, s, sp) : plan_and_run<64, false>(a, p, s, sp);
+}
+
+cudaError_t launch_split_prefix(const FwdArgs& a, int nseg, int seg_len, float* scratch, cudaStream_t s) {
+  bool ok = false;
+  const Plan p = base_plan(a, max_smem_optin(), &ok);
+  if (!ok) return cudaErrorInvalidConfiguration;
+  auto go = [&](auto tag) -> cudaError_t {
+    using K = decltype(tag);
+    return K::prefix(a, p.C, nseg, seg_len, scratch, s);
+  };
+  if (a.d_k == 128) {
+    if (a.bf16) {
+      switch (p.RG) {
+        case 64: return go(Kernels<128, true, 64>{});
+        case 32: return go(Kernels<128, true, 32>{});
+        case 16: return go(Kernels<128, true, 16>{});
+        default: return go(Kernels<128, true, 8>{});
+      }
+    }
+    switch (p.RG) {
+      case 64: return go(Kernels<128, false, 64>{});
+      case 32: return go(Kernels<128, false, 32>{});
+      case 16: return go(Kernels<128, false, 16>{});
+      default: return go(Kernels<128, false, 8>{});
+    }
+  }
+  if (a.bf16) {
+    switch (p.RG) {
+      case 64: return go(Kernels<64, true, 64>{});
+      case 32: return go(Kernels<64, true, 32>{});
+      case 16: return go(Kernels<64, true, 16>{});
+      default: return go(Kernels<64, true, 8>{});
+    }
+  }
+  switch (p.RG) {
+    case 64: return go(Kernels<64, false, 64>{});
+    case 32: return go(Kernels<64, false, 32>{});
+    case 16: return go(Kernels<64, false, 16>{});
+    default: return go(Kernels<64, false, 8>{});
+  }
 }
 
 cudaError_t plan_forward(const FwdArgs& a, int* nseg, int* seg_len) {

@@ -10,7 +10,10 @@
 //
 // The kernel shares the forward's staging (bulk-copy ring, bounded waits,
 // once-per-CTA conversion) and thread tile (2 rows x d_k / 8 columns, row
-// teams of 8 lanes), and keeps only mu in registers. Per state element and
+// teams of 8 lanes), and keeps only mu in registers. Time split: its state
+// m = I_prior mu follows Palimpsa's M recurrence exactly (m_t = alpha m_{t-1} +
+// (beta_i v_i) k_j), so the forward's passes A and B give m at every segment
+// start and this kernel runs each segment from m / I_prior. Per state element and
 // token it costs one FMUL and two FFMA (1.5 packed f32x2 instructions) and no
 // reciprocal, against Palimpsa's 3 packed instructions plus one SFU
 // reciprocal: the measured ratio is the price of metaplasticity.
@@ -25,15 +28,16 @@ constexpr int kRows = 2;  // rows per thread
 
 template <int DK, bool BF16, int RG>
 __global__ void __launch_bounds__(RG / (4 * kRows) * 32)
-palimpsa_fwd_nometa_kernel(FwdArgs a, int C) {
+palimpsa_fwd_nometa_kernel(FwdArgs a, int C, int nseg, int seg_len, const float* __restrict__ seg_state) {
   constexpr int R = kRows;
   constexpr int NV = DK / 32;
   constexpr int NTH = RG / (4 * R) * 32;
   constexpr int ES = BF16 ? 2 : 4;
   extern __shared__ __align__(128) unsigned char smem[];
 
-  const int DV = a.d_v, T = a.T;
-  const Tile tl = tile_of(a, RG, 1, T > 0 ? T : 1);
+  const int DV = a.d_v;
+  const Tile tl = tile_of(a, RG, nseg, seg_len);
+  if (tl.bad || tl.seg > tl.last_seg) return;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int cg = lane & (kLanesPerRow - 1);
   const int rt = lane >> 3;
@@ -50,7 +54,7 @@ palimpsa_fwd_nometa_kernel(FwdArgs a, int C) {
   bool domain_bad = !(pos_finite(A_h) && pos_finite(Ip));
   const float rIp = 1.f / Ip;
 
-  const size_t head_tok = (size_t)tl.bh * T;
+  const size_t head_tok = tl.head_tok;
   ChunkPipe<DK, ES> pipe(L, smem, static_cast<const char*>(a.q) + head_tok * DK * ES,
                          static_cast<const char*>(a.k) + head_tok * DK * ES,
                          static_cast<const char*>(a.v) + head_tok * DV * ES,
@@ -59,19 +63,30 @@ palimpsa_fwd_nometa_kernel(FwdArgs a, int C) {
 
   float2 mu[R][2 * NV];
   const size_t state_base = ((size_t)tl.bh * DV + tl.row0) * DK;
+  // segments after the first start from the carried m = I_prior mu
+  const float* carried = nullptr;
+  if (tl.seg > 0) carried = seg_state + ((size_t)tl.bh * (nseg - 1) + (tl.seg - 1)) * 2 * DV * DK;
+  else if (nseg > 1)  // the carry's copy of m_0 = I_prior mu0 (never the caller's mu0, which mu_T may alias)
+    carried = seg_state + SplitScratch((long long)a.B * a.H, nseg, (long long)DV * DK).init + (size_t)tl.bh * 2 * DV * DK;
 #pragma unroll
   for (int r = 0; r < R; ++r) {
 #pragma unroll
     for (int s = 0; s < NV; ++s) {
       const size_t off = state_base + (size_t)(lr0 + r) * DK + 32 * s + 4 * cg;
-      const float4 u = a.mu0 ? *reinterpret_cast<const float4*>(a.mu0 + off) : make_float4(0.f, 0.f, 0.f, 0.f);
+      float4 u;
+      if (carried) {
+        const float4 m = *reinterpret_cast<const float4*>(carried + (size_t)(tl.row0 + lr0 + r) * DK + 32 * s + 4 * cg);
+        u = make_float4(m.x * rIp, m.y * rIp, m.z * rIp, m.w * rIp);
+      } else {
+        u = a.mu0 ? *reinterpret_cast<const float4*>(a.mu0 + off) : make_float4(0.f, 0.f, 0.f, 0.f);
+      }
       mu[r][2 * s] = make_float2(u.x, u.y);
       mu[r][2 * s + 1] = make_float2(u.z, u.w);
     }
   }
 
-  float* gy = a.y + head_tok * DV + tl.row0 + lr0;
-  const float* gd = a.d_t + head_tok;
+  float* gy = a.y + (head_tok + tl.tb) * DV + tl.row0 + lr0;
+  const float* gd = a.d_t + head_tok + tl.tb;
   for (int c = 0; c < pipe.nch; ++c) {
     const int t0 = pipe.t0_of(c), tc = pipe.tc_of(c);
     if (!pipe.wait(c, a.wait_timeout_ns, a.status)) return;
@@ -128,42 +143,47 @@ palimpsa_fwd_nometa_kernel(FwdArgs a, int C) {
     __syncthreads();  // operands of this chunk fully read before the next conversion
   }
 
+  if (tl.seg == tl.last_seg) {  // the sequence's final state
 #pragma unroll
-  for (int r = 0; r < R; ++r) {
+    for (int r = 0; r < R; ++r) {
 #pragma unroll
-    for (int s = 0; s < NV; ++s) {
-      const size_t off = state_base + (size_t)(lr0 + r) * DK + 32 * s + 4 * cg;
-      const float2 m01 = mu[r][2 * s], m23 = mu[r][2 * s + 1];
-      *reinterpret_cast<float4*>(a.mu_T + off) = make_float4(m01.x, m01.y, m23.x, m23.y);
+      for (int s = 0; s < NV; ++s) {
+        const size_t off = state_base + (size_t)(lr0 + r) * DK + 32 * s + 4 * cg;
+        const float2 m01 = mu[r][2 * s], m23 = mu[r][2 * s + 1];
+        *reinterpret_cast<float4*>(a.mu_T + off) = make_float4(m01.x, m01.y, m23.x, m23.y);
+      }
     }
   }
   if (__any_sync(0xffffffffu, domain_bad) && lane == 0) latch_status(a.status, kStatusDomain);
 }
 
 template <int DK, bool BF16, int RG>
-cudaError_t launch_t(const FwdArgs& a, int C, cudaStream_t s) {
+cudaError_t launch_t(const FwdArgs& a, int C, int nseg, int seg_len, const float* st, cudaStream_t s) {
   const FwdSmem L(C, DK, a.d_v, RG, BF16 ? 2 : 4);
   auto kern = palimpsa_fwd_nometa_kernel<DK, BF16, RG>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)L.total);
   if (e != cudaSuccess) return e;
-  const long ctas = (long)a.B * a.H * (a.d_v / RG);
-  kern<<<(unsigned)ctas, RG / (4 * kRows) * 32, L.total, s>>>(a, C);
+  const long ctas = (long)a.B * a.H * nseg * (a.d_v / RG);
+  kern<<<(unsigned)ctas, RG / (4 * kRows) * 32, L.total, s>>>(a, C, nseg, seg_len, st);
   return cudaGetLastError();
 }
 
 template <int DK, bool BF16>
-cudaError_t launch_rg(const FwdArgs& a, int RG, int C, cudaStream_t s) {
+cudaError_t launch_rg(const FwdArgs& a, int RG, int C, int nseg, int seg_len, const float* st, cudaStream_t s) {
   switch (RG) {
-    case 64: return launch_t<DK, BF16, 64>(a, C, s);
-    case 32: return launch_t<DK, BF16, 32>(a, C, s);
-    case 16: return launch_t<DK, BF16, 16>(a, C, s);
-    default: return launch_t<DK, BF16, 8>(a, C, s);
+    case 64: return launch_t<DK, BF16, 64>(a, C, nseg, seg_len, st, s);
+    case 32: return launch_t<DK, BF16, 32>(a, C, nseg, seg_len, st, s);
+    case 16: return launch_t<DK, BF16, 16>(a, C, nseg, seg_len, st, s);
+    default: return launch_t<DK, BF16, 8>(a, C, nseg, seg_len, st, s);
   }
 }
 
 }  // namespace
 
-cudaError_t launch_forward_without_meta(const FwdArgs& a, cudaStream_t s) {
+// The comparator with the forward's time split: the same plan (segments from
+// the forward's planner), passes A and B for m = I_prior mu, then this kernel
+// over every segment.
+cudaError_t launch_forward_without_meta(const FwdArgs& a, cudaStream_t s, ScratchProvider* sp) {
   int dev = 0, max_smem = 227 * 1024;
   cudaGetDevice(&dev);
   cudaDeviceGetAttribute(&max_smem, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
@@ -174,8 +194,28 @@ cudaError_t launch_forward_without_meta(const FwdArgs& a, cudaStream_t s) {
   int C = a.chunk < 32 ? a.chunk : 32;
   while (C > 16 && FwdSmem(C, a.d_k, a.d_v, RG, es).total > (size_t)max_smem / 3) C /= 2;
   if (FwdSmem(C, a.d_k, a.d_v, RG, es).total > (size_t)max_smem) return cudaErrorInvalidConfiguration;
-  if (a.d_k == 128) return a.bf16 ? launch_rg<128, true>(a, RG, C, s) : launch_rg<128, false>(a, RG, C, s);
-  return a.bf16 ? launch_rg<64, true>(a, RG, C, s) : launch_rg<64, false>(a, RG, C, s);
+  int nseg = 1, seg_len = a.T > 0 ? a.T : 1;
+  cudaError_t e = plan_forward(a, &nseg, &seg_len);
+  if (e != cudaSuccess) return e;
+  float* scratch = nullptr;
+  if (nseg > 1) {
+    const size_t bytes = SplitScratch((long long)a.B * a.H, nseg, (long long)a.d_v * a.d_k).total * sizeof(float);
+    if ((e = sp->acquire(bytes, s, &scratch)) != cudaSuccess) return e;
+    e = launch_split_prefix(a, nseg, seg_len, scratch, s);
+  }
+  if (e == cudaSuccess) {
+    if (a.d_k == 128)
+      e = a.bf16 ? launch_rg<128, true>(a, RG, C, nseg, seg_len, scratch, s)
+                 : launch_rg<128, false>(a, RG, C, nseg, seg_len, scratch, s);
+    else
+      e = a.bf16 ? launch_rg<64, true>(a, RG, C, nseg, seg_len, scratch, s)
+                 : launch_rg<64, false>(a, RG, C, nseg, seg_len, scratch, s);
+  }
+  if (scratch) {
+    const cudaError_t e2 = sp->release(scratch, s);
+    if (e == cudaSuccess) e = e2;
+  }
+  return e;
 }
 
 }  // namespace palimpsa

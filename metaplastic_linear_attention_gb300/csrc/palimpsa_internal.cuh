@@ -106,8 +106,26 @@ struct ScratchProvider {
 // Launchers (return the launch error, cudaSuccess on success). Arguments are
 // validated by the caller.
 cudaError_t launch_forward_chunked(const FwdArgs& a, cudaStream_t s, ScratchProvider* sp);
+// Scratch of a time split, in floats: the carried states [heads][nseg - 1][2][d_v d_k]
+// (summaries until the carry turns them into segment-start states), the gammas
+// [heads][nseg - 1], then, 16-byte aligned, each head's initial state (M_0, I_0)
+// [heads][2][d_v d_k], copied there by the carry so that the first segment never
+// reads mu0 / I0, which the caller may alias with mu_T / I_T.
+struct SplitScratch {
+  size_t gammas, init, total;  // offsets and size in floats
+  __host__ __device__ SplitScratch(long long heads, int nseg, long long dvk) {
+    gammas = (size_t)heads * (nseg - 1) * 2 * dvk;
+    init = (gammas + (size_t)heads * (nseg - 1) + 3) / 4 * 4;
+    total = init + (size_t)heads * 2 * dvk;
+  }
+};
+
 // The time-split plan launch_forward_chunked would use (queries the device; launches nothing).
 cudaError_t plan_forward(const FwdArgs& a, int* nseg, int* seg_len);
+// Passes A and B of a time split with that plan into scratch laid out as
+// SplitScratch: the (M, Ibar) state at the start of segments 1 .. nseg - 1 of
+// every head, and each head's initial (M_0, I_0).
+cudaError_t launch_split_prefix(const FwdArgs& a, int nseg, int seg_len, float* scratch, cudaStream_t s);
 cudaError_t launch_step(const StepArgs& a, cudaStream_t s);
 // Summary of the whole token range of each head from a zero state (pass A over
 // the planned segments, then folded): summary [B,H,2,d_v,d_k] = (dM, dIbar),
@@ -148,8 +166,8 @@ struct FoldArgs {
 };
 cudaError_t launch_fold(const FoldArgs& f, cudaStream_t s);
 // The "without Meta" comparator (importance frozen at I_prior); uses a.mu0,
-// a.y, a.mu_T and ignores a.I0, a.I_T.
-cudaError_t launch_forward_without_meta(const FwdArgs& a, cudaStream_t s);
+// a.y, a.mu_T and ignores a.I0, a.I_T; time split as the forward plans it.
+cudaError_t launch_forward_without_meta(const FwdArgs& a, cudaStream_t s, ScratchProvider* sp);
 // Backward: scratch of backward_scratch_bytes(a) bytes holds the checkpoints.
 size_t backward_scratch_bytes(const BwdArgs& a);
 cudaError_t launch_backward(const BwdArgs& a, float* scratch, cudaStream_t s);

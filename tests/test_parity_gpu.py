@@ -375,9 +375,10 @@ def test_step_sequence_host_pipeline_matches_token_by_token(monkeypatch):
 
 # ----------------------------------------------------------------- "without Meta" comparator
 
+@pytest.mark.parametrize("S", [0, 1, 3])
 @pytest.mark.parametrize("B,H,T,dk,dv,bf16", [(1, 2, 1, 128, 64, True), (2, 3, 77, 128, 64, True),
                                               (1, 2, 130, 64, 24, False), (3, 1, 200, 128, 128, False)])
-def test_without_meta_matches_oracle(B, H, T, dk, dv, bf16):
+def test_without_meta_matches_oracle(B, H, T, dk, dv, bf16, S):
     from oracle import reference_np as rnp
     wl = syn.WORKLOADS["small_layer"].with_(B=B, H=H, T=T, d_k=dk, d_v=dv, bf16=bf16)
     inp = syn.sequence_inputs(wl, seed=900 + T)
@@ -388,8 +389,12 @@ def test_without_meta_matches_oracle(B, H, T, dk, dv, bf16):
                                        mu0=f(mu0))
     gi = _gpu(inp)
     m = mu0.to(DEV)
-    y, mT = pal.palimpsa_forward_without_meta(gi["q"], gi["k"], gi["v"], gi["beta"], gi["d_t"], gi["A"],
-                                              gi["I_prior"], m, mu_T=m)       # in place
+    pal.palimpsa_set_forward_segments(S)   # 0: the forward's automatic plan
+    try:
+        y, mT = pal.palimpsa_forward_without_meta(gi["q"], gi["k"], gi["v"], gi["beta"], gi["d_t"], gi["A"],
+                                                  gi["I_prior"], m, mu_T=m)   # in place
+    finally:
+        pal.palimpsa_set_forward_segments(0)
     assert pal.palimpsa_get_device_status() == 0
     assert rel_l2(y.cpu(), ry) <= TIGHT and rel_l2(mT.cpu(), rmu) <= TIGHT
 
@@ -470,7 +475,9 @@ def test_forward_plan_reports_the_split():
     assert wide["segments"] == 1 and wide["launches"] == 1 and wide["scratch_bytes"] == 0
     few = pal.palimpsa_forward_plan(1, 32, 32768, 128, 64)
     assert few["segments"] > 1 and few["launches"] == 3
-    assert few["scratch_bytes"] == 32 * (few["segments"] - 1) * (2 * 64 * 128 + 1) * 4
+    b = few["segments"] - 1                                    # boundaries
+    states, gammas, init = 32 * b * 2 * 64 * 128, 32 * b, 32 * 2 * 64 * 128
+    assert few["scratch_bytes"] == 4 * ((states + gammas + 3) // 4 * 4 + init)
     assert few["segment_len"] * few["segments"] >= 32768 > few["segment_len"] * (few["segments"] - 1)
     pal.palimpsa_set_forward_segments(4)
     try:
