@@ -283,6 +283,10 @@ SPLIT_CASES = [
     (1, 1, 1000, 128, 24, True, 16),
     (2, 2, 64, 128, 128, False, 4),
     (1, 2, 17, 128, 64, True, 5),      # more segments requested than whole chunks exist
+    # tensor-core summaries at each d_v they serve (TMEM columns 64 / 128 / 256)
+    (1, 2, 300, 128, 32, True, 3),
+    (1, 1, 500, 128, 96, True, 4),
+    (2, 1, 400, 128, 128, True, 5),
 ]
 
 
@@ -301,8 +305,10 @@ def test_time_split_matches_oracle(B, H, T, dk, dv, bf16, S):
         pal.palimpsa_set_forward_segments(0)
     _check_all(out, ref, tol_for(inp), TIGHT)
     unsplit = _fwd(gi, mu0.to(DEV), I0.to(DEV), chunk=16)
+    # bf16 summaries come from the tensor cores (two-part bf16 operands, at most
+    # 2^-18 relative per product), fp32 ones from FFMA
     for a, b in zip(out, unsplit):
-        assert rel_l2(a.cpu(), b.cpu()) < 1e-6
+        assert rel_l2(a.cpu(), b.cpu()) < (1e-5 if bf16 else 1e-6)
 
 
 def test_time_split_with_default_state_and_in_place():
