@@ -244,13 +244,17 @@ def test_domain_violation_is_reported_not_faulted():
     _fwd(gi)
 
 
-def test_withheld_copy_times_out_and_context_survives():
+@pytest.mark.parametrize("S", [1, 3])
+def test_withheld_copy_times_out_and_context_survives(S):
     """A staged copy that never arrives: the bounded mbarrier wait gives up, the
-    kernel latches PALIMPSA_ERR_TIMEOUT and returns; later calls work."""
+    kernel latches PALIMPSA_ERR_TIMEOUT and returns; later calls work. With S = 3
+    the tensor-core summary kernel times out first: it must drain and free its
+    tensor memory, or the next call's summaries could not allocate any."""
     wl = syn.WORKLOADS["small_layer"].with_(B=1, H=2, T=100)
     inp = syn.sequence_inputs(wl)
     gi = _gpu(inp)
     pal.palimpsa_set_wait_timeout_ns(2_000_000)
+    pal.palimpsa_set_forward_segments(S)
     pal.palimpsa_debug_withhold_first_copy(True)
     try:
         pal.palimpsa_forward_chunked(gi["q"], gi["k"], gi["v"], gi["beta"], gi["d_t"], gi["A"],
@@ -259,7 +263,10 @@ def test_withheld_copy_times_out_and_context_survives():
     finally:
         pal.palimpsa_debug_withhold_first_copy(False)
         pal.palimpsa_set_wait_timeout_ns(2_000_000_000)
-    out = _fwd(gi, chunk=32)
+    try:
+        out = _fwd(gi, chunk=32)
+    finally:
+        pal.palimpsa_set_forward_segments(0)
     _check_all(out, oracle_forward_from(inp), tol_for(inp), TIGHT)
 
 
