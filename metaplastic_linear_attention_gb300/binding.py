@@ -541,9 +541,15 @@ def palimpsa_step(q, k, v, beta, d_t, A, I_prior, mu, I, *, y=None, stream=None)
 HOST_BLOCK_BYTES = 256 << 20   # host input bytes per pipelined block
 
 
-def _blocks(n, per_item_bytes, target=None):
+# Each pipelined forward launch covers at least this many heads, about eight
+# waves of CTAs on a 152-SM part: a launch of few waves pays a partial last wave.
+MIN_HEADS_PER_FORWARD_BLOCK = 2432
+
+
+def _blocks(n, per_item_bytes, target=None, min_items=1):
     target = HOST_BLOCK_BYTES if target is None else target
-    size = max(1, min(n, target // max(1, per_item_bytes)))
+    size = max(1, min_items, min(n, target // max(1, per_item_bytes)))
+    size = min(size, max(1, n))
     return [(i, min(n, i + size)) for i in range(0, n, size)], size
 
 
@@ -607,7 +613,7 @@ def _forward_from_host(q, k, v, beta, d_t, A, I_prior, mu0, I0, y, mu_T, I_T, ch
     d_v = v.shape[-1]
     f32 = torch.float32
     per_b = sum(_nbytes(t) // max(1, B) for t in (q, k, v, beta, d_t, mu0, I0))
-    blocks, nb = _blocks(B, per_b)
+    blocks, nb = _blocks(B, per_b, min_items=-(-MIN_HEADS_PER_FORWARD_BLOCK // max(1, H)))
     outs = []
     for t, shape in ((y, (B, H, T, d_v)), (mu_T, (B, H, d_v, d_k)), (I_T, (B, H, d_v, d_k))):
         outs.append(t if (t is not None and t.is_cuda) else _host_out(t, shape, f32))

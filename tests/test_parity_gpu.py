@@ -347,19 +347,22 @@ def test_host_forward_pipeline_matches_device_path(monkeypatch):
     I0 = 0.5 + torch.rand((5, 3, 64, 128), generator=g)
     ref = _fwd(_gpu(inp), mu0.to(DEV), I0.to(DEV))
     monkeypatch.setattr(b, "HOST_BLOCK_BYTES", 1)          # one batch entry per block: 5 blocks
+    monkeypatch.setattr(b, "MIN_HEADS_PER_FORWARD_BLOCK", 1)
     host = {k: v.pin_memory() for k, v in inp.items()}
     y, mT, IT = pal.palimpsa_forward_chunked(host["q"], host["k"], host["v"], host["beta"], host["d_t"], host["A"],
                                              host["I_prior"], mu0.pin_memory(), I0.pin_memory())
     assert y.device.type == "cpu" and mT.device.type == "cpu"
+    # 3-head blocks may be planned with other time splits than the 15-head call, and
+    # bf16 segment summaries agree to ~1e-6 across splits (tensor-core operands)
     for a_, r_ in zip((y, mT, IT), ref):
-        assert rel_l2(a_, r_.cpu()) < 1e-6
+        assert rel_l2(a_, r_.cpu()) < 1e-5
     # state outputs on the device, y to the host
     m_d, i_d = torch.empty_like(mu0, device=DEV), torch.empty_like(I0, device=DEV)
     y2, m2, i2 = pal.palimpsa_forward_chunked(host["q"], host["k"], host["v"], host["beta"], host["d_t"], host["A"],
                                               host["I_prior"], y=torch.empty_like(y).pin_memory(), mu_T=m_d, I_T=i_d)
     assert m2.data_ptr() == m_d.data_ptr() and y2.device.type == "cpu"
     ref_default = _fwd(_gpu(inp))
-    assert rel_l2(y2, ref_default[0].cpu()) < 1e-6 and rel_l2(m2.cpu(), ref_default[1].cpu()) < 1e-6
+    assert rel_l2(y2, ref_default[0].cpu()) < 1e-5 and rel_l2(m2.cpu(), ref_default[1].cpu()) < 1e-5
 
 
 def test_step_sequence_host_pipeline_matches_token_by_token(monkeypatch):
