@@ -500,3 +500,72 @@ def test_forward_plan_reports_the_split():
         assert pal.palimpsa_forward_plan(2, 3, 1000, 128, 64)["segments"] == 4
     finally:
         pal.palimpsa_set_forward_segments(0)
+
+
+# ----------------------------------------------------------------- extreme gates and states
+
+def _extreme_inputs(bf16, seed):
+    """Gates at both ends (alpha = 1 exactly, alpha underflowing to 0, and values in
+    between), beta zero on whole tokens and rows, initial precisions over six
+    orders of magnitude."""
+    B, H, T, dk, dv = 2, 2, 150, 128, 64
+    wl = syn.WORKLOADS["small_layer"].with_(B=B, H=H, T=T, bf16=bf16)
+    inp = syn.sequence_inputs(wl, seed=seed)
+    g = torch.Generator().manual_seed(seed)
+    pick_dt = torch.tensor([0.0, 1e-4, 0.05, 1.0, 30.0, 500.0])
+    inp["d_t"] = pick_dt[torch.randint(0, len(pick_dt), (B, H, T), generator=g)].contiguous()
+    beta = inp["beta"].float()
+    beta[:, :, ::7] = 0.0                   # tokens that write nothing
+    beta[:, :, :, ::5] = 0.0                # value rows that never learn
+    inp["beta"] = beta.to(inp["beta"].dtype).contiguous()
+    mu0 = torch.randn((B, H, dv, dk), generator=g)
+    I0 = 10.0 ** (6.0 * torch.rand((B, H, dv, dk), generator=g) - 3.0)   # 1e-3 .. 1e3
+    return inp, mu0, I0
+
+
+@pytest.mark.parametrize("bf16", [False, True])
+@pytest.mark.parametrize("S", [1, 3])
+def test_forward_extreme_gates_and_states(bf16, S):
+    inp, mu0, I0 = _extreme_inputs(bf16, 4100 + S)
+    ref = oracle_forward_from(inp, mu0=mu0, I0=I0)
+    pal.palimpsa_set_forward_segments(S)
+    try:
+        out = _fwd(_gpu(inp), mu0.to(DEV), I0.to(DEV))
+    finally:
+        pal.palimpsa_set_forward_segments(0)
+    _check_all(out, ref, tol_for(inp), TIGHT)
+
+
+def test_step_extreme_gates_and_states():
+    inp, mu0, I0 = _extreme_inputs(True, 4200)
+    gi = _gpu(inp)
+    mu, I = mu0.to(DEV), I0.to(DEV)
+    f = syn.as_float64_numpy
+    mu_r, I_r = f(mu0), f(I0)
+    import oracle
+    for t in range(12):
+        tok = {k: (gi[k][:, :, t].contiguous() if gi[k].dim() >= 3 else gi[k]) for k in ("q", "k", "v", "beta", "d_t")}
+        y = pal.palimpsa_step(tok["q"], tok["k"], tok["v"], tok["beta"], tok["d_t"], gi["A"], gi["I_prior"], mu, I)
+        y_r, mu_r, I_r = oracle.step(*(f(inp[n][:, :, t]) for n in ("q", "k", "v", "beta", "d_t")),
+                                     f(inp["A"]), f(inp["I_prior"]), mu_r, I_r)
+        assert rel_l2(y.cpu().numpy(), y_r) <= TIGHT
+    assert pal.palimpsa_get_device_status() == 0
+    assert rel_l2(mu.cpu().numpy(), mu_r) <= TIGHT and rel_l2(I.cpu().numpy(), I_r) <= TIGHT
+
+
+def test_backward_extreme_gates_and_states():
+    from oracle import autograd as oag
+    inp, mu0, I0 = _extreme_inputs(False, 4300)
+    g = torch.Generator().manual_seed(4301)
+    dy = torch.randn(inp["q"].shape[:3] + (64,), generator=g)
+    f = syn.as_float64_numpy
+    ref = oag.gradients({n: f(t) for n, t in dict(q=inp["q"], k=inp["k"], v=inp["v"], beta=inp["beta"],
+                                                  d_t=inp["d_t"], A=inp["A"], I_prior=inp["I_prior"],
+                                                  mu0=mu0, I0=I0).items()}, f(dy))
+    gi = _gpu(inp)
+    got = pal.palimpsa_backward(gi["q"], gi["k"], gi["v"], gi["beta"], gi["d_t"], gi["A"], gi["I_prior"],
+                                mu0.to(DEV), I0.to(DEV), dy.to(DEV))
+    assert pal.palimpsa_get_device_status() == 0
+    errs = {n: rel_l2(got[n].cpu().numpy(), ref[n[1:]]) for n in
+            ("dq", "dk", "dv", "dbeta", "dd_t", "dA", "dI_prior", "dmu0", "dI0")}
+    assert max(errs.values()) <= TIGHT, errs
