@@ -396,10 +396,36 @@ def run_ours(args, ws, rank, local):
         b1.record(stream)
         torch.cuda.synchronize()
         bwd_ms = b0.elapsed_time(b1) / 3
+        # the training pair: a forward that writes the 32-token checkpoints, and the
+        # backward that reads them instead of recomputing them
+        ck = pal.palimpsa_forward_checkpointed(inp["q"], inp["k"], inp["v"], inp["beta"], inp["d_t"], inp["A"],
+                                               inp["I_prior"], y=y_pre, mu_T=mu, I_T=I, chunk=wl.chunk)[3]
+        b0.record(stream)
+        for _ in range(3):
+            pal.palimpsa_forward_checkpointed(inp["q"], inp["k"], inp["v"], inp["beta"], inp["d_t"], inp["A"],
+                                              inp["I_prior"], y=y_pre, mu_T=mu, I_T=I, ckpt=ck, chunk=wl.chunk)
+        b1.record(stream)
+        torch.cuda.synchronize()
+        fwd_ck_ms = b0.elapsed_time(b1) / 3
+
+        def _bwd_ck():
+            pal.palimpsa_backward(inp["q"], inp["k"], inp["v"], inp["beta"], inp["d_t"], inp["A"], inp["I_prior"],
+                                  None, None, dy, want_state_grads=False, ckpt=ck)
+        _bwd_ck()
+        b0.record(stream)
+        for _ in range(3):
+            _bwd_ck()
+        b1.record(stream)
+        torch.cuda.synchronize()
+        bwd_ck_ms = b0.elapsed_time(b1) / 3
+        del ck
         kernels["palimpsa_backward"] = {"avg_ms": bwd_ms, "head_tokens_per_s": B * H * T / (bwd_ms / 1e3),
                                         "over_forward": bwd_ms / fwd_avg_ms,
+                                        "checkpointed_forward_ms": fwd_ck_ms,
+                                        "from_checkpoints_ms": bwd_ck_ms,
                                         "note": "gradients of <dy, y> w.r.t. q, k, v, beta, d_t, A, I_prior; "
-                                                "timed after the timed region"}
+                                                "from_checkpoints: reading the states a checkpointed forward "
+                                                "wrote; timed after the timed region"}
 
     e2e = None
     if not args.no_e2e:

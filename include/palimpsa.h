@@ -403,6 +403,44 @@ palimpsa_status palimpsa_backward(
     int B, int H, int T, int d_k, int d_v,
     palimpsa_dtype in_dtype, void* cuda_stream);
 
+/*
+ * Training pair. palimpsa_forward_checkpointed is palimpsa_forward_chunked that
+ * also writes the state of every head before tokens 0, 32, 64, ... into
+ * `ckpt`. palimpsa_backward_checkpointed is palimpsa_backward reading those
+ * states instead of recomputing them with a forward sweep of its own, which
+ * saves about a sixth of the backward's work and all of its scratch memory.
+ *
+ *   ckpt  fp32 [B, H, ceil(T / 32), d_v, 2, d_k], palimpsa_checkpoint_bytes()
+ *         bytes, 16-byte aligned: for checkpoint c and value row i, the natural
+ *         parameter M_i = I_i (.) mu_i over the d_k keys, then I_i.
+ *
+ * The forward writes ckpt in addition to its usual outputs (other arguments
+ * and errors as for palimpsa_forward_chunked). The backward's other arguments
+ * and errors are those of palimpsa_backward; its ckpt must come from a forward
+ * call on the same inputs (q, k, v, beta, d_t, A, I_prior, mu0, I0), which the
+ * library cannot check.
+ */
+size_t palimpsa_checkpoint_bytes(int B, int H, int T, int d_k, int d_v);
+
+palimpsa_status palimpsa_forward_checkpointed(
+    const void* q, const void* k, const void* v, const void* beta,
+    const float* d_t, const float* A, const float* I_prior,
+    const float* mu0, const float* I0,
+    float* y, float* mu_T, float* I_T, float* ckpt,
+    int B, int H, int T, int d_k, int d_v, int chunk,
+    palimpsa_dtype in_dtype, void* cuda_stream);
+
+palimpsa_status palimpsa_backward_checkpointed(
+    const void* q, const void* k, const void* v, const void* beta,
+    const float* d_t, const float* A, const float* I_prior,
+    const float* mu0, const float* I0,
+    const float* dy, const float* dmu_T, const float* dI_T,
+    float* dq, float* dk, float* dv, float* dbeta, float* dd_t,
+    float* dA, float* dI_prior, float* dmu0, float* dI0,
+    const float* ckpt,
+    int B, int H, int T, int d_k, int d_v,
+    palimpsa_dtype in_dtype, void* cuda_stream);
+
 /* Static English text for a status code (never NULL). */
 const char* palimpsa_status_string(palimpsa_status s);
 

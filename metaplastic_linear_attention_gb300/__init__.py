@@ -20,7 +20,9 @@ from .binding import (  # noqa: F401
     load_library,
     palimpsa_abi_version,
     palimpsa_backward,
+    palimpsa_checkpoint_bytes,
     palimpsa_debug_withhold_first_copy,
+    palimpsa_forward_checkpointed,
     palimpsa_forward_chunked,
     palimpsa_forward_fused,
     palimpsa_forward_plan,

@@ -81,6 +81,14 @@ def load_library(path: str | None = None):
         lib.palimpsa_segment_summary.argtypes = [vp, vp, vp, vp, fp, fp, fp, fp, fp, i, i, i, i, i, i, i, vp]
         lib.palimpsa_state_combine.restype = i
         lib.palimpsa_state_combine.argtypes = [fp, fp, i, fp, fp, fp, fp, fp, i, i, i, i, vp]
+        lib.palimpsa_checkpoint_bytes.restype = ctypes.c_size_t
+        lib.palimpsa_checkpoint_bytes.argtypes = [i, i, i, i, i]
+        lib.palimpsa_forward_checkpointed.restype = i
+        lib.palimpsa_forward_checkpointed.argtypes = [vp, vp, vp, vp, fp, fp, fp, fp, fp, fp, fp, fp, fp,
+                                                      i, i, i, i, i, i, i, vp]
+        lib.palimpsa_backward_checkpointed.restype = i
+        lib.palimpsa_backward_checkpointed.argtypes = [vp, vp, vp, vp, fp, fp, fp, fp, fp, fp, fp, fp, fp, fp, fp,
+                                                       fp, fp, fp, fp, fp, fp, fp, i, i, i, i, i, i, vp]
         lib.palimpsa_forward_plan.restype = i
         lib.palimpsa_forward_plan.argtypes = [i, i, i, i, i, i, i, ctypes.POINTER(ctypes.c_int),
                                               ctypes.POINTER(ctypes.c_int), ctypes.POINTER(ctypes.c_int),
@@ -441,9 +449,37 @@ def palimpsa_forward_without_meta(q, k, v, beta, d_t, A, I_prior, mu0=None, *, y
     return y, mu_T
 
 
+def palimpsa_checkpoint_bytes(B, H, T, d_k, d_v) -> int:
+    """Bytes of the training checkpoints of a forward of these sizes (see palimpsa.h)."""
+    return int(load_library().palimpsa_checkpoint_bytes(int(B), int(H), int(T), int(d_k), int(d_v)))
+
+
+def palimpsa_forward_checkpointed(q, k, v, beta, d_t, A, I_prior, mu0=None, I0=None, *, ckpt=None, y=None,
+                                  mu_T=None, I_T=None, chunk: int = 0, stream=None):
+    """The forward for training (see palimpsa.h): palimpsa_forward_chunked that also
+    writes the state before every 32nd token, for palimpsa_backward(ckpt=...).
+    Device tensors. Returns (y, mu_T, I_T, ckpt); ckpt is [B,H,ceil(T/32),d_v,2,d_k]."""
+    B, H, T, d_k, d_v, dev = _check_forward_inputs(q, k, v, beta, d_t, A, I_prior, mu0, I0, ("beta", "d_t"))
+    y, mu_T, I_T = _forward_outputs(B, H, T, d_k, d_v, dev, y, mu_T, I_T)
+    shape = (B, H, -(-T // 32), d_v, 2, d_k)
+    ckpt = torch.empty(shape, dtype=torch.float32, device=dev) if ckpt is None else ckpt
+    _check(ckpt, "ckpt", shape, torch.float32, dev)
+    lib = load_library()
+    with torch.cuda.device(dev):
+        rc = lib.palimpsa_forward_checkpointed(
+            _ptr(q), _ptr(k), _ptr(v), _ptr(beta), _ptr(d_t), _ptr(A), _ptr(I_prior), _ptr(mu0), _ptr(I0), _ptr(y),
+            _ptr(mu_T), _ptr(I_T), _ptr(ckpt), B, H, T, d_k, d_v, int(chunk), _in_dtype(q),
+            ctypes.c_void_p(_stream_handle(stream)))
+    if rc != 0:
+        raise PalimpsaError(rc, "palimpsa_forward_checkpointed")
+    return y, mu_T, I_T, ckpt
+
+
 def palimpsa_backward(q, k, v, beta, d_t, A, I_prior, mu0, I0, dy, dmu_T=None, dI_T=None, *, want_state_grads=True,
-                      stream=None):
+                      ckpt=None, stream=None):
     """Gradients through palimpsa_forward_chunked (see palimpsa.h). Device tensors.
+    With ckpt (from palimpsa_forward_checkpointed on the same inputs) the
+    backward reads the states instead of recomputing them.
 
     Returns a dict: dq, dk, dv, dbeta, dd_t, dA, dI_prior, and dmu0 / dI0 when
     want_state_grads (fp32 throughout)."""
@@ -468,14 +504,18 @@ def palimpsa_backward(q, k, v, beta, d_t, A, I_prior, mu0, I0, dy, dmu_T=None, d
         g["dmu0"] = e(B, H, d_v, d_k)
         g["dI0"] = e(B, H, d_v, d_k)
     lib = load_library()
-    with torch.cuda.device(dev):
-        rc = lib.palimpsa_backward(
-            _ptr(q), _ptr(k), _ptr(v), _ptr(beta), _ptr(d_t), _ptr(A), _ptr(I_prior), _ptr(mu0), _ptr(I0), _ptr(dy),
+    args = [_ptr(q), _ptr(k), _ptr(v), _ptr(beta), _ptr(d_t), _ptr(A), _ptr(I_prior), _ptr(mu0), _ptr(I0), _ptr(dy),
             _ptr(dmu_T), _ptr(dI_T), _ptr(g["dq"]), _ptr(g["dk"]), _ptr(g["dv"]), _ptr(g["dbeta"]), _ptr(g["dd_t"]),
-            _ptr(g["dA"]), _ptr(g["dI_prior"]), _ptr(g.get("dmu0")), _ptr(g.get("dI0")), B, H, T, d_k, d_v,
-            _in_dtype(q), ctypes.c_void_p(_stream_handle(stream)))
+            _ptr(g["dA"]), _ptr(g["dI_prior"]), _ptr(g.get("dmu0")), _ptr(g.get("dI0"))]
+    tail = [B, H, T, d_k, d_v, _in_dtype(q), ctypes.c_void_p(_stream_handle(stream))]
+    with torch.cuda.device(dev):
+        if ckpt is None:
+            rc, name = lib.palimpsa_backward(*args, *tail), "palimpsa_backward"
+        else:
+            _check(ckpt, "ckpt", (B, H, -(-T // 32), d_v, 2, d_k), f32, dev)
+            rc, name = lib.palimpsa_backward_checkpointed(*args, _ptr(ckpt), *tail), "palimpsa_backward_checkpointed"
     if rc != 0:
-        raise PalimpsaError(rc, "palimpsa_backward")
+        raise PalimpsaError(rc, name)
     return g
 
 

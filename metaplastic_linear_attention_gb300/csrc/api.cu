@@ -104,7 +104,8 @@ bool sizes_ok(long long B, long long H, long long T, int d_k, int d_v) {
 palimpsa_status forward_impl(const void* q, const void* k, const void* v, const void* beta, const float* d_t,
                              const float* A, const float* I_prior, const float* mu0, const float* I0, float* y,
                              float* mu_T, float* I_T, int B, int H, int T, int d_k, int d_v, int chunk,
-                             palimpsa_dtype in_dtype, void* cuda_stream, const Prologue& pro) {
+                             palimpsa_dtype in_dtype, void* cuda_stream, const Prologue& pro,
+                             float* ckpt = nullptr) {
   if (!A || !I_prior || !mu_T || !I_T) return PALIMPSA_ERR_NULL;
   // With T == 0 the per-token arrays are empty and may be NULL.
   if (T != 0 && (!q || !k || !v || !beta || !d_t || !y)) return PALIMPSA_ERR_NULL;
@@ -112,7 +113,7 @@ palimpsa_status forward_impl(const void* q, const void* k, const void* v, const 
   if (!sizes_ok(B, H, T, d_k, d_v)) return PALIMPSA_ERR_SHAPE;
   if (!supported_dims(d_k, d_v)) return PALIMPSA_ERR_UNSUPPORTED;
   if (chunk != 0 && chunk != 16 && chunk != 32 && chunk != 64) return PALIMPSA_ERR_UNSUPPORTED;
-  const void* a16[] = {q, k, v, beta, y, mu_T, I_T, mu0, I0};
+  const void* a16[] = {q, k, v, beta, y, mu_T, I_T, mu0, I0, ckpt};
   for (const void* p : a16)
     if (p && !aligned(p, 16)) return PALIMPSA_ERR_ALIGN;
   const void* a4[] = {d_t, A, I_prior};
@@ -123,6 +124,7 @@ palimpsa_status forward_impl(const void* q, const void* k, const void* v, const 
   FwdArgs a{q, k, v, beta, d_t, A, I_prior, mu0, I0, y, mu_T, I_T, B, H, T, d_k, d_v,
             chunk == 0 ? 32 : chunk, in_dtype == PALIMPSA_BF16, st,
             g_wait_timeout_ns.load(), g_withhold_first_copy.load(), g_forward_segments.load(), pro};
+  a.ckpt = ckpt;
   StreamOrderedScratch scratch;
   if (launch_forward_chunked(a, static_cast<cudaStream_t>(cuda_stream), &scratch) != cudaSuccess)
     return PALIMPSA_ERR_CUDA;
@@ -322,19 +324,24 @@ palimpsa_status palimpsa_forward_without_meta(const void* q, const void* k, cons
   return PALIMPSA_OK;
 }
 
-palimpsa_status palimpsa_backward(const void* q, const void* k, const void* v, const void* beta, const float* d_t,
-                                  const float* A, const float* I_prior, const float* mu0, const float* I0,
-                                  const float* dy, const float* dmu_T, const float* dI_T, float* dq, float* dk,
-                                  float* dv, float* dbeta, float* dd_t, float* dA, float* dI_prior, float* dmu0,
-                                  float* dI0, int B, int H, int T, int d_k, int d_v, palimpsa_dtype in_dtype,
-                                  void* cuda_stream) {
+}  // extern "C"
+
+namespace palimpsa {
+namespace {
+
+palimpsa_status backward_impl(const void* q, const void* k, const void* v, const void* beta, const float* d_t,
+                              const float* A, const float* I_prior, const float* mu0, const float* I0,
+                              const float* dy, const float* dmu_T, const float* dI_T, float* dq, float* dk,
+                              float* dv, float* dbeta, float* dd_t, float* dA, float* dI_prior, float* dmu0,
+                              float* dI0, const float* ckpt, int B, int H, int T, int d_k, int d_v,
+                              palimpsa_dtype in_dtype, void* cuda_stream) {
   if (!A || !I_prior || !dA || !dI_prior) return PALIMPSA_ERR_NULL;
   if (T != 0 && (!q || !k || !v || !beta || !d_t || !dy || !dq || !dk || !dv || !dbeta || !dd_t))
     return PALIMPSA_ERR_NULL;
   if (in_dtype != PALIMPSA_F32 && in_dtype != PALIMPSA_BF16) return PALIMPSA_ERR_DTYPE;
   if (!sizes_ok(B, H, T, d_k, d_v)) return PALIMPSA_ERR_SHAPE;
   if (!supported_dims(d_k, d_v)) return PALIMPSA_ERR_UNSUPPORTED;
-  const void* a16[] = {q, k, v, beta, mu0, I0, dy, dmu_T, dI_T, dq, dk, dv, dbeta, dmu0, dI0};
+  const void* a16[] = {q, k, v, beta, mu0, I0, dy, dmu_T, dI_T, dq, dk, dv, dbeta, dmu0, dI0, ckpt};
   for (const void* p : a16)
     if (p && !aligned(p, 16)) return PALIMPSA_ERR_ALIGN;
   const void* a4[] = {d_t, A, I_prior, dd_t, dA, dI_prior};
@@ -343,6 +350,7 @@ palimpsa_status palimpsa_backward(const void* q, const void* k, const void* v, c
   cudaStream_t s = static_cast<cudaStream_t>(cuda_stream);
   BwdArgs a{q, k, v, beta, d_t, A, I_prior, mu0, I0, dy, dmu_T, dI_T, dq, dk, dv, dbeta, dd_t, dA, dI_prior,
             dmu0, dI0, B, H, T, d_k, d_v, in_dtype == PALIMPSA_BF16};
+  a.ckpt_in = ckpt;
   const size_t tok = (size_t)B * H * T;
   // outputs that the kernel accumulates into start at zero
   if (T != 0 && (cudaMemsetAsync(dq, 0, tok * d_k * sizeof(float), s) != cudaSuccess ||
@@ -360,6 +368,48 @@ palimpsa_status palimpsa_backward(const void* q, const void* k, const void* v, c
   const cudaError_t e2 = ck ? scratch.release(ck, s) : cudaSuccess;
   if (e != cudaSuccess || e2 != cudaSuccess) return PALIMPSA_ERR_CUDA;
   return PALIMPSA_OK;
+}
+
+}  // namespace
+}  // namespace palimpsa
+
+extern "C" {
+
+palimpsa_status palimpsa_backward(const void* q, const void* k, const void* v, const void* beta, const float* d_t,
+                                  const float* A, const float* I_prior, const float* mu0, const float* I0,
+                                  const float* dy, const float* dmu_T, const float* dI_T, float* dq, float* dk,
+                                  float* dv, float* dbeta, float* dd_t, float* dA, float* dI_prior, float* dmu0,
+                                  float* dI0, int B, int H, int T, int d_k, int d_v, palimpsa_dtype in_dtype,
+                                  void* cuda_stream) {
+  return backward_impl(q, k, v, beta, d_t, A, I_prior, mu0, I0, dy, dmu_T, dI_T, dq, dk, dv, dbeta, dd_t, dA,
+                       dI_prior, dmu0, dI0, nullptr, B, H, T, d_k, d_v, in_dtype, cuda_stream);
+}
+
+palimpsa_status palimpsa_backward_checkpointed(const void* q, const void* k, const void* v, const void* beta,
+                                               const float* d_t, const float* A, const float* I_prior,
+                                               const float* mu0, const float* I0, const float* dy,
+                                               const float* dmu_T, const float* dI_T, float* dq, float* dk,
+                                               float* dv, float* dbeta, float* dd_t, float* dA, float* dI_prior,
+                                               float* dmu0, float* dI0, const float* ckpt, int B, int H, int T,
+                                               int d_k, int d_v, palimpsa_dtype in_dtype, void* cuda_stream) {
+  if (!ckpt && T != 0) return PALIMPSA_ERR_NULL;
+  return backward_impl(q, k, v, beta, d_t, A, I_prior, mu0, I0, dy, dmu_T, dI_T, dq, dk, dv, dbeta, dd_t, dA,
+                       dI_prior, dmu0, dI0, ckpt, B, H, T, d_k, d_v, in_dtype, cuda_stream);
+}
+
+size_t palimpsa_checkpoint_bytes(int B, int H, int T, int d_k, int d_v) {
+  if (B < 1 || H < 1 || T < 0 || d_k < 1 || d_v < 1) return 0;
+  return checkpoint_floats((long long)B * H, T, d_k, d_v) * sizeof(float);
+}
+
+palimpsa_status palimpsa_forward_checkpointed(const void* q, const void* k, const void* v, const void* beta,
+                                              const float* d_t, const float* A, const float* I_prior,
+                                              const float* mu0, const float* I0, float* y, float* mu_T, float* I_T,
+                                              float* ckpt, int B, int H, int T, int d_k, int d_v, int chunk,
+                                              palimpsa_dtype in_dtype, void* cuda_stream) {
+  if (!ckpt && T != 0) return PALIMPSA_ERR_NULL;
+  return forward_impl(q, k, v, beta, d_t, A, I_prior, mu0, I0, y, mu_T, I_T, B, H, T, d_k, d_v, chunk, in_dtype,
+                      cuda_stream, Prologue{}, ckpt);
 }
 
 palimpsa_status palimpsa_step(const void* q, const void* k, const void* v, const void* beta,

@@ -246,6 +246,21 @@ __device__ __forceinline__ void step_pairs(float2 (&M)[NP], float2 (&I)[NP], con
   }
 }
 
+// Adjoints at t = T of one lane's element pairs, from the final state (M, I):
+// gM = dmu_T / I, gI = dI_T - dmu_T mu_T / I.
+template <int NP>
+__device__ __forceinline__ void init_adjoints(const BwdArgs& a, size_t soff, const float2 (&M)[NP],
+                                              const float2 (&I)[NP], float2 (&gM)[NP], float2 (&gI)[NP]) {
+#pragma unroll
+  for (int p = 0; p < NP; ++p) {
+    const float2 dmu = a.dmu_T ? *reinterpret_cast<const float2*>(a.dmu_T + soff + 2 * p) : make_float2(0.f, 0.f);
+    const float2 dI = a.dI_T ? *reinterpret_cast<const float2*>(a.dI_T + soff + 2 * p) : make_float2(0.f, 0.f);
+    const float2 r = make_float2(1.f / I[p].x, 1.f / I[p].y);
+    gM[p] = __fmul2_rn(dmu, r);
+    gI[p] = make_float2(dI.x - dmu.x * (M[p].x * r.x) * r.x, dI.y - dmu.y * (M[p].y * r.y) * r.y);
+  }
+}
+
 template <int DK, bool BF16>
 __global__ void __launch_bounds__(kThreads)
 palimpsa_bwd_kernel(BwdArgs a, float* __restrict__ ckpt) {
@@ -273,7 +288,11 @@ palimpsa_bwd_kernel(BwdArgs a, float* __restrict__ ckpt) {
   const size_t head_tok = (size_t)bh * T;
   const float A_h = a.A[h], Ip = a.I_prior[h];
   const int nseg = (T + kSeg - 1) / kSeg;
-  float* my_ckpt = ckpt + (size_t)blockIdx.x * nseg * kRowsPerCta * DK * 2;
+  static_assert(kSeg == kCheckpointTokens, "backward segments are the training checkpoints");
+  // checkpoints [head][segment][value row][M | I]: from the forward, or written by phase 1
+  const size_t ck_head = (size_t)bh * nseg * DV * 2 * DK;
+  float* ck_out = ckpt ? ckpt + ck_head : nullptr;  // null when the forward's checkpoints are used
+  const float* ck_in = (a.ckpt_in ? a.ckpt_in : ckpt) + ck_head;
 
   // ---- initial state
   float2 M[NP], I[NP], mu0v[NP], I0v[NP];
@@ -287,7 +306,14 @@ palimpsa_bwd_kernel(BwdArgs a, float* __restrict__ ckpt) {
   }
 
   // ---- phase 1: forward sweep, checkpoint at every segment start; segment
-  // s + 1 is being copied in while segment s computes.
+  // s + 1 is being copied in while segment s computes. Skipped when the forward
+  // wrote the checkpoints: then only the last segment is staged for phase 2.
+  if (a.ckpt_in) {
+    if (nseg > 0)
+      stage_segment<DK, ES>(bsm + (size_t)((nseg - 1) & 1) * L.stage, L, a, head_tok, row0, (nseg - 1) * kSeg,
+                            T - (nseg - 1) * kSeg);
+    cp_async_commit();
+  } else {
   if (nseg > 0) stage_segment<DK, ES>(bsm, L, a, head_tok, row0, 0, min(kSeg, T));
   cp_async_commit();
   for (int s = 0; s < nseg; ++s) {
@@ -301,7 +327,7 @@ palimpsa_bwd_kernel(BwdArgs a, float* __restrict__ ckpt) {
     const unsigned char* st = bsm + (size_t)(s & 1) * L.stage;
     prepare_segment<DK, BF16>(st, bsm, L, tn, A_h, Ip);
     const float* kf = reinterpret_cast<const float*>(BF16 ? bsm + L.kf : st + L.k);
-    float* cp = my_ckpt + ((size_t)s * kRowsPerCta + rl) * DK * 2;
+    float* cp = ck_out + ((size_t)s * DV + i) * DK * 2;
 #pragma unroll
     for (int p = 0; p < NP; ++p) {
       *reinterpret_cast<float2*>(cp + c0 + 2 * p) = M[p];
@@ -315,17 +341,13 @@ palimpsa_bwd_kernel(BwdArgs a, float* __restrict__ ckpt) {
     }
     __syncthreads();  // this stage and the tables are free again
   }
-
-  // ---- adjoints at t = T from the final-state gradients
-  float2 gM[NP], gI[NP];
-#pragma unroll
-  for (int p = 0; p < NP; ++p) {
-    const float2 dmu = a.dmu_T ? *reinterpret_cast<const float2*>(a.dmu_T + soff + 2 * p) : f2(0.f);
-    const float2 dI = a.dI_T ? *reinterpret_cast<const float2*>(a.dI_T + soff + 2 * p) : f2(0.f);
-    const float2 r = make_float2(1.f / I[p].x, 1.f / I[p].y);
-    gM[p] = __fmul2_rn(dmu, r);
-    gI[p] = make_float2(dI.x - dmu.x * (M[p].x * r.x) * r.x, dI.y - dmu.y * (M[p].y * r.y) * r.y);
   }
+
+  // The adjoints start at t = T from the final-state gradients: set from the
+  // final state, which the re-run of the last segment reaches (or the initial
+  // state when T = 0).
+  float2 gM[NP], gI[NP];
+  if (nseg == 0) init_adjoints<NP>(a, soff, M, I, gM, gI);
   float dIp_acc = 0.f, dA_acc = 0.f;
 
   // ---- phase 2: segments in reverse; segment s - 1 is being copied in while
@@ -342,7 +364,7 @@ palimpsa_bwd_kernel(BwdArgs a, float* __restrict__ ckpt) {
     prepare_segment<DK, BF16>(st, bsm, L, tn, A_h, Ip);
     const float* kf = reinterpret_cast<const float*>(BF16 ? bsm + L.kf : st + L.k);
     const float* qf = reinterpret_cast<const float*>(BF16 ? bsm + L.qf : st + L.q);
-    const float* cp = my_ckpt + ((size_t)s * kRowsPerCta + rl) * DK * 2;
+    const float* cp = ck_in + ((size_t)s * DV + i) * DK * 2;
 #pragma unroll
     for (int p = 0; p < NP; ++p) {
       M[p] = *reinterpret_cast<const float2*>(cp + c0 + 2 * p);
@@ -362,6 +384,7 @@ palimpsa_bwd_kernel(BwdArgs a, float* __restrict__ ckpt) {
       f32_pairs<NC>(kf, DK, u, c0, k);
       step_pairs<NP>(M, I, k, tok(bsm, L, u, rl));
     }
+    if (s == nseg - 1) init_adjoints<NP>(a, soff, M, I, gM, gI);  // M, I: the final state
     const int nwin = (tn + kWin - 1) / kWin;
     for (int wi = nwin - 1; wi >= 0; --wi) {
       const int uw = wi * kWin, n = min(kWin, tn - uw);
@@ -488,9 +511,8 @@ palimpsa_bwd_kernel(BwdArgs a, float* __restrict__ ckpt) {
 }  // namespace
 
 size_t backward_scratch_bytes(const BwdArgs& a) {
-  const size_t ctas = (size_t)a.B * a.H * (a.d_v / kRowsPerCta);
-  const size_t nseg = (size_t)(a.T + kSeg - 1) / kSeg;
-  return ctas * nseg * kRowsPerCta * a.d_k * 2 * sizeof(float);
+  if (a.ckpt_in) return 0;  // the forward's checkpoints replace phase 1
+  return checkpoint_floats((long long)a.B * a.H, a.T, a.d_k, a.d_v) * sizeof(float);
 }
 
 template <int DK, bool BF16>

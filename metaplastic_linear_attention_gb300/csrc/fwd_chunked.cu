@@ -133,8 +133,24 @@ palimpsa_fwd_chunked_kernel(FwdArgs a, int C, int nseg, int seg_len, const float
 
   float* gy = a.y + (head_tok + tl.tb) * DV + tl.row0 + lr0;
   const float* gd = a.d_t + head_tok + tl.tb;
+  // training checkpoints: the state before every 32nd token of the sequence
+  float* ckh = a.ckpt ? a.ckpt + (size_t)tl.bh * ((a.T + kCheckpointTokens - 1) / kCheckpointTokens) * DV * 2 * DK
+                      : nullptr;
   for (int c = 0; c < pipe.nch; ++c) {
     const int t0 = pipe.t0_of(c), tc = pipe.tc_of(c);
+    if (ckh && (tl.tb + t0) % kCheckpointTokens == 0) {
+      float* ck = ckh + (size_t)((tl.tb + t0) / kCheckpointTokens) * DV * 2 * DK;
+#pragma unroll
+      for (int r = 0; r < R; ++r) {
+#pragma unroll
+        for (int s = 0; s < NV; ++s) {
+          const size_t e = (size_t)(tl.row0 + lr0 + r) * 2 * DK + 32 * s + 4 * cg;
+          const float2 m01 = Mst[r][2 * s], m23 = Mst[r][2 * s + 1], i01 = Ist[r][2 * s], i23 = Ist[r][2 * s + 1];
+          *reinterpret_cast<float4*>(ck + e) = make_float4(m01.x, m01.y, m23.x, m23.y);
+          *reinterpret_cast<float4*>(ck + DK + e) = make_float4(i01.x, i01.y, i23.x, i23.y);
+        }
+      }
+    }
     if (!pipe.wait(c, a.wait_timeout_ns, a.status)) return;
     // ---- convert the staged chunk to fp32 operands shared by all rows
     const unsigned char* raw = pipe.raw(c);

@@ -45,6 +45,7 @@ struct FwdArgs {
   int withhold_first_copy;
   int force_segments;  // 0: the library chooses the time split
   Prologue pro{};
+  float* ckpt = nullptr;  // training checkpoints out (dense layout only), or null
   // Packed variable-length batch (palimpsa_forward_varlen): B counts sequences,
   // T is the longest sequence, and sequence n is tokens [cu[n], cu[n+1]) of each
   // head's total_T tokens. NULL for the dense [B, H, T] layout.
@@ -93,7 +94,19 @@ struct BwdArgs {
   float* dI0;          // may be null
   int B, H, T, d_k, d_v;
   bool bf16;
+  // Training checkpoints written by the forward (layout of kCheckpointTokens
+  // below), or null: the backward then recomputes them with a forward sweep.
+  const float* ckpt_in = nullptr;
 };
+
+// Training checkpoints: the state (M, I) of every head before tokens 0, 32,
+// 64, ... laid out [head][checkpoint][value row i][M_i0 .. M_i(d_k-1), I_i0 ..
+// I_i(d_k-1)], fp32. Written by the forward when asked, read by the backward.
+constexpr int kCheckpointTokens = 32;
+inline size_t checkpoint_floats(long long heads, long long T, int d_k, int d_v) {
+  const long long n = (T + kCheckpointTokens - 1) / kCheckpointTokens;
+  return (size_t)heads * n * d_v * 2 * d_k;
+}
 
 // Source of temporary device memory for a launch that needs scratch (the time
 // split of the forward). acquire/release are stream-ordered on `s`.

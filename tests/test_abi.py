@@ -256,3 +256,35 @@ def test_forward_plan_rejects_bad_arguments(lib, over, code):
     assert lib.palimpsa_forward_plan(args["B"], args["H"], args["T"], args["d_k"], args["d_v"], args["chunk"],
                                      args["dtype"], args["segments"], args["seg_len"], args["launches"],
                                      args["scratch"]) == code
+
+
+def test_checkpoint_bytes_formula(lib):
+    lib.palimpsa_checkpoint_bytes.restype = ctypes.c_size_t
+    assert lib.palimpsa_checkpoint_bytes(4, 16, 2048, 128, 64) == 4 * 16 * 64 * 64 * 2 * 128 * 4
+    assert lib.palimpsa_checkpoint_bytes(1, 2, 33, 64, 8) == 1 * 2 * 2 * 8 * 2 * 64 * 4
+    assert lib.palimpsa_checkpoint_bytes(1, 1, 0, 128, 64) == 0
+    assert lib.palimpsa_checkpoint_bytes(0, 1, 10, 128, 64) == 0
+
+
+@pytest.mark.parametrize("over,code", [(dict(ck=None), ERR_NULL), (dict(ck=P + 4), ERR_ALIGN),
+                                       (dict(q=None), ERR_NULL), (dict(d_k=96), ERR_UNSUPPORTED)])
+def test_forward_checkpointed_rejects_bad_arguments(lib, over, code):
+    args = dict(q=P, k=P, v=P, beta=P, d=P, A=P, I_prior=P, mu0=None, I0=None, y=P, mu_T=P, I_T=P, ck=P, B=1, H=2,
+                T=16, d_k=128, d_v=64, chunk=0, dtype=1)
+    args.update(over)
+    assert lib.palimpsa_forward_checkpointed(
+        args["q"], args["k"], args["v"], args["beta"], args["d"], args["A"], args["I_prior"], args["mu0"], args["I0"],
+        args["y"], args["mu_T"], args["I_T"], args["ck"], args["B"], args["H"], args["T"], args["d_k"], args["d_v"],
+        args["chunk"], args["dtype"], None) == code
+
+
+@pytest.mark.parametrize("over,code", [(dict(ck=None), ERR_NULL), (dict(ck=P + 8), ERR_ALIGN),
+                                       (dict(dy=None), ERR_NULL), (dict(dtype=7), ERR_DTYPE)])
+def test_backward_checkpointed_rejects_bad_arguments(lib, over, code):
+    a = dict(q=P, k=P, v=P, beta=P, d=P, A=P, I_prior=P, mu0=None, I0=None, dy=P, dmu=None, dI=None, dq=P, dk=P, dv=P,
+             db=P, dd=P, dA=P, dIp=P, dmu0=None, dI0=None, ck=P, B=1, H=2, T=16, d_k=128, d_v=64, dtype=1)
+    a.update(over)
+    assert lib.palimpsa_backward_checkpointed(
+        a["q"], a["k"], a["v"], a["beta"], a["d"], a["A"], a["I_prior"], a["mu0"], a["I0"], a["dy"], a["dmu"], a["dI"],
+        a["dq"], a["dk"], a["dv"], a["db"], a["dd"], a["dA"], a["dIp"], a["dmu0"], a["dI0"], a["ck"], a["B"], a["H"],
+        a["T"], a["d_k"], a["d_v"], a["dtype"], None) == code

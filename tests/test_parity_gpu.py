@@ -569,3 +569,63 @@ def test_backward_extreme_gates_and_states():
     errs = {n: rel_l2(got[n].cpu().numpy(), ref[n[1:]]) for n in
             ("dq", "dk", "dv", "dbeta", "dd_t", "dA", "dI_prior", "dmu0", "dI0")}
     assert max(errs.values()) <= TIGHT, errs
+
+
+# ----------------------------------------------------------------- training checkpoints
+
+@pytest.mark.parametrize("B,H,T,bf16,S", [(2, 2, 150, True, 1), (1, 2, 150, True, 3), (1, 3, 97, False, 1),
+                                          (2, 1, 32, True, 1), (1, 1, 1, False, 1)])
+def test_forward_checkpoints_are_the_states_every_32_tokens(B, H, T, bf16, S):
+    """Checkpoint c holds (M, I) = (I mu, I) before token 32 c, as the oracle computes it."""
+    wl = syn.WORKLOADS["small_layer"].with_(B=B, H=H, T=T, bf16=bf16)
+    inp = syn.sequence_inputs(wl, seed=5000 + T + S)
+    mu0, I0 = _random_state(B, H, 64, 128, 5001)
+    gi = _gpu(inp)
+    pal.palimpsa_set_forward_segments(S)
+    try:
+        y, mT, IT, ck = pal.palimpsa_forward_checkpointed(gi["q"], gi["k"], gi["v"], gi["beta"], gi["d_t"], gi["A"],
+                                                          gi["I_prior"], mu0.to(DEV), I0.to(DEV))
+    finally:
+        pal.palimpsa_set_forward_segments(0)
+    assert pal.palimpsa_get_device_status() == 0
+    _check_all((y, mT, IT), oracle_forward_from(inp, mu0=mu0, I0=I0), tol_for(inp), TIGHT)
+    ck = ck.cpu().numpy()
+    for c in range(ck.shape[2]):
+        t = 32 * c
+        if t == 0:
+            mu_r, I_r = syn.as_float64_numpy(mu0), syn.as_float64_numpy(I0)
+        else:
+            prefix = {n: (x[:, :, :t].contiguous() if x.dim() >= 3 else x) for n, x in inp.items()}
+            _, mu_r, I_r = oracle_forward_from(prefix, mu0=mu0, I0=I0)
+        assert rel_l2(ck[:, :, c, :, 0, :], mu_r * I_r) <= TIGHT, c
+        assert rel_l2(ck[:, :, c, :, 1, :], I_r) <= TIGHT, c
+
+
+@pytest.mark.parametrize("B,H,T,dk,dv,bf16,with_state,with_final", [
+    (2, 2, 150, 128, 64, True, True, True), (1, 3, 97, 64, 40, False, False, False),
+    (1, 2, 1, 128, 64, True, True, False), (2, 1, 64, 128, 64, False, True, True)])
+def test_backward_from_forward_checkpoints(B, H, T, dk, dv, bf16, with_state, with_final):
+    """The backward reading the forward's checkpoints matches fp64 autograd, and the
+    backward that recomputes its own checkpoints."""
+    out, ref, _ = _bwd_case(B, H, T, dk, dv, bf16, with_state, with_final, seed=5100 + T)
+    wl = syn.WORKLOADS["small_layer"].with_(B=B, H=H, T=T, d_k=dk, d_v=dv, bf16=bf16)
+    inp = syn.sequence_inputs(wl, seed=5100 + T)
+    g = torch.Generator().manual_seed(5100 + T + 1)
+    mu0 = torch.randn((B, H, dv, dk), generator=g) if with_state else None
+    I0 = (0.5 + 2.0 * torch.rand((B, H, dv, dk), generator=g)) if with_state else None
+    dy = torch.randn((B, H, T, dv), generator=g)
+    dmu = torch.randn((B, H, dv, dk), generator=g) if with_final else None
+    dI = torch.randn((B, H, dv, dk), generator=g) if with_final else None
+    d = lambda t: None if t is None else t.to(DEV)
+    gi = _gpu(inp)
+    _, _, _, ck = pal.palimpsa_forward_checkpointed(gi["q"], gi["k"], gi["v"], gi["beta"], gi["d_t"], gi["A"],
+                                                    gi["I_prior"], d(mu0), d(I0))
+    got = pal.palimpsa_backward(gi["q"], gi["k"], gi["v"], gi["beta"], gi["d_t"], gi["A"], gi["I_prior"], d(mu0),
+                                d(I0), d(dy), d(dmu), d(dI), ckpt=ck)
+    assert pal.palimpsa_get_device_status() == 0
+    pairs = [("dq", "q"), ("dk", "k"), ("dv", "v"), ("dbeta", "beta"), ("dd_t", "d_t"), ("dA", "A"),
+             ("dI_prior", "I_prior")] + ([("dmu0", "mu0"), ("dI0", "I0")] if with_state else [])
+    errs = {n: rel_l2(got[n].cpu(), ref[m]) for n, m in pairs}
+    assert max(errs.values()) <= TIGHT, errs
+    same = {n: rel_l2(got[n].cpu(), out[n].cpu()) for n, _ in pairs}
+    assert max(same.values()) <= 1e-5, same
