@@ -216,9 +216,9 @@ def run_ours(args, ws, rank, local):
                                      inp["I_prior"], y=y_pre, mu_T=mu, I_T=I, chunk=wl.chunk)
         if record:
             e1.record(stream)
-        for s in range(S):
-            pal.palimpsa_step(dec["q"][s], dec["k"][s], dec["v"][s], dec["beta"][s], dec["d_t"][s], inp["A"],
-                              inp["I_prior"], mu, I, y=y_dec[s])
+        if S:  # the S tokens in order, one palimpsa_step launch each
+            pal.palimpsa_step(dec["q"], dec["k"], dec["v"], dec["beta"], dec["d_t"], inp["A"], inp["I_prior"], mu, I,
+                              y=y_dec[:S])
         if record:
             e2.record(stream)
             ev.append((e0, e1, e2))

@@ -690,6 +690,28 @@ def _forward_from_host(q, k, v, beta, d_t, A, I_prior, mu0, I0, y, mu_T, I_T, ch
     return tuple(outs)
 
 
+def _steps_direct(q, k, v, beta, d_t, A, I_prior, mu, I, y, n, stream_handle):
+    """n decode tokens as direct library calls. q, k, v, beta, d_t and y are
+    contiguous device tensors whose leading index is the token, validated by the
+    caller; per token only the addresses move, so the host work per step is one
+    foreign call (the GPU time of a step is ~165 us at B=256, H=32)."""
+    lib = load_library()
+    _, B, H, d_k = q.shape
+    d_v = v.shape[-1]
+    dtype = _in_dtype(q)
+    stream = ctypes.c_void_p(stream_handle)
+    ts = (q, k, v, beta, d_t, y)
+    bases = [t.data_ptr() for t in ts]
+    strides = [t.stride(0) * t.element_size() for t in ts]
+    cA, cIp, cmu, cI = (ctypes.c_void_p(t.data_ptr()) for t in (A, I_prior, mu, I))
+    step = lib.palimpsa_step
+    for t in range(n):
+        a = [b + t * st for b, st in zip(bases, strides)]
+        rc = step(a[0], a[1], a[2], a[3], a[4], cA, cIp, cmu, cI, a[5], B, H, d_k, d_v, dtype, stream)
+        if rc != 0:
+            raise PalimpsaError(rc, "palimpsa_step")
+
+
 def _step_sequence(q, k, v, beta, d_t, A, I_prior, mu, I, y, stream):
     """S decode tokens in order; host inputs are pipelined over blocks of tokens
     while the state stays resident on the device."""
@@ -697,11 +719,33 @@ def _step_sequence(q, k, v, beta, d_t, A, I_prior, mu, I, y, stream):
     d_v = v.shape[-1]
     f32 = torch.float32
     if q.device.type != "cpu":
-        y = torch.empty((S, B, H, d_v), dtype=f32, device=q.device) if y is None else y
-        for t in range(S):
-            palimpsa_step(q[t], k[t], v[t], beta[t], d_t[t], A, I_prior, mu, I, y=y[t], stream=stream)
+        dev = q.device
+        _check(k, "k", q.shape, q.dtype, dev)
+        _check(q, "q", q.shape, None, dev)
+        _check(v, "v", (S, B, H, d_v), q.dtype, dev)
+        _check(beta, "beta", (S, B, H, d_v), q.dtype, dev)
+        _check(d_t, "d_t", (S, B, H), f32, dev)
+        _check(A, "A", (H,), f32, dev)
+        _check(I_prior, "I_prior", (H,), f32, dev)
+        _check(mu, "mu", (B, H, d_v, d_k), f32, dev)
+        _check(I, "I", (B, H, d_v, d_k), f32, dev)
+        y = torch.empty((S, B, H, d_v), dtype=f32, device=dev) if y is None else y
+        _check(y, "y", (S, B, H, d_v), f32, dev)
+        with torch.cuda.device(dev):
+            _steps_direct(q, k, v, beta, d_t, A, I_prior, mu, I, y, S, _stream_handle(stream))
         return y
     dev = _compute_device(mu, I, y)
+    _check(k, "k", q.shape, q.dtype)
+    _check(q, "q", q.shape)
+    _check(v, "v", (S, B, H, d_v), q.dtype)
+    _check(beta, "beta", (S, B, H, d_v), q.dtype)
+    _check(d_t, "d_t", (S, B, H), f32)
+    _check(A, "A", (H,), f32)
+    _check(I_prior, "I_prior", (H,), f32)
+    _check(mu, "mu", (B, H, d_v, d_k), f32)
+    _check(I, "I", (B, H, d_v, d_k), f32)
+    _check(y, "y", (S, B, H, d_v), f32)
+    _in_dtype(q)
     per_step = sum(_nbytes(t) // max(1, S) for t in (q, k, v, beta, d_t))
     blocks, ns = _blocks(S, per_step)
     y_dev_direct = y is not None and y.is_cuda
@@ -721,9 +765,7 @@ def _step_sequence(q, k, v, beta, d_t, A, I_prior, mu, I, y, stream):
             s, n = i % 2, s1 - s0
             p.load(s, [(slots[s][j][:n], t[s0:s1]) for j, t in enumerate(ins)])
             yd = y[s0:s1] if y_dev_direct else yslots[s][:n]
-            for t in range(n):
-                palimpsa_step(slots[s][0][t], slots[s][1][t], slots[s][2][t], slots[s][3][t], slots[s][4][t],
-                              A_d, Ip_d, mu_d, I_d, y=yd[t], stream=p.comp)
+            _steps_direct(*slots[s], A_d, Ip_d, mu_d, I_d, yd, n, p.comp.cuda_stream)
             ev = p.computed(s)
             if not y_dev_direct:
                 p.store(s, ev, [(y[s0:s1], yd)])
