@@ -288,6 +288,25 @@ palimpsa_status palimpsa_step(
     palimpsa_dtype in_dtype, void* cuda_stream);
 
 /*
+ * palimpsa_step_sequence — S decode tokens in order, as S palimpsa_step
+ * launches enqueued by one call (arguments validated once). Token s reads
+ * q[s], k[s], v[s], beta[s], d_t[s] and writes y[s]; the state (mu, I) is
+ * updated in place after every token, exactly as S palimpsa_step calls would.
+ *
+ *   q, k     [S, B, H, d_k]  in_dtype
+ *   v, beta  [S, B, H, d_v]  in_dtype
+ *   d_t      [S, B, H]       fp32 (each token's slice must stay 4-byte aligned)
+ *   y        [S, B, H, d_v]  fp32
+ *   other arguments as for palimpsa_step; S >= 0.
+ */
+palimpsa_status palimpsa_step_sequence(
+    const void* q, const void* k, const void* v, const void* beta,
+    const float* d_t, const float* A, const float* I_prior,
+    float* mu, float* I, float* y,
+    int S, int B, int H, int d_k, int d_v,
+    palimpsa_dtype in_dtype, void* cuda_stream);
+
+/*
  * Options of the fused entry points (bit flags; combine with |).
  *   PALIMPSA_FUSE_QK_NORM  divide q_t and k_t by their L2 norm over d_k
  *                          (x / max(||x||_2, 1e-12)), as the Palimpsa-D block

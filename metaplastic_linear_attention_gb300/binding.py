@@ -97,6 +97,8 @@ def load_library(path: str | None = None):
         lib.palimpsa_step_fused.argtypes = [vp, vp, vp, vp, fp, fp, fp, fp, fp, fp, fp, i, i, i, i, u, i, vp]
         lib.palimpsa_step.restype = i
         lib.palimpsa_step.argtypes = [vp, vp, vp, vp, fp, fp, fp, fp, fp, fp, i, i, i, i, i, vp]
+        lib.palimpsa_step_sequence.restype = i
+        lib.palimpsa_step_sequence.argtypes = [vp, vp, vp, vp, fp, fp, fp, fp, fp, fp, i, i, i, i, i, i, vp]
         lib.palimpsa_status_string.restype = ctypes.c_char_p
         lib.palimpsa_status_string.argtypes = [i]
         lib.palimpsa_get_device_status.restype = i
@@ -691,25 +693,16 @@ def _forward_from_host(q, k, v, beta, d_t, A, I_prior, mu0, I0, y, mu_T, I_T, ch
 
 
 def _steps_direct(q, k, v, beta, d_t, A, I_prior, mu, I, y, n, stream_handle):
-    """n decode tokens as direct library calls. q, k, v, beta, d_t and y are
-    contiguous device tensors whose leading index is the token, validated by the
-    caller; per token only the addresses move, so the host work per step is one
-    foreign call (the GPU time of a step is ~165 us at B=256, H=32)."""
-    lib = load_library()
+    """The first n tokens of contiguous device tensors whose leading index is the
+    token (validated by the caller), as one palimpsa_step_sequence call: the
+    library enqueues the n step launches itself."""
     _, B, H, d_k = q.shape
     d_v = v.shape[-1]
-    dtype = _in_dtype(q)
-    stream = ctypes.c_void_p(stream_handle)
-    ts = (q, k, v, beta, d_t, y)
-    bases = [t.data_ptr() for t in ts]
-    strides = [t.stride(0) * t.element_size() for t in ts]
-    cA, cIp, cmu, cI = (ctypes.c_void_p(t.data_ptr()) for t in (A, I_prior, mu, I))
-    step = lib.palimpsa_step
-    for t in range(n):
-        a = [b + t * st for b, st in zip(bases, strides)]
-        rc = step(a[0], a[1], a[2], a[3], a[4], cA, cIp, cmu, cI, a[5], B, H, d_k, d_v, dtype, stream)
-        if rc != 0:
-            raise PalimpsaError(rc, "palimpsa_step")
+    rc = load_library().palimpsa_step_sequence(
+        _ptr(q), _ptr(k), _ptr(v), _ptr(beta), _ptr(d_t), _ptr(A), _ptr(I_prior), _ptr(mu), _ptr(I), _ptr(y), int(n),
+        B, H, d_k, d_v, _in_dtype(q), ctypes.c_void_p(stream_handle))
+    if rc != 0:
+        raise PalimpsaError(rc, "palimpsa_step_sequence")
 
 
 def _step_sequence(q, k, v, beta, d_t, A, I_prior, mu, I, y, stream):

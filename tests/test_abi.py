@@ -288,3 +288,24 @@ def test_backward_checkpointed_rejects_bad_arguments(lib, over, code):
         a["q"], a["k"], a["v"], a["beta"], a["d"], a["A"], a["I_prior"], a["mu0"], a["I0"], a["dy"], a["dmu"], a["dI"],
         a["dq"], a["dk"], a["dv"], a["db"], a["dd"], a["dA"], a["dIp"], a["dmu0"], a["dI0"], a["ck"], a["B"], a["H"],
         a["T"], a["d_k"], a["d_v"], a["dtype"], None) == code
+
+
+def _seq(lib, **over):
+    args = dict(q=P, k=P, v=P, beta=P, d=P, A=P, I_prior=P, mu=P, I=P, y=P, S=4, B=4, H=2, d_k=128, d_v=64, dtype=1)
+    args.update(over)
+    return lib.palimpsa_step_sequence(args["q"], args["k"], args["v"], args["beta"], args["d"], args["A"],
+                                      args["I_prior"], args["mu"], args["I"], args["y"], args["S"], args["B"],
+                                      args["H"], args["d_k"], args["d_v"], args["dtype"], None)
+
+
+@pytest.mark.parametrize("over,code", [
+    (dict(S=-1), ERR_SHAPE), (dict(q=None), ERR_NULL), (dict(mu=None), ERR_NULL), (dict(dtype=3), ERR_DTYPE),
+    (dict(B=0), ERR_SHAPE), (dict(d_v=12), ERR_UNSUPPORTED), (dict(y=P + 4), ERR_ALIGN),
+])
+def test_step_sequence_rejects_bad_arguments(lib, over, code):
+    assert _seq(lib, **over) == code
+
+
+def test_step_sequence_of_no_tokens_does_nothing(lib):
+    # S = 0 returns before any pointer is looked at or any device call is made
+    assert _seq(lib, S=0, q=None, k=None, v=None, beta=None, d=None, y=None) == OK

@@ -629,3 +629,22 @@ def test_backward_from_forward_checkpoints(B, H, T, dk, dv, bf16, with_state, wi
     assert max(errs.values()) <= TIGHT, errs
     same = {n: rel_l2(got[n].cpu(), out[n].cpu()) for n, _ in pairs}
     assert max(same.values()) <= 1e-5, same
+
+
+def test_step_sequence_equals_token_by_token_bitwise():
+    """One palimpsa_step_sequence call (4-D inputs on the device) enqueues the same
+    launches as S palimpsa_step calls: identical bits."""
+    wl = syn.WORKLOADS["decode"].with_(B=3, H=2)
+    seq = _gpu(syn.sequence_inputs(wl, T=1, seed=81))
+    steps = _gpu(syn.decode_inputs(wl, 9, seed=81))
+    g = torch.Generator().manual_seed(82)
+    mu0 = torch.randn((3, 2, 64, 128), generator=g).to(DEV)
+    I0 = (0.5 + torch.rand((3, 2, 64, 128), generator=g)).to(DEV)
+    mu_a, I_a = mu0.clone(), I0.clone()
+    y_a = pal.palimpsa_step(steps["q"], steps["k"], steps["v"], steps["beta"], steps["d_t"], seq["A"],
+                            seq["I_prior"], mu_a, I_a)
+    mu_b, I_b = mu0.clone(), I0.clone()
+    y_b = torch.stack([pal.palimpsa_step(steps["q"][t], steps["k"][t], steps["v"][t], steps["beta"][t],
+                                         steps["d_t"][t], seq["A"], seq["I_prior"], mu_b, I_b) for t in range(9)])
+    assert pal.palimpsa_get_device_status() == 0
+    assert torch.equal(y_a, y_b) and torch.equal(mu_a, mu_b) and torch.equal(I_a, I_b)
