@@ -266,6 +266,21 @@ palimpsa_status palimpsa_state_combine(
     int B, int H, int d_k, int d_v, void* cuda_stream);
 
 /*
+ * palimpsa_forward_varlen_fused — palimpsa_forward_varlen with the prologue
+ * of palimpsa_forward_fused: raw q, k, v (or v*), beta_raw, d_raw in the packed
+ * layout, b_scale [H] or NULL, flags (palimpsa_fuse_flags). Everything else as
+ * for palimpsa_forward_varlen.
+ */
+palimpsa_status palimpsa_forward_varlen_fused(
+    const void* q, const void* k, const void* v, const void* beta_raw,
+    const float* d_raw, const float* A, const float* I_prior,
+    const float* b_scale, const float* mu0, const float* I0,
+    float* y, float* mu_T, float* I_T,
+    const int* cu_seqlens, int N, int H, int total_T, int max_seqlen,
+    int d_k, int d_v, int chunk, unsigned int flags,
+    palimpsa_dtype in_dtype, void* cuda_stream);
+
+/*
  * palimpsa_step — one recurrent (decode) token for B x H heads, in place.
  *
  * The recurrent inference update of slide 22 / paper App. A.13 (Fig. 7):

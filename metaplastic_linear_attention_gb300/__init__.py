@@ -27,6 +27,7 @@ from .binding import (  # noqa: F401
     palimpsa_forward_fused,
     palimpsa_forward_plan,
     palimpsa_forward_varlen,
+    palimpsa_forward_varlen_fused,
     palimpsa_forward_without_meta,
     palimpsa_get_device_status,
     palimpsa_segment_summary,

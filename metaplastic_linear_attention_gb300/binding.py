@@ -74,6 +74,9 @@ def load_library(path: str | None = None):
         lib.palimpsa_forward_fused.restype = i
         lib.palimpsa_forward_fused.argtypes = [vp, vp, vp, vp, fp, fp, fp, fp, fp, fp, fp, fp, fp,
                                                i, i, i, i, i, i, u, i, vp]
+        lib.palimpsa_forward_varlen_fused.restype = i
+        lib.palimpsa_forward_varlen_fused.argtypes = [vp, vp, vp, vp, fp, fp, fp, fp, fp, fp, fp, fp, fp, vp,
+                                                      i, i, i, i, i, i, i, ctypes.c_uint, i, vp]
         lib.palimpsa_forward_varlen.restype = i
         lib.palimpsa_forward_varlen.argtypes = [vp, vp, vp, vp, fp, fp, fp, fp, fp, fp, fp, fp, vp,
                                                 i, i, i, i, i, i, i, i, vp]
@@ -278,8 +281,22 @@ def palimpsa_forward_varlen(q, k, v, beta, d_t, A, I_prior, cu_seqlens, mu0=None
     d_v, d_k] or None. max_seqlen: the longest sequence (read from cu_seqlens
     when not given, which synchronises). Device tensors otherwise. Returns
     (y [H, total_T, d_v], mu_T [N, H, d_v, d_k], I_T)."""
+    return _varlen(q, k, v, beta, d_t, A, I_prior, cu_seqlens, mu0, I0, max_seqlen, y, mu_T, I_T, chunk, stream,
+                   None)
+
+
+def palimpsa_forward_varlen_fused(q, k, v, beta_raw, d_raw, A, I_prior, cu_seqlens, b_scale=None, mu0=None, I0=None, *,
+                                  qk_norm=False, v_star=False, max_seqlen=None, y=None, mu_T=None, I_T=None,
+                                  chunk: int = 0, stream=None):
+    """palimpsa_forward_varlen from raw projections with the fused prologue of
+    palimpsa_forward_fused (see palimpsa.h)."""
+    return _varlen(q, k, v, beta_raw, d_raw, A, I_prior, cu_seqlens, mu0, I0, max_seqlen, y, mu_T, I_T, chunk, stream,
+                   (b_scale, _fuse_flags(qk_norm, v_star)))
+
+
+def _varlen(q, k, v, beta, d_t, A, I_prior, cu_seqlens, mu0, I0, max_seqlen, y, mu_T, I_T, chunk, stream, fused):
     if q.device.type != "cuda":
-        raise ValueError("palimpsa_forward_varlen takes device tensors")
+        raise ValueError("the packed forward takes device tensors")
     H, total_T, d_k = q.shape
     d_v = v.shape[-1]
     dev = q.device
@@ -291,12 +308,13 @@ def palimpsa_forward_varlen(q, k, v, beta, d_t, A, I_prior, cu_seqlens, mu0=None
         host = cu_seqlens.cpu()
         max_seqlen = int((host[1:] - host[:-1]).max())
     cu_d = cu_seqlens if cu_seqlens.is_cuda else cu_seqlens.to(dev)
+    names = ("beta", "d_t") if fused is None else ("beta_raw", "d_raw")
     _check(cu_d, "cu_seqlens", (N + 1,), torch.int32, dev)
     _check(k, "k", q.shape, q.dtype, dev)
     _check(q, "q", q.shape, None, dev)
     _check(v, "v", (H, total_T, d_v), q.dtype, dev)
-    _check(beta, "beta", (H, total_T, d_v), q.dtype, dev)
-    _check(d_t, "d_t", (H, total_T), f32, dev)
+    _check(beta, names[0], (H, total_T, d_v), q.dtype, dev)
+    _check(d_t, names[1], (H, total_T), f32, dev)
     _check(A, "A", (H,), f32, dev)
     _check(I_prior, "I_prior", (H,), f32, dev)
     _check(mu0, "mu0", (N, H, d_v, d_k), f32, dev)
@@ -308,13 +326,20 @@ def palimpsa_forward_varlen(q, k, v, beta, d_t, A, I_prior, cu_seqlens, mu0=None
     _check(mu_T, "mu_T", (N, H, d_v, d_k), f32, dev)
     _check(I_T, "I_T", (N, H, d_v, d_k), f32, dev)
     lib = load_library()
+    head = [_ptr(q), _ptr(k), _ptr(v), _ptr(beta), _ptr(d_t), _ptr(A), _ptr(I_prior)]
+    mid = [_ptr(mu0), _ptr(I0), _ptr(y), _ptr(mu_T), _ptr(I_T), _ptr(cu_d), N, H, total_T, int(max_seqlen), d_k, d_v,
+           int(chunk)]
+    st = ctypes.c_void_p(_stream_handle(stream))
     with torch.cuda.device(dev):
-        rc = lib.palimpsa_forward_varlen(
-            _ptr(q), _ptr(k), _ptr(v), _ptr(beta), _ptr(d_t), _ptr(A), _ptr(I_prior), _ptr(mu0), _ptr(I0), _ptr(y),
-            _ptr(mu_T), _ptr(I_T), _ptr(cu_d), N, H, total_T, int(max_seqlen), d_k, d_v, int(chunk), _in_dtype(q),
-            ctypes.c_void_p(_stream_handle(stream)))
+        if fused is None:
+            rc, name = lib.palimpsa_forward_varlen(*head, *mid, _in_dtype(q), st), "palimpsa_forward_varlen"
+        else:
+            b_scale, flags = fused
+            _check(b_scale, "b_scale", (H,), f32, dev)
+            rc, name = (lib.palimpsa_forward_varlen_fused(*head, _ptr(b_scale), *mid, flags, _in_dtype(q), st),
+                        "palimpsa_forward_varlen_fused")
     if rc != 0:
-        raise PalimpsaError(rc, "palimpsa_forward_varlen")
+        raise PalimpsaError(rc, name)
     return y, mu_T, I_T
 
 

@@ -198,11 +198,12 @@ palimpsa_status palimpsa_forward_plan(int B, int H, int T, int d_k, int d_v, int
   return PALIMPSA_OK;
 }
 
-palimpsa_status palimpsa_forward_varlen(const void* q, const void* k, const void* v, const void* beta,
-                                        const float* d_t, const float* A, const float* I_prior, const float* mu0,
-                                        const float* I0, float* y, float* mu_T, float* I_T, const int* cu_seqlens,
-                                        int N, int H, int total_T, int max_seqlen, int d_k, int d_v, int chunk,
-                                        palimpsa_dtype in_dtype, void* cuda_stream) {
+// Validation and launch shared by palimpsa_forward_varlen and _varlen_fused.
+static palimpsa_status varlen_impl(const void* q, const void* k, const void* v, const void* beta, const float* d_t,
+                                   const float* A, const float* I_prior, const float* mu0, const float* I0, float* y,
+                                   float* mu_T, float* I_T, const int* cu_seqlens, int N, int H, int total_T,
+                                   int max_seqlen, int d_k, int d_v, int chunk, palimpsa_dtype in_dtype,
+                                   void* cuda_stream, const Prologue& pro) {
   if (!A || !I_prior || !mu_T || !I_T || !cu_seqlens) return PALIMPSA_ERR_NULL;
   if (total_T != 0 && (!q || !k || !v || !beta || !d_t || !y)) return PALIMPSA_ERR_NULL;
   if (in_dtype != PALIMPSA_F32 && in_dtype != PALIMPSA_BF16) return PALIMPSA_ERR_DTYPE;
@@ -213,20 +214,40 @@ palimpsa_status palimpsa_forward_varlen(const void* q, const void* k, const void
   const void* a16[] = {q, k, v, beta, y, mu_T, I_T, mu0, I0};
   for (const void* p : a16)
     if (p && !aligned(p, 16)) return PALIMPSA_ERR_ALIGN;
-  const void* a4[] = {d_t, A, I_prior, cu_seqlens};
+  const void* a4[] = {d_t, A, I_prior, cu_seqlens, pro.b_scale};
   for (const void* p : a4)
     if (p && !aligned(p, 4)) return PALIMPSA_ERR_ALIGN;
   unsigned int* st = nullptr;
   if (palimpsa_status s = status_word(&st)) return s;
   FwdArgs a{q, k, v, beta, d_t, A, I_prior, mu0, I0, y, mu_T, I_T, N, H, max_seqlen, d_k, d_v,
             chunk == 0 ? 32 : chunk, in_dtype == PALIMPSA_BF16, st,
-            g_wait_timeout_ns.load(), g_withhold_first_copy.load(), g_forward_segments.load(), Prologue{}};
+            g_wait_timeout_ns.load(), g_withhold_first_copy.load(), g_forward_segments.load(), pro};
   a.cu_seqlens = cu_seqlens;
   a.total_T = total_T;
   StreamOrderedScratch scratch;
   if (launch_forward_chunked(a, static_cast<cudaStream_t>(cuda_stream), &scratch) != cudaSuccess)
     return PALIMPSA_ERR_CUDA;
   return PALIMPSA_OK;
+}
+
+palimpsa_status palimpsa_forward_varlen(const void* q, const void* k, const void* v, const void* beta,
+                                        const float* d_t, const float* A, const float* I_prior, const float* mu0,
+                                        const float* I0, float* y, float* mu_T, float* I_T, const int* cu_seqlens,
+                                        int N, int H, int total_T, int max_seqlen, int d_k, int d_v, int chunk,
+                                        palimpsa_dtype in_dtype, void* cuda_stream) {
+  return varlen_impl(q, k, v, beta, d_t, A, I_prior, mu0, I0, y, mu_T, I_T, cu_seqlens, N, H, total_T, max_seqlen,
+                     d_k, d_v, chunk, in_dtype, cuda_stream, Prologue{});
+}
+
+palimpsa_status palimpsa_forward_varlen_fused(const void* q, const void* k, const void* v, const void* beta_raw,
+                                              const float* d_raw, const float* A, const float* I_prior,
+                                              const float* b_scale, const float* mu0, const float* I0, float* y,
+                                              float* mu_T, float* I_T, const int* cu_seqlens, int N, int H,
+                                              int total_T, int max_seqlen, int d_k, int d_v, int chunk,
+                                              unsigned int flags, palimpsa_dtype in_dtype, void* cuda_stream) {
+  if (flags & ~kKnownFuseFlags) return PALIMPSA_ERR_UNSUPPORTED;
+  return varlen_impl(q, k, v, beta_raw, d_raw, A, I_prior, mu0, I0, y, mu_T, I_T, cu_seqlens, N, H, total_T,
+                     max_seqlen, d_k, d_v, chunk, in_dtype, cuda_stream, fused_prologue(b_scale, flags));
 }
 
 palimpsa_status palimpsa_segment_summary(const void* q, const void* k, const void* v, const void* beta,

@@ -157,13 +157,14 @@ def varlen_lengths(total: int, n: int, seed: int):
     return [int(x) for x in raw]
 
 
-def packed_inputs(wl: Workload, lengths, *, H=None, device="cpu", seed=None):
+def packed_inputs(wl: Workload, lengths, *, H=None, device="cpu", seed=None, raw=False):
     """A packed variable-length batch with the workload's recipe: q, k
     [H, total_T, d_k]; v, beta [H, total_T, d_v]; d_t [H, total_T]; A, I_prior
-    [H]; cu_seqlens [N + 1] int32 with sequence n = tokens [cu[n], cu[n+1])."""
+    [H]; cu_seqlens [N + 1] int32 with sequence n = tokens [cu[n], cu[n+1]).
+    With `raw`, the pre-activation draws as in ``sequence_inputs``."""
     H = wl.H if H is None else H
     total = int(sum(lengths))
-    inp = sequence_inputs(wl, B=1, H=H, T=total, device=device, seed=seed)
+    inp = sequence_inputs(wl, B=1, H=H, T=total, device=device, seed=seed, raw=raw)
     out = {k: (v[0].contiguous() if v.dim() >= 3 else v) for k, v in inp.items()}
     cu = [0]
     for n in lengths:

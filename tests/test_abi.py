@@ -309,3 +309,15 @@ def test_step_sequence_rejects_bad_arguments(lib, over, code):
 def test_step_sequence_of_no_tokens_does_nothing(lib):
     # S = 0 returns before any pointer is looked at or any device call is made
     assert _seq(lib, S=0, q=None, k=None, v=None, beta=None, d=None, y=None) == OK
+
+
+@pytest.mark.parametrize("over,code", [(dict(flags=8), ERR_UNSUPPORTED), (dict(b_scale=P + 2), ERR_ALIGN),
+                                       (dict(cu=None), ERR_NULL), (dict(max_seqlen=200), ERR_SHAPE)])
+def test_forward_varlen_fused_rejects_bad_arguments(lib, over, code):
+    a = dict(q=P, k=P, v=P, b=P, d=P, A=P, I_prior=P, b_scale=None, mu0=None, I0=None, y=P, mu_T=P, I_T=P, cu=P, N=3,
+             H=2, total_T=100, max_seqlen=50, d_k=128, d_v=64, chunk=0, flags=1, dtype=1)
+    a.update(over)
+    assert lib.palimpsa_forward_varlen_fused(
+        a["q"], a["k"], a["v"], a["b"], a["d"], a["A"], a["I_prior"], a["b_scale"], a["mu0"], a["I0"], a["y"],
+        a["mu_T"], a["I_T"], a["cu"], a["N"], a["H"], a["total_T"], a["max_seqlen"], a["d_k"], a["d_v"], a["chunk"],
+        a["flags"], a["dtype"], None) == code

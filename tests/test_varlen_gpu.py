@@ -124,3 +124,28 @@ def test_bad_offsets_are_reported_not_faulted():
         assert rel_l2(y[:, :20].cpu().numpy(), ref[0][:, :20]) <= TIGHT
         assert rel_l2(mu[0].cpu().numpy(), ref[1][0]) <= TIGHT
     _check(_gpu(inp), ref)
+
+
+@pytest.mark.parametrize("flags", [dict(qk_norm=True, v_star=False), dict(qk_norm=True, v_star=True),
+                                   dict(qk_norm=False, v_star=True)])
+@pytest.mark.parametrize("S", [0, 3])
+def test_varlen_fused_matches_oracle(flags, S):
+    """Packed sequences from raw projections: the prologue of the fused forward
+    applied per token, then each sequence from its own state."""
+    from oracle import prologue as opro
+    lengths = [120, 0, 33, 257, 1]
+    wl = syn.WORKLOADS["small_layer"].with_(seed=606)
+    raw = syn.packed_inputs(wl, lengths, H=2, raw=True)
+    q, k, v, beta, d_t = opro.apply(*(f64(raw[n])[None] for n in ("q", "k", "v", "beta_raw", "d_raw")),
+                                    b_scale=f64(raw["b_scale"]), qk_norm=flags["qk_norm"])
+    ref = ovl.forward(q[0], k[0], v[0], beta[0], d_t[0], f64(raw["A"]), f64(raw["I_prior"]),
+                      raw["cu_seqlens"].tolist(), v_star=flags["v_star"])
+    g = {n: t.to(DEV) for n, t in raw.items()}
+    pal.palimpsa_set_forward_segments(S)
+    try:
+        out = pal.palimpsa_forward_varlen_fused(g["q"], g["k"], g["v"], g["beta_raw"], g["d_raw"], g["A"],
+                                                g["I_prior"], g["cu_seqlens"], g["b_scale"], **flags)
+    finally:
+        pal.palimpsa_set_forward_segments(0)
+    assert pal.palimpsa_get_device_status() == 0
+    _check(out, ref)
