@@ -419,6 +419,32 @@ def run_ours(args, ws, rank, local):
         torch.cuda.synchronize()
         bwd_ck_ms = b0.elapsed_time(b1) / 3
         del ck
+        # the same training pair over the packed ragged batch of the varlen line
+        dyv = torch.randn((H, B * T, dv), dtype=f32, device=dev)
+        ckv = pal.palimpsa_forward_varlen_checkpointed(pk["q"], pk["k"], pk["v"], pk["beta"], pk["d_t"], pk["A"],
+                                                       pk["I_prior"], pk["cu_seqlens"], max_seqlen=mx, y=yv,
+                                                       mu_T=mv, I_T=Iv, chunk=wl.chunk)[3]
+
+        def _pair_varlen():
+            pal.palimpsa_forward_varlen_checkpointed(pk["q"], pk["k"], pk["v"], pk["beta"], pk["d_t"], pk["A"],
+                                                     pk["I_prior"], pk["cu_seqlens"], max_seqlen=mx, ckpt=ckv, y=yv,
+                                                     mu_T=mv, I_T=Iv, chunk=wl.chunk)
+            pal.palimpsa_backward_varlen(pk["q"], pk["k"], pk["v"], pk["beta"], pk["d_t"], pk["A"], pk["I_prior"],
+                                         pk["cu_seqlens"], None, None, dyv, max_seqlen=mx, want_state_grads=False,
+                                         ckpt=ckv)
+        _pair_varlen()
+        b0.record(stream)
+        for _ in range(3):
+            _pair_varlen()
+        b1.record(stream)
+        torch.cuda.synchronize()
+        pair_var_ms = b0.elapsed_time(b1) / 3
+        del ckv, dyv
+        kernels["palimpsa_train_pair_varlen"] = {
+            "avg_ms": pair_var_ms, "head_tokens_per_s": B * H * T / (pair_var_ms / 1e3),
+            "over_dense_pair": pair_var_ms / (fwd_ck_ms + bwd_ck_ms), "sequences": len(lengths), "max_seqlen": mx,
+            "note": "checkpointed packed forward + packed backward from its checkpoints over the varlen line's "
+                    "ragged batch; timed after the timed region"}
         kernels["palimpsa_backward"] = {"avg_ms": bwd_ms, "head_tokens_per_s": B * H * T / (bwd_ms / 1e3),
                                         "over_forward": bwd_ms / fwd_avg_ms,
                                         "checkpointed_forward_ms": fwd_ck_ms,

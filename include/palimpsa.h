@@ -475,6 +475,56 @@ palimpsa_status palimpsa_backward_checkpointed(
     int B, int H, int T, int d_k, int d_v,
     palimpsa_dtype in_dtype, void* cuda_stream);
 
+/*
+ * Packed training pair: palimpsa_forward_varlen_checkpointed and
+ * palimpsa_backward_varlen are the training pair above over the packed batch of
+ * palimpsa_forward_varlen (N sequences of different lengths, one state each;
+ * the gradient of each sequence is that of the recurrence run on it alone, and
+ * dA, dI_prior sum over all sequences).
+ *
+ *   per-token arrays (q, k, v, beta, d_t, dy and the gradients dq, dk, dv,
+ *             dbeta, dd_t) in the layout of palimpsa_forward_varlen:
+ *             [H, total_T, ...]; gradient rows of tokens outside every
+ *             sequence are zero (dq, dk, dd_t) or not written (dv, dbeta)
+ *   per-sequence states mu0, I0, dmu_T, dI_T, dmu0, dI0: [N, H, d_v, d_k]
+ *   cu_seqlens, N, H, total_T, max_seqlen as for palimpsa_forward_varlen
+ *   ckpt      fp32 [H, total_T / 32 + N, d_v, 2, d_k] (integer division),
+ *             palimpsa_checkpoint_bytes_varlen(N, H, total_T, d_k, d_v)
+ *             bytes, 16-byte aligned; memory grows with the tokens, not with
+ *             N x max_seqlen. Head h of sequence n (which starts at token s0)
+ *             keeps its state before its token 32 c in slot
+ *             s0 / 32 + n + c of head h, as (M_i, I_i) per value row i like
+ *             the dense checkpoints; sequences never share a slot, and slots
+ *             that no sequence owns are not written. For the backward, ckpt
+ *             may be NULL: it then recomputes the states with a forward sweep
+ *             into scratch of that size from the library's pool.
+ *
+ * Offsets that break the rules of palimpsa_forward_varlen are reported as
+ * there: the CTAs of that sequence touch nothing else and latch
+ * PALIMPSA_ERR_DOMAIN (its dmu0 / dI0 are then not written). Other errors as
+ * for palimpsa_backward.
+ */
+size_t palimpsa_checkpoint_bytes_varlen(int N, int H, int total_T, int d_k, int d_v);
+
+palimpsa_status palimpsa_forward_varlen_checkpointed(
+    const void* q, const void* k, const void* v, const void* beta,
+    const float* d_t, const float* A, const float* I_prior,
+    const float* mu0, const float* I0,
+    float* y, float* mu_T, float* I_T, float* ckpt,
+    const int* cu_seqlens, int N, int H, int total_T, int max_seqlen,
+    int d_k, int d_v, int chunk, palimpsa_dtype in_dtype, void* cuda_stream);
+
+palimpsa_status palimpsa_backward_varlen(
+    const void* q, const void* k, const void* v, const void* beta,
+    const float* d_t, const float* A, const float* I_prior,
+    const float* mu0, const float* I0,
+    const float* dy, const float* dmu_T, const float* dI_T,
+    float* dq, float* dk, float* dv, float* dbeta, float* dd_t,
+    float* dA, float* dI_prior, float* dmu0, float* dI0,
+    const float* ckpt,
+    const int* cu_seqlens, int N, int H, int total_T, int max_seqlen,
+    int d_k, int d_v, palimpsa_dtype in_dtype, void* cuda_stream);
+
 /* Static English text for a status code (never NULL). */
 const char* palimpsa_status_string(palimpsa_status s);
 

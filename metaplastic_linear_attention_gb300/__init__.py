@@ -28,6 +28,10 @@ from .binding import (  # noqa: F401
     palimpsa_forward_plan,
     palimpsa_forward_varlen,
     palimpsa_forward_varlen_fused,
+    palimpsa_forward_varlen_checkpointed,
+    palimpsa_backward_varlen,
+    palimpsa_checkpoint_bytes_varlen,
+    packed_checkpoint_shape,
     palimpsa_forward_without_meta,
     palimpsa_get_device_status,
     palimpsa_segment_summary,

@@ -92,6 +92,14 @@ def load_library(path: str | None = None):
         lib.palimpsa_backward_checkpointed.restype = i
         lib.palimpsa_backward_checkpointed.argtypes = [vp, vp, vp, vp, fp, fp, fp, fp, fp, fp, fp, fp, fp, fp, fp,
                                                        fp, fp, fp, fp, fp, fp, fp, i, i, i, i, i, i, vp]
+        lib.palimpsa_checkpoint_bytes_varlen.restype = ctypes.c_size_t
+        lib.palimpsa_checkpoint_bytes_varlen.argtypes = [i, i, i, i, i]
+        lib.palimpsa_forward_varlen_checkpointed.restype = i
+        lib.palimpsa_forward_varlen_checkpointed.argtypes = [vp, vp, vp, vp, fp, fp, fp, fp, fp, fp, fp, fp, fp, vp,
+                                                             i, i, i, i, i, i, i, i, vp]
+        lib.palimpsa_backward_varlen.restype = i
+        lib.palimpsa_backward_varlen.argtypes = [vp, vp, vp, vp, fp, fp, fp, fp, fp, fp, fp, fp, fp, fp, fp, fp, fp,
+                                                 fp, fp, fp, fp, fp, vp, i, i, i, i, i, i, i, vp]
         lib.palimpsa_forward_plan.restype = i
         lib.palimpsa_forward_plan.argtypes = [i, i, i, i, i, i, i, ctypes.POINTER(ctypes.c_int),
                                               ctypes.POINTER(ctypes.c_int), ctypes.POINTER(ctypes.c_int),
@@ -294,13 +302,8 @@ def palimpsa_forward_varlen_fused(q, k, v, beta_raw, d_raw, A, I_prior, cu_seqle
                    (b_scale, _fuse_flags(qk_norm, v_star)))
 
 
-def _varlen(q, k, v, beta, d_t, A, I_prior, cu_seqlens, mu0, I0, max_seqlen, y, mu_T, I_T, chunk, stream, fused):
-    if q.device.type != "cuda":
-        raise ValueError("the packed forward takes device tensors")
-    H, total_T, d_k = q.shape
-    d_v = v.shape[-1]
-    dev = q.device
-    f32 = torch.float32
+def _packed_offsets(cu_seqlens, max_seqlen, dev):
+    """(offsets on the device, N, max_seqlen) of a packed batch."""
     if cu_seqlens.dtype != torch.int32 or cu_seqlens.dim() != 1 or cu_seqlens.numel() < 2:
         raise ValueError("cu_seqlens must be a 1-D int32 tensor of N + 1 offsets")
     N = cu_seqlens.numel() - 1
@@ -308,8 +311,20 @@ def _varlen(q, k, v, beta, d_t, A, I_prior, cu_seqlens, mu0, I0, max_seqlen, y, 
         host = cu_seqlens.cpu()
         max_seqlen = int((host[1:] - host[:-1]).max())
     cu_d = cu_seqlens if cu_seqlens.is_cuda else cu_seqlens.to(dev)
-    names = ("beta", "d_t") if fused is None else ("beta_raw", "d_raw")
     _check(cu_d, "cu_seqlens", (N + 1,), torch.int32, dev)
+    return cu_d, N, int(max_seqlen)
+
+
+def _varlen(q, k, v, beta, d_t, A, I_prior, cu_seqlens, mu0, I0, max_seqlen, y, mu_T, I_T, chunk, stream, fused,
+            ckpt=None):
+    if q.device.type != "cuda":
+        raise ValueError("the packed forward takes device tensors")
+    H, total_T, d_k = q.shape
+    d_v = v.shape[-1]
+    dev = q.device
+    f32 = torch.float32
+    cu_d, N, max_seqlen = _packed_offsets(cu_seqlens, max_seqlen, dev)
+    names = ("beta", "d_t") if fused is None else ("beta_raw", "d_raw")
     _check(k, "k", q.shape, q.dtype, dev)
     _check(q, "q", q.shape, None, dev)
     _check(v, "v", (H, total_T, d_v), q.dtype, dev)
@@ -327,11 +342,16 @@ def _varlen(q, k, v, beta, d_t, A, I_prior, cu_seqlens, mu0, I0, max_seqlen, y, 
     _check(I_T, "I_T", (N, H, d_v, d_k), f32, dev)
     lib = load_library()
     head = [_ptr(q), _ptr(k), _ptr(v), _ptr(beta), _ptr(d_t), _ptr(A), _ptr(I_prior)]
-    mid = [_ptr(mu0), _ptr(I0), _ptr(y), _ptr(mu_T), _ptr(I_T), _ptr(cu_d), N, H, total_T, int(max_seqlen), d_k, d_v,
+    mid = [_ptr(mu0), _ptr(I0), _ptr(y), _ptr(mu_T), _ptr(I_T), _ptr(cu_d), N, H, total_T, max_seqlen, d_k, d_v,
            int(chunk)]
     st = ctypes.c_void_p(_stream_handle(stream))
     with torch.cuda.device(dev):
-        if fused is None:
+        if ckpt is not None:
+            _check(ckpt, "ckpt", packed_checkpoint_shape(N, H, total_T, d_k, d_v), f32, dev)
+            mid.insert(5, _ptr(ckpt))
+            rc, name = (lib.palimpsa_forward_varlen_checkpointed(*head, *mid, _in_dtype(q), st),
+                        "palimpsa_forward_varlen_checkpointed")
+        elif fused is None:
             rc, name = lib.palimpsa_forward_varlen(*head, *mid, _in_dtype(q), st), "palimpsa_forward_varlen"
         else:
             b_scale, flags = fused
@@ -543,6 +563,83 @@ def palimpsa_backward(q, k, v, beta, d_t, A, I_prior, mu0, I0, dy, dmu_T=None, d
             rc, name = lib.palimpsa_backward_checkpointed(*args, _ptr(ckpt), *tail), "palimpsa_backward_checkpointed"
     if rc != 0:
         raise PalimpsaError(rc, name)
+    return g
+
+
+def palimpsa_checkpoint_bytes_varlen(N, H, total_T, d_k, d_v) -> int:
+    """Bytes of the training checkpoints of a packed forward (see palimpsa.h)."""
+    return int(load_library().palimpsa_checkpoint_bytes_varlen(int(N), int(H), int(total_T), int(d_k), int(d_v)))
+
+
+def packed_checkpoint_shape(N, H, total_T, d_k, d_v):
+    """Shape of a packed batch's checkpoints: per head, total_T // 32 + N slots."""
+    return (H, total_T // 32 + N, d_v, 2, d_k)
+
+
+def palimpsa_forward_varlen_checkpointed(q, k, v, beta, d_t, A, I_prior, cu_seqlens, mu0=None, I0=None, *,
+                                         max_seqlen=None, ckpt=None, y=None, mu_T=None, I_T=None, chunk: int = 0,
+                                         stream=None):
+    """palimpsa_forward_varlen for training (see palimpsa.h): also writes each
+    sequence's state before its every 32nd token, for palimpsa_backward_varlen.
+    Returns (y, mu_T, I_T, ckpt); ckpt is [H, total_T//32 + N, d_v, 2, d_k], and
+    sequence n (from token s0) keeps its checkpoint c in slot s0//32 + n + c."""
+    if q.device.type != "cuda":
+        raise ValueError("the packed forward takes device tensors")
+    cu_d, N, max_seqlen = _packed_offsets(cu_seqlens, max_seqlen, q.device)
+    H, total_T, d_k = q.shape
+    d_v = v.shape[-1]
+    if ckpt is None:
+        ckpt = torch.empty(packed_checkpoint_shape(N, H, total_T, d_k, d_v), dtype=torch.float32, device=q.device)
+    y, mu_T, I_T = _varlen(q, k, v, beta, d_t, A, I_prior, cu_d, mu0, I0, max_seqlen, y, mu_T, I_T, chunk, stream,
+                           None, ckpt=ckpt)
+    return y, mu_T, I_T, ckpt
+
+
+def palimpsa_backward_varlen(q, k, v, beta, d_t, A, I_prior, cu_seqlens, mu0, I0, dy, dmu_T=None, dI_T=None, *,
+                             max_seqlen=None, want_state_grads=True, ckpt=None, stream=None):
+    """Gradients through palimpsa_forward_varlen (see palimpsa.h). Device
+    tensors in the packed layout; ckpt from palimpsa_forward_varlen_checkpointed
+    on the same inputs, or None to recompute the states.
+
+    Returns a dict as palimpsa_backward: dq, dk [H,total_T,d_k], dv, dbeta
+    [H,total_T,d_v], dd_t [H,total_T], dA, dI_prior [H] (summed over the
+    sequences), and dmu0 / dI0 [N,H,d_v,d_k] when want_state_grads. Rows of
+    tokens outside every sequence are zero."""
+    if q.device.type != "cuda":
+        raise ValueError("the packed backward takes device tensors")
+    H, total_T, d_k = q.shape
+    d_v = v.shape[-1]
+    dev = q.device
+    f32 = torch.float32
+    cu_d, N, max_seqlen = _packed_offsets(cu_seqlens, max_seqlen, dev)
+    _check(k, "k", q.shape, q.dtype, dev)
+    _check(q, "q", q.shape, None, dev)
+    _check(v, "v", (H, total_T, d_v), q.dtype, dev)
+    _check(beta, "beta", (H, total_T, d_v), q.dtype, dev)
+    _check(d_t, "d_t", (H, total_T), f32, dev)
+    _check(A, "A", (H,), f32, dev)
+    _check(I_prior, "I_prior", (H,), f32, dev)
+    for name, t in (("mu0", mu0), ("I0", I0), ("dmu_T", dmu_T), ("dI_T", dI_T)):
+        _check(t, name, (N, H, d_v, d_k), f32, dev)
+    _check(dy, "dy", (H, total_T, d_v), f32, dev)
+    _check(ckpt, "ckpt", packed_checkpoint_shape(N, H, total_T, d_k, d_v), f32, dev)
+    e = lambda *shape: torch.empty(shape, dtype=f32, device=dev)
+    z = lambda *shape: torch.zeros(shape, dtype=f32, device=dev)
+    # dq, dk, dd_t are zeroed by the library; dv, dbeta only where a sequence is
+    g = {"dq": e(H, total_T, d_k), "dk": e(H, total_T, d_k), "dv": z(H, total_T, d_v), "dbeta": z(H, total_T, d_v),
+         "dd_t": e(H, total_T), "dA": e(H), "dI_prior": e(H)}
+    if want_state_grads:
+        g["dmu0"] = e(N, H, d_v, d_k)
+        g["dI0"] = e(N, H, d_v, d_k)
+    lib = load_library()
+    with torch.cuda.device(dev):
+        rc = lib.palimpsa_backward_varlen(
+            _ptr(q), _ptr(k), _ptr(v), _ptr(beta), _ptr(d_t), _ptr(A), _ptr(I_prior), _ptr(mu0), _ptr(I0), _ptr(dy),
+            _ptr(dmu_T), _ptr(dI_T), _ptr(g["dq"]), _ptr(g["dk"]), _ptr(g["dv"]), _ptr(g["dbeta"]), _ptr(g["dd_t"]),
+            _ptr(g["dA"]), _ptr(g["dI_prior"]), _ptr(g.get("dmu0")), _ptr(g.get("dI0")), _ptr(ckpt), _ptr(cu_d),
+            N, H, total_T, max_seqlen, d_k, d_v, _in_dtype(q), ctypes.c_void_p(_stream_handle(stream)))
+    if rc != 0:
+        raise PalimpsaError(rc, "palimpsa_backward_varlen")
     return g
 
 

@@ -203,7 +203,7 @@ static palimpsa_status varlen_impl(const void* q, const void* k, const void* v, 
                                    const float* A, const float* I_prior, const float* mu0, const float* I0, float* y,
                                    float* mu_T, float* I_T, const int* cu_seqlens, int N, int H, int total_T,
                                    int max_seqlen, int d_k, int d_v, int chunk, palimpsa_dtype in_dtype,
-                                   void* cuda_stream, const Prologue& pro) {
+                                   void* cuda_stream, const Prologue& pro, float* ckpt = nullptr) {
   if (!A || !I_prior || !mu_T || !I_T || !cu_seqlens) return PALIMPSA_ERR_NULL;
   if (total_T != 0 && (!q || !k || !v || !beta || !d_t || !y)) return PALIMPSA_ERR_NULL;
   if (in_dtype != PALIMPSA_F32 && in_dtype != PALIMPSA_BF16) return PALIMPSA_ERR_DTYPE;
@@ -211,7 +211,7 @@ static palimpsa_status varlen_impl(const void* q, const void* k, const void* v, 
   if (!sizes_ok(N, H, max_seqlen, d_k, d_v) || !sizes_ok(1, H, total_T, d_k, d_v)) return PALIMPSA_ERR_SHAPE;
   if (!supported_dims(d_k, d_v)) return PALIMPSA_ERR_UNSUPPORTED;
   if (chunk != 0 && chunk != 16 && chunk != 32 && chunk != 64) return PALIMPSA_ERR_UNSUPPORTED;
-  const void* a16[] = {q, k, v, beta, y, mu_T, I_T, mu0, I0};
+  const void* a16[] = {q, k, v, beta, y, mu_T, I_T, mu0, I0, ckpt};
   for (const void* p : a16)
     if (p && !aligned(p, 16)) return PALIMPSA_ERR_ALIGN;
   const void* a4[] = {d_t, A, I_prior, cu_seqlens, pro.b_scale};
@@ -224,6 +224,7 @@ static palimpsa_status varlen_impl(const void* q, const void* k, const void* v, 
             g_wait_timeout_ns.load(), g_withhold_first_copy.load(), g_forward_segments.load(), pro};
   a.cu_seqlens = cu_seqlens;
   a.total_T = total_T;
+  a.ckpt = ckpt;
   StreamOrderedScratch scratch;
   if (launch_forward_chunked(a, static_cast<cudaStream_t>(cuda_stream), &scratch) != cudaSuccess)
     return PALIMPSA_ERR_CUDA;
@@ -248,6 +249,17 @@ palimpsa_status palimpsa_forward_varlen_fused(const void* q, const void* k, cons
   if (flags & ~kKnownFuseFlags) return PALIMPSA_ERR_UNSUPPORTED;
   return varlen_impl(q, k, v, beta_raw, d_raw, A, I_prior, mu0, I0, y, mu_T, I_T, cu_seqlens, N, H, total_T,
                      max_seqlen, d_k, d_v, chunk, in_dtype, cuda_stream, fused_prologue(b_scale, flags));
+}
+
+palimpsa_status palimpsa_forward_varlen_checkpointed(const void* q, const void* k, const void* v, const void* beta,
+                                                     const float* d_t, const float* A, const float* I_prior,
+                                                     const float* mu0, const float* I0, float* y, float* mu_T,
+                                                     float* I_T, float* ckpt, const int* cu_seqlens, int N, int H,
+                                                     int total_T, int max_seqlen, int d_k, int d_v, int chunk,
+                                                     palimpsa_dtype in_dtype, void* cuda_stream) {
+  if (!ckpt && max_seqlen != 0) return PALIMPSA_ERR_NULL;
+  return varlen_impl(q, k, v, beta, d_t, A, I_prior, mu0, I0, y, mu_T, I_T, cu_seqlens, N, H, total_T, max_seqlen,
+                     d_k, d_v, chunk, in_dtype, cuda_stream, Prologue{}, ckpt);
 }
 
 palimpsa_status palimpsa_segment_summary(const void* q, const void* k, const void* v, const void* beta,
@@ -355,26 +367,37 @@ palimpsa_status backward_impl(const void* q, const void* k, const void* v, const
                               const float* dy, const float* dmu_T, const float* dI_T, float* dq, float* dk,
                               float* dv, float* dbeta, float* dd_t, float* dA, float* dI_prior, float* dmu0,
                               float* dI0, const float* ckpt, int B, int H, int T, int d_k, int d_v,
-                              palimpsa_dtype in_dtype, void* cuda_stream) {
+                              palimpsa_dtype in_dtype, void* cuda_stream, const int* cu_seqlens = nullptr,
+                              int total_T = 0) {
+  // Dense layout: B sequences of T tokens each. Packed layout (cu_seqlens set):
+  // B sequences, at most T tokens each, total_T tokens in all.
+  const bool packed = cu_seqlens != nullptr;
+  const long long ntok = packed ? total_T : (long long)B * T;
   if (!A || !I_prior || !dA || !dI_prior) return PALIMPSA_ERR_NULL;
-  if (T != 0 && (!q || !k || !v || !beta || !d_t || !dy || !dq || !dk || !dv || !dbeta || !dd_t))
+  if (ntok != 0 && (!q || !k || !v || !beta || !d_t || !dy || !dq || !dk || !dv || !dbeta || !dd_t))
     return PALIMPSA_ERR_NULL;
   if (in_dtype != PALIMPSA_F32 && in_dtype != PALIMPSA_BF16) return PALIMPSA_ERR_DTYPE;
   if (!sizes_ok(B, H, T, d_k, d_v)) return PALIMPSA_ERR_SHAPE;
+  if (packed && (total_T < 0 || T > total_T || !sizes_ok(1, H, total_T, d_k, d_v))) return PALIMPSA_ERR_SHAPE;
   if (!supported_dims(d_k, d_v)) return PALIMPSA_ERR_UNSUPPORTED;
   const void* a16[] = {q, k, v, beta, mu0, I0, dy, dmu_T, dI_T, dq, dk, dv, dbeta, dmu0, dI0, ckpt};
   for (const void* p : a16)
     if (p && !aligned(p, 16)) return PALIMPSA_ERR_ALIGN;
-  const void* a4[] = {d_t, A, I_prior, dd_t, dA, dI_prior};
+  const void* a4[] = {d_t, A, I_prior, dd_t, dA, dI_prior, cu_seqlens};
   for (const void* p : a4)
     if (p && !aligned(p, 4)) return PALIMPSA_ERR_ALIGN;
   cudaStream_t s = static_cast<cudaStream_t>(cuda_stream);
   BwdArgs a{q, k, v, beta, d_t, A, I_prior, mu0, I0, dy, dmu_T, dI_T, dq, dk, dv, dbeta, dd_t, dA, dI_prior,
             dmu0, dI0, B, H, T, d_k, d_v, in_dtype == PALIMPSA_BF16};
   a.ckpt_in = ckpt;
-  const size_t tok = (size_t)B * H * T;
+  if (packed) {
+    a.cu_seqlens = cu_seqlens;
+    a.total_T = total_T;
+    if (palimpsa_status st = status_word(&a.status)) return st;
+  }
+  const size_t tok = packed ? (size_t)H * total_T : (size_t)B * H * T;
   // outputs that the kernel accumulates into start at zero
-  if (T != 0 && (cudaMemsetAsync(dq, 0, tok * d_k * sizeof(float), s) != cudaSuccess ||
+  if (tok != 0 && (cudaMemsetAsync(dq, 0, tok * d_k * sizeof(float), s) != cudaSuccess ||
                  cudaMemsetAsync(dk, 0, tok * d_k * sizeof(float), s) != cudaSuccess ||
                  cudaMemsetAsync(dd_t, 0, tok * sizeof(float), s) != cudaSuccess))
     return PALIMPSA_ERR_CUDA;
@@ -418,9 +441,27 @@ palimpsa_status palimpsa_backward_checkpointed(const void* q, const void* k, con
                        dI_prior, dmu0, dI0, ckpt, B, H, T, d_k, d_v, in_dtype, cuda_stream);
 }
 
+palimpsa_status palimpsa_backward_varlen(const void* q, const void* k, const void* v, const void* beta,
+                                         const float* d_t, const float* A, const float* I_prior, const float* mu0,
+                                         const float* I0, const float* dy, const float* dmu_T, const float* dI_T,
+                                         float* dq, float* dk, float* dv, float* dbeta, float* dd_t, float* dA,
+                                         float* dI_prior, float* dmu0, float* dI0, const float* ckpt,
+                                         const int* cu_seqlens, int N, int H, int total_T, int max_seqlen, int d_k,
+                                         int d_v, palimpsa_dtype in_dtype, void* cuda_stream) {
+  if (!cu_seqlens) return PALIMPSA_ERR_NULL;
+  return backward_impl(q, k, v, beta, d_t, A, I_prior, mu0, I0, dy, dmu_T, dI_T, dq, dk, dv, dbeta, dd_t, dA,
+                       dI_prior, dmu0, dI0, ckpt, N, H, max_seqlen, d_k, d_v, in_dtype, cuda_stream, cu_seqlens,
+                       total_T);
+}
+
 size_t palimpsa_checkpoint_bytes(int B, int H, int T, int d_k, int d_v) {
   if (B < 1 || H < 1 || T < 0 || d_k < 1 || d_v < 1) return 0;
   return checkpoint_floats((long long)B * H, T, d_k, d_v) * sizeof(float);
+}
+
+size_t palimpsa_checkpoint_bytes_varlen(int N, int H, int total_T, int d_k, int d_v) {
+  if (N < 1 || H < 1 || total_T < 0 || d_k < 1 || d_v < 1) return 0;
+  return (size_t)H * packed_checkpoint_slots(total_T, N) * d_v * 2 * d_k * sizeof(float);
 }
 
 palimpsa_status palimpsa_forward_checkpointed(const void* q, const void* k, const void* v, const void* beta,

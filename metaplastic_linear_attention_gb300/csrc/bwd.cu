@@ -261,7 +261,7 @@ __device__ __forceinline__ void init_adjoints(const BwdArgs& a, size_t soff, con
   }
 }
 
-template <int DK, bool BF16>
+template <int DK, bool BF16, bool PACKED>
 __global__ void __launch_bounds__(kThreads)
 palimpsa_bwd_kernel(BwdArgs a, float* __restrict__ ckpt) {
   constexpr int NC = DK / 32;       // key columns per lane
@@ -276,7 +276,7 @@ palimpsa_bwd_kernel(BwdArgs a, float* __restrict__ ckpt) {
   auto rowp = reinterpret_cast<float (*)[kWin][kRowsPerCta][3]>(bsm + L.rowp);
   const float* al = reinterpret_cast<const float*>(bsm + L.al);
 
-  const int DV = a.d_v, T = a.T;
+  const int DV = a.d_v;
   const int groups = DV / kRowsPerCta;
   const long bh = blockIdx.x / groups;
   const int row0 = (blockIdx.x % groups) * kRowsPerCta;
@@ -285,12 +285,27 @@ palimpsa_bwd_kernel(BwdArgs a, float* __restrict__ ckpt) {
   const int rl = lane >> 2;                 // this lane's row within the CTA
   const int i = row0 + rl;                  // ... and within the head
   const int c0 = w * CW + (lane & 3) * NC;  // this lane's first key column
-  const size_t head_tok = (size_t)bh * T;
+  // this head's sequence: all T tokens, or a packed sequence's own range,
+  // checked before anything is read (a bad one is reported and skipped)
+  int T = a.T;
+  size_t head_tok = (size_t)bh * a.T;
+  // checkpoints [slot][value row][M | I], from the forward or written by phase 1
+  long long ck_slot0 = bh * (long long)((a.T + kSeg - 1) / kSeg);
+  if constexpr (PACKED) {
+    const long n = bh / a.H;
+    const int s0 = a.cu_seqlens[n], s1 = a.cu_seqlens[n + 1];
+    if (!(s0 >= 0 && s1 >= s0 && (long long)s1 <= a.total_T && s1 - s0 <= a.T)) {
+      if (threadIdx.x == 0 && a.status) latch_status(a.status, kStatusDomain);
+      return;
+    }
+    T = s1 - s0;
+    head_tok = (size_t)h * (size_t)a.total_T + (size_t)s0;
+    ck_slot0 = packed_checkpoint_slot0(h, n, s0, a.total_T, a.B);
+  }
   const float A_h = a.A[h], Ip = a.I_prior[h];
   const int nseg = (T + kSeg - 1) / kSeg;
   static_assert(kSeg == kCheckpointTokens, "backward segments are the training checkpoints");
-  // checkpoints [head][segment][value row][M | I]: from the forward, or written by phase 1
-  const size_t ck_head = (size_t)bh * nseg * DV * 2 * DK;
+  const size_t ck_head = (size_t)ck_slot0 * DV * 2 * DK;
   float* ck_out = ckpt ? ckpt + ck_head : nullptr;  // null when the forward's checkpoints are used
   const float* ck_in = (a.ckpt_in ? a.ckpt_in : ckpt) + ck_head;
 
@@ -512,23 +527,31 @@ palimpsa_bwd_kernel(BwdArgs a, float* __restrict__ ckpt) {
 
 size_t backward_scratch_bytes(const BwdArgs& a) {
   if (a.ckpt_in) return 0;  // the forward's checkpoints replace phase 1
+  if (a.cu_seqlens)
+    return (size_t)a.H * packed_checkpoint_slots(a.total_T, a.B) * a.d_v * 2 * a.d_k * sizeof(float);
   return checkpoint_floats((long long)a.B * a.H, a.T, a.d_k, a.d_v) * sizeof(float);
 }
 
-template <int DK, bool BF16>
+template <int DK, bool BF16, bool PACKED>
 cudaError_t launch_t(const BwdArgs& a, float* scratch, cudaStream_t s) {
   const unsigned ctas = (unsigned)((long)a.B * a.H * (a.d_v / kRowsPerCta));
   const size_t smem = BwdSmem(DK, BF16 ? 2 : 4).total;
-  auto kern = palimpsa_bwd_kernel<DK, BF16>;
+  auto kern = palimpsa_bwd_kernel<DK, BF16, PACKED>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   kern<<<ctas, kThreads, smem, s>>>(a, scratch);
   return cudaGetLastError();
 }
 
+template <bool PACKED>
+cudaError_t launch_layout(const BwdArgs& a, float* scratch, cudaStream_t s) {
+  if (a.d_k == 128)
+    return a.bf16 ? launch_t<128, true, PACKED>(a, scratch, s) : launch_t<128, false, PACKED>(a, scratch, s);
+  return a.bf16 ? launch_t<64, true, PACKED>(a, scratch, s) : launch_t<64, false, PACKED>(a, scratch, s);
+}
+
 cudaError_t launch_backward(const BwdArgs& a, float* scratch, cudaStream_t s) {
-  if (a.d_k == 128) return a.bf16 ? launch_t<128, true>(a, scratch, s) : launch_t<128, false>(a, scratch, s);
-  return a.bf16 ? launch_t<64, true>(a, scratch, s) : launch_t<64, false>(a, scratch, s);
+  return a.cu_seqlens ? launch_layout<true>(a, scratch, s) : launch_layout<false>(a, scratch, s);
 }
 
 }  // namespace palimpsa

@@ -134,8 +134,14 @@ palimpsa_fwd_chunked_kernel(FwdArgs a, int C, int nseg, int seg_len, const float
   float* gy = a.y + (head_tok + tl.tb) * DV + tl.row0 + lr0;
   const float* gd = a.d_t + head_tok + tl.tb;
   // training checkpoints: the state before every 32nd token of the sequence
-  float* ckh = a.ckpt ? a.ckpt + (size_t)tl.bh * ((a.T + kCheckpointTokens - 1) / kCheckpointTokens) * DV * 2 * DK
-                      : nullptr;
+  float* ckh = nullptr;
+  if (a.ckpt) {
+    const long long slot0 =
+        a.cu_seqlens ? packed_checkpoint_slot0(tl.h, tl.bh / a.H, (long long)(tl.head_tok - (size_t)tl.h * a.total_T),
+                                               a.total_T, a.B)
+                     : tl.bh * (long long)((a.T + kCheckpointTokens - 1) / kCheckpointTokens);
+    ckh = a.ckpt + (size_t)slot0 * DV * 2 * DK;
+  }
   for (int c = 0; c < pipe.nch; ++c) {
     const int t0 = pipe.t0_of(c), tc = pipe.tc_of(c);
     if (ckh && (tl.tb + t0) % kCheckpointTokens == 0) {

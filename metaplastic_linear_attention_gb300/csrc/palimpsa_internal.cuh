@@ -97,6 +97,11 @@ struct BwdArgs {
   // Training checkpoints written by the forward (layout of kCheckpointTokens
   // below), or null: the backward then recomputes them with a forward sweep.
   const float* ckpt_in = nullptr;
+  // Packed variable-length batch, as in FwdArgs (B counts sequences, T is the
+  // longest); null for the dense layout.
+  const int* cu_seqlens = nullptr;
+  long long total_T = 0;
+  unsigned int* status = nullptr;  // device status word (bad packed offsets)
 };
 
 // Training checkpoints: the state (M, I) of every head before tokens 0, 32,
@@ -106,6 +111,20 @@ constexpr int kCheckpointTokens = 32;
 inline size_t checkpoint_floats(long long heads, long long T, int d_k, int d_v) {
   const long long n = (T + kCheckpointTokens - 1) / kCheckpointTokens;
   return (size_t)heads * n * d_v * 2 * d_k;
+}
+// Packed batches keep their checkpoints without padding to the longest
+// sequence: per head, total_T / 32 + N slots, and head h of the sequence that
+// starts at token s0 (the n-th) owns the slots from
+//   h (total_T / 32 + N) + s0 / 32 + n.
+// A sequence of L tokens needs ceil(L / 32) slots, and the next one starts
+// floor((s0 + L) / 32) + 1 >= floor(s0 / 32) + ceil(L / 32) slots on, so
+// sequences never share a slot.
+__host__ __device__ inline long long packed_checkpoint_slots(long long total_T, long long N) {
+  return total_T / kCheckpointTokens + N;
+}
+__host__ __device__ inline long long packed_checkpoint_slot0(int h, long long n, long long s0, long long total_T,
+                                                             long long N) {
+  return (long long)h * packed_checkpoint_slots(total_T, N) + s0 / kCheckpointTokens + n;
 }
 
 // Source of temporary device memory for a launch that needs scratch (the time

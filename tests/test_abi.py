@@ -321,3 +321,72 @@ def test_forward_varlen_fused_rejects_bad_arguments(lib, over, code):
         a["q"], a["k"], a["v"], a["b"], a["d"], a["A"], a["I_prior"], a["b_scale"], a["mu0"], a["I0"], a["y"],
         a["mu_T"], a["I_T"], a["cu"], a["N"], a["H"], a["total_T"], a["max_seqlen"], a["d_k"], a["d_v"], a["chunk"],
         a["flags"], a["dtype"], None) == code
+
+
+def _bwd_varlen(lib, **over):
+    a = dict(q=P, k=P, v=P, beta=P, d=P, A=P, I_prior=P, mu0=None, I0=None, dy=P, dmu=None, dI=None, dq=P, dk=P, dv=P,
+             db=P, dd=P, dA=P, dIp=P, dmu0=None, dI0=None, ck=None, cu=P, N=3, H=2, total_T=100, max_seqlen=50,
+             d_k=128, d_v=64, dtype=1)
+    a.update(over)
+    return lib.palimpsa_backward_varlen(
+        a["q"], a["k"], a["v"], a["beta"], a["d"], a["A"], a["I_prior"], a["mu0"], a["I0"], a["dy"], a["dmu"], a["dI"],
+        a["dq"], a["dk"], a["dv"], a["db"], a["dd"], a["dA"], a["dIp"], a["dmu0"], a["dI0"], a["ck"], a["cu"], a["N"],
+        a["H"], a["total_T"], a["max_seqlen"], a["d_k"], a["d_v"], a["dtype"], None)
+
+
+@pytest.mark.parametrize("over,code", [
+    (dict(cu=None), ERR_NULL), (dict(dy=None), ERR_NULL), (dict(dA=None), ERR_NULL), (dict(cu=P + 2), ERR_ALIGN),
+    (dict(ck=P + 4), ERR_ALIGN), (dict(dq=P + 8), ERR_ALIGN), (dict(N=0), ERR_SHAPE), (dict(total_T=-1), ERR_SHAPE),
+    (dict(max_seqlen=101), ERR_SHAPE), (dict(max_seqlen=-1), ERR_SHAPE), (dict(dtype=4), ERR_DTYPE),
+    (dict(d_k=32), ERR_UNSUPPORTED),
+])
+def test_backward_varlen_rejects_bad_arguments(lib, over, code):
+    assert _bwd_varlen(lib, **over) == code
+
+
+def test_backward_varlen_empty_tokens_need_no_token_arrays(lib):
+    # total_T = 0: the token arrays may be NULL; the per-head gradients may not
+    assert _bwd_varlen(lib, total_T=0, max_seqlen=0, q=None, k=None, v=None, beta=None, d=None, dy=None, dq=None,
+                       dk=None, dv=None, db=None, dd=None, dA=None) == ERR_NULL
+
+
+@pytest.mark.parametrize("over,code", [(dict(ck=None), ERR_NULL), (dict(ck=P + 4), ERR_ALIGN),
+                                       (dict(cu=None), ERR_NULL), (dict(max_seqlen=101), ERR_SHAPE)])
+def test_forward_varlen_checkpointed_rejects_bad_arguments(lib, over, code):
+    a = dict(q=P, k=P, v=P, beta=P, d=P, A=P, I_prior=P, mu0=None, I0=None, y=P, mu_T=P, I_T=P, ck=P, cu=P, N=3, H=2,
+             total_T=100, max_seqlen=50, d_k=128, d_v=64, chunk=0, dtype=1)
+    a.update(over)
+    assert lib.palimpsa_forward_varlen_checkpointed(
+        a["q"], a["k"], a["v"], a["beta"], a["d"], a["A"], a["I_prior"], a["mu0"], a["I0"], a["y"], a["mu_T"],
+        a["I_T"], a["ck"], a["cu"], a["N"], a["H"], a["total_T"], a["max_seqlen"], a["d_k"], a["d_v"], a["chunk"],
+        a["dtype"], None) == code
+
+
+def test_checkpoint_bytes_varlen_formula(lib):
+    # per head total_T // 32 + N slots of d_v x 2 x d_k floats: proportional to the
+    # tokens, whatever the longest sequence
+    lib.palimpsa_checkpoint_bytes_varlen.restype = ctypes.c_size_t
+    assert lib.palimpsa_checkpoint_bytes_varlen(5, 16, 2048, 128, 64) == 16 * (64 + 5) * 64 * 2 * 128 * 4
+    assert lib.palimpsa_checkpoint_bytes_varlen(3, 2, 31, 64, 8) == 2 * (0 + 3) * 8 * 2 * 64 * 4
+    assert lib.palimpsa_checkpoint_bytes_varlen(0, 2, 31, 64, 8) == 0
+    assert lib.palimpsa_checkpoint_bytes_varlen(2, 1, -1, 128, 64) == 0
+
+
+def test_packed_checkpoint_slots_never_overlap():
+    """The slot rule for packed checkpoints (sequence n from token s0 owns slots
+    s0 // 32 + n onwards, ceil(L / 32) of them): no two sequences share a slot and
+    every slot lies inside total_T // 32 + N, over many random length mixes."""
+    import random
+    rnd = random.Random(5)
+    for _ in range(2000):
+        N = rnd.randint(1, 12)
+        lengths = [rnd.choice([0, 1, 31, 32, 33, 63, 64, 65, rnd.randint(0, 300)]) for _ in range(N)]
+        gap = rnd.randint(0, 40)
+        total = sum(lengths) + gap
+        used = set()
+        s0 = 0
+        for n, L in enumerate(lengths):
+            slots = {s0 // 32 + n + c for c in range(-(-L // 32))}
+            assert not (slots & used) and all(0 <= x < total // 32 + N for x in slots), (lengths, n)
+            used |= slots
+            s0 += L

@@ -82,3 +82,58 @@ def test_empty_sequences_and_unused_tokens():
     np.testing.assert_array_equal(y3[:, cu[1]:cu[2]], y[:, cu[1]:cu[2]])
     np.testing.assert_array_equal(mu3[1], muT[1])
     assert not np.allclose(mu3[3], muT[3])
+
+
+def _packed_loss(x, cu, dy, dmu, dI):
+    y, muT, IT = ovl.forward(x["q"], x["k"], x["v"], x["beta"], x["d_t"], x["A"], x["I_prior"], cu,
+                             mu0=x["mu0"], I0=x["I0"])
+    return float((y * dy).sum() + (muT * dmu).sum() + (IT * dI).sum())
+
+
+def test_packed_gradients_equal_finite_differences_of_the_packed_forward():
+    """Every input's gradient from ovl.gradients (per-sequence autograd, A and
+    I_prior summed) against central differences of the packed C-oracle forward:
+    a wrong offset, a state gradient filed under another sequence, or a dropped
+    sum over sequences fails here. Includes an empty sequence and unused tokens."""
+    rng = np.random.default_rng(11)
+    H, lengths, dk, dv = 2, [3, 0, 4], 4, 3
+    q, k, v, beta, d_t, A, Ip, cu = _packed(rng, H, lengths, dk, dv, gap=2)
+    N = len(lengths)
+    x = dict(q=q, k=k, v=v, beta=beta, d_t=d_t, A=A, I_prior=Ip,
+             mu0=rng.standard_normal((N, H, dv, dk)), I0=rng.uniform(0.5, 2.0, (N, H, dv, dk)))
+    dy = rng.standard_normal(v.shape)
+    dmu = rng.standard_normal((N, H, dv, dk))
+    dI = rng.standard_normal((N, H, dv, dk))
+    g = ovl.gradients(x, cu, dy, dmu, dI)
+    eps = 1e-6
+    for name in ("q", "k", "v", "beta", "d_t", "A", "I_prior", "mu0", "I0"):
+        fd = np.zeros_like(x[name])
+        for idx in np.ndindex(x[name].shape):
+            keep = x[name][idx]
+            x[name][idx] = keep + eps
+            lp = _packed_loss(x, cu, dy, dmu, dI)
+            x[name][idx] = keep - eps
+            lm = _packed_loss(x, cu, dy, dmu, dI)
+            x[name][idx] = keep
+            fd[idx] = (lp - lm) / (2 * eps)
+        np.testing.assert_allclose(g[name], fd, rtol=1e-6, atol=1e-7, err_msg=name)
+
+
+def test_packed_gradients_of_empty_sequences_and_unused_tokens():
+    """An empty sequence hands its state through unchanged, so its initial-state
+    gradients are the final-state ones exactly; tokens outside every sequence
+    get zero gradients."""
+    rng = np.random.default_rng(12)
+    H, lengths, dk, dv = 2, [0, 5, 0], 4, 3
+    q, k, v, beta, d_t, A, Ip, cu = _packed(rng, H, lengths, dk, dv, gap=3)
+    N = len(lengths)
+    x = dict(q=q, k=k, v=v, beta=beta, d_t=d_t, A=A, I_prior=Ip,
+             mu0=rng.standard_normal((N, H, dv, dk)), I0=rng.uniform(0.5, 2.0, (N, H, dv, dk)))
+    dmu = rng.standard_normal((N, H, dv, dk))
+    dI = rng.standard_normal((N, H, dv, dk))
+    g = ovl.gradients(x, cu, rng.standard_normal(v.shape), dmu, dI)
+    for n in (0, 2):
+        np.testing.assert_array_equal(g["mu0"][n], dmu[n])
+        np.testing.assert_array_equal(g["I0"][n], dI[n])
+    for name in ("q", "k", "v", "beta", "d_t"):
+        assert not g[name][:, 5:].any(), name

@@ -149,3 +149,143 @@ def test_varlen_fused_matches_oracle(flags, S):
         pal.palimpsa_set_forward_segments(0)
     assert pal.palimpsa_get_device_status() == 0
     _check(out, ref)
+
+
+# ---------------------------------------------------------------- packed training pair
+
+GRAD_PAIRS = [("dq", "q"), ("dk", "k"), ("dv", "v"), ("dbeta", "beta"), ("dd_t", "d_t"), ("dA", "A"),
+              ("dI_prior", "I_prior")]
+
+
+def _bwd_inputs(lengths, H, dk, dv, bf16, with_state, with_final, seed):
+    inp = _inputs(lengths, H, dk, dv, bf16, seed)
+    N, total = len(lengths), inp["q"].shape[1]
+    g = torch.Generator().manual_seed(seed + 1)
+    mu0 = torch.randn((N, H, dv, dk), generator=g) if with_state else None
+    I0 = (0.5 + 2.0 * torch.rand((N, H, dv, dk), generator=g)) if with_state else None
+    dy = torch.randn((H, total, dv), generator=g)
+    dmu = torch.randn((N, H, dv, dk), generator=g) if with_final else None
+    dI = torch.randn((N, H, dv, dk), generator=g) if with_final else None
+    return inp, mu0, I0, dy, dmu, dI
+
+
+def _bwd_oracle(inp, mu0, I0, dy, dmu, dI):
+    f = lambda t: None if t is None else f64(t)
+    x = {n: f64(inp[n]) for n in ("q", "k", "v", "beta", "d_t", "A", "I_prior")}
+    x.update(mu0=f(mu0), I0=f(I0))
+    return ovl.gradients(x, inp["cu_seqlens"].tolist(), f64(dy), f(dmu), f(dI))
+
+
+def _bwd_gpu(inp, mu0, I0, dy, dmu, dI, checkpointed):
+    d = lambda t: None if t is None else t.to(DEV)
+    g = {n: t.to(DEV) for n, t in inp.items()}
+    ck = None
+    if checkpointed:
+        _, _, _, ck = pal.palimpsa_forward_varlen_checkpointed(g["q"], g["k"], g["v"], g["beta"], g["d_t"], g["A"],
+                                                               g["I_prior"], g["cu_seqlens"], d(mu0), d(I0))
+    out = pal.palimpsa_backward_varlen(g["q"], g["k"], g["v"], g["beta"], g["d_t"], g["A"], g["I_prior"],
+                                       g["cu_seqlens"], d(mu0), d(I0), d(dy), d(dmu), d(dI), ckpt=ck)
+    assert pal.palimpsa_get_device_status() == 0
+    return out
+
+
+BWD_CASES = [
+    # (lengths, H, d_k, d_v, bf16, with_state, with_final, checkpointed)
+    ([1], 2, 128, 64, True, False, False, False),
+    ([5, 0, 17, 1, 64], 3, 128, 64, True, True, True, False),
+    ([5, 0, 17, 1, 64], 3, 128, 64, True, True, True, True),
+    ([130, 7, 0, 0, 61], 2, 64, 40, False, False, True, True),
+    ([33, 96, 2], 1, 64, 128, False, True, False, False),
+    ([200, 31, 32, 33], 2, 128, 256, True, True, True, True),
+]
+
+
+@pytest.mark.parametrize("lengths,H,dk,dv,bf16,with_state,with_final,ckpt", BWD_CASES)
+def test_varlen_backward_matches_fp64_autograd(lengths, H, dk, dv, bf16, with_state, with_final, ckpt):
+    """Gradients through the packed forward: each sequence's own gradients, dA and
+    dI_prior summed over sequences, zero rows outside every sequence."""
+    case = _bwd_inputs(lengths, H, dk, dv, bf16, with_state, with_final, seed=7000 + sum(lengths) + dv)
+    ref = _bwd_oracle(*case)
+    out = _bwd_gpu(*case, checkpointed=ckpt)
+    pairs = GRAD_PAIRS + ([("dmu0", "mu0"), ("dI0", "I0")] if with_state else [])
+    errs = {n: rel_l2(out[n].cpu().numpy(), ref[m]) for n, m in pairs}
+    assert max(errs.values()) <= TIGHT, errs
+
+
+def test_varlen_backward_with_and_without_checkpoints_agree():
+    case = _bwd_inputs([300, 45, 1, 199], 2, 128, 64, True, True, True, seed=7101)
+    a = _bwd_gpu(*case, checkpointed=False)
+    b = _bwd_gpu(*case, checkpointed=True)
+    same = {n: rel_l2(a[n].cpu().numpy(), b[n].cpu().numpy()) for n in a}
+    assert max(same.values()) <= 1e-5, same
+
+
+def test_varlen_backward_equal_lengths_equal_the_dense_backward():
+    """N equal sequences: the packed kernel does the dense kernel's arithmetic. The
+    outputs written without atomics are bit-identical; the atomically summed ones
+    (dq, dk, dd_t, dA, dI_prior) agree to rounding order."""
+    N, H, T, dk, dv = 3, 2, 150, 128, 64
+    inp, mu0, I0, dy, dmu, dI = _bwd_inputs([T] * N, H, dk, dv, True, True, True, seed=7202)
+    packed = _bwd_gpu(inp, mu0, I0, dy, dmu, dI, checkpointed=False)
+    dense = lambda x: x.reshape((H, N, T) + x.shape[2:]).transpose(0, 1).contiguous()
+    g = {n: dense(inp[n]).to(DEV) for n in ("q", "k", "v", "beta", "d_t")}
+    ref = pal.palimpsa_backward(g["q"], g["k"], g["v"], g["beta"], g["d_t"], inp["A"].to(DEV), inp["I_prior"].to(DEV),
+                                mu0.to(DEV), I0.to(DEV), dense(dy).to(DEV), dmu.to(DEV), dI.to(DEV))
+    for n in ("dv", "dbeta"):
+        assert torch.equal(dense(packed[n].cpu()), ref[n].cpu()), n
+    for n in ("dmu0", "dI0"):
+        assert torch.equal(packed[n], ref[n]), n
+    for n in ("dq", "dk", "dd_t"):
+        assert rel_l2(dense(packed[n].cpu()).numpy(), ref[n].cpu().numpy()) <= 1e-6, n
+    for n in ("dA", "dI_prior"):
+        assert rel_l2(packed[n].cpu().numpy(), ref[n].cpu().numpy()) <= 1e-6, n
+
+
+def test_varlen_backward_bad_offsets_are_reported_not_faulted():
+    """Offsets that break the rules: that sequence's CTAs touch nothing, the call
+    latches a domain error, the other sequences' gradients are still right."""
+    lengths = [20, 30, 10]
+    inp, mu0, I0, dy, dmu, dI = _bwd_inputs(lengths, 2, 128, 64, True, True, True, seed=7303)
+    ref = _bwd_oracle(inp, mu0, I0, dy, dmu, dI)
+    g = {n: t.to(DEV) for n, t in inp.items()}
+    d = lambda t: t.to(DEV)
+    for cu in ([0, 20, 15, 60], [0, 20, 50, 60 + 40], [0, 20, 50, 60]):
+        cu_d = torch.tensor(cu, dtype=torch.int32, device=DEV)
+        out = pal.palimpsa_backward_varlen(g["q"], g["k"], g["v"], g["beta"], g["d_t"], g["A"], g["I_prior"], cu_d,
+                                           d(mu0), d(I0), d(dy), d(dmu), d(dI), max_seqlen=25)
+        assert pal.palimpsa_get_device_status() == 5  # PALIMPSA_ERR_DOMAIN
+        for n, m in (("dq", "q"), ("dv", "v"), ("dd_t", "d_t")):
+            assert rel_l2(out[n][:, :20].cpu().numpy(), ref[m][:, :20]) <= TIGHT, n
+        assert rel_l2(out["dmu0"][0].cpu().numpy(), ref["mu0"][0]) <= TIGHT
+    out = _bwd_gpu(inp, mu0, I0, dy, dmu, dI, checkpointed=False)
+    errs = {n: rel_l2(out[n].cpu().numpy(), ref[m]) for n, m in GRAD_PAIRS}
+    assert max(errs.values()) <= TIGHT, errs
+
+
+def test_varlen_checkpoints_are_each_sequences_states():
+    """Checkpoint c of sequence n (from token s0) sits in slot s0 // 32 + n + c
+    of each head and holds its state before its token 32 c, as (M = I mu, I)
+    per value row, from the forward split into segments or not."""
+    lengths = [70, 0, 33, 5]
+    inp = _inputs(lengths, 2, 128, 64, True, seed=7404)
+    cu = inp["cu_seqlens"].tolist()
+    g = {n: t.to(DEV) for n, t in inp.items()}
+    for S in (0, 2):
+        pal.palimpsa_set_forward_segments(S)
+        try:
+            _, _, _, ck = pal.palimpsa_forward_varlen_checkpointed(g["q"], g["k"], g["v"], g["beta"], g["d_t"],
+                                                                   g["A"], g["I_prior"], g["cu_seqlens"])
+        finally:
+            pal.palimpsa_set_forward_segments(0)
+        assert pal.palimpsa_get_device_status() == 0
+        ck = ck.cpu().numpy()
+        for n, L in enumerate(lengths):
+            for c in range(-(-L // 32)):
+                t = 32 * c
+                sub = {m: inp[m][:, cu[n]:cu[n] + t] for m in ("q", "k", "v", "beta", "d_t")}
+                sub["cu_seqlens"] = torch.tensor([0, t], dtype=torch.int32)
+                sub.update(A=inp["A"], I_prior=inp["I_prior"])
+                _, mu_r, I_r = _oracle(sub)
+                slot = cu[n] // 32 + n + c
+                assert rel_l2(ck[:, slot, :, 0, :], mu_r[0] * I_r[0]) <= TIGHT, (n, c)
+                assert rel_l2(ck[:, slot, :, 1, :], I_r[0]) <= TIGHT, (n, c)
