@@ -15,36 +15,45 @@
 //             gI_t = alpha_{t+1} gI_{t+1} - dy_i q_j mu_t r_t
 //   grads     dq_j   += sum_i dy_i mu_t                dk_j += sum_i gM bv_i + 2 gI beta_i k_j
 //             d(bv)_i = sum_j gM k_j  -> dv_i = d(bv)_i beta_i,  dbeta_i = d(bv)_i v_i + sum_j gI k_j^2
-//             dalpha_t = sum_ij gM_t M_{t-1} + gI_t (I_{t-1} - I_prior)
-//             dd_t = -A alpha_t dalpha_t,  dA += -d_t alpha_t dalpha_t,  dI_prior += (1 - alpha_t) sum_ij gI_t
+//             dalpha_t = sum_ij gM_t M_{t-1} + gI_t (I_{t-1} - I_prior), taken as
+//             alpha_t dalpha_t = sum_ij gM_t (M_t - bv_i k_j) + gI_t (I_t - I_prior - beta_i k_j^2)
+//               = sum_ij (gM_t M_t + gI_t I_t) - sum_i (bv_i d(bv)_i + beta_i sum_j gI k_j^2) - I_prior sum_ij gI_t,
+//             which needs only the state after token t and sums the kernel forms anyway;
+//             dd_t = -A (alpha_t dalpha_t),  dA += -d_t (alpha_t dalpha_t),  dI_prior += (1 - alpha_t) sum_ij gI_t
 //   start     (t = T) gM = dmu_T r_T, gI = dI_T - dmu_T mu_T r_T;  (t = 0) dmu0 = gM_0 I0, dI0 = gI_0 + gM_0 mu0.
 //
 // Numerics: the state is never stepped backwards (I_{t-1} = (I_t - c_t) /
 // alpha_t cancels badly when alpha is small). A forward sweep stores a
-// checkpoint every 32 tokens; each 32-token segment is re-run forward to keep
-// its 8-token window starts in shared memory; each window is re-run forward
-// into registers and then swept backwards. Every state used is thus computed
-// in the forward direction, exactly as the forward kernel computes it.
+// checkpoint every 32 tokens (or the forward wrote them); each 32-token
+// segment is re-run forward to keep its 8-token window starts in shared
+// memory; each window is re-run forward into registers and then swept
+// backwards. Every state used is computed in the forward direction, exactly as
+// the forward kernel computes it.
 //
-// Layout: one CTA per (head, 8 value rows), one warp per row, a lane owns
-// d_k / 32 consecutive key columns. Sums over columns are warp shuffles; sums
-// over rows (dq, dk, dalpha) go through shared memory and then, across the
-// d_v / 8 CTAs of a head, into fp32 atomics on outputs the library zeroes first.
+// Layout: one CTA of 4 warps per (head, 8 value rows). A lane owns two value
+// rows (lane bits 4, 3 pick the row pair) and d_k / 32 consecutive key columns
+// (lane bits 2..0 and the warp pick them), so the per-token loads, the column
+// sums over rows and the row sums over columns are shared by twice the
+// elements of a one-row lane. Column sums (dq, dk) finish over the four row
+// pairs of a warp with a reduce-scatter and go to fp32 atomics (the d_v / 8
+// CTAs of a head add into the same dq, dk; the library zeroes them first). Row
+// sums (d(bv), sum gI k^2) and the alpha partial finish over the 8 column
+// lanes with shuffles and over the 4 warps through shared memory once per
+// 8-token window.
 //
 // Staging: every operand a segment needs (q, k and the CTA's 8 rows of v, beta,
 // dy, plus d_t) is copied into shared memory once per CTA with cp.async, into
 // a double buffer: the next segment's copies are in flight while the current
 // one computes (forwards in the first sweep, backwards in the second; the
 // last segment staged by the first sweep is reused by the second). The token
-// loops then read only shared memory: k and q as one 8- or 16-byte vector per
-// lane, the row and gate scalars as broadcasts.
+// loops then read only shared memory.
 #include "palimpsa_internal.cuh"
 
 namespace palimpsa {
 namespace {
 
-constexpr int kRowsPerCta = 8;     // one warp per value row
-constexpr int kWarps = 8;
+constexpr int kRowsPerCta = 8;     // value rows per CTA: 4 row pairs
+constexpr int kWarps = 4;          // warps split the key columns
 constexpr int kThreads = kWarps * 32;
 constexpr int kSeg = 32;           // checkpoint spacing and staging unit (tokens)
 constexpr int kWin = 8;            // window re-run into registers (tokens)
@@ -55,7 +64,7 @@ __host__ __device__ constexpr size_t al16(size_t x) { return (x + 15) / 16 * 16;
 // Shared-memory carve-up (byte offsets; every piece 16-byte aligned).
 struct BwdSmem {
   size_t k, q, v, b, dy, dt, stage;   // one staged segment (offsets inside a stage)
-  size_t kf, qf, win, rowp, rb, rbv, al, om, oma, total;
+  size_t kf, qf, win, rowp, adap, rb, rbv, al, om, oma, total;
 
   __host__ __device__ BwdSmem(int DK, int ES) {
     size_t o = 0;
@@ -70,8 +79,9 @@ struct BwdSmem {
     // fp32 copies of the current segment's k and q (bf16 inputs; fp32 inputs are read in place)
     kf = o;    o += ES == 2 ? (size_t)kSeg * DK * 4 : 0;
     qf = o;    o += ES == 2 ? (size_t)kSeg * DK * 4 : 0;
-    win = o;   o += (size_t)2 * kRowsPerCta * kNW * DK * 4;   // window starts [M | I][window][pair][thread]
-    rowp = o;  o += (size_t)kWarps * kWin * kRowsPerCta * 3 * 4;  // row-sum partials [warp][token][row][3]
+    win = o;   o += (size_t)2 * kRowsPerCta * kNW * DK * 4;   // window starts [window][M | I][row][pair][thread]
+    rowp = o;  o += (size_t)kWarps * kWin * kRowsPerCta * 2 * 4;  // row-sum partials [warp][token][row][2]
+    adap = o;  o += (size_t)kWarps * kWin * 4 * 4;            // alpha-gradient partials [warp][token][row pair]
     rb = o;    o += (size_t)kSeg * kRowsPerCta * 4;           // beta_i of the segment's tokens [token][row]
     rbv = o;   o += (size_t)kSeg * kRowsPerCta * 4;           // beta_i v_i
     al = o;    o += (size_t)kSeg * 4;                         // alpha of the segment's tokens
@@ -138,33 +148,21 @@ __device__ __forceinline__ float warp_sum(float x) {
 
 __device__ __forceinline__ float2 f2(float x) { return make_float2(x, x); }
 
-// Reduce-scatter of V = 2 NC column partials over the 8 lanes that share this
-// lane's columns (lane bits 4, 3, 2, i.e. the 8 rows): each level halves the
-// values a lane keeps and adds its partner's half. Returns the lane's finished
-// value; its index is (lane >> 2) & 7 for V = 8 and (lane >> 3) & 3 for V = 4
-// (the last level then only completes the sum, on both partners).
-template <int V>
-__device__ __forceinline__ float reduce_scatter_rows(float (&x)[V], int lane) {
-  int n = V;
+// One level of a reduce-scatter over the two lanes that differ in lane bit
+// `m`: of its first N partials a lane keeps the half its side owns (bit set:
+// the upper half) and adds the partner's copy of that half. After the levels
+// for bits 16 and 8 (in that order) a lane of row pair g holds partials
+// g * V / 4 .. g * V / 4 + V / 4 - 1 of the original V, summed over the warp's
+// four row pairs.
+template <int V, int N>
+__device__ __forceinline__ void rs_level(float (&x)[V], int lane, int m) {
+  const bool hi = (lane & m) != 0;
 #pragma unroll
-  for (int m = 16; m >= 4; m >>= 1) {
-    const bool hi = (lane & m) != 0;
-    if (n >= 2) {
-      const int half = n / 2;
-#pragma unroll
-      for (int v = 0; v < V / 2; ++v) {
-        if (v < half) {
-          const float send = hi ? x[v] : x[v + half];
-          const float keep = hi ? x[v + half] : x[v];
-          x[v] = keep + __shfl_xor_sync(0xffffffffu, send, m);
-        }
-      }
-      n = half;
-    } else {
-      x[0] += __shfl_xor_sync(0xffffffffu, x[0], m);
-    }
+  for (int v = 0; v < N / 2; ++v) {
+    const float send = hi ? x[v] : x[v + N / 2];
+    const float keep = hi ? x[v + N / 2] : x[v];
+    x[v] = keep + __shfl_xor_sync(0xffffffffu, send, m);
   }
-  return x[0];
 }
 
 // All threads, once per staged segment: the gate tables (alpha, (1 - alpha)
@@ -206,11 +204,11 @@ __device__ __forceinline__ void prepare_segment(const unsigned char* st, unsigne
   }
 }
 
-// This lane's NC key columns of token u of the fp32 k or q, as NC / 2 pairs.
-template <int NC>
-__device__ __forceinline__ void f32_pairs(const float* base, int DK, int u, int c0, float2 (&x)[NC / 2]) {
+// This lane's 2 NP key columns of token u of the fp32 k or q, as NP pairs.
+template <int NP>
+__device__ __forceinline__ void lane_pairs(const float* base, int DK, int u, int c0, float2 (&x)[NP]) {
   const float* p = base + (size_t)u * DK + c0;
-  if constexpr (NC == 4) {
+  if constexpr (NP == 2) {
     const float4 w = *reinterpret_cast<const float4*>(p);
     x[0] = make_float2(w.x, w.y);
     x[1] = make_float2(w.z, w.w);
@@ -219,62 +217,96 @@ __device__ __forceinline__ void f32_pairs(const float* base, int DK, int u, int 
   }
 }
 
-// Per-token scalars of the forward update for one value row, from the tables.
-struct Tok {
-  float alpha, om, oma, b, bv;
+// Per-token scalars of the forward update for the lane's two value rows.
+struct Tok2 {
+  float alpha, om;
+  float2 b, bv;  // beta_i and beta_i v_i of rows 2g, 2g + 1
 };
 
-__device__ __forceinline__ Tok tok(const unsigned char* bsm, const BwdSmem& L, int u, int r) {
-  Tok t;
+__device__ __forceinline__ Tok2 tok2(const unsigned char* bsm, const BwdSmem& L, int u, int g) {
+  Tok2 t;
   t.alpha = reinterpret_cast<const float*>(bsm + L.al)[u];
   t.om = reinterpret_cast<const float*>(bsm + L.om)[u];
-  t.oma = reinterpret_cast<const float*>(bsm + L.oma)[u];
-  t.b = reinterpret_cast<const float*>(bsm + L.rb)[u * kRowsPerCta + r];
-  t.bv = reinterpret_cast<const float*>(bsm + L.rbv)[u * kRowsPerCta + r];
+  t.b = reinterpret_cast<const float2*>(bsm + L.rb)[(u * kRowsPerCta) / 2 + g];
+  t.bv = reinterpret_cast<const float2*>(bsm + L.rbv)[(u * kRowsPerCta) / 2 + g];
   return t;
 }
 
-// One forward step of a lane's state pairs (the forward kernel's update, packed):
+// One forward step of the lane's two rows (the forward kernel's update, packed):
 //   I = alpha I + (beta_i k_j^2 + (1 - alpha) I_prior),  M = alpha M + (beta_i v_i) k_j.
 template <int NP>
-__device__ __forceinline__ void step_pairs(float2 (&M)[NP], float2 (&I)[NP], const float2 (&k)[NP], const Tok& t) {
-  const float2 a2 = f2(t.alpha), om2 = f2(t.om), b2 = f2(t.b), bv2 = f2(t.bv);
+__device__ __forceinline__ void step_rows(float2 (&M)[2][NP], float2 (&I)[2][NP], const float2 (&k)[NP],
+                                          const Tok2& t) {
+  const float2 a2 = f2(t.alpha), om2 = f2(t.om);
+  float2 kk[NP];
 #pragma unroll
-  for (int p = 0; p < NP; ++p) {
-    I[p] = __ffma2_rn(a2, I[p], __ffma2_rn(b2, __fmul2_rn(k[p], k[p]), om2));
-    M[p] = __ffma2_rn(a2, M[p], __fmul2_rn(bv2, k[p]));
+  for (int p = 0; p < NP; ++p) kk[p] = __fmul2_rn(k[p], k[p]);
+#pragma unroll
+  for (int r = 0; r < 2; ++r) {
+    const float2 b2 = f2(r ? t.b.y : t.b.x), bv2 = f2(r ? t.bv.y : t.bv.x);
+#pragma unroll
+    for (int p = 0; p < NP; ++p) {
+      I[r][p] = __ffma2_rn(a2, I[r][p], __ffma2_rn(b2, kk[p], om2));
+      M[r][p] = __ffma2_rn(a2, M[r][p], __fmul2_rn(bv2, k[p]));
+    }
   }
 }
 
-// Adjoints at t = T of one lane's element pairs, from the final state (M, I):
-// gM = dmu_T / I, gI = dI_T - dmu_T mu_T / I.
+// Adjoints at t = T of the lane's elements, from the final state (M, I):
+// gM = dmu_T / I, gI = dI_T - dmu_T mu_T / I. soff is row 2g's offset; row
+// 2g + 1 follows d_k floats later.
 template <int NP>
-__device__ __forceinline__ void init_adjoints(const BwdArgs& a, size_t soff, const float2 (&M)[NP],
-                                              const float2 (&I)[NP], float2 (&gM)[NP], float2 (&gI)[NP]) {
+__device__ __forceinline__ void init_adjoints(const BwdArgs& a, size_t soff, int DK, const float2 (&M)[2][NP],
+                                              const float2 (&I)[2][NP], float2 (&gM)[2][NP], float2 (&gI)[2][NP]) {
 #pragma unroll
-  for (int p = 0; p < NP; ++p) {
-    const float2 dmu = a.dmu_T ? *reinterpret_cast<const float2*>(a.dmu_T + soff + 2 * p) : make_float2(0.f, 0.f);
-    const float2 dI = a.dI_T ? *reinterpret_cast<const float2*>(a.dI_T + soff + 2 * p) : make_float2(0.f, 0.f);
-    const float2 r = make_float2(1.f / I[p].x, 1.f / I[p].y);
-    gM[p] = __fmul2_rn(dmu, r);
-    gI[p] = make_float2(dI.x - dmu.x * (M[p].x * r.x) * r.x, dI.y - dmu.y * (M[p].y * r.y) * r.y);
+  for (int r = 0; r < 2; ++r) {
+#pragma unroll
+    for (int p = 0; p < NP; ++p) {
+      const size_t o = soff + (size_t)r * DK + 2 * p;
+      const float2 dmu = a.dmu_T ? *reinterpret_cast<const float2*>(a.dmu_T + o) : f2(0.f);
+      const float2 dI = a.dI_T ? *reinterpret_cast<const float2*>(a.dI_T + o) : f2(0.f);
+      const float2 rr = make_float2(1.f / I[r][p].x, 1.f / I[r][p].y);
+      gM[r][p] = __fmul2_rn(dmu, rr);
+      gI[r][p] = make_float2(dI.x - dmu.x * (M[r][p].x * rr.x) * rr.x, dI.y - dmu.y * (M[r][p].y * rr.y) * rr.y);
+    }
   }
+}
+
+// The lane's elements of a row-major array at (row 2g, column c0): two rows,
+// `rs` floats apart, of NP pairs each.
+template <int NP>
+__device__ __forceinline__ void load_rows(const float* base, size_t rs, float2 (&x)[2][NP]) {
+#pragma unroll
+  for (int r = 0; r < 2; ++r)
+#pragma unroll
+    for (int p = 0; p < NP; ++p) x[r][p] = *reinterpret_cast<const float2*>(base + r * rs + 2 * p);
+}
+template <int NP>
+__device__ __forceinline__ void store_rows(float* base, size_t rs, const float2 (&x)[2][NP]) {
+#pragma unroll
+  for (int r = 0; r < 2; ++r)
+#pragma unroll
+    for (int p = 0; p < NP; ++p) *reinterpret_cast<float2*>(base + r * rs + 2 * p) = x[r][p];
 }
 
 template <int DK, bool BF16, bool PACKED>
-__global__ void __launch_bounds__(kThreads)
+__global__ void __launch_bounds__(kThreads, 2)
 palimpsa_bwd_kernel(BwdArgs a, float* __restrict__ ckpt) {
-  constexpr int NC = DK / 32;       // key columns per lane
-  constexpr int NP = NC / 2;        // packed pairs per lane
-  constexpr int CW = DK / kWarps;   // key columns per warp
+  constexpr int C = DK / 32;          // key columns per lane
+  constexpr int NP = C / 2;           // column pairs per lane and row
+  constexpr int CWARP = DK / kWarps;  // key columns per warp
   constexpr int ES = BF16 ? 2 : 4;
+  static_assert(CWARP == 8 * C, "eight column lanes per warp");
   extern __shared__ __align__(128) unsigned char bsm[];
   const BwdSmem L(DK, ES);
-  // window starts, lane-linear (only the owning lane reads them back): [window][pair][thread]
-  float2* winM = reinterpret_cast<float2*>(bsm + L.win);
-  float2* winI = winM + kNW * NP * kThreads;
-  auto rowp = reinterpret_cast<float (*)[kWin][kRowsPerCta][3]>(bsm + L.rowp);
-  const float* al = reinterpret_cast<const float*>(bsm + L.al);
+  // window starts, lane-linear (only the owning lane reads them back): [window][M | I][row][pair][thread]
+  float2* winS = reinterpret_cast<float2*>(bsm + L.win);
+  auto win_at = [&](int wi, int mi, int r, int p) -> float2& {
+    return winS[(((wi * 2 + mi) * 2 + r) * NP + p) * kThreads + threadIdx.x];
+  };
+  auto rowp = reinterpret_cast<float (*)[kWin][kRowsPerCta][2]>(bsm + L.rowp);
+  auto adap = reinterpret_cast<float (*)[kWin][4]>(bsm + L.adap);
+  const float* oma = reinterpret_cast<const float*>(bsm + L.oma);
 
   const int DV = a.d_v;
   const int groups = DV / kRowsPerCta;
@@ -282,9 +314,8 @@ palimpsa_bwd_kernel(BwdArgs a, float* __restrict__ ckpt) {
   const int row0 = (blockIdx.x % groups) * kRowsPerCta;
   const int h = (int)(bh % a.H);
   const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
-  const int rl = lane >> 2;                 // this lane's row within the CTA
-  const int i = row0 + rl;                  // ... and within the head
-  const int c0 = w * CW + (lane & 3) * NC;  // this lane's first key column
+  const int g = lane >> 3;                    // this lane's row pair: CTA rows 2g, 2g + 1
+  const int c0 = w * CWARP + (lane & 7) * C;  // this lane's first key column
   // this head's sequence: all T tokens, or a packed sequence's own range,
   // checked before anything is read (a bad one is reported and skipped)
   int T = a.T;
@@ -306,18 +337,24 @@ palimpsa_bwd_kernel(BwdArgs a, float* __restrict__ ckpt) {
   const int nseg = (T + kSeg - 1) / kSeg;
   static_assert(kSeg == kCheckpointTokens, "backward segments are the training checkpoints");
   const size_t ck_head = (size_t)ck_slot0 * DV * 2 * DK;
-  float* ck_out = ckpt ? ckpt + ck_head : nullptr;  // null when the forward's checkpoints are used
-  const float* ck_in = (a.ckpt_in ? a.ckpt_in : ckpt) + ck_head;
+  const size_t ck_lane = (size_t)(row0 + 2 * g) * 2 * DK + c0;   // the lane's first element in a checkpoint
+  float* ck_out = ckpt ? ckpt + ck_head + ck_lane : nullptr;  // null when the forward's checkpoints are used
+  const float* ck_in = (a.ckpt_in ? a.ckpt_in : ckpt) + ck_head + ck_lane;
+  const size_t ck_step = (size_t)DV * 2 * DK;                  // one checkpoint of the head
+  const size_t soff = ((size_t)bh * DV + row0 + 2 * g) * DK + c0;  // the lane's first state element
 
   // ---- initial state
-  float2 M[NP], I[NP], mu0v[NP], I0v[NP];
-  const size_t soff = ((size_t)bh * DV + i) * DK + c0;
+  float2 M[2][NP], I[2][NP];
 #pragma unroll
-  for (int p = 0; p < NP; ++p) {
-    I0v[p] = a.I0 ? *reinterpret_cast<const float2*>(a.I0 + soff + 2 * p) : f2(Ip);
-    mu0v[p] = a.mu0 ? *reinterpret_cast<const float2*>(a.mu0 + soff + 2 * p) : f2(0.f);
-    I[p] = I0v[p];
-    M[p] = __fmul2_rn(I0v[p], mu0v[p]);
+  for (int r = 0; r < 2; ++r) {
+#pragma unroll
+    for (int p = 0; p < NP; ++p) {
+      const size_t o = soff + (size_t)r * DK + 2 * p;
+      const float2 i0 = a.I0 ? *reinterpret_cast<const float2*>(a.I0 + o) : f2(Ip);
+      const float2 m0 = a.mu0 ? *reinterpret_cast<const float2*>(a.mu0 + o) : f2(0.f);
+      I[r][p] = i0;
+      M[r][p] = __fmul2_rn(i0, m0);
+    }
   }
 
   // ---- phase 1: forward sweep, checkpoint at every segment start; segment
@@ -329,40 +366,37 @@ palimpsa_bwd_kernel(BwdArgs a, float* __restrict__ ckpt) {
                             T - (nseg - 1) * kSeg);
     cp_async_commit();
   } else {
-  if (nseg > 0) stage_segment<DK, ES>(bsm, L, a, head_tok, row0, 0, min(kSeg, T));
-  cp_async_commit();
-  for (int s = 0; s < nseg; ++s) {
-    const int ts = s * kSeg, tn = min(kSeg, T - ts);
-    if (s + 1 < nseg)
-      stage_segment<DK, ES>(bsm + (size_t)((s + 1) & 1) * L.stage, L, a, head_tok, row0, ts + kSeg,
-                            min(kSeg, T - ts - kSeg));
+    if (nseg > 0) stage_segment<DK, ES>(bsm, L, a, head_tok, row0, 0, min(kSeg, T));
     cp_async_commit();
-    cp_async_wait_1();
-    __syncthreads();  // segment s staged by every thread
-    const unsigned char* st = bsm + (size_t)(s & 1) * L.stage;
-    prepare_segment<DK, BF16>(st, bsm, L, tn, A_h, Ip);
-    const float* kf = reinterpret_cast<const float*>(BF16 ? bsm + L.kf : st + L.k);
-    float* cp = ck_out + ((size_t)s * DV + i) * DK * 2;
-#pragma unroll
-    for (int p = 0; p < NP; ++p) {
-      *reinterpret_cast<float2*>(cp + c0 + 2 * p) = M[p];
-      *reinterpret_cast<float2*>(cp + DK + c0 + 2 * p) = I[p];
+    for (int s = 0; s < nseg; ++s) {
+      const int ts = s * kSeg, tn = min(kSeg, T - ts);
+      if (s + 1 < nseg)
+        stage_segment<DK, ES>(bsm + (size_t)((s + 1) & 1) * L.stage, L, a, head_tok, row0, ts + kSeg,
+                              min(kSeg, T - ts - kSeg));
+      cp_async_commit();
+      cp_async_wait_1();
+      __syncthreads();  // segment s staged by every thread
+      const unsigned char* st = bsm + (size_t)(s & 1) * L.stage;
+      prepare_segment<DK, BF16>(st, bsm, L, tn, A_h, Ip);
+      const float* kf = reinterpret_cast<const float*>(BF16 ? bsm + L.kf : st + L.k);
+      float* cp = ck_out + (size_t)s * ck_step;
+      store_rows<NP>(cp, 2 * DK, M);
+      store_rows<NP>(cp + DK, 2 * DK, I);
+      __syncthreads();  // gates ready
+      for (int u = 0; u < tn; ++u) {
+        float2 k[NP];
+        lane_pairs<NP>(kf, DK, u, c0, k);
+        step_rows<NP>(M, I, k, tok2(bsm, L, u, g));
+      }
+      __syncthreads();  // this stage and the tables are free again
     }
-    __syncthreads();  // gates ready
-    for (int u = 0; u < tn; ++u) {
-      float2 k[NP];
-      f32_pairs<NC>(kf, DK, u, c0, k);
-      step_pairs<NP>(M, I, k, tok(bsm, L, u, rl));
-    }
-    __syncthreads();  // this stage and the tables are free again
-  }
   }
 
   // The adjoints start at t = T from the final-state gradients: set from the
   // final state, which the re-run of the last segment reaches (or the initial
   // state when T = 0).
-  float2 gM[NP], gI[NP];
-  if (nseg == 0) init_adjoints<NP>(a, soff, M, I, gM, gI);
+  float2 gM[2][NP], gI[2][NP];
+  if (nseg == 0) init_adjoints<NP>(a, soff, DK, M, I, gM, gI);
   float dIp_acc = 0.f, dA_acc = 0.f;
 
   // ---- phase 2: segments in reverse; segment s - 1 is being copied in while
@@ -375,49 +409,47 @@ palimpsa_bwd_kernel(BwdArgs a, float* __restrict__ ckpt) {
     __syncthreads();  // segment s staged by every thread
     const unsigned char* st = bsm + (size_t)(s & 1) * L.stage;
     const float* dts = reinterpret_cast<const float*>(st + L.dt);
-    const float* dys = reinterpret_cast<const float*>(st + L.dy);
+    const float2* dys = reinterpret_cast<const float2*>(st + L.dy);
     prepare_segment<DK, BF16>(st, bsm, L, tn, A_h, Ip);
     const float* kf = reinterpret_cast<const float*>(BF16 ? bsm + L.kf : st + L.k);
     const float* qf = reinterpret_cast<const float*>(BF16 ? bsm + L.qf : st + L.q);
-    const float* cp = ck_in + ((size_t)s * DV + i) * DK * 2;
-#pragma unroll
-    for (int p = 0; p < NP; ++p) {
-      M[p] = *reinterpret_cast<const float2*>(cp + c0 + 2 * p);
-      I[p] = *reinterpret_cast<const float2*>(cp + DK + c0 + 2 * p);
-    }
+    load_rows<NP>(ck_in + (size_t)s * ck_step, 2 * DK, M);
+    load_rows<NP>(ck_in + (size_t)s * ck_step + DK, 2 * DK, I);
     __syncthreads();  // gates ready
     // re-run the segment, keeping the state at each window start (this lane's elements only)
     for (int u = 0; u < tn; ++u) {
       if (u % kWin == 0) {
 #pragma unroll
-        for (int p = 0; p < NP; ++p) {
-          winM[((u / kWin) * NP + p) * kThreads + threadIdx.x] = M[p];
-          winI[((u / kWin) * NP + p) * kThreads + threadIdx.x] = I[p];
-        }
+        for (int r = 0; r < 2; ++r)
+#pragma unroll
+          for (int p = 0; p < NP; ++p) {
+            win_at(u / kWin, 0, r, p) = M[r][p];
+            win_at(u / kWin, 1, r, p) = I[r][p];
+          }
       }
       float2 k[NP];
-      f32_pairs<NC>(kf, DK, u, c0, k);
-      step_pairs<NP>(M, I, k, tok(bsm, L, u, rl));
+      lane_pairs<NP>(kf, DK, u, c0, k);
+      step_rows<NP>(M, I, k, tok2(bsm, L, u, g));
     }
-    if (s == nseg - 1) init_adjoints<NP>(a, soff, M, I, gM, gI);  // M, I: the final state
+    if (s == nseg - 1) init_adjoints<NP>(a, soff, DK, M, I, gM, gI);  // M, I: the final state
     const int nwin = (tn + kWin - 1) / kWin;
     for (int wi = nwin - 1; wi >= 0; --wi) {
       const int uw = wi * kWin, n = min(kWin, tn - uw);
-      // re-run the window into registers: state before token uw + uu is (Ms[uu], Is[uu])
-      float2 Ms[kWin + 1][NP], Is[kWin + 1][NP];
-#pragma unroll
-      for (int p = 0; p < NP; ++p) {
-        Ms[0][p] = winM[(wi * NP + p) * kThreads + threadIdx.x];
-        Is[0][p] = winI[(wi * NP + p) * kThreads + threadIdx.x];
-      }
+      // re-run the window into registers: (Ms[uu], Is[uu]) is the state after token uw + uu
+      float2 Ms[kWin][2][NP], Is[kWin][2][NP];
 #pragma unroll
       for (int uu = 0; uu < kWin; ++uu) {
         if (uu < n) {
-          float2 k[NP];
-          f32_pairs<NC>(kf, DK, uw + uu, c0, k);
 #pragma unroll
-          for (int p = 0; p < NP; ++p) { Ms[uu + 1][p] = Ms[uu][p]; Is[uu + 1][p] = Is[uu][p]; }
-          step_pairs<NP>(Ms[uu + 1], Is[uu + 1], k, tok(bsm, L, uw + uu, rl));
+          for (int r = 0; r < 2; ++r)
+#pragma unroll
+            for (int p = 0; p < NP; ++p) {
+              Ms[uu][r][p] = uu ? Ms[uu - 1][r][p] : win_at(wi, 0, r, p);
+              Is[uu][r][p] = uu ? Is[uu - 1][r][p] : win_at(wi, 1, r, p);
+            }
+          float2 k[NP];
+          lane_pairs<NP>(kf, DK, uw + uu, c0, k);
+          step_rows<NP>(Ms[uu], Is[uu], k, tok2(bsm, L, uw + uu, g));
         }
       }
       // sweep the window backwards
@@ -425,59 +457,88 @@ palimpsa_bwd_kernel(BwdArgs a, float* __restrict__ ckpt) {
       for (int uu = kWin - 1; uu >= 0; --uu) {
         if (uu < n) {
           const int u = uw + uu;
-          float2 k[NP], q[NP];
-          f32_pairs<NC>(kf, DK, u, c0, k);
-          f32_pairs<NC>(qf, DK, u, c0, q);
-          const Tok tr = tok(bsm, L, u, rl);
-          const float dyi = dys[u * kRowsPerCta + rl];
-          const float2 dy2 = f2(dyi), ndy2 = f2(-dyi), bv2 = f2(tr.bv), tb2 = f2(2.f * tr.b), nIp2 = f2(-Ip);
-          float2 sbv = f2(0.f), sb = f2(0.f), sal = f2(0.f), sgi = f2(0.f);
-          float cs[2 * NC];  // column partials: dq then dk
+          float2 k[NP], q[NP], kk[NP], dqa[NP], dkM[NP], dkI[NP];
+          lane_pairs<NP>(kf, DK, u, c0, k);
+          lane_pairs<NP>(qf, DK, u, c0, q);
+          const Tok2 tr = tok2(bsm, L, u, g);
+          const float2 dyp = dys[(u * kRowsPerCta) / 2 + g];
 #pragma unroll
           for (int p = 0; p < NP; ++p) {
-            const float2 Ic = Is[uu + 1][p];
-            const float2 r = make_float2(rcp_approx(Ic.x), rcp_approx(Ic.y));
-            const float2 mu = __fmul2_rn(Ms[uu + 1][p], r);
-            gM[p] = __ffma2_rn(__fmul2_rn(dy2, q[p]), r, gM[p]);
-            gI[p] = __ffma2_rn(__fmul2_rn(__fmul2_rn(ndy2, q[p]), mu), r, gI[p]);
-            const float2 dq2 = __fmul2_rn(dy2, mu);
-            sbv = __ffma2_rn(gM[p], k[p], sbv);
-            sb = __ffma2_rn(gI[p], __fmul2_rn(k[p], k[p]), sb);
-            const float2 dk2 = __ffma2_rn(gM[p], bv2, __fmul2_rn(gI[p], __fmul2_rn(tb2, k[p])));
-            sal = __ffma2_rn(gM[p], Ms[uu][p], __ffma2_rn(gI[p], __fadd2_rn(Is[uu][p], nIp2), sal));
-            sgi = __fadd2_rn(sgi, gI[p]);
-            cs[2 * p] = dq2.x; cs[2 * p + 1] = dq2.y;
-            cs[NC + 2 * p] = dk2.x; cs[NC + 2 * p + 1] = dk2.y;
+            kk[p] = __fmul2_rn(k[p], k[p]);
+            dqa[p] = dkM[p] = dkI[p] = f2(0.f);
           }
-          // columns: finished over the 8 rows inside the warp, one global atomic per lane
-          const float cv = reduce_scatter_rows<2 * NC>(cs, lane);
-          {
-            const int t = ts + u;
-            const int v = NC == 4 ? rl : (rl >> 1);
-            if (NC == 4 || (lane & 4) == 0)
-              atomicAdd((v < NC ? a.dq : a.dk) + (head_tok + t) * DK + c0 + (v % NC), cv);
-          }
-          // rows: over this warp's columns (the row's 4 lanes), then per warp into shared memory
-          float r_bv = sbv.x + sbv.y, r_b = sb.x + sb.y, r_al = sal.x + sal.y;
+          float2 rM[2], rI[2], ada[2], sgi = f2(0.f);
 #pragma unroll
-          for (int m = 1; m <= 2; m <<= 1) {
-            r_bv += __shfl_xor_sync(0xffffffffu, r_bv, m);
-            r_b += __shfl_xor_sync(0xffffffffu, r_b, m);
-            r_al += __shfl_xor_sync(0xffffffffu, r_al, m);
+          for (int r = 0; r < 2; ++r) {
+            const float2 ndy2 = f2(-(r ? dyp.y : dyp.x));
+            const float2 bv2 = f2(r ? tr.bv.y : tr.bv.x), b2 = f2(r ? tr.b.y : tr.b.x);
+            rM[r] = rI[r] = ada[r] = f2(0.f);
+#pragma unroll
+            for (int p = 0; p < NP; ++p) {
+              const float2 Ic = Is[uu][r][p], Mc = Ms[uu][r][p];
+              const float2 nr = make_float2(rcp_approx(-Ic.x), rcp_approx(-Ic.y));  // -1 / I
+              const float2 mun = __fmul2_rn(Mc, nr);                                 // -mu
+              dqa[p] = __ffma2_rn(ndy2, mun, dqa[p]);                                // + dy_i mu
+              const float2 ndyq = __fmul2_rn(ndy2, q[p]);                            // -dy_i q_j
+              gM[r][p] = __ffma2_rn(ndyq, nr, gM[r][p]);                             // + dy q / I
+              gI[r][p] = __ffma2_rn(ndyq, __fmul2_rn(mun, nr), gI[r][p]);            // - dy q mu / I
+              dkM[p] = __ffma2_rn(gM[r][p], bv2, dkM[p]);
+              dkI[p] = __ffma2_rn(gI[r][p], b2, dkI[p]);
+              rM[r] = __ffma2_rn(gM[r][p], k[p], rM[r]);
+              rI[r] = __ffma2_rn(gI[r][p], kk[p], rI[r]);
+              ada[r] = __ffma2_rn(gM[r][p], Mc, __ffma2_rn(gI[r][p], Ic, ada[r]));
+              sgi = __fadd2_rn(sgi, gI[r][p]);
+            }
           }
-          if ((lane & 3) == 0) {
-            rowp[w][uu][rl][0] = r_bv;
-            rowp[w][uu][rl][1] = r_b;
-            rowp[w][uu][rl][2] = r_al;
+          // columns: dq_j and dk_j = sum gM bv + 2 k_j sum gI beta over the lane's
+          // rows, then over the warp's 4 row pairs; one fp32 atomic per kept pair
+          float cs[2 * C];
+#pragma unroll
+          for (int p = 0; p < NP; ++p) {
+            const float2 dk2 = __ffma2_rn(__fadd2_rn(k[p], k[p]), dkI[p], dkM[p]);
+            cs[2 * p] = dqa[p].x;
+            cs[2 * p + 1] = dqa[p].y;
+            cs[C + 2 * p] = dk2.x;
+            cs[C + 2 * p + 1] = dk2.y;
           }
-          dIp_acc = fmaf(tr.oma, sgi.x + sgi.y, dIp_acc);  // (1 - alpha_t) sum gI; reduced at the end
+          rs_level<2 * C, 2 * C>(cs, lane, 16);
+          rs_level<2 * C, C>(cs, lane, 8);
+          {
+            constexpr int KEEP = C / 2;   // partials g * KEEP .. g * KEEP + KEEP - 1 of cs
+            const int o = g * KEEP;
+            float* dst = (o < C ? a.dq : a.dk) + (head_tok + ts + u) * DK + c0 + (o % C);
+            if constexpr (KEEP == 2) atomicAdd(reinterpret_cast<float2*>(dst), make_float2(cs[0], cs[1]));
+            else atomicAdd(dst, cs[0]);
+          }
+          // rows: d(bv)_i and sum_j gI k_j^2 over the lane's columns, then over the
+          // warp's 8 column lanes; alpha_t dL/dalpha_t over the lane's elements
+          float rv[4] = {rM[0].x + rM[0].y, rM[1].x + rM[1].y, rI[0].x + rI[0].y, rI[1].x + rI[1].y};
+          const float sg = sgi.x + sgi.y;
+          float ap = ((ada[0].x + ada[0].y) + (ada[1].x + ada[1].y)) -
+                     (tr.bv.x * rv[0] + tr.bv.y * rv[1]) - (tr.b.x * rv[2] + tr.b.y * rv[3]) - Ip * sg;
+          dIp_acc = fmaf(oma[u], sg, dIp_acc);  // (1 - alpha) sum gI; reduced at the end
+          rs_level<4, 4>(rv, lane, 4);
+          rs_level<4, 2>(rv, lane, 2);
+          rv[0] += __shfl_xor_sync(0xffffffffu, rv[0], 1);
+#pragma unroll
+          for (int m = 1; m <= 4; m <<= 1) ap += __shfl_xor_sync(0xffffffffu, ap, m);
+          if ((lane & 1) == 0) {
+            const int o = (lane >> 1) & 3;   // row 2g + (o & 1); d(bv) for o < 2, else sum gI k^2
+            rowp[w][uu][2 * g + (o & 1)][o >> 1] = rv[0];
+          }
+          if ((lane & 7) == 0) adap[w][uu][g] = ap;
           // carry the adjoints to t - 1
           const float2 a2 = f2(tr.alpha);
 #pragma unroll
-          for (int p = 0; p < NP; ++p) { gM[p] = __fmul2_rn(gM[p], a2); gI[p] = __fmul2_rn(gI[p], a2); }
+          for (int r = 0; r < 2; ++r)
+#pragma unroll
+            for (int p = 0; p < NP; ++p) {
+              gM[r][p] = __fmul2_rn(gM[r][p], a2);
+              gI[r][p] = __fmul2_rn(gI[r][p], a2);
+            }
         }
       }
-      // the window's row sums: dv, dbeta per (token, row); dalpha per token
+      // the window's row sums: dv, dbeta per (token, row); alpha dalpha per token
       __syncthreads();
       for (int x = threadIdx.x; x < n * kRowsPerCta; x += kThreads) {
         const int uu = x / kRowsPerCta, r = x % kRowsPerCta, u = uw + uu;
@@ -490,13 +551,13 @@ palimpsa_bwd_kernel(BwdArgs a, float* __restrict__ ckpt) {
       }
       if (threadIdx.x < n) {
         const int uu = threadIdx.x, u = uw + uu;
-        float dal = 0.f;
+        float ad = 0.f;  // alpha_t dL/dalpha_t over the CTA's rows
 #pragma unroll
         for (int ww = 0; ww < kWarps; ++ww)
 #pragma unroll
-          for (int r = 0; r < kRowsPerCta; ++r) dal += rowp[ww][uu][r][2];
-        atomicAdd(a.dd_t + head_tok + ts + u, -A_h * al[u] * dal);
-        dA_acc = fmaf(-dts[u] * al[u], dal, dA_acc);
+          for (int gg = 0; gg < 4; ++gg) ad += adap[ww][uu][gg];
+        atomicAdd(a.dd_t + head_tok + ts + u, -A_h * ad);
+        dA_acc = fmaf(-dts[u], ad, dA_acc);
       }
       __syncthreads();  // the row partials are free for the next window
     }
@@ -507,11 +568,17 @@ palimpsa_bwd_kernel(BwdArgs a, float* __restrict__ ckpt) {
   // ---- initial-state gradients: M_0 = I0 (.) mu0, I_0 = I0
   float s_ip0 = 0.f;
 #pragma unroll
-  for (int p = 0; p < NP; ++p) {
-    const float2 dI0 = __ffma2_rn(gM[p], mu0v[p], gI[p]);
-    if (a.dmu0) *reinterpret_cast<float2*>(a.dmu0 + soff + 2 * p) = __fmul2_rn(gM[p], I0v[p]);
-    if (a.dI0) *reinterpret_cast<float2*>(a.dI0 + soff + 2 * p) = dI0;
-    s_ip0 += dI0.x + dI0.y;
+  for (int r = 0; r < 2; ++r) {
+#pragma unroll
+    for (int p = 0; p < NP; ++p) {
+      const size_t o = soff + (size_t)r * DK + 2 * p;
+      const float2 i0 = a.I0 ? *reinterpret_cast<const float2*>(a.I0 + o) : f2(Ip);
+      const float2 m0 = a.mu0 ? *reinterpret_cast<const float2*>(a.mu0 + o) : f2(0.f);
+      const float2 dI0 = __ffma2_rn(gM[r][p], m0, gI[r][p]);
+      if (a.dmu0) *reinterpret_cast<float2*>(a.dmu0 + o) = __fmul2_rn(gM[r][p], i0);
+      if (a.dI0) *reinterpret_cast<float2*>(a.dI0 + o) = dI0;
+      s_ip0 += dI0.x + dI0.y;
+    }
   }
   // With I0 absent the initial precision is I_prior itself.
   if (!a.I0) dIp_acc += s_ip0;
