@@ -437,106 +437,114 @@ palimpsa_bwd_kernel(BwdArgs a, float* __restrict__ ckpt) {
       const int uw = wi * kWin, n = min(kWin, tn - uw);
       // re-run the window into registers: (Ms[uu], Is[uu]) is the state after token uw + uu
       float2 Ms[kWin][2][NP], Is[kWin][2][NP];
+      auto rerun = [&](const int uu) {
 #pragma unroll
-      for (int uu = 0; uu < kWin; ++uu) {
-        if (uu < n) {
-#pragma unroll
-          for (int r = 0; r < 2; ++r)
-#pragma unroll
-            for (int p = 0; p < NP; ++p) {
-              Ms[uu][r][p] = uu ? Ms[uu - 1][r][p] : win_at(wi, 0, r, p);
-              Is[uu][r][p] = uu ? Is[uu - 1][r][p] : win_at(wi, 1, r, p);
-            }
-          float2 k[NP];
-          lane_pairs<NP>(kf, DK, uw + uu, c0, k);
-          step_rows<NP>(Ms[uu], Is[uu], k, tok2(bsm, L, uw + uu, g));
-        }
-      }
-      // sweep the window backwards
-#pragma unroll
-      for (int uu = kWin - 1; uu >= 0; --uu) {
-        if (uu < n) {
-          const int u = uw + uu;
-          float2 k[NP], q[NP], kk[NP], dqa[NP], dkM[NP], dkI[NP];
-          lane_pairs<NP>(kf, DK, u, c0, k);
-          lane_pairs<NP>(qf, DK, u, c0, q);
-          const Tok2 tr = tok2(bsm, L, u, g);
-          const float2 dyp = dys[(u * kRowsPerCta) / 2 + g];
+        for (int r = 0; r < 2; ++r)
 #pragma unroll
           for (int p = 0; p < NP; ++p) {
-            kk[p] = __fmul2_rn(k[p], k[p]);
-            dqa[p] = dkM[p] = dkI[p] = f2(0.f);
+            Ms[uu][r][p] = uu ? Ms[uu - 1][r][p] : win_at(wi, 0, r, p);
+            Is[uu][r][p] = uu ? Is[uu - 1][r][p] : win_at(wi, 1, r, p);
           }
-          float2 rM[2], rI[2], ada[2], sgi = f2(0.f);
+        float2 k[NP];
+        lane_pairs<NP>(kf, DK, uw + uu, c0, k);
+        step_rows<NP>(Ms[uu], Is[uu], k, tok2(bsm, L, uw + uu, g));
+      };
+      // one token of the backward sweep: the adjoints take token uw + uu's
+      // readout, its gradient sums are formed and handed on, then the adjoints
+      // are carried to the token before. Accumulators start from their first
+      // product.
+      auto sweep = [&](const int uu) {
+        const int u = uw + uu;
+        float2 k[NP], q[NP], kk[NP], dqa[NP], dkM[NP], dkI[NP];
+        lane_pairs<NP>(kf, DK, u, c0, k);
+        lane_pairs<NP>(qf, DK, u, c0, q);
+        const Tok2 tr = tok2(bsm, L, u, g);
+        const float2 dyp = dys[(u * kRowsPerCta) / 2 + g];
 #pragma unroll
-          for (int r = 0; r < 2; ++r) {
-            const float2 ndy2 = f2(-(r ? dyp.y : dyp.x));
-            const float2 bv2 = f2(r ? tr.bv.y : tr.bv.x), b2 = f2(r ? tr.b.y : tr.b.x);
-            rM[r] = rI[r] = ada[r] = f2(0.f);
+        for (int p = 0; p < NP; ++p) kk[p] = __fmul2_rn(k[p], k[p]);
+        float2 rM[2], rI[2], ada[2], sgi[2];
 #pragma unroll
-            for (int p = 0; p < NP; ++p) {
-              const float2 Ic = Is[uu][r][p], Mc = Ms[uu][r][p];
-              const float2 nr = make_float2(rcp_approx(-Ic.x), rcp_approx(-Ic.y));  // -1 / I
-              const float2 mun = __fmul2_rn(Mc, nr);                                 // -mu
-              dqa[p] = __ffma2_rn(ndy2, mun, dqa[p]);                                // + dy_i mu
-              const float2 ndyq = __fmul2_rn(ndy2, q[p]);                            // -dy_i q_j
-              gM[r][p] = __ffma2_rn(ndyq, nr, gM[r][p]);                             // + dy q / I
-              gI[r][p] = __ffma2_rn(ndyq, __fmul2_rn(mun, nr), gI[r][p]);            // - dy q mu / I
-              dkM[p] = __ffma2_rn(gM[r][p], bv2, dkM[p]);
-              dkI[p] = __ffma2_rn(gI[r][p], b2, dkI[p]);
-              rM[r] = __ffma2_rn(gM[r][p], k[p], rM[r]);
-              rI[r] = __ffma2_rn(gI[r][p], kk[p], rI[r]);
-              ada[r] = __ffma2_rn(gM[r][p], Mc, __ffma2_rn(gI[r][p], Ic, ada[r]));
-              sgi = __fadd2_rn(sgi, gI[r][p]);
-            }
-          }
-          // columns: dq_j and dk_j = sum gM bv + 2 k_j sum gI beta over the lane's
-          // rows, then over the warp's 4 row pairs; one fp32 atomic per kept pair
-          float cs[2 * C];
+        for (int r = 0; r < 2; ++r) {
+          const float2 ndy2 = f2(-(r ? dyp.y : dyp.x));
+          const float2 bv2 = f2(r ? tr.bv.y : tr.bv.x), b2 = f2(r ? tr.b.y : tr.b.x);
 #pragma unroll
           for (int p = 0; p < NP; ++p) {
-            const float2 dk2 = __ffma2_rn(__fadd2_rn(k[p], k[p]), dkI[p], dkM[p]);
-            cs[2 * p] = dqa[p].x;
-            cs[2 * p + 1] = dqa[p].y;
-            cs[C + 2 * p] = dk2.x;
-            cs[C + 2 * p + 1] = dk2.y;
+            const float2 Ic = Is[uu][r][p], Mc = Ms[uu][r][p];
+            const float2 nr = make_float2(rcp_approx(-Ic.x), rcp_approx(-Ic.y));  // -1 / I
+            const float2 mun = __fmul2_rn(Mc, nr);                                 // -mu
+            dqa[p] = r ? __ffma2_rn(ndy2, mun, dqa[p]) : __fmul2_rn(ndy2, mun);   // + dy_i mu
+            const float2 ndyq = __fmul2_rn(ndy2, q[p]);                            // -dy_i q_j
+            gM[r][p] = __ffma2_rn(ndyq, nr, gM[r][p]);                             // + dy q / I
+            gI[r][p] = __ffma2_rn(ndyq, __fmul2_rn(mun, nr), gI[r][p]);            // - dy q mu / I
+            dkM[p] = r ? __ffma2_rn(gM[r][p], bv2, dkM[p]) : __fmul2_rn(gM[r][p], bv2);
+            dkI[p] = r ? __ffma2_rn(gI[r][p], b2, dkI[p]) : __fmul2_rn(gI[r][p], b2);
+            rM[r] = p ? __ffma2_rn(gM[r][p], k[p], rM[r]) : __fmul2_rn(gM[r][p], k[p]);
+            rI[r] = p ? __ffma2_rn(gI[r][p], kk[p], rI[r]) : __fmul2_rn(gI[r][p], kk[p]);
+            const float2 t = p ? __ffma2_rn(gI[r][p], Ic, ada[r]) : __fmul2_rn(gI[r][p], Ic);
+            ada[r] = __ffma2_rn(gM[r][p], Mc, t);
+            sgi[r] = p ? __fadd2_rn(sgi[r], gI[r][p]) : gI[r][p];
           }
-          rs_level<2 * C, 2 * C>(cs, lane, 16);
-          rs_level<2 * C, C>(cs, lane, 8);
-          {
-            constexpr int KEEP = C / 2;   // partials g * KEEP .. g * KEEP + KEEP - 1 of cs
-            const int o = g * KEEP;
-            float* dst = (o < C ? a.dq : a.dk) + (head_tok + ts + u) * DK + c0 + (o % C);
-            if constexpr (KEEP == 2) atomicAdd(reinterpret_cast<float2*>(dst), make_float2(cs[0], cs[1]));
-            else atomicAdd(dst, cs[0]);
-          }
-          // rows: d(bv)_i and sum_j gI k_j^2 over the lane's columns, then over the
-          // warp's 8 column lanes; alpha_t dL/dalpha_t over the lane's elements
-          float rv[4] = {rM[0].x + rM[0].y, rM[1].x + rM[1].y, rI[0].x + rI[0].y, rI[1].x + rI[1].y};
-          const float sg = sgi.x + sgi.y;
-          float ap = ((ada[0].x + ada[0].y) + (ada[1].x + ada[1].y)) -
-                     (tr.bv.x * rv[0] + tr.bv.y * rv[1]) - (tr.b.x * rv[2] + tr.b.y * rv[3]) - Ip * sg;
-          dIp_acc = fmaf(oma[u], sg, dIp_acc);  // (1 - alpha) sum gI; reduced at the end
-          rs_level<4, 4>(rv, lane, 4);
-          rs_level<4, 2>(rv, lane, 2);
-          rv[0] += __shfl_xor_sync(0xffffffffu, rv[0], 1);
-#pragma unroll
-          for (int m = 1; m <= 4; m <<= 1) ap += __shfl_xor_sync(0xffffffffu, ap, m);
-          if ((lane & 1) == 0) {
-            const int o = (lane >> 1) & 3;   // row 2g + (o & 1); d(bv) for o < 2, else sum gI k^2
-            rowp[w][uu][2 * g + (o & 1)][o >> 1] = rv[0];
-          }
-          if ((lane & 7) == 0) adap[w][uu][g] = ap;
-          // carry the adjoints to t - 1
-          const float2 a2 = f2(tr.alpha);
-#pragma unroll
-          for (int r = 0; r < 2; ++r)
-#pragma unroll
-            for (int p = 0; p < NP; ++p) {
-              gM[r][p] = __fmul2_rn(gM[r][p], a2);
-              gI[r][p] = __fmul2_rn(gI[r][p], a2);
-            }
         }
+        // columns: dq_j and dk_j = sum gM bv + 2 k_j sum gI beta over the lane's
+        // rows, then over the warp's 4 row pairs; one fp32 atomic per kept pair
+        float cs[2 * C];
+#pragma unroll
+        for (int p = 0; p < NP; ++p) {
+          const float2 dk2 = __ffma2_rn(__fadd2_rn(k[p], k[p]), dkI[p], dkM[p]);
+          cs[2 * p] = dqa[p].x;
+          cs[2 * p + 1] = dqa[p].y;
+          cs[C + 2 * p] = dk2.x;
+          cs[C + 2 * p + 1] = dk2.y;
+        }
+        rs_level<2 * C, 2 * C>(cs, lane, 16);
+        rs_level<2 * C, C>(cs, lane, 8);
+        {
+          constexpr int KEEP = C / 2;   // partials g * KEEP .. g * KEEP + KEEP - 1 of cs
+          const int o = g * KEEP;
+          float* dst = (o < C ? a.dq : a.dk) + (head_tok + ts + u) * DK + c0 + (o % C);
+          if constexpr (KEEP == 2) atomicAdd(reinterpret_cast<float2*>(dst), make_float2(cs[0], cs[1]));
+          else atomicAdd(dst, cs[0]);
+        }
+        // rows: d(bv)_i and sum_j gI k_j^2 over the lane's columns, then over the
+        // warp's 8 column lanes; alpha_t dL/dalpha_t over the lane's elements
+        float rv[4] = {rM[0].x + rM[0].y, rM[1].x + rM[1].y, rI[0].x + rI[0].y, rI[1].x + rI[1].y};
+        const float sg = (sgi[0].x + sgi[0].y) + (sgi[1].x + sgi[1].y);
+        float ap = ((ada[0].x + ada[0].y) + (ada[1].x + ada[1].y)) -
+                   (tr.bv.x * rv[0] + tr.bv.y * rv[1]) - (tr.b.x * rv[2] + tr.b.y * rv[3]) - Ip * sg;
+        dIp_acc = fmaf(oma[u], sg, dIp_acc);  // (1 - alpha) sum gI; reduced at the end
+        rs_level<4, 4>(rv, lane, 4);
+        rs_level<4, 2>(rv, lane, 2);
+        rv[0] += __shfl_xor_sync(0xffffffffu, rv[0], 1);
+#pragma unroll
+        for (int m = 1; m <= 4; m <<= 1) ap += __shfl_xor_sync(0xffffffffu, ap, m);
+        if ((lane & 1) == 0) {
+          const int o = (lane >> 1) & 3;   // row 2g + (o & 1); d(bv) for o < 2, else sum gI k^2
+          rowp[w][uu][2 * g + (o & 1)][o >> 1] = rv[0];
+        }
+        if ((lane & 7) == 0) adap[w][uu][g] = ap;
+        // carry the adjoints to t - 1
+        const float2 a2 = f2(tr.alpha);
+#pragma unroll
+        for (int r = 0; r < 2; ++r)
+#pragma unroll
+          for (int p = 0; p < NP; ++p) {
+            gM[r][p] = __fmul2_rn(gM[r][p], a2);
+            gI[r][p] = __fmul2_rn(gI[r][p], a2);
+          }
+      };
+      // full windows without per-token guards, so that neighbouring tokens interleave
+      if (n == kWin) {
+#pragma unroll
+        for (int uu = 0; uu < kWin; ++uu) rerun(uu);
+#pragma unroll
+        for (int uu = kWin - 1; uu >= 0; --uu) sweep(uu);
+      } else {
+#pragma unroll
+        for (int uu = 0; uu < kWin; ++uu)
+          if (uu < n) rerun(uu);
+#pragma unroll
+        for (int uu = kWin - 1; uu >= 0; --uu)
+          if (uu < n) sweep(uu);
       }
       // the window's row sums: dv, dbeta per (token, row); alpha dalpha per token
       __syncthreads();
