@@ -36,9 +36,12 @@ MUFU_RCP_PER_CLK_PER_SM = 16     # SFU reciprocal issue rate per SM (one per ele
 # DRAM bytes per launch (dram__bytes_read.sum + dram__bytes_write.sum) of a kernel from one ncu
 # capture at the bench's full size (profiles/launches_decode_B256_H32.md), valid only while the
 # kernel's source file is byte-identical to the one captured (sha256 below); otherwise null.
+# The decode step's figure is the mean of consecutive steps captured without cache flushes
+# (--cache-control none), as they run in the timed region: each step finds the rows the
+# previous one stored last still in L2.
 NCU_TRAFFIC = {
-    "palimpsa_step": {"bytes_per_launch": 1019104171, "source": "csrc/step.cu",
-                      "sha256": "a6071dc649bba97d682ba9c5b9511c1cad7feedc2cb5726ae9b569ec3fbcc0c0"},
+    "palimpsa_step": {"bytes_per_launch": 909054464, "source": "csrc/step.cu",
+                      "sha256": "6e910ab6d6995dd60256518d989bdad194cb450255d360c7aca6b0c98e7ac06a"},
 }
 
 

@@ -562,6 +562,18 @@ void palimpsa_debug_withhold_first_copy(int on);
  */
 void palimpsa_set_forward_segments(int segments);
 
+/*
+ * palimpsa_set_step_l2_keep_bytes — process-wide tuning of the decode step
+ * (palimpsa_step, palimpsa_step_sequence, palimpsa_step_fused). The step
+ * streams the whole state through HBM. Consecutive launches walk it in
+ * opposite orders, and each launch stores the last `bytes` of its walk with
+ * an evict-last L2 policy instead of streaming them, so the next launch starts
+ * on rows that are still in L2. 0 turns this off: every launch then walks in
+ * the same order and streams everything. Default 96 MiB. Results are the same
+ * bits either way; only the DRAM traffic changes.
+ */
+void palimpsa_set_step_l2_keep_bytes(long long bytes);
+
 #ifdef __cplusplus
 }
 #endif

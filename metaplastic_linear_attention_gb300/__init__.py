@@ -36,6 +36,7 @@ from .binding import (  # noqa: F401
     palimpsa_get_device_status,
     palimpsa_segment_summary,
     palimpsa_set_forward_segments,
+    palimpsa_set_step_l2_keep_bytes,
     palimpsa_set_wait_timeout_ns,
     palimpsa_state_combine,
     palimpsa_status_string,

@@ -122,6 +122,8 @@ def load_library(path: str | None = None):
         lib.palimpsa_debug_withhold_first_copy.argtypes = [i]
         lib.palimpsa_set_forward_segments.restype = None
         lib.palimpsa_set_forward_segments.argtypes = [i]
+        lib.palimpsa_set_step_l2_keep_bytes.restype = None
+        lib.palimpsa_set_step_l2_keep_bytes.argtypes = [ctypes.c_longlong]
         _lib = lib
         return lib
 
@@ -156,6 +158,12 @@ def palimpsa_debug_withhold_first_copy(on: bool) -> None:
 
 def palimpsa_set_forward_segments(segments: int) -> None:
     load_library().palimpsa_set_forward_segments(int(segments))
+
+
+def palimpsa_set_step_l2_keep_bytes(nbytes: int) -> None:
+    """Bytes of the decode state each step leaves in L2 for the next, which walks
+    the state the other way (0 = stream everything in one order; see palimpsa.h)."""
+    load_library().palimpsa_set_step_l2_keep_bytes(int(nbytes))
 
 
 def _stream_handle(stream) -> int:

@@ -20,6 +20,8 @@ unsigned int* g_status_ptr[kMaxDevices] = {};
 std::atomic<unsigned long long> g_wait_timeout_ns{2000000000ull};
 std::atomic<int> g_withhold_first_copy{0};
 std::atomic<int> g_forward_segments{0};
+// Bytes of state each decode step leaves in L2 for the next one.
+std::atomic<long long> g_step_l2_keep_bytes{96ll << 20};
 
 // The library's own stream-ordered memory pool on the current device, created
 // on first use. Its release threshold is unbounded, so memory freed by one
@@ -148,6 +150,7 @@ palimpsa_status step_impl(const void* q, const void* k, const void* v, const voi
   unsigned int* st = nullptr;
   if (palimpsa_status s = status_word(&st)) return s;
   StepArgs a{q, k, v, beta, d_t, A, I_prior, mu, I, y, B, H, d_k, d_v, in_dtype == PALIMPSA_BF16, st, pro};
+  a.l2_keep_bytes = g_step_l2_keep_bytes.load();
   if (launch_step(a, static_cast<cudaStream_t>(cuda_stream)) != cudaSuccess) return PALIMPSA_ERR_CUDA;
   return PALIMPSA_OK;
 }
@@ -502,10 +505,12 @@ palimpsa_status palimpsa_step_sequence(const void* q, const void* k, const void*
   const char* ck = static_cast<const char*>(k);
   const char* cv = static_cast<const char*>(v);
   const char* cb = static_cast<const char*>(beta);
+  const long long keep = g_step_l2_keep_bytes.load();
   for (int s = 1; s < S; ++s) {
     StepArgs a{cq + s * bh * d_k * es, ck + s * bh * d_k * es, cv + s * bh * d_v * es, cb + s * bh * d_v * es,
                d_t + s * bh, A, I_prior, mu, I, y + s * bh * d_v, B, H, d_k, d_v, in_dtype == PALIMPSA_BF16, sw,
                Prologue{}};
+    a.l2_keep_bytes = keep;
     if (launch_step(a, static_cast<cudaStream_t>(cuda_stream)) != cudaSuccess) return PALIMPSA_ERR_CUDA;
   }
   return PALIMPSA_OK;
@@ -549,6 +554,8 @@ void palimpsa_set_wait_timeout_ns(uint64_t ns) { g_wait_timeout_ns.store(ns); }
 void palimpsa_debug_withhold_first_copy(int on) { g_withhold_first_copy.store(on ? 1 : 0); }
 
 void palimpsa_set_forward_segments(int segments) { g_forward_segments.store(segments > 0 ? segments : 0); }
+
+void palimpsa_set_step_l2_keep_bytes(long long bytes) { g_step_l2_keep_bytes.store(bytes > 0 ? bytes : 0); }
 
 }  // extern "C"
 

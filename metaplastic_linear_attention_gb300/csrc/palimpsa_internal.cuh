@@ -68,6 +68,10 @@ struct StepArgs {
   bool bf16;
   unsigned int* status;
   Prologue pro{};
+  // Bytes of the state that the step stores last and leaves in L2 for the
+  // next step, which walks the state in the opposite order (0: every step
+  // streams the whole state in the same order).
+  long long l2_keep_bytes = 0;
 };
 
 struct BwdArgs {

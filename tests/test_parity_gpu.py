@@ -12,6 +12,7 @@ import pytest
 import torch
 
 import metaplastic_linear_attention_gb300 as pal
+import oracle
 from metaplastic_linear_attention_gb300 import synthetic as syn
 from tests._helpers import TIGHT, oracle_forward_from, pick, rel_l2, tol_for
 
@@ -648,3 +649,42 @@ def test_step_sequence_equals_token_by_token_bitwise():
                                          steps["d_t"][t], seq["A"], seq["I_prior"], mu_b, I_b) for t in range(9)])
     assert pal.palimpsa_get_device_status() == 0
     assert torch.equal(y_a, y_b) and torch.equal(mu_a, mu_b) and torch.equal(I_a, I_b)
+
+
+@pytest.mark.parametrize("keep", [0, 128 << 10, 96 << 20])
+def test_step_walk_order_and_l2_keep_change_no_bits(keep):
+    """Decode steps walk the state in alternating orders and store the end of
+    each walk with an L2-keeping policy. With the whole state kept, part of it or
+    none (walk order fixed), the results are bit-identical to each other and
+    match the oracle."""
+    wl = syn.WORKLOADS["decode"].with_(B=6, H=4)
+    seq = _gpu(syn.sequence_inputs(wl, T=1, seed=91))
+    steps = _gpu(syn.decode_inputs(wl, 7, seed=91))
+    g = torch.Generator().manual_seed(92)
+    mu0 = torch.randn((6, 4, 64, 128), generator=g)
+    I0 = 0.5 + torch.rand((6, 4, 64, 128), generator=g)
+
+    def run(nbytes):
+        pal.palimpsa_set_step_l2_keep_bytes(nbytes)
+        try:
+            mu, I = mu0.to(DEV), I0.to(DEV)
+            y = pal.palimpsa_step(steps["q"], steps["k"], steps["v"], steps["beta"], steps["d_t"], seq["A"],
+                                  seq["I_prior"], mu, I)
+        finally:
+            pal.palimpsa_set_step_l2_keep_bytes(96 << 20)
+        assert pal.palimpsa_get_device_status() == 0
+        return y.cpu(), mu.cpu(), I.cpu()
+
+    ref = run(0)
+    for _ in range(2):  # both walk directions come first once
+        got = run(keep)
+        assert all(torch.equal(a, b) for a, b in zip(got, ref))
+    f = syn.as_float64_numpy
+    ys, mu_r, I_r = [], f(mu0), f(I0)
+    for t in range(7):
+        y_t, mu_r, I_r = oracle.forward(*(f(steps[n][t])[:, :, None] for n in ("q", "k", "v", "beta")),
+                                        f(steps["d_t"][t])[:, :, None], f(seq["A"]), f(seq["I_prior"]),
+                                        mu0=mu_r, I0=I_r)
+        ys.append(y_t[:, :, 0])
+    assert rel_l2(ref[0].numpy(), np.stack(ys)) <= TIGHT
+    assert rel_l2(ref[1].numpy(), mu_r) <= TIGHT and rel_l2(ref[2].numpy(), I_r) <= TIGHT
