@@ -7,7 +7,7 @@ import torch
 import oracle
 from metaplastic_linear_attention_gb300.synthetic import as_float64_numpy
 
-# Relative-L2 bars (spec tolerances): fp32 inputs 1e-4; bf16 inputs with
+# Relative-L2 bars (the target tolerances): fp32 inputs 1e-4; bf16 inputs with
 # fp32 state 2e-2 (the oracle consumes the same bf16-rounded values, so the GPU
 # is in practice far inside the bf16 bar; TIGHT records that stronger claim).
 TOL_F32 = 1e-4
