@@ -40,8 +40,8 @@ MUFU_RCP_PER_CLK_PER_SM = 16     # SFU reciprocal issue rate per SM (one per ele
 # (--cache-control none), as they run in the timed region: each step finds the rows the
 # previous one stored last still in L2.
 NCU_TRAFFIC = {
-    "palimpsa_step": {"bytes_per_launch": 909054464, "source": "csrc/step.cu",
-                      "sha256": "6e910ab6d6995dd60256518d989bdad194cb450255d360c7aca6b0c98e7ac06a"},
+    "palimpsa_step": {"bytes_per_launch": 925541157, "source": "csrc/step.cu",
+                      "sha256": "77ceeef2f560f5d1cf8249d25849db6e62ed97c78bb9a4d76c43c9af0926bf5f"},
 }
 
 
