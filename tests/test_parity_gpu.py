@@ -688,3 +688,27 @@ def test_step_walk_order_and_l2_keep_change_no_bits(keep):
         ys.append(y_t[:, :, 0])
     assert rel_l2(ref[0].numpy(), np.stack(ys)) <= TIGHT
     assert rel_l2(ref[1].numpy(), mu_r) <= TIGHT and rel_l2(ref[2].numpy(), I_r) <= TIGHT
+
+
+def test_backward_full_size_small_layer_sampled_head():
+    """The backward at the small layer's full size (B=4, H=16, T=2048, bf16), as the
+    benchmark runs it, against fp64 autograd on one head across the whole batch:
+    its per-token gradients, and dA, dI_prior of that head (sums over the batch)."""
+    from oracle import autograd as ag
+    wl = syn.WORKLOADS["small_layer"]
+    inp = syn.sequence_inputs(wl)
+    g = torch.Generator().manual_seed(4242)
+    dy = torch.randn((wl.B, wl.H, wl.T, wl.d_v), generator=g)
+    gi = _gpu(inp)
+    out = pal.palimpsa_backward(gi["q"], gi["k"], gi["v"], gi["beta"], gi["d_t"], gi["A"], gi["I_prior"], None,
+                                None, dy.to(DEV), want_state_grads=False)
+    assert pal.palimpsa_get_device_status() == 0
+    h = 5
+    f = syn.as_float64_numpy
+    sub = {n: f(inp[n][:, h:h + 1]) for n in ("q", "k", "v", "beta", "d_t")}
+    sub.update(A=f(inp["A"][h:h + 1]), I_prior=f(inp["I_prior"][h:h + 1]), mu0=None, I0=None)
+    ref = ag.gradients(sub, f(dy[:, h:h + 1]))
+    for n, m in (("dq", "q"), ("dk", "k"), ("dv", "v"), ("dbeta", "beta"), ("dd_t", "d_t")):
+        assert rel_l2(out[n][:, h:h + 1].cpu().numpy(), ref[m]) <= TIGHT, n
+    for n, m in (("dA", "A"), ("dI_prior", "I_prior")):
+        assert rel_l2(out[n][h:h + 1].cpu().numpy(), ref[m]) <= TIGHT, n

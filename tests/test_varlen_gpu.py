@@ -4,6 +4,7 @@ against the fp64 oracle, which runs each sequence on its own.
 Source: Bonnet et al., "Learning to Remember, Learn, and Forget in
 Attention-Based Models" — slide 7 / Eq. (5) per sequence, slide 9 (the state
 carried along a sequence, and across segments by the affine scan)."""
+import numpy as np
 import pytest
 import torch
 
@@ -289,3 +290,32 @@ def test_varlen_checkpoints_are_each_sequences_states():
                 slot = cu[n] // 32 + n + c
                 assert rel_l2(ck[:, slot, :, 0, :], mu_r[0] * I_r[0]) <= TIGHT, (n, c)
                 assert rel_l2(ck[:, slot, :, 1, :], I_r[0]) <= TIGHT, (n, c)
+
+
+def test_varlen_backward_bench_packing_sampled_sequences():
+    """The packed training pair at the benchmark's packing of the small layer (its
+    B*T tokens per head as 4*B ragged sequences, bf16): the checkpointed forward
+    and the backward reading its checkpoints, against fp64 autograd on two
+    sequences of one head."""
+    from oracle import autograd as ag
+    wl = syn.WORKLOADS["small_layer"]
+    lengths = syn.varlen_lengths(wl.B * wl.T, 4 * wl.B, wl.seed)
+    pk = syn.packed_inputs(wl, lengths, H=wl.H, seed=wl.seed)
+    g = torch.Generator().manual_seed(77)
+    dy = torch.randn((wl.H, wl.B * wl.T, wl.d_v), generator=g)
+    d = {n: t.to(DEV) for n, t in pk.items()}
+    _, _, _, ck = pal.palimpsa_forward_varlen_checkpointed(d["q"], d["k"], d["v"], d["beta"], d["d_t"], d["A"],
+                                                           d["I_prior"], d["cu_seqlens"])
+    out = pal.palimpsa_backward_varlen(d["q"], d["k"], d["v"], d["beta"], d["d_t"], d["A"], d["I_prior"],
+                                       d["cu_seqlens"], None, None, dy.to(DEV), want_state_grads=False, ckpt=ck)
+    assert pal.palimpsa_get_device_status() == 0
+    cu = pk["cu_seqlens"].tolist()
+    h = 3
+    f = syn.as_float64_numpy
+    for n in (0, int(np.argmax(lengths))):
+        s0, s1 = cu[n], cu[n + 1]
+        sub = {m: f(pk[m][h:h + 1, s0:s1])[None] for m in ("q", "k", "v", "beta", "d_t")}
+        sub.update(A=f(pk["A"][h:h + 1]), I_prior=f(pk["I_prior"][h:h + 1]), mu0=None, I0=None)
+        ref = ag.gradients(sub, f(dy[h:h + 1, s0:s1])[None])
+        for name, m in (("dq", "q"), ("dk", "k"), ("dv", "v"), ("dbeta", "beta"), ("dd_t", "d_t")):
+            assert rel_l2(out[name][h:h + 1, s0:s1].cpu().numpy(), ref[m][0]) <= TIGHT, (n, name)
