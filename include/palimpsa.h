@@ -381,6 +381,20 @@ palimpsa_status palimpsa_step_fused(
     palimpsa_dtype in_dtype, void* cuda_stream);
 
 /*
+ * palimpsa_step_sequence_fused — palimpsa_step_fused for S tokens in order,
+ * enqueued by one call as palimpsa_step_sequence does for palimpsa_step: the
+ * inputs carry a leading token index (q, k [S, B, H, d_k]; v, beta_raw
+ * [S, B, H, d_v]; d_raw [S, B, H]) and y is [S, B, H, d_v]. Arguments are
+ * validated once; other arguments and errors as for palimpsa_step_fused.
+ */
+palimpsa_status palimpsa_step_sequence_fused(
+    const void* q, const void* k, const void* v, const void* beta_raw,
+    const float* d_raw, const float* A, const float* I_prior,
+    const float* b_scale, float* mu, float* I, float* y,
+    int S, int B, int H, int d_k, int d_v, unsigned int flags,
+    palimpsa_dtype in_dtype, void* cuda_stream);
+
+/*
  * palimpsa_forward_without_meta — the "without Meta" comparator: the same
  * recurrence with the importance frozen at its prior (I_t = I_prior), i.e. the
  * Mamba2 limit of Eq. (5) (slide 11; slide 10 names Mamba2 as Palimpsa-M's

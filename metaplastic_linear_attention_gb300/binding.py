@@ -108,6 +108,9 @@ def load_library(path: str | None = None):
         lib.palimpsa_step_fused.argtypes = [vp, vp, vp, vp, fp, fp, fp, fp, fp, fp, fp, i, i, i, i, u, i, vp]
         lib.palimpsa_step.restype = i
         lib.palimpsa_step.argtypes = [vp, vp, vp, vp, fp, fp, fp, fp, fp, fp, i, i, i, i, i, vp]
+        lib.palimpsa_step_sequence_fused.restype = i
+        lib.palimpsa_step_sequence_fused.argtypes = [vp, vp, vp, vp, fp, fp, fp, fp, fp, fp, fp, i, i, i, i, i, u,
+                                                     i, vp]
         lib.palimpsa_step_sequence.restype = i
         lib.palimpsa_step_sequence.argtypes = [vp, vp, vp, vp, fp, fp, fp, fp, fp, fp, i, i, i, i, i, i, vp]
         lib.palimpsa_status_string.restype = ctypes.c_char_p
@@ -442,35 +445,42 @@ def palimpsa_forward_fused(q, k, v, beta_raw, d_raw, A, I_prior, b_scale=None, m
 
 def palimpsa_step_fused(q, k, v, beta_raw, d_raw, A, I_prior, mu, I, b_scale=None, *, qk_norm=False, v_star=False,
                         y=None, stream=None):
-    """One decode token from raw inputs (see palimpsa.h): q, k [B,H,d_k], v and
-    beta_raw [B,H,d_v], d_raw [B,H]; mu, I updated in place. Device tensors.
-    Returns y [B,H,d_v]."""
+    """Decode tokens from raw inputs (see palimpsa.h); mu, I updated in place.
+    Device tensors. One token: q, k [B,H,d_k], v and beta_raw [B,H,d_v], d_raw
+    [B,H] -> y [B,H,d_v]. S tokens: a leading steps dimension on q, k, v,
+    beta_raw, d_raw -> y [S,B,H,d_v], enqueued by one palimpsa_step_sequence_fused
+    call."""
     if q.device.type != "cuda":
         raise ValueError("palimpsa_step_fused takes device tensors")
-    B, H, d_k = q.shape
+    seq = q.dim() == 4
+    lead = (q.shape[0],) if seq else ()
+    B, H, d_k = q.shape[-3:]
     d_v = v.shape[-1]
     dev = q.device
     f32 = torch.float32
     _check(k, "k", q.shape, q.dtype, dev)
     _check(q, "q", q.shape, None, dev)
-    _check(v, "v", (B, H, d_v), q.dtype, dev)
-    _check(beta_raw, "beta_raw", (B, H, d_v), q.dtype, dev)
-    _check(d_raw, "d_raw", (B, H), f32, dev)
+    _check(v, "v", lead + (B, H, d_v), q.dtype, dev)
+    _check(beta_raw, "beta_raw", lead + (B, H, d_v), q.dtype, dev)
+    _check(d_raw, "d_raw", lead + (B, H), f32, dev)
     _check(A, "A", (H,), f32, dev)
     _check(I_prior, "I_prior", (H,), f32, dev)
     _check(b_scale, "b_scale", (H,), f32, dev)
     _check(mu, "mu", (B, H, d_v, d_k), f32, dev)
     _check(I, "I", (B, H, d_v, d_k), f32, dev)
-    y = torch.empty((B, H, d_v), dtype=f32, device=dev) if y is None else y
-    _check(y, "y", (B, H, d_v), f32, dev)
+    y = torch.empty(lead + (B, H, d_v), dtype=f32, device=dev) if y is None else y
+    _check(y, "y", lead + (B, H, d_v), f32, dev)
     lib = load_library()
+    head = [_ptr(q), _ptr(k), _ptr(v), _ptr(beta_raw), _ptr(d_raw), _ptr(A), _ptr(I_prior), _ptr(b_scale), _ptr(mu),
+            _ptr(I), _ptr(y)]
+    tail = [B, H, d_k, d_v, _fuse_flags(qk_norm, v_star), _in_dtype(q), ctypes.c_void_p(_stream_handle(stream))]
     with torch.cuda.device(dev):
-        rc = lib.palimpsa_step_fused(_ptr(q), _ptr(k), _ptr(v), _ptr(beta_raw), _ptr(d_raw), _ptr(A), _ptr(I_prior),
-                                     _ptr(b_scale), _ptr(mu), _ptr(I), _ptr(y), B, H, d_k, d_v,
-                                     _fuse_flags(qk_norm, v_star), _in_dtype(q),
-                                     ctypes.c_void_p(_stream_handle(stream)))
+        if seq:
+            rc, name = lib.palimpsa_step_sequence_fused(*head, int(q.shape[0]), *tail), "palimpsa_step_sequence_fused"
+        else:
+            rc, name = lib.palimpsa_step_fused(*head, *tail), "palimpsa_step_fused"
     if rc != 0:
-        raise PalimpsaError(rc, "palimpsa_step_fused")
+        raise PalimpsaError(rc, name)
     return y
 
 

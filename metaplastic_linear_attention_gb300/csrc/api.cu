@@ -155,6 +155,40 @@ palimpsa_status step_impl(const void* q, const void* k, const void* v, const voi
   return PALIMPSA_OK;
 }
 
+// S tokens in order (palimpsa_step_sequence, palimpsa_step_sequence_fused):
+// the arguments are validated once, on the first token (every token's slice
+// has the same sizes and alignment, since a token of q, k is 2 or 4 * d_k bytes
+// and of v, beta, y d_v * 2 or 4 bytes, both multiples of 16; d_t only needs
+// 4), then one step launch per token is enqueued.
+palimpsa_status step_sequence_impl(const void* q, const void* k, const void* v, const void* beta, const float* d_t,
+                                   const float* A, const float* I_prior, float* mu, float* I, float* y, int S,
+                                   int B, int H, int d_k, int d_v, palimpsa_dtype in_dtype, void* cuda_stream,
+                                   const Prologue& pro) {
+  if (S < 0) return PALIMPSA_ERR_SHAPE;
+  if (S == 0) return PALIMPSA_OK;
+  palimpsa_status st = step_impl(q, k, v, beta, d_t, A, I_prior, mu, I, y, B, H, d_k, d_v, in_dtype, cuda_stream,
+                                 pro);
+  if (st != PALIMPSA_OK) return st;
+  if ((long long)S * B * H > (1LL << 40)) return PALIMPSA_ERR_SHAPE;
+  unsigned int* sw = nullptr;
+  if (palimpsa_status s2 = status_word(&sw)) return s2;
+  const size_t es = in_dtype == PALIMPSA_BF16 ? 2 : 4;
+  const size_t bh = (size_t)B * H;
+  const char* cq = static_cast<const char*>(q);
+  const char* ck = static_cast<const char*>(k);
+  const char* cv = static_cast<const char*>(v);
+  const char* cb = static_cast<const char*>(beta);
+  const long long keep = g_step_l2_keep_bytes.load();
+  for (int s = 1; s < S; ++s) {
+    StepArgs a{cq + s * bh * d_k * es, ck + s * bh * d_k * es, cv + s * bh * d_v * es, cb + s * bh * d_v * es,
+               d_t + s * bh, A, I_prior, mu, I, y + s * bh * d_v, B, H, d_k, d_v, in_dtype == PALIMPSA_BF16, sw,
+               pro};
+    a.l2_keep_bytes = keep;
+    if (launch_step(a, static_cast<cudaStream_t>(cuda_stream)) != cudaSuccess) return PALIMPSA_ERR_CUDA;
+  }
+  return PALIMPSA_OK;
+}
+
 constexpr unsigned int kKnownFuseFlags = PALIMPSA_FUSE_QK_NORM | PALIMPSA_FUSE_V_STAR;
 
 Prologue fused_prologue(const float* b_scale, unsigned int flags) {
@@ -488,32 +522,18 @@ palimpsa_status palimpsa_step_sequence(const void* q, const void* k, const void*
                                        const float* d_t, const float* A, const float* I_prior, float* mu, float* I,
                                        float* y, int S, int B, int H, int d_k, int d_v, palimpsa_dtype in_dtype,
                                        void* cuda_stream) {
-  if (S < 0) return PALIMPSA_ERR_SHAPE;
-  if (S == 0) return PALIMPSA_OK;
-  // validate once, on the first token (every token's slice has the same sizes and
-  // alignment, since a token of q, k is 2 or 4 * d_k bytes and of v, beta, y
-  // d_v * 2 or 4 bytes, both multiples of 16; d_t only needs 4)
-  palimpsa_status st = step_impl(q, k, v, beta, d_t, A, I_prior, mu, I, y, B, H, d_k, d_v, in_dtype, cuda_stream,
-                                 Prologue{});
-  if (st != PALIMPSA_OK) return st;
-  if ((long long)S * B * H > (1LL << 40)) return PALIMPSA_ERR_SHAPE;
-  unsigned int* sw = nullptr;
-  if (palimpsa_status s2 = status_word(&sw)) return s2;
-  const size_t es = in_dtype == PALIMPSA_BF16 ? 2 : 4;
-  const size_t bh = (size_t)B * H;
-  const char* cq = static_cast<const char*>(q);
-  const char* ck = static_cast<const char*>(k);
-  const char* cv = static_cast<const char*>(v);
-  const char* cb = static_cast<const char*>(beta);
-  const long long keep = g_step_l2_keep_bytes.load();
-  for (int s = 1; s < S; ++s) {
-    StepArgs a{cq + s * bh * d_k * es, ck + s * bh * d_k * es, cv + s * bh * d_v * es, cb + s * bh * d_v * es,
-               d_t + s * bh, A, I_prior, mu, I, y + s * bh * d_v, B, H, d_k, d_v, in_dtype == PALIMPSA_BF16, sw,
-               Prologue{}};
-    a.l2_keep_bytes = keep;
-    if (launch_step(a, static_cast<cudaStream_t>(cuda_stream)) != cudaSuccess) return PALIMPSA_ERR_CUDA;
-  }
-  return PALIMPSA_OK;
+  return palimpsa::step_sequence_impl(q, k, v, beta, d_t, A, I_prior, mu, I, y, S, B, H, d_k, d_v, in_dtype,
+                                      cuda_stream, palimpsa::Prologue{});
+}
+
+palimpsa_status palimpsa_step_sequence_fused(const void* q, const void* k, const void* v, const void* beta_raw,
+                                             const float* d_raw, const float* A, const float* I_prior,
+                                             const float* b_scale, float* mu, float* I, float* y, int S, int B,
+                                             int H, int d_k, int d_v, unsigned int flags, palimpsa_dtype in_dtype,
+                                             void* cuda_stream) {
+  if (flags & ~kKnownFuseFlags) return PALIMPSA_ERR_UNSUPPORTED;
+  return palimpsa::step_sequence_impl(q, k, v, beta_raw, d_raw, A, I_prior, mu, I, y, S, B, H, d_k, d_v,
+                                      in_dtype, cuda_stream, fused_prologue(b_scale, flags));
 }
 
 const char* palimpsa_status_string(palimpsa_status s) {

@@ -24,11 +24,19 @@
 //   keeps reading while they hit. Measured on GB300 at B=256, H=32: 6 % less
 //   time per step with 96 MiB kept;
 // * q, k of the head are loaded once per warp; k^2, alpha and (1 - alpha)
-//   I_prior once per lane;
+//   I_prior once per lane; beta_i (through the prologue when it is on) and
+//   beta_i v_i of the warp's 8 rows are formed by 8 lanes, one row each, and
+//   handed to the row loop by shuffles, so no lane waits on a load or repeats
+//   a gate inside it;
 // * y_i is a butterfly shuffle reduction over the lanes of the row.
 // The update uses the mean/precision form of Eq. (5) directly:
 //   I' = alpha I + (1 - alpha) I_prior + beta_i k_j^2
-//   mu' = (alpha I mu + beta_i v_i k_j) / I'      (IEEE division)
+//   mu' = (alpha I mu + beta_i v_i k_j) / I'
+// with IEEE division in the plain step and the fast division (within 2 ulp)
+// in the fused one, whose launch bounds also hold it to 128 registers: on
+// GB300 each of these choices measured fastest for its variant (the fused
+// step compiles to over 128 registers otherwise and loses its second CTA per
+// SM).
 // The fused variant (PRO, palimpsa_step_fused) first applies the layer's
 // prologue to the token's raw inputs: softplus to the gate input, b_scale *
 // sigmoid to beta, optionally the L2 norm of q and k (one more butterfly over
@@ -67,7 +75,7 @@ __device__ __forceinline__ void st_evict_last(float* p, float4 v, unsigned long 
 }
 
 template <int DK, bool BF16, bool PRO>
-__global__ void __launch_bounds__(kWarpsPerBlock * 32)
+__global__ void __launch_bounds__(kWarpsPerBlock * 32, PRO ? 2 : 1)
 palimpsa_step_kernel(StepArgs a, bool reverse, long keep_from) {
   constexpr int LPR = DK / 4;       // lanes per row
   constexpr int RPI = 32 / LPR;     // rows per warp instruction
@@ -102,6 +110,21 @@ palimpsa_step_kernel(StepArgs a, bool reverse, long keep_from) {
     mu4[it] = __ldcs(reinterpret_cast<const float4*>(a.mu + off));
     I4[it] = __ldcs(reinterpret_cast<const float4*>(a.I + off));
   }
+  // ... then the rows' beta and v: lane r (r < 8) takes row r's, forms the
+  // row's gate values once for the warp (through the prologue when it is on),
+  // and the row loop reads them back by shuffle.
+  // (With the prologue each lane still loads v for every row: on GB300 that
+  // measured faster than shuffling beta_i v_i, which would wait on the gate.)
+  const int i_base = (int)(row_base - bh * a.d_v);
+  const size_t row_in = (size_t)bh * a.d_v + i_base + (lane % kRowsPerWarp);
+  float b_row = load1<BF16>(a.beta, row_in);
+  float v_row = 0.f, v_in[NIT];
+  if constexpr (PRO) {
+#pragma unroll
+    for (int it = 0; it < NIT; ++it) v_in[it] = load1<BF16>(a.v, (size_t)bh * a.d_v + i_base + it * RPI + sub);
+  } else {
+    v_row = load1<BF16>(a.v, row_in);
+  }
 
   float4 q4 = load4<BF16>(a.q, (size_t)bh * DK + col);
   float4 k4 = load4<BF16>(a.k, (size_t)bh * DK + col);
@@ -110,6 +133,7 @@ palimpsa_step_kernel(StepArgs a, bool reverse, long keep_from) {
   if constexpr (PRO) {
     d = softplus_f(d);
     if (a.pro.b_scale) bsc = a.pro.b_scale[h];
+    b_row = bsc * sigmoid_f(b_row);
     if (a.pro.qk_norm) {  // the LPR lanes of a row hold the whole q and k of the head
       float sq = q4.x * q4.x + q4.y * q4.y + q4.z * q4.z + q4.w * q4.w;
       float sk = k4.x * k4.x + k4.y * k4.y + k4.z * k4.z + k4.w * k4.w;
@@ -123,6 +147,7 @@ palimpsa_step_kernel(StepArgs a, bool reverse, long keep_from) {
       k4 = make_float4(k4.x * ik, k4.y * ik, k4.z * ik, k4.w * ik);
     }
   }
+  const float bv_row = b_row * v_row;  // beta_i v_i of the lane's row (without the prologue)
   const float A_h = a.A[h], Ip = a.I_prior[h];
   bool bad = !(pos_finite(A_h) && pos_finite(Ip) && nonneg_finite(d));
   const float x = -A_h * d;
@@ -134,15 +159,13 @@ palimpsa_step_kernel(StepArgs a, bool reverse, long keep_from) {
 #pragma unroll
   for (int e = 0; e < 4; ++e) kk[e] = kj[e] * kj[e];
 
-  const int i_base = (int)(row_base - bh * a.d_v);
 #pragma unroll
   for (int it = 0; it < NIT; ++it) {
     const long row = row_base + it * RPI + sub;
-    const size_t in_off = (size_t)bh * a.d_v + i_base + it * RPI + sub;
-    float b = load1<BF16>(a.beta, in_off);
-    const float vi = load1<BF16>(a.v, in_off);
-    if constexpr (PRO) b = bsc * sigmoid_f(b);
-    const float bv = (PRO && a.pro.v_star) ? vi : b * vi;
+    const float b = __shfl_sync(0xffffffffu, b_row, it * RPI + sub);
+    float bv;
+    if constexpr (PRO) bv = a.pro.v_star ? v_in[it] : b * v_in[it];
+    else bv = __shfl_sync(0xffffffffu, bv_row, it * RPI + sub);
     bad |= !nonneg_finite(b);
     float Io[4] = {I4[it].x, I4[it].y, I4[it].z, I4[it].w};
     float mo[4] = {mu4[it].x, mu4[it].y, mu4[it].z, mu4[it].w};
@@ -152,7 +175,9 @@ palimpsa_step_kernel(StepArgs a, bool reverse, long keep_from) {
     for (int e = 0; e < 4; ++e) {
       bad |= !pos_finite(Io[e]);
       In[e] = fmaf(al, Io[e], fmaf(b, kk[e], om));
-      mn[e] = fmaf(al * Io[e], mo[e], bv * kj[e]) / In[e];
+      const float num = fmaf(al * Io[e], mo[e], bv * kj[e]);
+      if constexpr (PRO) mn[e] = __fdividef(num, In[e]);
+      else mn[e] = num / In[e];
       yp = fmaf(mn[e], qj[e], yp);
     }
 #pragma unroll

@@ -390,3 +390,14 @@ def test_packed_checkpoint_slots_never_overlap():
             assert not (slots & used) and all(0 <= x < total // 32 + N for x in slots), (lengths, n)
             used |= slots
             s0 += L
+
+
+@pytest.mark.parametrize("over,code", [(dict(S=-1), ERR_SHAPE), (dict(flags=16), ERR_UNSUPPORTED),
+                                       (dict(q=None), ERR_NULL), (dict(b_scale=P + 2), ERR_ALIGN)])
+def test_step_sequence_fused_rejects_bad_arguments(lib, over, code):
+    a = dict(q=P, k=P, v=P, b=P, d=P, A=P, I_prior=P, b_scale=None, mu=P, I=P, y=P, S=4, B=4, H=2, d_k=128, d_v=64,
+             flags=1, dtype=1)
+    a.update(over)
+    assert lib.palimpsa_step_sequence_fused(
+        a["q"], a["k"], a["v"], a["b"], a["d"], a["A"], a["I_prior"], a["b_scale"], a["mu"], a["I"], a["y"], a["S"],
+        a["B"], a["H"], a["d_k"], a["d_v"], a["flags"], a["dtype"], None) == code

@@ -162,3 +162,24 @@ def test_negative_b_scale_is_reported_not_faulted():
     # the context stays usable
     out = _gpu_fused(inp, qk_norm=True)
     _check(out, _oracle(inp, qk_norm=True))
+
+
+@pytest.mark.parametrize("flags", FLAG_SETS, ids=["plain", "qknorm", "vstar", "qknorm_vstar"])
+def test_fused_step_sequence_equals_token_by_token_bitwise(flags):
+    """One palimpsa_step_sequence_fused call (4-D raw inputs) enqueues the same
+    launches as S palimpsa_step_fused calls: identical bits."""
+    wl = syn.WORKLOADS["decode"].with_(B=3, H=2, seed=515)
+    pre = syn.sequence_inputs(wl, T=1, raw=True)
+    steps = {n: t.to(DEV) for n, t in syn.decode_inputs(wl, 7, raw=True).items()}
+    A, Ip, bsc = pre["A"].to(DEV), pre["I_prior"].to(DEV), pre["b_scale"].to(DEV)
+    g = torch.Generator().manual_seed(516)
+    mu0 = torch.randn((3, 2, 64, 128), generator=g).to(DEV)
+    I0 = (0.5 + torch.rand((3, 2, 64, 128), generator=g)).to(DEV)
+    mu_a, I_a = mu0.clone(), I0.clone()
+    y_a = pal.palimpsa_step_fused(steps["q"], steps["k"], steps["v"], steps["beta_raw"], steps["d_raw"], A, Ip, mu_a,
+                                  I_a, bsc, **flags)
+    mu_b, I_b = mu0.clone(), I0.clone()
+    y_b = torch.stack([pal.palimpsa_step_fused(steps["q"][t], steps["k"][t], steps["v"][t], steps["beta_raw"][t],
+                                               steps["d_raw"][t], A, Ip, mu_b, I_b, bsc, **flags) for t in range(7)])
+    assert pal.palimpsa_get_device_status() == 0
+    assert torch.equal(y_a, y_b) and torch.equal(mu_a, mu_b) and torch.equal(I_a, I_b)
