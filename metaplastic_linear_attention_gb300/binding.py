@@ -313,15 +313,23 @@ def palimpsa_forward_varlen_fused(q, k, v, beta_raw, d_raw, A, I_prior, cu_seqle
                    (b_scale, _fuse_flags(qk_norm, v_star)))
 
 
-def _packed_offsets(cu_seqlens, max_seqlen, dev):
-    """(offsets on the device, N, max_seqlen) of a packed batch."""
+def _packed_offsets(cu_seqlens, max_seqlen, dev, stream=None):
+    """(offsets on the device, N, max_seqlen) of a packed batch. Host offsets are
+    copied on the stream the library will use, and the copy is recorded there so
+    that the allocator keeps it until that stream is done with it."""
     if cu_seqlens.dtype != torch.int32 or cu_seqlens.dim() != 1 or cu_seqlens.numel() < 2:
         raise ValueError("cu_seqlens must be a 1-D int32 tensor of N + 1 offsets")
     N = cu_seqlens.numel() - 1
     if max_seqlen is None:
         host = cu_seqlens.cpu()
         max_seqlen = int((host[1:] - host[:-1]).max())
-    cu_d = cu_seqlens if cu_seqlens.is_cuda else cu_seqlens.to(dev)
+    if cu_seqlens.is_cuda:
+        cu_d = cu_seqlens
+    else:
+        st = stream if stream is not None else torch.cuda.current_stream(dev)
+        with torch.cuda.stream(st):
+            cu_d = cu_seqlens.to(dev, non_blocking=False)
+        cu_d.record_stream(st)
     _check(cu_d, "cu_seqlens", (N + 1,), torch.int32, dev)
     return cu_d, N, int(max_seqlen)
 
@@ -334,7 +342,7 @@ def _varlen(q, k, v, beta, d_t, A, I_prior, cu_seqlens, mu0, I0, max_seqlen, y, 
     d_v = v.shape[-1]
     dev = q.device
     f32 = torch.float32
-    cu_d, N, max_seqlen = _packed_offsets(cu_seqlens, max_seqlen, dev)
+    cu_d, N, max_seqlen = _packed_offsets(cu_seqlens, max_seqlen, dev, stream)
     names = ("beta", "d_t") if fused is None else ("beta_raw", "d_raw")
     _check(k, "k", q.shape, q.dtype, dev)
     _check(q, "q", q.shape, None, dev)
@@ -603,7 +611,7 @@ def palimpsa_forward_varlen_checkpointed(q, k, v, beta, d_t, A, I_prior, cu_seql
     sequence n (from token s0) keeps its checkpoint c in slot s0//32 + n + c."""
     if q.device.type != "cuda":
         raise ValueError("the packed forward takes device tensors")
-    cu_d, N, max_seqlen = _packed_offsets(cu_seqlens, max_seqlen, q.device)
+    cu_d, N, max_seqlen = _packed_offsets(cu_seqlens, max_seqlen, q.device, stream)
     H, total_T, d_k = q.shape
     d_v = v.shape[-1]
     if ckpt is None:
@@ -629,7 +637,7 @@ def palimpsa_backward_varlen(q, k, v, beta, d_t, A, I_prior, cu_seqlens, mu0, I0
     d_v = v.shape[-1]
     dev = q.device
     f32 = torch.float32
-    cu_d, N, max_seqlen = _packed_offsets(cu_seqlens, max_seqlen, dev)
+    cu_d, N, max_seqlen = _packed_offsets(cu_seqlens, max_seqlen, dev, stream)
     _check(k, "k", q.shape, q.dtype, dev)
     _check(q, "q", q.shape, None, dev)
     _check(v, "v", (H, total_T, d_v), q.dtype, dev)
@@ -673,16 +681,19 @@ def palimpsa_step(q, k, v, beta, d_t, A, I_prior, mu, I, *, y=None, stream=None)
     if q.device.type == "cpu":
         # Host inputs: the state stays where it is when it is on the device (the
         # resident decode state); host state is copied in and back.
+        # Every copy and the step run on one stream, in order.
         dev = _compute_device(mu, I, y)
-        dq = _to_device([q, k, v, beta, d_t, A, I_prior, mu, I], dev)
-        ydev = y if (y is not None and y.is_cuda) else None
-        ry = palimpsa_step(*dq, y=ydev, stream=stream)
-        if not mu.is_cuda:
-            mu.copy_(dq[7], non_blocking=True)
-        if not I.is_cuda:
-            I.copy_(dq[8], non_blocking=True)
-        out = _deliver(y, ry)
-        (stream or torch.cuda.current_stream()).synchronize()
+        st = stream if stream is not None else torch.cuda.current_stream(dev)
+        with torch.cuda.device(dev), torch.cuda.stream(st):
+            dq = _to_device([q, k, v, beta, d_t, A, I_prior, mu, I], dev)
+            ydev = y if (y is not None and y.is_cuda) else None
+            ry = palimpsa_step(*dq, y=ydev, stream=st)
+            if not mu.is_cuda:
+                mu.copy_(dq[7], non_blocking=True)
+            if not I.is_cuda:
+                I.copy_(dq[8], non_blocking=True)
+            out = _deliver(y, ry)
+        st.synchronize()
         return out
 
     B, H, d_k = q.shape

@@ -712,3 +712,34 @@ def test_backward_full_size_small_layer_sampled_head():
         assert rel_l2(out[n][:, h:h + 1].cpu().numpy(), ref[m]) <= TIGHT, n
     for n, m in (("dA", "A"), ("dI_prior", "I_prior")):
         assert rel_l2(out[n][h:h + 1].cpu().numpy(), ref[m]) <= TIGHT, n
+
+
+def test_host_inputs_on_a_side_stream():
+    """Host inputs with a caller's stream: the copies in, the kernels and the
+    copies out all run on that stream, so the results equal the device path's."""
+    wl = syn.WORKLOADS["decode"].with_(B=4, H=3)
+    seq = syn.sequence_inputs(wl, T=1, seed=97)
+    tok = syn.decode_inputs(wl, 1, seed=97)
+    g = torch.Generator().manual_seed(98)
+    mu0 = torch.randn((4, 3, 64, 128), generator=g)
+    I0 = 0.5 + torch.rand((4, 3, 64, 128), generator=g)
+    args = [tok[n][0] for n in ("q", "k", "v", "beta", "d_t")] + [seq["A"], seq["I_prior"]]
+    mu_d, I_d = mu0.to(DEV), I0.to(DEV)
+    y_ref = pal.palimpsa_step(*[t.to(DEV) for t in args], mu_d, I_d).cpu()
+    side = torch.cuda.Stream()
+    mu_h, I_h = mu0.clone().pin_memory(), I0.clone().pin_memory()
+    y = pal.palimpsa_step(*[t.pin_memory() for t in args], mu_h, I_h, stream=side)
+    assert pal.palimpsa_get_device_status() == 0
+    assert torch.equal(y, y_ref) and torch.equal(mu_h, mu_d.cpu()) and torch.equal(I_h, I_d.cpu())
+
+    lengths = [50, 0, 77]
+    wlv = syn.WORKLOADS["small_layer"].with_(seed=99)
+    pk = syn.packed_inputs(wlv, lengths, H=2)
+    d = {n: t.to(DEV) for n, t in pk.items() if n != "cu_seqlens"}
+    ref = pal.palimpsa_forward_varlen(d["q"], d["k"], d["v"], d["beta"], d["d_t"], d["A"], d["I_prior"],
+                                      pk["cu_seqlens"].to(DEV))
+    out = pal.palimpsa_forward_varlen(d["q"], d["k"], d["v"], d["beta"], d["d_t"], d["A"], d["I_prior"],
+                                      pk["cu_seqlens"], max_seqlen=77, stream=side)
+    side.synchronize()
+    assert pal.palimpsa_get_device_status() == 0
+    assert all(torch.equal(a, b) for a, b in zip(out, ref))
