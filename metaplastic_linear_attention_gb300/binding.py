@@ -170,8 +170,15 @@ def palimpsa_set_step_l2_keep_bytes(nbytes: int) -> None:
 
 
 def _stream_handle(stream) -> int:
+    """The raw handle of the stream the library launches on. A caller's stream
+    other than the current one first waits for the current stream, where the
+    binding (and usually the caller) made the inputs and outputs."""
     if stream is None:
         stream = torch.cuda.current_stream()
+    else:
+        cur = torch.cuda.current_stream(stream.device)
+        if cur.cuda_stream != stream.cuda_stream:
+            stream.wait_stream(cur)
     return int(stream.cuda_stream)
 
 
