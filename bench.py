@@ -288,6 +288,11 @@ def run_ours(args, ws, rank, local):
         roofline = {"bound": "hbm", "kernel": "palimpsa_step", "achieved": ach, "peak": hbm_peak, "unit": "GB/s",
                     "frac": ach / hbm_peak, "traffic": traffic, "peak_source": f"{peak_kind} hbm_gbs",
                     "bytes_per_launch": db}
+        if traffic:
+            # DRAM's own rate over the step: the measured bytes per launch (less than the
+            # algorithmic ones, as consecutive steps hand rows over in L2) over the live time
+            roofline["dram_gbs"] = traffic / (dec_avg_ms / 1e3) / 1e9
+            roofline["dram_frac"] = roofline["dram_gbs"] / hbm_peak
     else:
         a = kernels["palimpsa_fwd_chunked"]["alu"]
         roofline = {"bound": "alu", "kernel": "palimpsa_fwd_chunked", "achieved": a["achieved"], "peak": alu_peak,
