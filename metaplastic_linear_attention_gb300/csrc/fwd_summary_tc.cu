@@ -131,11 +131,15 @@ __device__ __forceinline__ void tc_ld32(uint32_t taddr, float (&v)[32]) {
   for (int q = 0; q < 32; ++q) v[q] = __uint_as_float(r[q]);
 }
 
-// bf16 bits of x rounded to nearest even, and of the rounding remainder.
-__device__ __forceinline__ void split_bf16(float x, uint32_t& hi, uint32_t& lo) {
-  const __nv_bfloat16 h = __float2bfloat16_rn(x);
-  hi = __bfloat16_as_ushort(h);
-  lo = __bfloat16_as_ushort(__float2bfloat16_rn(x - __bfloat162float(h)));
+// Two fp32 values as packed bf16 pairs (x0 in the low half): each rounded to
+// nearest even, and the rounding remainders, rounded again. One paired
+// conversion per pair instead of one per value.
+__device__ __forceinline__ void split_bf16x2(float x0, float x1, uint32_t& hi, uint32_t& lo) {
+  const __nv_bfloat162 h = __floats2bfloat162_rn(x0, x1);
+  const float2 hf = __bfloat1622float2(h);
+  const __nv_bfloat162 l = __floats2bfloat162_rn(x0 - hf.x, x1 - hf.y);
+  hi = *reinterpret_cast<const uint32_t*>(&h);
+  lo = *reinterpret_cast<const uint32_t*>(&l);
 }
 
 // Thread 0: copy segment-local tokens [t0, t0 + tc) of k, v, beta into a raw stage.
@@ -160,17 +164,15 @@ __device__ __forceinline__ void build_key_tiles(const unsigned char* raw, unsign
     uint32_t kt[4], kh[4], kl[4];
 #pragma unroll
     for (int u = 0; u < 8; u += 2) {
-      uint32_t b[2], h[2], l[2];
+      uint32_t b[2];
 #pragma unroll
       for (int e = 0; e < 2; ++e) {
         const int t = 8 * g + u + e;
         b[e] = t < tc ? rk[t * kTcDK + j] : 0u;
-        const float kf = __uint_as_float(b[e] << 16);
-        split_bf16(kf * kf, h[e], l[e]);  // k^2 is exact in fp32 and in hi + lo
       }
+      const float k0 = __uint_as_float(b[0] << 16), k1 = __uint_as_float(b[1] << 16);
       kt[u / 2] = b[0] | (b[1] << 16);
-      kh[u / 2] = h[0] | (h[1] << 16);
-      kl[u / 2] = l[0] | (l[1] << 16);
+      split_bf16x2(k0 * k0, k1 * k1, kh[u / 2], kl[u / 2]);  // k^2 is exact in fp32 and in hi + lo
     }
     const uint32_t off = (uint32_t)((g >> 1) * L.a_tile) + kmajor_off(j, (g & 1) * 8);
     *reinterpret_cast<uint4*>(ob + L.kt + off) = make_uint4(kt[0], kt[1], kt[2], kt[3]);
@@ -195,26 +197,23 @@ __device__ __forceinline__ void build_row_tiles(const unsigned char* raw, unsign
     uint32_t xh[4], xl[4], yh[4], yl[4];
 #pragma unroll
     for (int u = 0; u < 8; u += 2) {
-      uint32_t h0[2], l0[2], h1[2], l1[2];
+      float x[2], y[2];
 #pragma unroll
       for (int e = 0; e < 2; ++e) {
         const int t = 8 * g + u + e;
-        float x = 0.f, y = 0.f;
+        x[e] = 0.f;
+        y[e] = 0.f;
         if (t < tc) {
           float b = __uint_as_float((uint32_t)rb[t * DV + i] << 16);
           const float v = __uint_as_float((uint32_t)rv[t * DV + i] << 16);
           if (pro.on) b = bsc * sigmoid_f(b);
           const float ws = wf[t] * ns[t];
-          y = ws * ns[t] * b;
-          x = pro.v_star ? ws * v : ws * b * v;
+          y[e] = ws * ns[t] * b;
+          x[e] = pro.v_star ? ws * v : ws * b * v;
         }
-        split_bf16(x, h0[e], l0[e]);
-        split_bf16(y, h1[e], l1[e]);
       }
-      xh[u / 2] = h0[0] | (h0[1] << 16);
-      xl[u / 2] = l0[0] | (l0[1] << 16);
-      yh[u / 2] = h1[0] | (h1[1] << 16);
-      yl[u / 2] = l1[0] | (l1[1] << 16);
+      split_bf16x2(x[0], x[1], xh[u / 2], xl[u / 2]);
+      split_bf16x2(y[0], y[1], yh[u / 2], yl[u / 2]);
     }
     const uint32_t off = (uint32_t)((g >> 1) * L.b_tile) + kmajor_off(i, (g & 1) * 8);
     *reinterpret_cast<uint4*>(ob + L.xh + off) = make_uint4(xh[0], xh[1], xh[2], xh[3]);
