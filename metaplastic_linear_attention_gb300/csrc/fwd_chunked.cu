@@ -94,6 +94,12 @@ palimpsa_fwd_chunked_kernel(FwdArgs a, int C, int nseg, int seg_len, const float
                          static_cast<const char*>(a.beta) + head_tok * DV * ES, C, tl.tb, tl.tn, DV, false);
   pipe.init(a.withhold_first_copy != 0);
 
+  // In a time split this kernel follows the carry kernel with programmatic
+  // dependent launch: the first chunks' copies above read only the caller's
+  // inputs; the carried state, and every write below, wait for the carry.
+  // (Launched normally, the wait returns at once.)
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+
   // ---- initial state: M = I0 (.) mu0, I = I0 for the first segment (defaults
   // mu0 = 0, I0 = I_prior); M = carried M, I = I_prior + carried Ibar otherwise.
   float2 Ist[R][2 * NV], Mst[R][2 * NV];
@@ -420,6 +426,10 @@ palimpsa_fwd_carry_kernel(FwdArgs a, int nseg, int seg_len, float* __restrict__ 
   float* init = seg_state + SplitScratch((long long)a.B * a.H, nseg, (long long)DVK).init + (size_t)bh * 2 * DVK;
   *reinterpret_cast<float4*>(init + e) = m;
   *reinterpret_cast<float4*>(init + DVK + e) = i0;
+  // the summaries come from pass A, which may still be running (programmatic
+  // dependent launch); pass C may be scheduled from here on
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   for (int s = 0; s < nb; ++s) {
     const float g = seg_gamma[(size_t)bh * (nseg - 1) + s];
     float* slot = seg_state + ((size_t)bh * (nseg - 1) + s) * 2 * DVK;
@@ -433,6 +443,25 @@ palimpsa_fwd_carry_kernel(FwdArgs a, int nseg, int seg_len, float* __restrict__ 
 }
 
 // ------------------------------------------------------------------ host side
+
+// A launch that may start while the kernel before it in the stream drains
+// (programmatic dependent launch); the kernel waits (griddepcontrol.wait)
+// before it reads what that kernel wrote.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_dependent(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                             Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, args...);
+}
 
 constexpr int kRowsPerThread = 2;
 
@@ -458,6 +487,11 @@ struct Kernels {
     cudaError_t e = cudaFuncSetAttribute(main_k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
     if (e != cudaSuccess) return e;
     if (nseg > 1 && (e = prefix(a, C, nseg, seg_len, scratch, s)) != cudaSuccess) return e;
+    if (nseg > 1) {
+      e = launch_dependent(main_k, dim3((unsigned)(heads * nseg * groups)), dim3(kThreads), sm, s, a, C, nseg,
+                           seg_len, (const float*)scratch);
+      return e != cudaSuccess ? e : cudaGetLastError();
+    }
     main_k<<<(unsigned)(heads * nseg * groups), kThreads, sm, s>>>(a, C, nseg, seg_len, scratch);
     return cudaGetLastError();
   }
@@ -470,8 +504,9 @@ struct Kernels {
     cudaError_t e = summaries(a, C, nseg - 1, seg_len, scratch, seg_gamma, s);
     if (e != cudaSuccess) return e;
     const long quads = heads * a.d_v * a.d_k / 4;
-    palimpsa_fwd_carry_kernel<<<(unsigned)((quads + 255) / 256), 256, 0, s>>>(a, nseg, seg_len, scratch, seg_gamma);
-    return cudaGetLastError();
+    e = launch_dependent(palimpsa_fwd_carry_kernel, dim3((unsigned)((quads + 255) / 256)), dim3(256), 0, s, a, nseg,
+                         seg_len, scratch, (const float*)seg_gamma);
+    return e != cudaSuccess ? e : cudaGetLastError();
   }
 
   // Pass A over segments 0 .. nseg - 1 of every head (summary slots [bh][seg]):
