@@ -79,8 +79,10 @@ palimpsa_fwd_chunked_kernel(FwdArgs a, int C, int nseg, int seg_len, const float
   float* qf = reinterpret_cast<float*>(smem + L.qf);
   float* bvf = reinterpret_cast<float*>(smem + L.bvf);
   float* bfv = reinterpret_cast<float*>(smem + L.bf);
-  float* alf = reinterpret_cast<float*>(smem + L.alf);
-  float* omf = reinterpret_cast<float*>(smem + L.omf);
+  // the chunk's gates as (alpha, (1 - alpha) I_prior) pairs, one load per token:
+  // they fill the alf and omf arrays, which are adjacent (C * 4 bytes each, a
+  // multiple of 16)
+  float2* gate = reinterpret_cast<float2*>(smem + L.alf);
 
   const float A_h = a.A[tl.h];
   const float Ip = a.I_prior[tl.h];
@@ -182,15 +184,15 @@ palimpsa_fwd_chunked_kernel(FwdArgs a, int C, int nseg, int seg_len, const float
       if (a.pro.on) d = softplus_f(d);
       domain_bad |= !nonneg_finite(d);
       const float x = -A_h * d;
-      alf[t] = expf(x);
-      omf[t] = -expm1f(x) * Ip;  // (1 - alpha) I_prior without cancellation
+      gate[t] = make_float2(expf(x), -expm1f(x) * Ip);  // (1 - alpha) I_prior without cancellation
     }
     __syncthreads();
     pipe.refill(c);
 
     // ---- the recurrence over the chunk's tokens, state in registers
     for (int t = 0; t < tc; ++t) {
-      const float2 a2 = f2(alf[t]), om2 = f2(omf[t]);
+      const float2 gt = gate[t];
+      const float2 a2 = f2(gt.x), om2 = f2(gt.y);
       float brow[R], bvrow[R];
       if constexpr (R == 2) {
         const float2 bb = *reinterpret_cast<const float2*>(bfv + t * RG + lr0);
@@ -226,16 +228,20 @@ palimpsa_fwd_chunked_kernel(FwdArgs a, int C, int nseg, int seg_len, const float
           }
         }
       }
-      float yv[R];
+      if constexpr (R == 2) {
+        // both rows' sums over the row's 8 lanes: the first level hands each half
+        // of the lanes one row (lane bit 2), the last two complete the sums
+        const float y0 = acc[0].x + acc[0].y, y1 = acc[1].x + acc[1].y;
+        const bool hi = (lane & 4) != 0;
+        float yk = (hi ? y1 : y0) + __shfl_xor_sync(0xffffffffu, hi ? y0 : y1, 4);
+        yk += __shfl_xor_sync(0xffffffffu, yk, 2);
+        yk += __shfl_xor_sync(0xffffffffu, yk, 1);
+        if ((cg & 3) == 0) gy[(size_t)(t0 + t) * DV + (cg >> 2)] = yk;
+      } else {
+        float yv = acc[0].x + acc[0].y;
 #pragma unroll
-      for (int r = 0; r < R; ++r) {
-        yv[r] = acc[r].x + acc[r].y;
-#pragma unroll
-        for (int m = 1; m < kLanesPerRow; m <<= 1) yv[r] += __shfl_xor_sync(0xffffffffu, yv[r], m);
-      }
-      if (cg == 0) {
-        if constexpr (R == 2) *reinterpret_cast<float2*>(gy + (size_t)(t0 + t) * DV) = make_float2(yv[0], yv[1]);
-        else gy[(size_t)(t0 + t) * DV] = yv[0];
+        for (int m = 1; m < kLanesPerRow; m <<= 1) yv += __shfl_xor_sync(0xffffffffu, yv, m);
+        if (cg == 0) gy[(size_t)(t0 + t) * DV] = yv;
       }
     }
     // (the barrier at the top of the next chunk orders these reads before the
