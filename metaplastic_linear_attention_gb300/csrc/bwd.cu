@@ -64,7 +64,7 @@ __host__ __device__ constexpr size_t al16(size_t x) { return (x + 15) / 16 * 16;
 // Shared-memory carve-up (byte offsets; every piece 16-byte aligned).
 struct BwdSmem {
   size_t k, q, v, b, dy, dt, stage;   // one staged segment (offsets inside a stage)
-  size_t kf, qf, win, rowp, adap, rb, rbv, al, om, oma, total;
+  size_t kf, qf, win, rowp, adap, rb, rbv, gate, total;
 
   __host__ __device__ BwdSmem(int DK, int ES) {
     size_t o = 0;
@@ -84,9 +84,7 @@ struct BwdSmem {
     adap = o;  o += (size_t)kWarps * kWin * 4 * 4;            // alpha-gradient partials [warp][token][row pair]
     rb = o;    o += (size_t)kSeg * kRowsPerCta * 4;           // beta_i of the segment's tokens [token][row]
     rbv = o;   o += (size_t)kSeg * kRowsPerCta * 4;           // beta_i v_i
-    al = o;    o += (size_t)kSeg * 4;                         // alpha of the segment's tokens
-    om = o;    o += (size_t)kSeg * 4;                         // (1 - alpha) I_prior
-    oma = o;   o += (size_t)kSeg * 4;                         // 1 - alpha
+    gate = o;  o += (size_t)kSeg * 16;                        // [token](alpha, (1 - alpha) I_prior, 1 - alpha, 0)
     total = (o + 127) / 128 * 128;
   }
 };
@@ -165,23 +163,19 @@ __device__ __forceinline__ void rs_level(float (&x)[V], int lane, int m) {
   }
 }
 
-// All threads, once per staged segment: the gate tables (alpha, (1 - alpha)
-// I_prior, 1 - alpha), the row tables (beta_i, beta_i v_i of the CTA's 8 rows)
+// All threads, once per staged segment: the gate table (alpha, (1 - alpha)
+// I_prior, 1 - alpha per token, one 16-byte load), the row tables (beta_i, beta_i v_i of the CTA's 8 rows)
 // and, for bf16 inputs, fp32 copies of k and q. Callers order this with
 // barriers on both sides.
 template <int DK, bool BF16>
 __device__ __forceinline__ void prepare_segment(const unsigned char* st, unsigned char* bsm, const BwdSmem& L, int tn,
                                                 float A_h, float Ip) {
   const float* dt = reinterpret_cast<const float*>(st + L.dt);
-  float* al = reinterpret_cast<float*>(bsm + L.al);
-  float* om = reinterpret_cast<float*>(bsm + L.om);
-  float* oma = reinterpret_cast<float*>(bsm + L.oma);
+  float4* gate = reinterpret_cast<float4*>(bsm + L.gate);
   for (int u = threadIdx.x; u < tn; u += kThreads) {
     const float x = -A_h * dt[u];
-    al[u] = expf(x);
     const float one_minus = -expm1f(x);  // 1 - alpha without cancellation
-    oma[u] = one_minus;
-    om[u] = one_minus * Ip;
+    gate[u] = make_float4(expf(x), one_minus * Ip, one_minus, 0.f);
   }
   float* rb = reinterpret_cast<float*>(bsm + L.rb);
   float* rbv = reinterpret_cast<float*>(bsm + L.rbv);
@@ -219,14 +213,16 @@ __device__ __forceinline__ void lane_pairs(const float* base, int DK, int u, int
 
 // Per-token scalars of the forward update for the lane's two value rows.
 struct Tok2 {
-  float alpha, om;
+  float alpha, om, oma;
   float2 b, bv;  // beta_i and beta_i v_i of rows 2g, 2g + 1
 };
 
 __device__ __forceinline__ Tok2 tok2(const unsigned char* bsm, const BwdSmem& L, int u, int g) {
   Tok2 t;
-  t.alpha = reinterpret_cast<const float*>(bsm + L.al)[u];
-  t.om = reinterpret_cast<const float*>(bsm + L.om)[u];
+  const float4 gv = reinterpret_cast<const float4*>(bsm + L.gate)[u];
+  t.alpha = gv.x;
+  t.om = gv.y;
+  t.oma = gv.z;
   t.b = reinterpret_cast<const float2*>(bsm + L.rb)[(u * kRowsPerCta) / 2 + g];
   t.bv = reinterpret_cast<const float2*>(bsm + L.rbv)[(u * kRowsPerCta) / 2 + g];
   return t;
@@ -306,7 +302,6 @@ palimpsa_bwd_kernel(BwdArgs a, float* __restrict__ ckpt) {
   };
   auto rowp = reinterpret_cast<float (*)[kWin][kRowsPerCta][2]>(bsm + L.rowp);
   auto adap = reinterpret_cast<float (*)[kWin][4]>(bsm + L.adap);
-  const float* oma = reinterpret_cast<const float*>(bsm + L.oma);
 
   const int DV = a.d_v;
   const int groups = DV / kRowsPerCta;
@@ -511,7 +506,7 @@ palimpsa_bwd_kernel(BwdArgs a, float* __restrict__ ckpt) {
         const float sg = (sgi[0].x + sgi[0].y) + (sgi[1].x + sgi[1].y);
         float ap = ((ada[0].x + ada[0].y) + (ada[1].x + ada[1].y)) -
                    (tr.bv.x * rv[0] + tr.bv.y * rv[1]) - (tr.b.x * rv[2] + tr.b.y * rv[3]) - Ip * sg;
-        dIp_acc = fmaf(oma[u], sg, dIp_acc);  // (1 - alpha) sum gI; reduced at the end
+        dIp_acc = fmaf(tr.oma, sg, dIp_acc);  // (1 - alpha) sum gI; reduced at the end
         rs_level<4, 4>(rv, lane, 4);
         rs_level<4, 2>(rv, lane, 2);
         rv[0] += __shfl_xor_sync(0xffffffffu, rv[0], 1);
