@@ -40,8 +40,8 @@ MUFU_RCP_PER_CLK_PER_SM = 16     # SFU reciprocal issue rate per SM (one per ele
 # (--cache-control none), as they run in the timed region: each step finds the rows the
 # previous one stored last still in L2.
 NCU_TRAFFIC = {
-    "palimpsa_step": {"bytes_per_launch": 925623259, "source": "csrc/step.cu",
-                      "sha256": "6bd53947955da4422faf8ba94c57a762570887a2cc437eec2fe4f70b9b74ee3f"},
+    "palimpsa_step": {"bytes_per_launch": 928755127, "source": "csrc/step.cu",
+                      "sha256": "34ad408d5a1022309f5b164ce25944375ba4fda52a6e92b51d0877381f9a4e56"},
 }
 
 

@@ -9,9 +9,11 @@
 // and I is read once and written once (16 bytes per element), against ~1 KB of
 // per-head inputs and outputs. It is therefore bound by HBM bandwidth, and the
 // kernel is built as a copy kernel with arithmetic in the middle:
-// * one warp owns 8 value rows of one head; a lane owns 4 consecutive key
-//   columns (one 16-byte vector of mu and one of I per row, d_k = 128) or two
-//   rows are interleaved per warp instruction (d_k = 64);
+// * a CTA is one warp (measured fastest against 2, 4 and 8 warps on GB300:
+//   CTAs start and retire independently) and owns 8 value rows of one head;
+//   a lane owns 4 consecutive key columns (one 16-byte vector of mu and one
+//   of I per row, d_k = 128) or two rows are interleaved per warp instruction
+//   (d_k = 64);
 // * all 16 state loads of a lane are issued before any arithmetic, so every
 //   SM keeps well over the ~45 KB in flight that 6.8 TB/s needs at ~1 us of
 //   latency; loads and most stores use the streaming (evict-first) cache
@@ -53,7 +55,7 @@ namespace palimpsa {
 namespace {
 
 constexpr int kRowsPerWarp = 8;
-constexpr int kWarpsPerBlock = 8;
+constexpr int kWarpsPerBlock = 1;
 
 template <bool BF16>
 __device__ __forceinline__ float4 load4(const void* base, size_t idx) {
