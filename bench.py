@@ -41,7 +41,7 @@ MUFU_RCP_PER_CLK_PER_SM = 16     # SFU reciprocal issue rate per SM (one per ele
 # previous one stored last still in L2.
 NCU_TRAFFIC = {
     "palimpsa_step": {"bytes_per_launch": 928755127, "source": "csrc/step.cu",
-                      "sha256": "34ad408d5a1022309f5b164ce25944375ba4fda52a6e92b51d0877381f9a4e56"},
+                      "sha256": "a99e48cc88dad37e653c648b985da9e595766bb149603d3a12dfc0fe1c5e09b3"},
 }
 
 

@@ -114,9 +114,9 @@ palimpsa_step_kernel(StepArgs a, bool reverse, long keep_from) {
   const int sub = lane / LPR;
   const int col = 4 * (lane % LPR);
 
-  // ... then the rows' beta and v: lane r (r < 8) takes row r's, forms the
-  // row's gate values once for the warp (through the prologue when it is on),
-  // and the row loop reads them back by shuffle.
+  // The rows' beta and v: lane r (r < 8) takes row r's, forms the row's gate
+  // values once for the warp (through the prologue when it is on), and the
+  // row loop reads them back by shuffle.
   // (With the prologue each lane still loads v for every row: on GB300 that
   // measured faster than shuffling beta_i v_i, which would wait on the gate.)
   const int i_base = (int)(row_base - bh * a.d_v);
