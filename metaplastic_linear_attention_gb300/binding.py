@@ -681,8 +681,8 @@ def palimpsa_step(q, k, v, beta, d_t, A, I_prior, mu, I, *, y=None, stream=None)
 
     One token: q, k [B,H,d_k], v, beta [B,H,d_v], d_t [B,H] -> y [B,H,d_v].
     A sequence of S tokens: a leading steps dimension on q, k, v, beta, d_t
-    -> y [S,B,H,d_v]; each token is one palimpsa_step call, in order.
-    """
+    -> y [S,B,H,d_v]; the tokens go in order, enqueued by one palimpsa_step_sequence
+    call (device inputs) or by blocks of tokens streamed from the host (host inputs)."""
     if q.dim() == 4:
         return _step_sequence(q, k, v, beta, d_t, A, I_prior, mu, I, y, stream)
     if q.device.type == "cpu":
