@@ -37,9 +37,10 @@
 // elements of a one-row lane. Column sums (dq, dk) finish over the four row
 // pairs of a warp with a reduce-scatter and go to fp32 atomics (the d_v / 8
 // CTAs of a head add into the same dq, dk; the library zeroes them first). Row
-// sums (d(bv), sum gI k^2) and the alpha partial finish over the 8 column
-// lanes with shuffles and over the 4 warps through shared memory once per
-// 8-token window.
+// sums (d(bv), sum gI k^2) finish over the 8 column lanes with shuffles and
+// over the 4 warps through shared memory once per 8-token window; the alpha
+// partial of every lane goes to shared memory as it is and is summed over the
+// CTA's 128 lanes once per window.
 //
 // Staging: every operand a segment needs (q, k and the CTA's 8 rows of v, beta,
 // dy, plus d_t) is copied into shared memory once per CTA with cp.async, into
@@ -81,7 +82,7 @@ struct BwdSmem {
     qf = o;    o += ES == 2 ? (size_t)kSeg * DK * 4 : 0;
     win = o;   o += (size_t)2 * kRowsPerCta * kNW * DK * 4;   // window starts [window][M | I][row][pair][thread]
     rowp = o;  o += (size_t)kWarps * kWin * kRowsPerCta * 2 * 4;  // row-sum partials [warp][token][row][2]
-    adap = o;  o += (size_t)kWarps * kWin * 4 * 4;            // alpha-gradient partials [warp][token][row pair]
+    adap = o;  o += (size_t)kWin * kThreads * 4;              // alpha-gradient partials [token][thread]
     rb = o;    o += (size_t)kSeg * kRowsPerCta * 4;           // beta_i of the segment's tokens [token][row]
     rbv = o;   o += (size_t)kSeg * kRowsPerCta * 4;           // beta_i v_i
     gate = o;  o += (size_t)kSeg * 16;                        // [token](alpha, (1 - alpha) I_prior, 1 - alpha, 0)
@@ -301,7 +302,7 @@ palimpsa_bwd_kernel(BwdArgs a, float* __restrict__ ckpt) {
     return winS[(((wi * 2 + mi) * 2 + r) * NP + p) * kThreads + threadIdx.x];
   };
   auto rowp = reinterpret_cast<float (*)[kWin][kRowsPerCta][2]>(bsm + L.rowp);
-  auto adap = reinterpret_cast<float (*)[kWin][4]>(bsm + L.adap);
+  auto adap = reinterpret_cast<float (*)[kThreads]>(bsm + L.adap);
 
   const int DV = a.d_v;
   const int groups = DV / kRowsPerCta;
@@ -510,13 +511,11 @@ palimpsa_bwd_kernel(BwdArgs a, float* __restrict__ ckpt) {
         rs_level<4, 4>(rv, lane, 4);
         rs_level<4, 2>(rv, lane, 2);
         rv[0] += __shfl_xor_sync(0xffffffffu, rv[0], 1);
-#pragma unroll
-        for (int m = 1; m <= 4; m <<= 1) ap += __shfl_xor_sync(0xffffffffu, ap, m);
         if ((lane & 1) == 0) {
           const int o = (lane >> 1) & 3;   // row 2g + (o & 1); d(bv) for o < 2, else sum gI k^2
           rowp[w][uu][2 * g + (o & 1)][o >> 1] = rv[0];
         }
-        if ((lane & 7) == 0) adap[w][uu][g] = ap;
+        adap[uu][threadIdx.x] = ap;  // summed once per window
         // carry the adjoints to t - 1
         const float2 a2 = f2(tr.alpha);
 #pragma unroll
@@ -552,15 +551,21 @@ palimpsa_bwd_kernel(BwdArgs a, float* __restrict__ ckpt) {
         a.dv[o] = s_bv * row_val<BF16>(st + L.b, u, r);
         a.dbeta[o] = fmaf(s_bv, row_val<BF16>(st + L.v, u, r), s_b);
       }
-      if (threadIdx.x < n) {
-        const int uu = threadIdx.x, u = uw + uu;
-        float ad = 0.f;  // alpha_t dL/dalpha_t over the CTA's rows
+      {  // alpha_t dL/dalpha_t of each token: its 128 lane partials, 16 threads a token
+        const int uu = threadIdx.x >> 4, part = threadIdx.x & 15;
+        float ad = 0.f;
+        if (uu < n) {
+          const float4* src = reinterpret_cast<const float4*>(&adap[uu][part * 8]);
+          const float4 p0 = src[0], p1 = src[1];
+          ad = ((p0.x + p0.y) + (p0.z + p0.w)) + ((p1.x + p1.y) + (p1.z + p1.w));
+        }
 #pragma unroll
-        for (int ww = 0; ww < kWarps; ++ww)
-#pragma unroll
-          for (int gg = 0; gg < 4; ++gg) ad += adap[ww][uu][gg];
-        atomicAdd(a.dd_t + head_tok + ts + u, -A_h * ad);
-        dA_acc = fmaf(-dts[u], ad, dA_acc);
+        for (int m = 8; m >= 1; m >>= 1) ad += __shfl_xor_sync(0xffffffffu, ad, m);
+        if (part == 0 && uu < n) {
+          const int u = uw + uu;
+          atomicAdd(a.dd_t + head_tok + ts + u, -A_h * ad);
+          dA_acc = fmaf(-dts[u], ad, dA_acc);
+        }
       }
       __syncthreads();  // the row partials are free for the next window
     }
@@ -587,10 +592,8 @@ palimpsa_bwd_kernel(BwdArgs a, float* __restrict__ ckpt) {
   if (!a.I0) dIp_acc += s_ip0;
   dIp_acc = warp_sum(dIp_acc);
   if (lane == 0) atomicAdd(a.dI_prior + h, dIp_acc);
-  if (w == 0) {  // threads 0 .. kWin - 1 hold the dA partials of their token slots
-    dA_acc = warp_sum(dA_acc);
-    if (lane == 0) atomicAdd(a.dA + h, dA_acc);
-  }
+  dA_acc = warp_sum(dA_acc);  // threads 16 u hold the dA partials of token slot u
+  if (lane == 0) atomicAdd(a.dA + h, dA_acc);
 }
 
 }  // namespace
