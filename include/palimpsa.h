@@ -294,6 +294,14 @@ palimpsa_status palimpsa_forward_varlen_fused(
  *   I_prior  [H]             fp32, > 0
  *   mu, I    [B, H, d_v, d_k] fp32 state, updated in place (I > 0)
  *   y        [B, H, d_v]     fp32 output (must not overlap the state)
+ *
+ * Launch: the step goes out with programmatic dependent launch. It may start
+ * while the kernel before it in the stream finishes, and waits for that kernel
+ * before its first read. It lets the next kernel in the stream start early, so
+ * a kernel launched after it with the programmatic-serialization attribute
+ * must wait (cudaGridDependencySynchronize / griddepcontrol.wait) before it
+ * reads y or the state; kernels launched normally, copies and events are
+ * ordered as usual.
  */
 palimpsa_status palimpsa_step(
     const void* q, const void* k, const void* v, const void* beta,
