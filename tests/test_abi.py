@@ -401,3 +401,13 @@ def test_step_sequence_fused_rejects_bad_arguments(lib, over, code):
     assert lib.palimpsa_step_sequence_fused(
         a["q"], a["k"], a["v"], a["b"], a["d"], a["A"], a["I_prior"], a["b_scale"], a["mu"], a["I"], a["y"], a["S"],
         a["B"], a["H"], a["d_k"], a["d_v"], a["flags"], a["dtype"], None) == code
+
+
+def test_packed_checkpoint_shape_matches_the_library_size(lib):
+    # the binding allocates packed checkpoints from packed_checkpoint_shape; the
+    # library sizes them with palimpsa_checkpoint_bytes_varlen: the two must agree
+    import math
+    for N, H, total_T, d_k, d_v in ((1, 1, 0, 64, 8), (5, 16, 2048, 128, 64), (7, 3, 1001, 64, 40),
+                                    (64, 32, 131072, 128, 64)):
+        shape = pal.packed_checkpoint_shape(N, H, total_T, d_k, d_v)
+        assert math.prod(shape) * 4 == pal.palimpsa_checkpoint_bytes_varlen(N, H, total_T, d_k, d_v)
