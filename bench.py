@@ -30,11 +30,12 @@ sys.path.insert(0, ROOT)
 METRIC = "Palimpsa scan throughput (B·H·T tokens/s) and % of GB300 HBM roofline"
 UNIT = "head-tokens/s"
 FALLBACK_HBM_GBS = 6800.0
-SM_COUNT_GB300 = 152
-MUFU_RCP_PER_CLK_PER_SM = 16     # SFU reciprocal issue rate per SM (one per element-token)
+# The ALU-bound kernels (chunked forward, backward) spend one SFU reciprocal per
+# element-token; their roofline is the reciprocal rate per clock and SM, measured
+# live by the library's issue-rate probe, x the SM count x the maximum SM clock.
 
 # DRAM bytes per launch (dram__bytes_read.sum + dram__bytes_write.sum) of a kernel from one ncu
-# capture at the bench's full size (profiles/launches_decode_B256_H32.md), valid only while the
+# capture, valid only while the
 # kernel's source file is byte-identical to the one captured (sha256 below); otherwise null.
 # The decode step's figure is the mean of consecutive steps captured without cache flushes
 # (--cache-control none), as they run in the timed region: each step finds the rows the
@@ -138,6 +139,54 @@ class ClockSampler:
 
 # ----------------------------------------------------------------------------- multi-rank host logic
 
+def _free_port() -> int:
+    import socket
+    with socket.socket() as sk:
+        sk.bind(("127.0.0.1", 0))
+        return sk.getsockname()[1]
+
+
+def _rank_bootstrap(rank, n, port, target, args):
+    """Entry of one spawned rank: the environment torchrun would give it, then the target."""
+    os.environ.update(RANK=str(rank), LOCAL_RANK=str(rank), WORLD_SIZE=str(n), LOCAL_WORLD_SIZE=str(n),
+                      MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port))
+    target(*args)
+
+
+def spawn_ranks(n: int, target, args=(), poll_s: float = 0.2):
+    """Run target(*args) as n local ranks, one process each (rank r on GPU r), with
+    RANK, LOCAL_RANK, WORLD_SIZE and MASTER_ADDR/MASTER_PORT (127.0.0.1, a free port)
+    set as torchrun sets them. Processes start with the spawn method, so none
+    inherits a CUDA context. Waits for all of them; if one fails, the others are
+    stopped (they could otherwise wait forever at a barrier) and SystemExit is
+    raised naming the failed ranks."""
+    import multiprocessing as mp
+    ctx = mp.get_context("spawn")
+    port = _free_port()
+    procs = [ctx.Process(target=_rank_bootstrap, args=(r, n, port, target, tuple(args))) for r in range(n)]
+    for pr in procs:
+        pr.start()
+    failed = []
+    while True:
+        alive = [pr for pr in procs if pr.exitcode is None]
+        failed = [r for r, pr in enumerate(procs) if pr.exitcode not in (None, 0)]
+        if failed or not alive:
+            break
+        alive[0].join(poll_s)
+    if failed:
+        for pr in procs:
+            if pr.exitcode is None:
+                pr.terminate()
+        for pr in procs:
+            pr.join()
+        raise SystemExit(f"bench: rank(s) {failed} of {n} failed "
+                         f"(exit codes {[procs[r].exitcode for r in failed]})")
+
+
+def _run_rank(argv):
+    main(argv)
+
+
 def replica_seed(base_seed: int, rank: int) -> int:
     """Each rank runs an independent replica of the workload (weak scaling): its own inputs."""
     return base_seed + 1000 * rank
@@ -193,6 +242,7 @@ def run_ours(args, ws, rank, local):
         dist.init_process_group("nccl", device_id=dev)
     build_lib.build()
     pal.load_library()
+    rates = issue_rates(pal)
     wl = _workload(args)
     seed = replica_seed(wl.seed, rank)
     inp = syn.sequence_inputs(wl, device=dev, seed=seed)
@@ -268,7 +318,9 @@ def run_ours(args, ws, rank, local):
     fb = forward_bytes(B, H, T, dk, dv, in_bytes)
     E_fwd = B * H * T * dv * dk
     sm_max = float(peaks.get("sm_max_mhz", 2070.0))
-    alu_peak = SM_COUNT_GB300 * MUFU_RCP_PER_CLK_PER_SM * sm_max * 1e6 / 1e9   # G element-updates/s
+    n_sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    rcp_rate = rates["rcp"]
+    alu_peak = n_sms * rcp_rate * sm_max * 1e6 / 1e9   # G element-updates/s
     kernels["palimpsa_fwd_chunked"] = {
         "launches_per_step": 1, "avg_ms": fwd_avg_ms,
         "head_tokens_per_s": B * H * T / (fwd_avg_ms / 1e3),
@@ -297,7 +349,8 @@ def run_ours(args, ws, rank, local):
         a = kernels["palimpsa_fwd_chunked"]["alu"]
         roofline = {"bound": "alu", "kernel": "palimpsa_fwd_chunked", "achieved": a["achieved"], "peak": alu_peak,
                     "unit": "G element-updates/s", "frac": a["frac"], "traffic": args.traffic,
-                    "peak_source": f"{SM_COUNT_GB300} SMs x {MUFU_RCP_PER_CLK_PER_SM} rcp/clk x {sm_max:.0f} MHz"}
+                    "peak_source": f"{n_sms} SMs x {rcp_rate:.2f} rcp/clk/SM (measured by palimpsa_probe_issue_rate) "
+                                   f"x {sm_max:.0f} MHz"}
 
     # The "without Meta" comparator (importance frozen at I_prior) on the same scan
     # inputs, timed outside the timed region: what metaplasticity costs here.
@@ -480,10 +533,35 @@ def run_ours(args, ws, rank, local):
                        "parallelism": f"replicas x{ws}" if ws > 1 else "single GPU"},
             "roofline": roofline, "kernels": kernels, "cpu_baseline": cpu, "e2e": e2e,
             "gpu_launches": (fwd_launches + S) * args.steps, "clocks": clocks,
+            "issue_rates_per_clk_per_sm": rates,
         }
         print(json.dumps(line), flush=True)
     if ws > 1:
         dist.destroy_process_group()
+
+
+def issue_rates(pal):
+    """Instructions per clock and SM of the SFU reciprocal, the SFU 2^x and the FP32 FMA,
+    measured on this GPU by the library's probe (one CTA per SM, SM cycle counter)."""
+    return {op: pal.palimpsa_probe_issue_rate(op) for op in ("rcp", "ex2", "ffma")}
+
+
+def run_probe_rates(local):
+    import torch
+
+    import metaplastic_linear_attention_gb300 as pal
+    from metaplastic_linear_attention_gb300 import build_lib
+    torch.cuda.set_device(local)
+    build_lib.build()
+    pal.load_library()
+    props = torch.cuda.get_device_properties(local)
+    peaks, kind = _measured_peaks()
+    reps = [issue_rates(pal) for _ in range(5)]
+    med = {op: statistics.median(r[op] for r in reps) for op in reps[0]}
+    sm_max = float(peaks.get("sm_max_mhz", 2070.0))
+    print(json.dumps({"gpu": props.name, "sms": props.multi_processor_count, "per_clk_per_sm_runs": reps,
+                      "per_clk_per_sm_median": med, "sm_max_mhz": sm_max,
+                      "rcp_peak_G_per_s": props.multi_processor_count * med["rcp"] * sm_max / 1e3}), flush=True)
 
 
 def _workload(args):
@@ -614,7 +692,7 @@ def run_reference(args, ws, rank):
     print(json.dumps(line), flush=True)
 
 
-def main():
+def main(argv=None):
     p = argparse.ArgumentParser(description=__doc__.split("\n\n")[0])
     p.add_argument("--gpus", type=int, default=1)
     p.add_argument("--steps", type=int, default=5)
@@ -630,15 +708,35 @@ def main():
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--cpu-seconds", type=float, default=12.0, help="target oracle time for cpu_baseline")
     p.add_argument("--ref-step-seconds", type=float, default=4.0)
+    p.add_argument("--probe-rates", action="store_true",
+                   help="only measure the SFU / FMA issue rates per clock and SM, print them and exit")
     p.add_argument("--traffic", type=float, default=None,
                    help="DRAM bytes per launch of the dominant kernel from an ncu capture (else null)")
-    args = p.parse_args()
+    args = p.parse_args(argv)
     if args.warmup < 3:
         p.error("--warmup must be >= 3")
-    ws, rank, local = _dist_env()
-    if args.impl == "reference":
-        run_reference(args, ws, rank)
+    if args.gpus < 1:
+        p.error("--gpus must be >= 1")
+    launched = "WORLD_SIZE" in os.environ
+    if launched and int(os.environ["WORLD_SIZE"]) != args.gpus:
+        p.error(f"--gpus {args.gpus} disagrees with WORLD_SIZE={os.environ['WORLD_SIZE']} set by the launcher")
+    if args.probe_rates:
+        run_probe_rates(_dist_env()[2])
         return
+    if args.impl == "reference":
+        # the CPU oracle: rank 0 alone does the work (in this process when no launcher started ranks)
+        ws, rank, _ = _dist_env()
+        run_reference(args, args.gpus, rank)
+        return
+    if not launched and args.gpus > 1:
+        # no launcher: start one rank per GPU here, each an independent replica
+        import torch
+        have = torch.cuda.device_count()
+        if have < args.gpus:
+            raise SystemExit(f"bench: --gpus {args.gpus} needs {args.gpus} visible GPUs, found {have}")
+        spawn_ranks(args.gpus, _run_rank, (list(argv) if argv is not None else sys.argv[1:],))
+        return
+    ws, rank, local = _dist_env()
     run_ours(args, ws, rank, local)
 
 

@@ -1,7 +1,8 @@
 """Host logic of the multi-GPU benchmark path, run as world_size-2 gloo ranks on CPU.
 
 The path shards by independent heads: every rank runs its own replica (no data-path
-collective); only the timing is combined, as the max over ranks."""
+collective); only the timing is combined, as the max over ranks. Without a launcher,
+``bench.py --gpus N`` starts the N ranks itself (``bench.spawn_ranks``)."""
 import os
 import socket
 
@@ -49,3 +50,51 @@ def test_single_rank_helpers():
     assert bench.max_over_ranks(3.5, 1) == 3.5
     assert bench.whole_job_rate(12_582_912, 1, 0.18) == pytest.approx(12_582_912 / 0.18)
     assert bench.replica_seed(5, 0) == 5
+
+
+def _launched_rank(out_dir):
+    """A rank started by bench.spawn_ranks: the environment torchrun would set, a gloo
+    group built from it, and the benchmark's cross-rank timing."""
+    ws, rank, local = bench._dist_env()
+    assert os.environ["MASTER_ADDR"] == "127.0.0.1" and local == rank
+    dist.init_process_group("gloo")
+    try:
+        assert dist.get_world_size() == ws and dist.get_rank() == rank
+        worst = bench.max_over_ranks(20.0 + rank, ws)
+        with open(os.path.join(out_dir, f"rank{rank}.txt"), "w") as f:
+            f.write(f"{ws} {rank} {worst}")
+    finally:
+        dist.destroy_process_group()
+
+
+def _failing_rank(out_dir):
+    """Rank 1 fails before the group forms; rank 0 would wait for it at the rendezvous."""
+    ws, rank, _ = bench._dist_env()
+    if rank == 1:
+        raise RuntimeError("injected rank failure")
+    dist.init_process_group("gloo")
+    dist.destroy_process_group()
+
+
+def test_spawned_ranks_get_the_launcher_environment_and_time_as_the_slowest(tmp_path):
+    bench.spawn_ranks(2, _launched_rank, (str(tmp_path),))
+    got = sorted(open(tmp_path / f"rank{r}.txt").read().split() for r in range(2))
+    assert got == [["2", "0", "21.0"], ["2", "1", "21.0"]]
+
+
+def test_a_failed_spawned_rank_stops_the_others_and_fails_the_run(tmp_path):
+    with pytest.raises(SystemExit, match=r"rank\(s\) \[1\] of 2 failed"):
+        bench.spawn_ranks(2, _failing_rank, (str(tmp_path),))
+
+
+def test_gpus_beyond_the_visible_devices_fail_loudly(monkeypatch):
+    monkeypatch.delenv("WORLD_SIZE", raising=False)
+    monkeypatch.setattr(torch.cuda, "device_count", lambda: 1)
+    with pytest.raises(SystemExit, match="needs 4 visible GPUs, found 1"):
+        bench.main(["--gpus", "4"])
+
+
+def test_gpus_must_agree_with_the_launcher(monkeypatch):
+    monkeypatch.setenv("WORLD_SIZE", "2")
+    with pytest.raises(SystemExit):
+        bench.main(["--gpus", "4"])
