@@ -24,6 +24,8 @@
  * ---------------------------------------
  * - Memory: every array argument is a DEVICE pointer owned by the caller;
  *   nothing is copied, retained or freed. All arrays are dense row-major.
+ *   The library's own working memory is described under "Scratch memory"
+ *   near the end of this header.
  * - Alignment: every array pointer must be 16-byte aligned, except d_t, A and
  *   I_prior (4-byte aligned). Misaligned pointers give PALIMPSA_ERR_ALIGN.
  * - Sizes: 1 <= B, H; d_k in {64, 128}; d_v a multiple of 8 in [8, 256].
@@ -107,7 +109,10 @@ typedef enum {
  *            overlap between inputs and outputs is undefined.
  *   T >= 0. T = 0 copies the initial state to (mu_T, I_T); q, k, v, beta,
  *            d_t and y are then not read and may be NULL.
- *   chunk    0 (library default) or one of {16, 32, 64}.
+ *   chunk    0 (library default) or one of {16, 32, 64, 128} tokens. The
+ *            result does not depend on it: it only sets the staging
+ *            granularity, and the kernels stage at most 32 tokens at a
+ *            time, so 64 and 128 are staged as 32-token chunks.
  */
 palimpsa_status palimpsa_forward_chunked(
     const void* q, const void* k, const void* v, const void* beta,
@@ -595,6 +600,63 @@ void palimpsa_set_forward_segments(int segments);
  * bits either way; only the DRAM traffic changes.
  */
 void palimpsa_set_step_l2_keep_bytes(long long bytes);
+
+/*
+ * Scratch memory. The time-split forward and the backward need device scratch
+ * for the length of one call (the segment states of the time split, the
+ * backward's 32-token state checkpoints). The library takes it in stream order
+ * from a memory pool of its own, one per device, created on the first call
+ * that needs scratch; it is freed in stream order when the call's work ends.
+ * Freed pages stay mapped for the next call, up to a retention bound, so that
+ * repeated calls do not pay to map fresh pages; at each synchronisation of the
+ * stream, an event or the device, the pool gives back to the driver whatever
+ * it holds above that bound. No other memory is kept between calls.
+ *
+ * palimpsa_set_scratch_retention — sets the retention bound, in bytes, of
+ *   every device's pool, existing and future (process-wide). Default 512 MiB:
+ *   well above the forward's time-split scratch at the layer sizes this
+ *   library is tuned on (64 to 132 MiB; the split is planned to fill a few
+ *   waves of CTAs, each of which carries 64 KiB of state at d_v = 64,
+ *   d_k = 128), so the forward keeps its pages, while a large backward's
+ *   scratch above the bound is given back. 0 keeps nothing mapped between
+ *   synchronisations. Returns PALIMPSA_ERR_CUDA if a pool refuses the bound.
+ * palimpsa_release_scratch — gives all freed scratch of the CURRENT device's
+ *   pool back to the driver now. It first synchronises the device (so that no
+ *   work in flight still uses the scratch), then trims the pool to zero. OK
+ *   when the library has no pool on this device; PALIMPSA_ERR_CUDA when the
+ *   synchronisation or the trim fails.
+ * palimpsa_scratch_reserved_bytes — the bytes the CURRENT device's pool holds
+ *   mapped (in use or kept), 0 without a pool. PALIMPSA_ERR_NULL for a NULL
+ *   `bytes`.
+ * These calls have no counterpart on the pages; they manage this library's
+ * own working memory.
+ */
+palimpsa_status palimpsa_set_scratch_retention(unsigned long long bytes);
+palimpsa_status palimpsa_release_scratch(void);
+palimpsa_status palimpsa_scratch_reserved_bytes(size_t* bytes);
+
+/*
+ * palimpsa_probe_issue_rate — measures how many instructions of one kind an SM
+ * of the current device completes per clock: the denominator of the roofline
+ * the ALU-bound kernels are reported against. The chunked forward and the
+ * backward spend one SFU reciprocal per element-token on the readout's M / I
+ * (slide 9; paper App. A.12), so their bound is PALIMPSA_PROBE_RCP's rate x
+ * SMs x clock. The probe runs one CTA per SM (32 warps, 8 independent chains
+ * of the instruction per thread), times it with the SM cycle counter and
+ * returns the median over SMs in *per_clk_per_sm. It is synchronous on
+ * `cuda_stream` (about a millisecond) and allocates a few bytes of device
+ * memory for the cycle counts.
+ *   op  PALIMPSA_PROBE_RCP (rcp.approx.ftz.f32), PALIMPSA_PROBE_EX2
+ *       (ex2.approx.ftz.f32) or PALIMPSA_PROBE_FFMA (fma.rn.f32).
+ * Errors: PALIMPSA_ERR_NULL, PALIMPSA_ERR_UNSUPPORTED (unknown op),
+ * PALIMPSA_ERR_CUDA. This call has no counterpart on the pages.
+ */
+typedef enum {
+  PALIMPSA_PROBE_RCP = 0,
+  PALIMPSA_PROBE_EX2 = 1,
+  PALIMPSA_PROBE_FFMA = 2
+} palimpsa_probe_op;
+palimpsa_status palimpsa_probe_issue_rate(int op, double* per_clk_per_sm, void* cuda_stream);
 
 #ifdef __cplusplus
 }

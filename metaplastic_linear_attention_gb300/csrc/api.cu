@@ -23,35 +23,50 @@ std::atomic<int> g_forward_segments{0};
 // Bytes of state each decode step leaves in L2 for the next one.
 std::atomic<long long> g_step_l2_keep_bytes{96ll << 20};
 
+// Bytes of freed scratch each device's pool keeps mapped between calls.
+std::atomic<unsigned long long> g_scratch_keep_bytes{512ull << 20};
+std::mutex g_pool_mu;
+cudaMemPool_t g_pools[kMaxDevices] = {};
+
 // The library's own stream-ordered memory pool on the current device, created
-// on first use. Its release threshold is unbounded, so memory freed by one
-// call stays mapped for the next instead of being returned to the driver at
-// every synchronisation (re-mapping fresh pages costs the time-split passes a
-// few percent); the pool holds at most the largest scratch any call needed.
+// on first use. Memory freed by one call stays mapped for the next, up to the
+// pool's release threshold (g_scratch_keep_bytes; 512 MiB by default): at the
+// next synchronisation the pool gives back what it holds above that. The
+// forward's time-split scratch (tens to a few hundred MiB) therefore stays
+// mapped from call to call (re-mapping fresh pages cost the time-split passes
+// a few percent), while a large backward's scratch goes back to the driver
+// once the caller synchronises.
 cudaError_t scratch_pool(cudaMemPool_t* out) {
-  static std::mutex mu;
-  static cudaMemPool_t pools[kMaxDevices] = {};
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
-  std::lock_guard<std::mutex> lock(mu);
-  if (!pools[dev]) {
+  std::lock_guard<std::mutex> lock(g_pool_mu);
+  if (!g_pools[dev]) {
     cudaMemPoolProps props = {};
     props.allocType = cudaMemAllocationTypePinned;
     props.location.type = cudaMemLocationTypeDevice;
     props.location.id = dev;
     cudaMemPool_t pool = nullptr;
     if ((e = cudaMemPoolCreate(&pool, &props)) != cudaSuccess) return e;
-    unsigned long long keep = ~0ull;
+    unsigned long long keep = g_scratch_keep_bytes.load();
     if ((e = cudaMemPoolSetAttribute(pool, cudaMemPoolAttrReleaseThreshold, &keep)) != cudaSuccess) {
       cudaMemPoolDestroy(pool);
       return e;
     }
-    pools[dev] = pool;
+    g_pools[dev] = pool;
   }
-  *out = pools[dev];
+  *out = g_pools[dev];
   return cudaSuccess;
+}
+
+// The current device's pool if one was created, else nullptr.
+palimpsa_status existing_pool(cudaMemPool_t* out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return PALIMPSA_ERR_CUDA;
+  std::lock_guard<std::mutex> lock(g_pool_mu);
+  *out = g_pools[dev];
+  return PALIMPSA_OK;
 }
 
 // Scratch from that pool, allocated and freed in stream order on the launch
@@ -84,6 +99,12 @@ palimpsa_status status_word(unsigned int** out) {
   return PALIMPSA_OK;
 }
 
+// The caller's chunk: 0 (library default) or one of 16, 32, 64, 128 tokens. The
+// result does not depend on it (slide 9: the chunk only sets how many tokens are
+// staged on chip at a time); the kernels stage at most 32 tokens per chunk, so
+// longer chunks are staged as 32-token chunks.
+bool chunk_ok(int c) { return c == 0 || c == 16 || c == 32 || c == 64 || c == 128; }
+
 bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
 
 bool supported_dims(int d_k, int d_v) {
@@ -114,7 +135,7 @@ palimpsa_status forward_impl(const void* q, const void* k, const void* v, const 
   if (in_dtype != PALIMPSA_F32 && in_dtype != PALIMPSA_BF16) return PALIMPSA_ERR_DTYPE;
   if (!sizes_ok(B, H, T, d_k, d_v)) return PALIMPSA_ERR_SHAPE;
   if (!supported_dims(d_k, d_v)) return PALIMPSA_ERR_UNSUPPORTED;
-  if (chunk != 0 && chunk != 16 && chunk != 32 && chunk != 64) return PALIMPSA_ERR_UNSUPPORTED;
+  if (!chunk_ok(chunk)) return PALIMPSA_ERR_UNSUPPORTED;
   const void* a16[] = {q, k, v, beta, y, mu_T, I_T, mu0, I0, ckpt};
   for (const void* p : a16)
     if (p && !aligned(p, 16)) return PALIMPSA_ERR_ALIGN;
@@ -222,7 +243,7 @@ palimpsa_status palimpsa_forward_plan(int B, int H, int T, int d_k, int d_v, int
   if (in_dtype != PALIMPSA_F32 && in_dtype != PALIMPSA_BF16) return PALIMPSA_ERR_DTYPE;
   if (!sizes_ok(B, H, T, d_k, d_v)) return PALIMPSA_ERR_SHAPE;
   if (!supported_dims(d_k, d_v)) return PALIMPSA_ERR_UNSUPPORTED;
-  if (chunk != 0 && chunk != 16 && chunk != 32 && chunk != 64) return PALIMPSA_ERR_UNSUPPORTED;
+  if (!chunk_ok(chunk)) return PALIMPSA_ERR_UNSUPPORTED;
   FwdArgs a{nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr,
             nullptr, B, H, T, d_k, d_v, chunk == 0 ? 32 : chunk, in_dtype == PALIMPSA_BF16, nullptr, 0, 0,
             g_forward_segments.load(), Prologue{}};
@@ -247,7 +268,7 @@ static palimpsa_status varlen_impl(const void* q, const void* k, const void* v, 
   if (total_T < 0 || max_seqlen < 0 || max_seqlen > total_T) return PALIMPSA_ERR_SHAPE;
   if (!sizes_ok(N, H, max_seqlen, d_k, d_v) || !sizes_ok(1, H, total_T, d_k, d_v)) return PALIMPSA_ERR_SHAPE;
   if (!supported_dims(d_k, d_v)) return PALIMPSA_ERR_UNSUPPORTED;
-  if (chunk != 0 && chunk != 16 && chunk != 32 && chunk != 64) return PALIMPSA_ERR_UNSUPPORTED;
+  if (!chunk_ok(chunk)) return PALIMPSA_ERR_UNSUPPORTED;
   const void* a16[] = {q, k, v, beta, y, mu_T, I_T, mu0, I0, ckpt};
   for (const void* p : a16)
     if (p && !aligned(p, 16)) return PALIMPSA_ERR_ALIGN;
@@ -308,7 +329,7 @@ palimpsa_status palimpsa_segment_summary(const void* q, const void* k, const voi
   if (in_dtype != PALIMPSA_F32 && in_dtype != PALIMPSA_BF16) return PALIMPSA_ERR_DTYPE;
   if (!sizes_ok(B, H, T, d_k, d_v)) return PALIMPSA_ERR_SHAPE;
   if (!supported_dims(d_k, d_v)) return PALIMPSA_ERR_UNSUPPORTED;
-  if (chunk != 0 && chunk != 16 && chunk != 32 && chunk != 64) return PALIMPSA_ERR_UNSUPPORTED;
+  if (!chunk_ok(chunk)) return PALIMPSA_ERR_UNSUPPORTED;
   const void* a16[] = {q, k, v, beta, summary};
   for (const void* p : a16)
     if (p && !aligned(p, 16)) return PALIMPSA_ERR_ALIGN;
@@ -376,7 +397,7 @@ palimpsa_status palimpsa_forward_without_meta(const void* q, const void* k, cons
   if (in_dtype != PALIMPSA_F32 && in_dtype != PALIMPSA_BF16) return PALIMPSA_ERR_DTYPE;
   if (!sizes_ok(B, H, T, d_k, d_v)) return PALIMPSA_ERR_SHAPE;
   if (!supported_dims(d_k, d_v)) return PALIMPSA_ERR_UNSUPPORTED;
-  if (chunk != 0 && chunk != 16 && chunk != 32 && chunk != 64) return PALIMPSA_ERR_UNSUPPORTED;
+  if (!chunk_ok(chunk)) return PALIMPSA_ERR_UNSUPPORTED;
   const void* a16[] = {q, k, v, beta, y, mu_T, mu0};
   for (const void* p : a16)
     if (p && !aligned(p, 16)) return PALIMPSA_ERR_ALIGN;
@@ -577,6 +598,40 @@ void palimpsa_set_forward_segments(int segments) { g_forward_segments.store(segm
 
 void palimpsa_set_step_l2_keep_bytes(long long bytes) { g_step_l2_keep_bytes.store(bytes > 0 ? bytes : 0); }
 
+palimpsa_status palimpsa_set_scratch_retention(unsigned long long bytes) {
+  g_scratch_keep_bytes.store(bytes);
+  std::lock_guard<std::mutex> lock(g_pool_mu);
+  for (cudaMemPool_t pool : g_pools) {
+    if (!pool) continue;
+    unsigned long long keep = bytes;
+    if (cudaMemPoolSetAttribute(pool, cudaMemPoolAttrReleaseThreshold, &keep) != cudaSuccess) return PALIMPSA_ERR_CUDA;
+  }
+  return PALIMPSA_OK;
+}
+
+palimpsa_status palimpsa_release_scratch(void) {
+  cudaMemPool_t pool = nullptr;
+  if (palimpsa_status s = existing_pool(&pool)) return s;
+  if (!pool) return PALIMPSA_OK;
+  // every call's scratch is freed in stream order; once the device is idle
+  // none of it backs work in flight and all of it can go
+  if (cudaDeviceSynchronize() != cudaSuccess) return PALIMPSA_ERR_CUDA;
+  if (cudaMemPoolTrimTo(pool, 0) != cudaSuccess) return PALIMPSA_ERR_CUDA;
+  return PALIMPSA_OK;
+}
+
+palimpsa_status palimpsa_scratch_reserved_bytes(size_t* bytes) {
+  if (!bytes) return PALIMPSA_ERR_NULL;
+  *bytes = 0;
+  cudaMemPool_t pool = nullptr;
+  if (palimpsa_status s = existing_pool(&pool)) return s;
+  if (!pool) return PALIMPSA_OK;
+  unsigned long long v = 0;  // cuuint64_t
+  if (cudaMemPoolGetAttribute(pool, cudaMemPoolAttrReservedMemCurrent, &v) != cudaSuccess) return PALIMPSA_ERR_CUDA;
+  *bytes = (size_t)v;
+  return PALIMPSA_OK;
+}
+
 }  // extern "C"
 
 // ---------------------------------------------------------------------------
@@ -639,7 +694,7 @@ extern "C" palimpsa_status palimpsa_forward_chunked_noalloc(
   if (in_dtype != PALIMPSA_F32 && in_dtype != PALIMPSA_BF16) return PALIMPSA_ERR_DTYPE;
   if (!sizes_ok(B, H, T, d_k, d_v)) return PALIMPSA_ERR_SHAPE;
   if (!supported_dims(d_k, d_v)) return PALIMPSA_ERR_UNSUPPORTED;
-  if (chunk != 0 && chunk != 16 && chunk != 32 && chunk != 64) return PALIMPSA_ERR_UNSUPPORTED;
+  if (!chunk_ok(chunk)) return PALIMPSA_ERR_UNSUPPORTED;
   const void* a16[] = {q, k, v, beta, y, mu_T, I_T, mu0, I0};
   for (const void* p : a16)
     if (p && !aligned(p, 16)) return PALIMPSA_ERR_ALIGN;

@@ -95,7 +95,7 @@ def test_step_rejects_null(lib, field):
     (dict(B=0), ERR_SHAPE), (dict(H=0), ERR_SHAPE), (dict(T=-1), ERR_SHAPE), (dict(B=-3), ERR_SHAPE),
     (dict(d_k=96), ERR_UNSUPPORTED), (dict(d_k=32), ERR_UNSUPPORTED), (dict(d_v=12), ERR_UNSUPPORTED),
     (dict(d_v=0), ERR_UNSUPPORTED), (dict(d_v=264), ERR_UNSUPPORTED), (dict(chunk=48), ERR_UNSUPPORTED),
-    (dict(chunk=128), ERR_UNSUPPORTED),
+    (dict(chunk=256), ERR_UNSUPPORTED), (dict(chunk=8), ERR_UNSUPPORTED),
     (dict(q=P + 8), ERR_ALIGN), (dict(v=P + 4), ERR_ALIGN), (dict(y=P + 2), ERR_ALIGN),
     (dict(mu0=P + 8), ERR_ALIGN), (dict(I0=P + 4), ERR_ALIGN), (dict(d_t=P + 2), ERR_ALIGN),
 ])
@@ -411,3 +411,7 @@ def test_packed_checkpoint_shape_matches_the_library_size(lib):
                                     (64, 32, 131072, 128, 64)):
         shape = pal.packed_checkpoint_shape(N, H, total_T, d_k, d_v)
         assert math.prod(shape) * 4 == pal.palimpsa_checkpoint_bytes_varlen(N, H, total_T, d_k, d_v)
+
+
+def test_scratch_query_rejects_null(lib):
+    assert lib.palimpsa_scratch_reserved_bytes(None) == ERR_NULL
