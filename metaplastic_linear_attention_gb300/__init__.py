@@ -34,8 +34,12 @@ from .binding import (  # noqa: F401
     packed_checkpoint_shape,
     palimpsa_forward_without_meta,
     palimpsa_get_device_status,
+    palimpsa_probe_issue_rate,
+    palimpsa_release_scratch,
+    palimpsa_scratch_reserved_bytes,
     palimpsa_segment_summary,
     palimpsa_set_forward_segments,
+    palimpsa_set_scratch_retention,
     palimpsa_set_step_l2_keep_bytes,
     palimpsa_set_wait_timeout_ns,
     palimpsa_state_combine,

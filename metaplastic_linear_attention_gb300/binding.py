@@ -127,6 +127,14 @@ def load_library(path: str | None = None):
         lib.palimpsa_set_forward_segments.argtypes = [i]
         lib.palimpsa_set_step_l2_keep_bytes.restype = None
         lib.palimpsa_set_step_l2_keep_bytes.argtypes = [ctypes.c_longlong]
+        lib.palimpsa_set_scratch_retention.restype = i
+        lib.palimpsa_set_scratch_retention.argtypes = [ctypes.c_ulonglong]
+        lib.palimpsa_release_scratch.restype = i
+        lib.palimpsa_release_scratch.argtypes = []
+        lib.palimpsa_scratch_reserved_bytes.restype = i
+        lib.palimpsa_scratch_reserved_bytes.argtypes = [ctypes.POINTER(ctypes.c_size_t)]
+        lib.palimpsa_probe_issue_rate.restype = i
+        lib.palimpsa_probe_issue_rate.argtypes = [i, ctypes.POINTER(ctypes.c_double), vp]
         _lib = lib
         return lib
 
@@ -167,6 +175,46 @@ def palimpsa_set_step_l2_keep_bytes(nbytes: int) -> None:
     """Bytes of the decode state each step leaves in L2 for the next, which walks
     the state the other way (0 = stream everything in one order; see palimpsa.h)."""
     load_library().palimpsa_set_step_l2_keep_bytes(int(nbytes))
+
+
+def palimpsa_set_scratch_retention(nbytes: int) -> None:
+    """Bytes of freed scratch every device's pool keeps mapped between calls (see palimpsa.h)."""
+    rc = load_library().palimpsa_set_scratch_retention(int(nbytes))
+    if rc != 0:
+        raise PalimpsaError(rc, "palimpsa_set_scratch_retention")
+
+
+def palimpsa_release_scratch(device=None) -> None:
+    """Synchronise `device` (default: the current one) and give all of its freed
+    scratch back to the driver (see palimpsa.h)."""
+    with torch.cuda.device(device if device is not None else torch.cuda.current_device()):
+        rc = load_library().palimpsa_release_scratch()
+    if rc != 0:
+        raise PalimpsaError(rc, "palimpsa_release_scratch")
+
+
+def palimpsa_scratch_reserved_bytes(device=None) -> int:
+    """Bytes the library's scratch pool on `device` holds mapped (0 without a pool)."""
+    n = ctypes.c_size_t()
+    with torch.cuda.device(device if device is not None else torch.cuda.current_device()):
+        rc = load_library().palimpsa_scratch_reserved_bytes(ctypes.byref(n))
+    if rc != 0:
+        raise PalimpsaError(rc, "palimpsa_scratch_reserved_bytes")
+    return int(n.value)
+
+
+PROBE_OPS = {"rcp": 0, "ex2": 1, "ffma": 2}
+
+
+def palimpsa_probe_issue_rate(op: str, stream=None) -> float:
+    """Instructions of kind `op` ("rcp", "ex2" or "ffma") one SM of the current
+    device completes per clock, measured (see palimpsa.h)."""
+    r = ctypes.c_double()
+    rc = load_library().palimpsa_probe_issue_rate(PROBE_OPS[op], ctypes.byref(r),
+                                                  ctypes.c_void_p(_stream_handle(stream)))
+    if rc != 0:
+        raise PalimpsaError(rc, "palimpsa_probe_issue_rate")
+    return float(r.value)
 
 
 def _stream_handle(stream) -> int:

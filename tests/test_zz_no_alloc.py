@@ -6,9 +6,11 @@ device heap, a latency-critical loop. For them the time-split scratch of the
 chunked forward lives in a fixed array inside the library. These tests call
 that entry point through the C ABI and compare it with the allocating entry
 point on the same inputs, twice in a row (the array keeps the previous call's
-contents, which must not leak into the next result), and check that a call
-needing more scratch than the array holds is refused without touching its
-outputs. This file is collected last on purpose.
+contents, which must not leak into the next result) and with the fp64 oracle,
+so that a fault shared by both entry points (the time-split code they have in
+common) cannot pass unseen; and check that a call needing more scratch than the
+array holds is refused without touching its outputs. This file is collected
+last on purpose.
 """
 import ctypes
 
@@ -17,11 +19,12 @@ import torch
 
 import metaplastic_linear_attention_gb300 as pal
 from metaplastic_linear_attention_gb300 import synthetic as syn
-from tests._helpers import TIGHT, rel_l2, tol_for
+from tests._helpers import TIGHT, oracle_forward_from, rel_l2, tol_for
 
 pytestmark = pytest.mark.gpu
 DEV = "cuda"
 ERR_SCRATCH_LIMIT = 9
+NOALLOC_SCRATCH_BYTES = 16 << 20     # the fixed array's size, as the header states
 
 
 def _ptr(t):
@@ -57,6 +60,17 @@ def _run_both(lib, wl, seed, with_state):
     for ref, got in zip(outs[0], outs[1]):
         assert torch.isfinite(got).all()
         assert rel_l2(got.cpu(), ref.cpu()) <= min(tol_for(inp), TIGHT)
+    # the no-allocation results against the oracle on the same inputs, every head
+    oref = oracle_forward_from(inp, None if mu0 is None else mu0.cpu(), None if I0 is None else I0.cpu())
+    for got, ref in zip(outs[1], oref):
+        assert rel_l2(got.cpu().numpy(), ref) <= min(tol_for(inp), TIGHT)
+
+
+def _assert_split_fits(wl):
+    """The plan of this call splits time (so the fixed array is used) and fits the array."""
+    plan = pal.palimpsa_forward_plan(wl.B, wl.H, wl.T, wl.d_k, wl.d_v, chunk=wl.chunk, bf16=wl.bf16)
+    assert plan["segments"] > 1, plan
+    assert 0 < plan["scratch_bytes"] <= NOALLOC_SCRATCH_BYTES, plan
 
 
 def test_no_alloc_forward_matches_the_allocating_one_twice_in_a_row():
@@ -64,11 +78,14 @@ def test_no_alloc_forward_matches_the_allocating_one_twice_in_a_row():
     pal.palimpsa_set_forward_segments(0)
     try:
         # call 1: few heads, so the automatic plan splits time and uses the scratch array
-        _run_both(lib, syn.WORKLOADS["small_layer"].with_(B=1, H=4, T=600), seed=501, with_state=True)
+        wl1 = syn.WORKLOADS["small_layer"].with_(B=1, H=4, T=600)
+        _assert_split_fits(wl1)
+        _run_both(lib, wl1, seed=501, with_state=True)
         # call 2: another shape and a forced split, over what call 1 left in the array
         pal.palimpsa_set_forward_segments(5)
-        _run_both(lib, syn.WORKLOADS["small_layer"].with_(B=2, H=3, T=333, d_k=64, d_v=24, bf16=False,
-                                                          chunk=32), seed=502, with_state=False)
+        wl2 = syn.WORKLOADS["small_layer"].with_(B=2, H=3, T=333, d_k=64, d_v=24, bf16=False, chunk=32)
+        _assert_split_fits(wl2)
+        _run_both(lib, wl2, seed=502, with_state=False)
     finally:
         pal.palimpsa_set_forward_segments(0)
 
