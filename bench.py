@@ -35,13 +35,15 @@ FALLBACK_HBM_GBS = 6800.0
 # live by the library's issue-rate probe, x the SM count x the maximum SM clock.
 
 # DRAM bytes per launch (dram__bytes_read.sum + dram__bytes_write.sum) of a kernel from one ncu
-# capture, valid only while the
-# kernel's source file is byte-identical to the one captured (sha256 below); otherwise null.
-# The decode step's figure is the mean of consecutive steps captured without cache flushes
-# (--cache-control none), as they run in the timed region: each step finds the rows the
-# previous one stored last still in L2.
+# capture, valid only while the kernel's source file is byte-identical to the one captured
+# (sha256 below); otherwise null. The decode step's figure is the mean of four consecutive
+# steady-state steps at the full B=256, H=32 state (a 64-token prefill and 16 decode tokens
+# per bench step keep the device footprint near 1 GB), captured without cache flushes
+# (--cache-control none) as they run in the timed region: each step finds the rows the
+# previous one stored last still in L2. The traffic of a step does not depend on the prefill's
+# length or the number of steps after the first.
 NCU_TRAFFIC = {
-    "palimpsa_step": {"bytes_per_launch": 928755127, "source": "csrc/step.cu",
+    "palimpsa_step": {"bytes_per_launch": 932406848, "source": "csrc/step.cu",
                       "sha256": "a99e48cc88dad37e653c648b985da9e595766bb149603d3a12dfc0fe1c5e09b3"},
 }
 

@@ -25,7 +25,13 @@ template <int OP>
 __device__ __forceinline__ float probe_op(float x) {
   float r;
   if constexpr (OP == PALIMPSA_PROBE_RCP) {
-    asm volatile("rcp.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(x));
+    // 1 / (x + 1): an add in front of each reciprocal (as in the kernels, where
+    // I is formed just before its reciprocal) keeps the code generator from
+    // folding a reciprocal of a reciprocal back into its argument; the add runs
+    // on the FP32 pipe, whose rate is eight times the SFU's
+    asm volatile("{\n\t.reg .f32 t;\n\tadd.f32 t, %1, 0f3F800000;\n\trcp.approx.ftz.f32 %0, t;\n\t}"
+                 : "=f"(r)
+                 : "f"(x));
   } else if constexpr (OP == PALIMPSA_PROBE_EX2) {
     asm volatile("ex2.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(-x));  // 2^-x stays in (0, 1]
   } else {
