@@ -17,8 +17,16 @@
 //             d(bv)_i = sum_j gM k_j  -> dv_i = d(bv)_i beta_i,  dbeta_i = d(bv)_i v_i + sum_j gI k_j^2
 //             dalpha_t = sum_ij gM_t M_{t-1} + gI_t (I_{t-1} - I_prior), taken as
 //             alpha_t dalpha_t = sum_ij gM_t (M_t - bv_i k_j) + gI_t (I_t - I_prior - beta_i k_j^2)
-//               = sum_ij (gM_t M_t + gI_t I_t) - sum_i (bv_i d(bv)_i + beta_i sum_j gI k_j^2) - I_prior sum_ij gI_t,
-//             which needs only the state after token t and sums the kernel forms anyway;
+//               = F_t - R_t,  F_t = sum_ij gM_t M_t + gI_t (I_t - I_prior),
+//                             R_t = sum_i (bv_i d(bv)_i + beta_i sum_j gI k_j^2)   (row sums the kernel forms anyway);
+//             F itself needs no per-element work at most tokens: with gM_{t-1} = alpha_t gM_t + dy q r,
+//             gI_{t-1} = alpha_t gI_t - dy q mu r, the readout's two contributions to F_{t-1} cancel
+//             ((dy q r) M - (dy q mu r) I = 0), leaving the scalar recursion
+//               F_{t-1} = alpha_t dalpha_t - I_prior J_{t-1},  J_t = sum_ij (-dy_i q_j mu_ij r_ij)
+//             (J is summed from the injections themselves, not as a difference of two sums of gI,
+//             which would cancel when memory is long), so F is formed element by element only at
+//             the last token of each 8-token window and carried through the window by this
+//             recursion (over at most 7 tokens, so rounding cannot build up);
 //             dd_t = -A (alpha_t dalpha_t),  dA += -d_t (alpha_t dalpha_t),  dI_prior += (1 - alpha_t) sum_ij gI_t
 //   start     (t = T) gM = dmu_T r_T, gI = dI_T - dmu_T mu_T r_T;  (t = 0) dmu0 = gM_0 I0, dI0 = gI_0 + gM_0 mu0.
 //
@@ -38,9 +46,11 @@
 // pairs of a warp with a reduce-scatter and go to fp32 atomics (the d_v / 8
 // CTAs of a head add into the same dq, dk; the library zeroes them first). Row
 // sums (d(bv), sum gI k^2) finish over the 8 column lanes with shuffles and
-// over the 4 warps through shared memory once per 8-token window; the alpha
-// partial of every lane goes to shared memory as it is and is summed over the
-// CTA's 128 lanes once per window.
+// over the 4 warps through shared memory once per 8-token window; each lane's
+// sum of gI goes to shared memory as it is and is summed over the CTA's 128
+// lanes once per window. Then one warp turns the window's per-token sums into
+// the alpha gradients with the F recursion above (a suffix sum over the
+// window's tokens), while the other warps go on to the next window.
 //
 // Staging: every operand a segment needs (q, k and the CTA's 8 rows of v, beta,
 // dy, plus d_t) is copied into shared memory once per CTA with cp.async, into
@@ -65,7 +75,7 @@ __host__ __device__ constexpr size_t al16(size_t x) { return (x + 15) / 16 * 16;
 // Shared-memory carve-up (byte offsets; every piece 16-byte aligned).
 struct BwdSmem {
   size_t k, q, v, b, dy, dt, stage;   // one staged segment (offsets inside a stage)
-  size_t kf, qf, win, rowp, adap, rb, rbv, gate, total;
+  size_t kf, qf, win, rowp, adap, rb, rbv, gate, sgt, rmi, fw, total;
 
   __host__ __device__ BwdSmem(int DK, int ES) {
     size_t o = 0;
@@ -82,10 +92,13 @@ struct BwdSmem {
     qf = o;    o += ES == 2 ? (size_t)kSeg * DK * 4 : 0;
     win = o;   o += (size_t)2 * kRowsPerCta * kNW * DK * 4;   // window starts [window][M | I][row][pair][thread]
     rowp = o;  o += (size_t)kWarps * kWin * kRowsPerCta * 2 * 4;  // row-sum partials [warp][token][row][2]
-    adap = o;  o += (size_t)kWin * kThreads * 4;              // alpha-gradient partials [token][thread]
+    adap = o;  o += (size_t)kWin * kThreads * 4;              // J partials [token][thread]
     rb = o;    o += (size_t)kSeg * kRowsPerCta * 4;           // beta_i of the segment's tokens [token][row]
     rbv = o;   o += (size_t)kSeg * kRowsPerCta * 4;           // beta_i v_i
     gate = o;  o += (size_t)kSeg * 16;                        // [token](alpha, (1 - alpha) I_prior, 1 - alpha, 0)
+    sgt = o;   o += (size_t)kWin * 4;                         // the window's J per token (CTA)
+    rmi = o;   o += (size_t)kWin * 4;                         // the window's sum_i (bv_i d(bv)_i + beta_i sum_j gI k^2)
+    fw = o;    o += (size_t)2 * kWarps * 4;                   // F at the window's last token, per warp, two windows
     total = (o + 127) / 128 * 128;
   }
 };
@@ -303,6 +316,11 @@ palimpsa_bwd_kernel(BwdArgs a, float* __restrict__ ckpt) {
   };
   auto rowp = reinterpret_cast<float (*)[kWin][kRowsPerCta][2]>(bsm + L.rowp);
   auto adap = reinterpret_cast<float (*)[kThreads]>(bsm + L.adap);
+  float* sgt_w = reinterpret_cast<float*>(bsm + L.sgt);
+  float* rmi_w = reinterpret_cast<float*>(bsm + L.rmi);
+  float* fwin = reinterpret_cast<float*>(bsm + L.fw);
+  const float* rb_t = reinterpret_cast<const float*>(bsm + L.rb);
+  const float* rbv_t = reinterpret_cast<const float*>(bsm + L.rbv);
 
   const int DV = a.d_v;
   const int groups = DV / kRowsPerCta;
@@ -394,6 +412,7 @@ palimpsa_bwd_kernel(BwdArgs a, float* __restrict__ ckpt) {
   float2 gM[2][NP], gI[2][NP];
   if (nseg == 0) init_adjoints<NP>(a, soff, DK, M, I, gM, gI);
   float dIp_acc = 0.f, dA_acc = 0.f;
+  float acar = 1.f;  // alpha of the token after the one being swept (1 past the end)
 
   // ---- phase 2: segments in reverse; segment s - 1 is being copied in while
   // segment s computes (the last segment is still staged from phase 1).
@@ -412,23 +431,29 @@ palimpsa_bwd_kernel(BwdArgs a, float* __restrict__ ckpt) {
     load_rows<NP>(ck_in + (size_t)s * ck_step, 2 * DK, M);
     load_rows<NP>(ck_in + (size_t)s * ck_step + DK, 2 * DK, I);
     __syncthreads();  // gates ready
-    // re-run the segment, keeping the state at each window start (this lane's elements only)
-    for (int u = 0; u < tn; ++u) {
-      if (u % kWin == 0) {
+    // re-run the segment, keeping the state at each window start (this lane's elements only).
+    // Only the sequence's last segment goes on to its end, where the adjoints start; the others
+    // stop at their last window's start, which the window re-run below carries on from.
+    const int nwin = (tn + kWin - 1) / kWin;
+    const int last_start = (nwin - 1) * kWin;
+    const int stop = s == nseg - 1 ? tn : last_start;
+    auto keep_start = [&](const int wi) {
 #pragma unroll
-        for (int r = 0; r < 2; ++r)
+      for (int r = 0; r < 2; ++r)
 #pragma unroll
-          for (int p = 0; p < NP; ++p) {
-            win_at(u / kWin, 0, r, p) = M[r][p];
-            win_at(u / kWin, 1, r, p) = I[r][p];
-          }
-      }
+        for (int p = 0; p < NP; ++p) {
+          win_at(wi, 0, r, p) = M[r][p];
+          win_at(wi, 1, r, p) = I[r][p];
+        }
+    };
+    for (int u = 0; u < stop; ++u) {
+      if (u % kWin == 0) keep_start(u / kWin);
       float2 k[NP];
       lane_pairs<NP>(kf, DK, u, c0, k);
       step_rows<NP>(M, I, k, tok2(bsm, L, u, g));
     }
+    if (stop == last_start) keep_start(nwin - 1);
     if (s == nseg - 1) init_adjoints<NP>(a, soff, DK, M, I, gM, gI);  // M, I: the final state
-    const int nwin = (tn + kWin - 1) / kWin;
     for (int wi = nwin - 1; wi >= 0; --wi) {
       const int uw = wi * kWin, n = min(kWin, tn - uw);
       // re-run the window into registers: (Ms[uu], Is[uu]) is the state after token uw + uu
@@ -445,20 +470,22 @@ palimpsa_bwd_kernel(BwdArgs a, float* __restrict__ ckpt) {
         lane_pairs<NP>(kf, DK, uw + uu, c0, k);
         step_rows<NP>(Ms[uu], Is[uu], k, tok2(bsm, L, uw + uu, g));
       };
-      // one token of the backward sweep: the adjoints take token uw + uu's
-      // readout, its gradient sums are formed and handed on, then the adjoints
-      // are carried to the token before. Accumulators start from their first
-      // product.
-      auto sweep = [&](const int uu) {
+      // one token of the backward sweep: the adjoints are carried from the token
+      // after (times its alpha, acar) and take token uw + uu's readout, in one
+      // FMA each; then its gradient sums are formed and handed on. Accumulators
+      // start from their first product. At the window's last token (the first
+      // swept) the lane also forms its part of F (see the header).
+      auto sweep = [&](const int uu, const bool window_end) {
         const int u = uw + uu;
         float2 k[NP], q[NP], kk[NP], dqa[NP], dkM[NP], dkI[NP];
         lane_pairs<NP>(kf, DK, u, c0, k);
         lane_pairs<NP>(qf, DK, u, c0, q);
         const Tok2 tr = tok2(bsm, L, u, g);
         const float2 dyp = dys[(u * kRowsPerCta) / 2 + g];
+        const float2 ac2 = f2(acar);
 #pragma unroll
         for (int p = 0; p < NP; ++p) kk[p] = __fmul2_rn(k[p], k[p]);
-        float2 rM[2], rI[2], ada[2], sgi[2];
+        float2 rM[2], rI[2], sgi[2], ji[2], fp = f2(0.f);
 #pragma unroll
         for (int r = 0; r < 2; ++r) {
           const float2 ndy2 = f2(-(r ? dyp.y : dyp.x));
@@ -469,16 +496,17 @@ palimpsa_bwd_kernel(BwdArgs a, float* __restrict__ ckpt) {
             const float2 nr = make_float2(rcp_approx(-Ic.x), rcp_approx(-Ic.y));  // -1 / I
             const float2 mun = __fmul2_rn(Mc, nr);                                 // -mu
             dqa[p] = r ? __ffma2_rn(ndy2, mun, dqa[p]) : __fmul2_rn(ndy2, mun);   // + dy_i mu
-            const float2 ndyq = __fmul2_rn(ndy2, q[p]);                            // -dy_i q_j
-            gM[r][p] = __ffma2_rn(ndyq, nr, gM[r][p]);                             // + dy q / I
-            gI[r][p] = __ffma2_rn(ndyq, __fmul2_rn(mun, nr), gI[r][p]);            // - dy q mu / I
+            const float2 injM = __fmul2_rn(ndy2, __fmul2_rn(q[p], nr));            // + dy q / I
+            gM[r][p] = __ffma2_rn(ac2, gM[r][p], injM);
+            const float2 injI = __fmul2_rn(injM, mun);                             // - dy q mu / I
+            gI[r][p] = __ffma2_rn(ac2, gI[r][p], injI);
             dkM[p] = r ? __ffma2_rn(gM[r][p], bv2, dkM[p]) : __fmul2_rn(gM[r][p], bv2);
             dkI[p] = r ? __ffma2_rn(gI[r][p], b2, dkI[p]) : __fmul2_rn(gI[r][p], b2);
             rM[r] = p ? __ffma2_rn(gM[r][p], k[p], rM[r]) : __fmul2_rn(gM[r][p], k[p]);
             rI[r] = p ? __ffma2_rn(gI[r][p], kk[p], rI[r]) : __fmul2_rn(gI[r][p], kk[p]);
-            const float2 t = p ? __ffma2_rn(gI[r][p], Ic, ada[r]) : __fmul2_rn(gI[r][p], Ic);
-            ada[r] = __ffma2_rn(gM[r][p], Mc, t);
             sgi[r] = p ? __fadd2_rn(sgi[r], gI[r][p]) : gI[r][p];
+            ji[r] = p ? __fadd2_rn(ji[r], injI) : injI;
+            if (window_end) fp = __ffma2_rn(gM[r][p], Mc, __ffma2_rn(gI[r][p], Ic, fp));
           }
         }
         // columns: dq_j and dk_j = sum gM bv + 2 k_j sum gI beta over the lane's
@@ -502,11 +530,10 @@ palimpsa_bwd_kernel(BwdArgs a, float* __restrict__ ckpt) {
           else atomicAdd(dst, cs[0]);
         }
         // rows: d(bv)_i and sum_j gI k_j^2 over the lane's columns, then over the
-        // warp's 8 column lanes; alpha_t dL/dalpha_t over the lane's elements
+        // warp's 8 column lanes; sum gI and J over the lane's elements
         float rv[4] = {rM[0].x + rM[0].y, rM[1].x + rM[1].y, rI[0].x + rI[0].y, rI[1].x + rI[1].y};
         const float sg = (sgi[0].x + sgi[0].y) + (sgi[1].x + sgi[1].y);
-        float ap = ((ada[0].x + ada[0].y) + (ada[1].x + ada[1].y)) -
-                   (tr.bv.x * rv[0] + tr.bv.y * rv[1]) - (tr.b.x * rv[2] + tr.b.y * rv[3]) - Ip * sg;
+        const float jl = (ji[0].x + ji[0].y) + (ji[1].x + ji[1].y);
         dIp_acc = fmaf(tr.oma, sg, dIp_acc);  // (1 - alpha) sum gI; reduced at the end
         rs_level<4, 4>(rv, lane, 4);
         rs_level<4, 2>(rv, lane, 2);
@@ -515,63 +542,98 @@ palimpsa_bwd_kernel(BwdArgs a, float* __restrict__ ckpt) {
           const int o = (lane >> 1) & 3;   // row 2g + (o & 1); d(bv) for o < 2, else sum gI k^2
           rowp[w][uu][2 * g + (o & 1)][o >> 1] = rv[0];
         }
-        adap[uu][threadIdx.x] = ap;  // summed once per window
-        // carry the adjoints to t - 1
-        const float2 a2 = f2(tr.alpha);
-#pragma unroll
-        for (int r = 0; r < 2; ++r)
-#pragma unroll
-          for (int p = 0; p < NP; ++p) {
-            gM[r][p] = __fmul2_rn(gM[r][p], a2);
-            gI[r][p] = __fmul2_rn(gI[r][p], a2);
-          }
+        adap[uu][threadIdx.x] = jl;  // summed once per window
+        if (window_end) {  // this warp's part of F at the window's last token
+          const float f = warp_sum((fp.x + fp.y) - Ip * sg);
+          if (lane == 0) fwin[(wi & 1) * kWarps + w] = f;
+        }
+        acar = tr.alpha;  // carries the adjoints to the token before
       };
       // full windows without per-token guards, so that neighbouring tokens interleave
       if (n == kWin) {
 #pragma unroll
         for (int uu = 0; uu < kWin; ++uu) rerun(uu);
 #pragma unroll
-        for (int uu = kWin - 1; uu >= 0; --uu) sweep(uu);
+        for (int uu = kWin - 1; uu >= 0; --uu) sweep(uu, uu == kWin - 1);
       } else {
 #pragma unroll
         for (int uu = 0; uu < kWin; ++uu)
           if (uu < n) rerun(uu);
 #pragma unroll
         for (int uu = kWin - 1; uu >= 0; --uu)
-          if (uu < n) sweep(uu);
+          if (uu < n) sweep(uu, uu == n - 1);
       }
-      // the window's row sums: dv, dbeta per (token, row); alpha dalpha per token
       __syncthreads();
-      for (int x = threadIdx.x; x < n * kRowsPerCta; x += kThreads) {
-        const int uu = x / kRowsPerCta, r = x % kRowsPerCta, u = uw + uu;
-        float s_bv = 0.f, s_b = 0.f;
-#pragma unroll
-        for (int ww = 0; ww < kWarps; ++ww) { s_bv += rowp[ww][uu][r][0]; s_b += rowp[ww][uu][r][1]; }
-        const size_t o = (head_tok + ts + u) * DV + row0 + r;
-        a.dv[o] = s_bv * row_val<BF16>(st + L.b, u, r);
-        a.dbeta[o] = fmaf(s_bv, row_val<BF16>(st + L.v, u, r), s_b);
-      }
-      {  // alpha_t dL/dalpha_t of each token: its 128 lane partials, 16 threads a token
-        const int uu = threadIdx.x >> 4, part = threadIdx.x & 15;
-        float ad = 0.f;
+      if (threadIdx.x < kWin * kRowsPerCta) {
+        // warps 0, 1: the window's row sums: dv, dbeta per (token, row), and per token
+        // R = sum_i (bv_i d(bv)_i + beta_i sum_j gI k_j^2) over the CTA's rows (8 lanes a token)
+        const int uu = threadIdx.x / kRowsPerCta, r = threadIdx.x % kRowsPerCta, u = uw + uu;
+        float rr = 0.f;
         if (uu < n) {
-          const float4* src = reinterpret_cast<const float4*>(&adap[uu][part * 8]);
-          const float4 p0 = src[0], p1 = src[1];
-          ad = ((p0.x + p0.y) + (p0.z + p0.w)) + ((p1.x + p1.y) + (p1.z + p1.w));
+          float s_bv = 0.f, s_b = 0.f;
+#pragma unroll
+          for (int ww = 0; ww < kWarps; ++ww) { s_bv += rowp[ww][uu][r][0]; s_b += rowp[ww][uu][r][1]; }
+          const size_t o = (head_tok + ts + u) * DV + row0 + r;
+          a.dv[o] = s_bv * row_val<BF16>(st + L.b, u, r);
+          a.dbeta[o] = fmaf(s_bv, row_val<BF16>(st + L.v, u, r), s_b);
+          const int x = u * kRowsPerCta + r;
+          rr = fmaf(rbv_t[x], s_bv, rb_t[x] * s_b);
         }
 #pragma unroll
-        for (int m = 8; m >= 1; m >>= 1) ad += __shfl_xor_sync(0xffffffffu, ad, m);
-        if (part == 0 && uu < n) {
-          const int u = uw + uu;
+        for (int m = 4; m >= 1; m >>= 1) rr += __shfl_xor_sync(0xffffffffu, rr, m);
+        if (r == 0) rmi_w[uu] = rr;
+      } else {
+        // warps 2, 3: the window's J per token: its 128 lane partials, 8 threads a token
+        const int t2 = threadIdx.x - kWin * kRowsPerCta, uu = t2 >> 3, part = t2 & 7;
+        float sgs = 0.f;
+        if (uu < n) {
+          const float4* src = reinterpret_cast<const float4*>(&adap[uu][part * 16]);
+#pragma unroll
+          for (int c = 0; c < 4; ++c) {
+            const float4 v4 = src[c];
+            sgs += (v4.x + v4.y) + (v4.z + v4.w);
+          }
+        }
+#pragma unroll
+        for (int m = 4; m >= 1; m >>= 1) sgs += __shfl_xor_sync(0xffffffffu, sgs, m);
+        if (part == 0) sgt_w[uu] = sgs;
+      }
+      __syncthreads();  // the row partials are free for the next window; R, G and F are in place
+      if (w == 0) {
+        // alpha_t dL/dalpha_t = F_t - R_t, with F_{t-1} = F_t - X_t, X_t = R_t + I_prior J_{t-1}:
+        // lane uu < n takes token uw + uu; F_t = F(window end) - (X summed over the window's later tokens)
+        float X = 0.f, rr = 0.f;
+        if (lane < n) {
+          rr = rmi_w[lane];
+          if (lane > 0) X = fmaf(Ip, sgt_w[lane - 1], rr);
+        }
+        float suf = X;  // inclusive suffix sum over lanes (lanes >= n hold 0)
+#pragma unroll
+        for (int m = 1; m < kWin; m <<= 1) {
+          const float o = __shfl_down_sync(0xffffffffu, suf, m);
+          if (lane + m < 32) suf += o;
+        }
+        const float* fw = fwin + (wi & 1) * kWarps;
+        const float Fend = (fw[0] + fw[1]) + (fw[2] + fw[3]);
+        if (lane < n) {
+          const float ad = (Fend - (suf - X)) - rr;
+          const int u = uw + lane;
           atomicAdd(a.dd_t + head_tok + ts + u, -A_h * ad);
           dA_acc = fmaf(-dts[u], ad, dA_acc);
         }
       }
-      __syncthreads();  // the row partials are free for the next window
     }
     __syncthreads();  // this stage, the window starts and the gate tables are free again
   }
   asm volatile("cp.async.wait_all;" ::: "memory");
+  // the adjoints at t = 0: carried past the first token
+#pragma unroll
+  for (int r = 0; r < 2; ++r)
+#pragma unroll
+    for (int p = 0; p < NP; ++p) {
+      gM[r][p] = __fmul2_rn(gM[r][p], f2(acar));
+      gI[r][p] = __fmul2_rn(gI[r][p], f2(acar));
+    }
 
   // ---- initial-state gradients: M_0 = I0 (.) mu0, I_0 = I0
   float s_ip0 = 0.f;
@@ -592,7 +654,7 @@ palimpsa_bwd_kernel(BwdArgs a, float* __restrict__ ckpt) {
   if (!a.I0) dIp_acc += s_ip0;
   dIp_acc = warp_sum(dIp_acc);
   if (lane == 0) atomicAdd(a.dI_prior + h, dIp_acc);
-  dA_acc = warp_sum(dA_acc);  // threads 16 u hold the dA partials of token slot u
+  dA_acc = warp_sum(dA_acc);  // lanes of warp 0 hold the dA partials of their token slots
   if (lane == 0) atomicAdd(a.dA + h, dA_acc);
 }
 
