@@ -558,7 +558,7 @@ def run_probe_rates(local):
     pal.load_library()
     props = torch.cuda.get_device_properties(local)
     peaks, kind = _measured_peaks()
-    reps = [issue_rates(pal) for _ in range(5)]
+    reps = [{op: pal.palimpsa_probe_issue_rate(op) for op in pal.binding.PROBE_OPS} for _ in range(5)]
     med = {op: statistics.median(r[op] for r in reps) for op in reps[0]}
     sm_max = float(peaks.get("sm_max_mhz", 2070.0))
     print(json.dumps({"gpu": props.name, "sms": props.multi_processor_count, "per_clk_per_sm_runs": reps,

@@ -647,14 +647,18 @@ palimpsa_status palimpsa_scratch_reserved_bytes(size_t* bytes);
  * `cuda_stream` (about a millisecond) and allocates a few bytes of device
  * memory for the cycle counts.
  *   op  PALIMPSA_PROBE_RCP (rcp.approx.ftz.f32), PALIMPSA_PROBE_EX2
- *       (ex2.approx.ftz.f32) or PALIMPSA_PROBE_FFMA (fma.rn.f32).
+ *       (ex2.approx.ftz.f32), PALIMPSA_PROBE_FFMA (fma.rn.f32),
+ *       PALIMPSA_PROBE_RSQ (rsqrt.approx.ftz.f32) or PALIMPSA_PROBE_LG2
+ *       (lg2.approx.ftz.f32).
  * Errors: PALIMPSA_ERR_NULL, PALIMPSA_ERR_UNSUPPORTED (unknown op),
  * PALIMPSA_ERR_CUDA. This call has no counterpart on the pages.
  */
 typedef enum {
   PALIMPSA_PROBE_RCP = 0,
   PALIMPSA_PROBE_EX2 = 1,
-  PALIMPSA_PROBE_FFMA = 2
+  PALIMPSA_PROBE_FFMA = 2,
+  PALIMPSA_PROBE_RSQ = 3,
+  PALIMPSA_PROBE_LG2 = 4
 } palimpsa_probe_op;
 palimpsa_status palimpsa_probe_issue_rate(int op, double* per_clk_per_sm, void* cuda_stream);
 

@@ -203,11 +203,11 @@ def palimpsa_scratch_reserved_bytes(device=None) -> int:
     return int(n.value)
 
 
-PROBE_OPS = {"rcp": 0, "ex2": 1, "ffma": 2}
+PROBE_OPS = {"rcp": 0, "ex2": 1, "ffma": 2, "rsqrt": 3, "lg2": 4}
 
 
 def palimpsa_probe_issue_rate(op: str, stream=None) -> float:
-    """Instructions of kind `op` ("rcp", "ex2" or "ffma") one SM of the current
+    """Instructions of kind `op` ("rcp", "ex2", "ffma", "rsqrt" or "lg2") one SM of the current
     device completes per clock, measured (see palimpsa.h)."""
     r = ctypes.c_double()
     rc = load_library().palimpsa_probe_issue_rate(PROBE_OPS[op], ctypes.byref(r),

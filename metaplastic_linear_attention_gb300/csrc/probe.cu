@@ -34,6 +34,14 @@ __device__ __forceinline__ float probe_op(float x) {
                  : "f"(x));
   } else if constexpr (OP == PALIMPSA_PROBE_EX2) {
     asm volatile("ex2.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(-x));  // 2^-x stays in (0, 1]
+  } else if constexpr (OP == PALIMPSA_PROBE_RSQ) {
+    asm volatile("{\n\t.reg .f32 t;\n\tadd.f32 t, %1, 0f3F800000;\n\trsqrt.approx.ftz.f32 %0, t;\n\t}"
+                 : "=f"(r)
+                 : "f"(x));  // 1 / sqrt(x + 1) stays in (0, 1]
+  } else if constexpr (OP == PALIMPSA_PROBE_LG2) {
+    asm volatile("{\n\t.reg .f32 t;\n\tadd.f32 t, %1, 0f40000000;\n\tlg2.approx.ftz.f32 %0, t;\n\t}"
+                 : "=f"(r)
+                 : "f"(x));  // log2(x + 2) stays in [1, 2)
   } else {
     asm volatile("fma.rn.f32 %0, %1, 0f3F7FBE77, 0f3A83126F;" : "=f"(r) : "f"(x));  // x * 0.999 + 0.001
   }
@@ -69,8 +77,7 @@ using namespace palimpsa;
 
 extern "C" palimpsa_status palimpsa_probe_issue_rate(int op, double* per_clk_per_sm, void* cuda_stream) {
   if (!per_clk_per_sm) return PALIMPSA_ERR_NULL;
-  if (op != PALIMPSA_PROBE_RCP && op != PALIMPSA_PROBE_EX2 && op != PALIMPSA_PROBE_FFMA)
-    return PALIMPSA_ERR_UNSUPPORTED;
+  if (op < PALIMPSA_PROBE_RCP || op > PALIMPSA_PROBE_LG2) return PALIMPSA_ERR_UNSUPPORTED;
   int dev = 0, sms = 0, smem_sm = 0, smem_optin = 0;
   if (cudaGetDevice(&dev) != cudaSuccess ||
       cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
@@ -81,6 +88,8 @@ extern "C" palimpsa_status palimpsa_probe_issue_rate(int op, double* per_clk_per
   const int smem = std::min(smem_optin, smem_sm / 2 + 1024);
   auto kern = op == PALIMPSA_PROBE_RCP   ? palimpsa_probe_kernel<PALIMPSA_PROBE_RCP>
               : op == PALIMPSA_PROBE_EX2 ? palimpsa_probe_kernel<PALIMPSA_PROBE_EX2>
+              : op == PALIMPSA_PROBE_RSQ ? palimpsa_probe_kernel<PALIMPSA_PROBE_RSQ>
+              : op == PALIMPSA_PROBE_LG2 ? palimpsa_probe_kernel<PALIMPSA_PROBE_LG2>
                                          : palimpsa_probe_kernel<PALIMPSA_PROBE_FFMA>;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
     return PALIMPSA_ERR_CUDA;
