@@ -150,8 +150,15 @@ palimpsa_fwd_chunked_kernel(FwdArgs a, int C, int nseg, int seg_len, const float
                      : tl.bh * (long long)((a.T + kCheckpointTokens - 1) / kCheckpointTokens);
     ckh = a.ckpt + (size_t)slot0 * DV * 2 * DK;
   }
+  // d_t is read one chunk ahead (thread t holds token t of the next chunk; C <= 32), so
+  // that its global load lands during a chunk of compute instead of in front of the
+  // barrier that ends the next chunk's conversion
+  float d_next = 0.f;
+  if (pipe.nch > 0 && (int)threadIdx.x < pipe.tc_of(0)) d_next = gd[pipe.t0_of(0) + threadIdx.x];
   for (int c = 0; c < pipe.nch; ++c) {
     const int t0 = pipe.t0_of(c), tc = pipe.tc_of(c);
+    const float d_cur = d_next;
+    if (c + 1 < pipe.nch && (int)threadIdx.x < pipe.tc_of(c + 1)) d_next = gd[pipe.t0_of(c + 1) + threadIdx.x];
     if (ckh && (tl.tb + t0) % kCheckpointTokens == 0) {
       float* ck = ckh + (size_t)((tl.tb + t0) / kCheckpointTokens) * DV * 2 * DK;
 #pragma unroll
@@ -179,8 +186,8 @@ palimpsa_fwd_chunked_kernel(FwdArgs a, int C, int nseg, int seg_len, const float
       bvf[it] = a.pro.v_star ? vv : bb * vv;
       bfv[it] = bb;
     }
-    for (int t = threadIdx.x; t < tc; t += NTH) {
-      float d = gd[t0 + t];
+    for (int t = threadIdx.x; t < tc; t += NTH) {  // one token per thread at most (tc <= 32 <= NTH)
+      float d = d_cur;
       if (a.pro.on) d = softplus_f(d);
       domain_bad |= !nonneg_finite(d);
       const float x = -A_h * d;
@@ -327,14 +334,19 @@ palimpsa_fwd_summary_kernel(FwdArgs a, int C, int nseg, int seg_len, float* __re
     for (int j = 0; j < 2 * NV; ++j) { dI[r][j] = make_float2(0.f, 0.f); dM[r][j] = make_float2(0.f, 0.f); }
 
   const float* gd = a.d_t + head_tok + tl.tb;
+  // d_t one chunk ahead (warp 0, lane t = token t), so its load lands during a chunk of compute
+  float d_next = 0.f;
+  if (warp == 0 && pipe.nch > 0 && lane < pipe.tc_of(0)) d_next = gd[pipe.t0_of(0) + lane];
   for (int c = 0; c < pipe.nch; ++c) {
-    const int t0 = pipe.t0_of(c), tc = pipe.tc_of(c);
+    const int tc = pipe.tc_of(c);
+    const float d_cur = d_next;
+    if (warp == 0 && c + 1 < pipe.nch && lane < pipe.tc_of(c + 1)) d_next = gd[pipe.t0_of(c + 1) + lane];
     if (!pipe.wait(c, a.wait_timeout_ns, a.status)) return;
     const unsigned char* raw = pipe.raw(c);
     // suffix products inside the chunk (warp 0; at most 32 tokens per chunk):
     // W_t = carry * prod_{t < u < tc} alpha_u
     if (warp == 0) {
-      float d = lane < tc ? gd[t0 + lane] : 0.f;
+      float d = lane < tc ? d_cur : 0.f;
       if (a.pro.on) d = softplus_f(d);
       const float al = lane < tc ? expf(-A_h * d) : 1.f;
       float p = al;  // inclusive suffix product prod_{u >= lane}

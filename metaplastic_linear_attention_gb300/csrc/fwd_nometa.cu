@@ -87,8 +87,14 @@ palimpsa_fwd_nometa_kernel(FwdArgs a, int C, int nseg, int seg_len, const float*
 
   float* gy = a.y + (head_tok + tl.tb) * DV + tl.row0 + lr0;
   const float* gd = a.d_t + head_tok + tl.tb;
+  // d_t one chunk ahead (thread t holds token t of the next chunk; C <= 32), so its
+  // load lands during a chunk of compute
+  float d_next = 0.f;
+  if (pipe.nch > 0 && (int)threadIdx.x < pipe.tc_of(0)) d_next = gd[pipe.t0_of(0) + threadIdx.x];
   for (int c = 0; c < pipe.nch; ++c) {
     const int t0 = pipe.t0_of(c), tc = pipe.tc_of(c);
+    const float d_cur = d_next;
+    if (c + 1 < pipe.nch && (int)threadIdx.x < pipe.tc_of(c + 1)) d_next = gd[pipe.t0_of(c + 1) + threadIdx.x];
     if (!pipe.wait(c, a.wait_timeout_ns, a.status)) return;
     const unsigned char* raw = pipe.raw(c);
     convert_keys<DK, BF16, true, NTH>(raw, L, smem, tc, false);
@@ -99,8 +105,8 @@ palimpsa_fwd_nometa_kernel(FwdArgs a, int C, int nseg, int seg_len, const float*
       domain_bad |= !nonneg_finite(bb);
       wf[it] = (bb * vv) * rIp;
     }
-    for (int t = threadIdx.x; t < tc; t += NTH) {
-      const float d = gd[t0 + t];
+    for (int t = threadIdx.x; t < tc; t += NTH) {  // one token per thread at most (tc <= 32 <= NTH)
+      const float d = d_cur;
       domain_bad |= !nonneg_finite(d);
       alf[t] = expf(-A_h * d);
     }

@@ -301,8 +301,19 @@ palimpsa_fwd_summary_tc_kernel(FwdArgs a, int nslot, int seg_len, float* __restr
   }
   int c = 0;
   bool failed = false;
+  // d_t one chunk ahead (warp 0, lane t = token t), so its load lands during a chunk of compute
+  float d_next = 0.f;
+  if (warp == 0 && nch > 0) {
+    const int t0n = (nch - 1) * kTcC;
+    if (lane < min(kTcC, tl.tn - t0n)) d_next = gd[t0n + lane];
+  }
   for (; c < nch; ++c) {
     const int t0 = (nch - 1 - c) * kTcC, tc = min(kTcC, tl.tn - t0);
+    const float d_cur = d_next;
+    if (warp == 0 && c + 1 < nch) {
+      const int t0n = (nch - 2 - c) * kTcC;  // chunks before the last are whole
+      d_next = gd[t0n + lane];
+    }
     if (!mbar_wait_bounded(&bars[c & 1], (uint32_t)(c >> 1) & 1u, a.wait_timeout_ns)) *flag = 1;
     // operand buffer c & 1 was last read by the MMAs of chunk c - 2
     if (c >= 2 && !mbar_wait_bounded(&mbars[c & 1], (uint32_t)((c - 2) >> 1) & 1u, a.wait_timeout_ns)) *flag = 1;
@@ -315,7 +326,7 @@ palimpsa_fwd_summary_tc_kernel(FwdArgs a, int nslot, int seg_len, float* __restr
     const unsigned char* raw = smem + (size_t)(c & 1) * L.raw_bytes;
     unsigned char* ob = smem + L.ops + (size_t)(c & 1) * L.op_bytes;
     if (warp == 0) {  // W_t = carry * prod_{t < u < tc} alpha_u (suffix products inside the chunk)
-      float d = lane < tc ? gd[t0 + lane] : 0.f;
+      float d = lane < tc ? d_cur : 0.f;
       if (a.pro.on) d = softplus_f(d);
       const float al = lane < tc ? expf(-A_h * d) : 1.f;
       float p = al;  // inclusive suffix product prod_{u >= lane}
