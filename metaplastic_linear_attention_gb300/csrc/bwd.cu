@@ -42,9 +42,10 @@
 // rows (lane bits 4, 3 pick the row pair) and d_k / 32 consecutive key columns
 // (lane bits 2..0 and the warp pick them), so the per-token loads, the column
 // sums over rows and the row sums over columns are shared by twice the
-// elements of a one-row lane. Column sums (dq, dk) finish over the four row
-// pairs of a warp with a reduce-scatter and go to fp32 atomics (the d_v / 8
-// CTAs of a head add into the same dq, dk; the library zeroes them first). Row
+// elements of a one-row lane. Column sums (dq, dk) are summed over two of the
+// warp's four row pairs with one reduce-scatter level and go to fp32 atomics,
+// where the other two pairs and the d_v / 8 CTAs of a head add into the same
+// dq, dk (the library zeroes them first; one level fewer measured faster). Row
 // sums (d(bv), sum gI k^2) finish over the 8 column lanes with shuffles and
 // over the 4 warps through shared memory once per 8-token window; each lane's
 // sum of gI goes to shared memory as it is and is summed over the CTA's 128
@@ -520,14 +521,15 @@ palimpsa_bwd_kernel(BwdArgs a, float* __restrict__ ckpt) {
           cs[C + 2 * p] = dk2.x;
           cs[C + 2 * p + 1] = dk2.y;
         }
+        // one reduce-scatter level over the row pairs g and g ^ 2 (lane bit 4): a lane keeps its
+        // columns' dq sums (bit clear) or dk sums (bit set); the pairs g and g ^ 1 then meet
+        // in the fp32 atomics
         rs_level<2 * C, 2 * C>(cs, lane, 16);
-        rs_level<2 * C, C>(cs, lane, 8);
         {
-          constexpr int KEEP = C / 2;   // partials g * KEEP .. g * KEEP + KEEP - 1 of cs
-          const int o = g * KEEP;
-          float* dst = (o < C ? a.dq : a.dk) + (head_tok + ts + u) * DK + c0 + (o % C);
-          if constexpr (KEEP == 2) atomicAdd(reinterpret_cast<float2*>(dst), make_float2(cs[0], cs[1]));
-          else atomicAdd(dst, cs[0]);
+          float* dst = ((lane & 16) ? a.dk : a.dq) + (head_tok + ts + u) * DK + c0;
+#pragma unroll
+          for (int p = 0; p < NP; ++p)
+            atomicAdd(reinterpret_cast<float2*>(dst + 2 * p), make_float2(cs[2 * p], cs[2 * p + 1]));
         }
         // rows: d(bv)_i and sum_j gI k_j^2 over the lane's columns, then over the
         // warp's 8 column lanes; sum gI and J over the lane's elements
