@@ -200,14 +200,15 @@ __device__ __forceinline__ void prepare_segment(const unsigned char* st, unsigne
     rbv[x] = b * row_val<BF16>(st + L.v, x / kRowsPerCta, x % kRowsPerCta);
   }
   if constexpr (BF16) {
-    const int n8 = tn * DK / 8;  // 8 bf16 values = 16 bytes per item
-    for (int x = threadIdx.x; x < n8; x += kThreads) {
+    // 4 bf16 values (8 bytes) in, one float4 out per item: consecutive threads store
+    // consecutive 16 bytes, so the stores are free of bank conflicts
+    const int n4 = tn * DK / 4;
+    for (int x = threadIdx.x; x < n4; x += kThreads) {
 #pragma unroll
       for (int which = 0; which < 2; ++which) {
-        const uint4 w = reinterpret_cast<const uint4*>(st + (which ? L.q : L.k))[x];
-        float4* o = reinterpret_cast<float4*>(bsm + (which ? L.qf : L.kf)) + 2 * x;
-        o[0] = make_float4(bf16_lo(w.x), bf16_hi(w.x), bf16_lo(w.y), bf16_hi(w.y));
-        o[1] = make_float4(bf16_lo(w.z), bf16_hi(w.z), bf16_lo(w.w), bf16_hi(w.w));
+        const uint2 w = reinterpret_cast<const uint2*>(st + (which ? L.q : L.k))[x];
+        reinterpret_cast<float4*>(bsm + (which ? L.qf : L.kf))[x] =
+            make_float4(bf16_lo(w.x), bf16_hi(w.x), bf16_lo(w.y), bf16_hi(w.y));
       }
     }
   }
@@ -574,7 +575,11 @@ palimpsa_bwd_kernel(BwdArgs a, float* __restrict__ ckpt) {
         if (uu < n) {
           float s_bv = 0.f, s_b = 0.f;
 #pragma unroll
-          for (int ww = 0; ww < kWarps; ++ww) { s_bv += rowp[ww][uu][r][0]; s_b += rowp[ww][uu][r][1]; }
+          for (int ww = 0; ww < kWarps; ++ww) {
+            const float2 pr = *reinterpret_cast<const float2*>(&rowp[ww][uu][r][0]);
+            s_bv += pr.x;
+            s_b += pr.y;
+          }
           const size_t o = (head_tok + ts + u) * DV + row0 + r;
           a.dv[o] = s_bv * row_val<BF16>(st + L.b, u, r);
           a.dbeta[o] = fmaf(s_bv, row_val<BF16>(st + L.v, u, r), s_b);
@@ -588,11 +593,11 @@ palimpsa_bwd_kernel(BwdArgs a, float* __restrict__ ckpt) {
         // warps 2, 3: the window's J per token: its 128 lane partials, 8 threads a token
         const int t2 = threadIdx.x - kWin * kRowsPerCta, uu = t2 >> 3, part = t2 & 7;
         float sgs = 0.f;
-        if (uu < n) {
-          const float4* src = reinterpret_cast<const float4*>(&adap[uu][part * 16]);
+        if (uu < n) {  // float4 c * 8 + part: the 8 threads of a token read 128 consecutive bytes
+          const float4* src = reinterpret_cast<const float4*>(&adap[uu][0]);
 #pragma unroll
           for (int c = 0; c < 4; ++c) {
-            const float4 v4 = src[c];
+            const float4 v4 = src[c * 8 + part];
             sgs += (v4.x + v4.y) + (v4.z + v4.w);
           }
         }
