@@ -415,3 +415,12 @@ def test_packed_checkpoint_shape_matches_the_library_size(lib):
 
 def test_scratch_query_rejects_null(lib):
     assert lib.palimpsa_scratch_reserved_bytes(None) == ERR_NULL
+
+
+def test_issue_rate_probe_rejects_bad_arguments(lib):
+    import ctypes
+    out = ctypes.c_double()
+    assert lib.palimpsa_probe_issue_rate(0, None, None) == ERR_NULL
+    assert lib.palimpsa_probe_issue_rate(-1, ctypes.byref(out), None) == ERR_UNSUPPORTED
+    assert lib.palimpsa_probe_issue_rate(5, ctypes.byref(out), None) == ERR_UNSUPPORTED
+    assert set(pal.binding.PROBE_OPS) == {"rcp", "ex2", "ffma", "rsqrt", "lg2"}
