@@ -341,6 +341,11 @@ palimpsa_status palimpsa_segment_summary(const void* q, const void* k, const voi
   FwdArgs a{q, k, v, beta, d_t, A, I_prior, nullptr, nullptr, nullptr, nullptr, nullptr, B, H, T, d_k, d_v,
             chunk == 0 ? 32 : chunk, in_dtype == PALIMPSA_BF16, st,
             g_wait_timeout_ns.load(), g_withhold_first_copy.load(), g_forward_segments.load(), Prologue{}};
+  // pass A does not test the preconditions as it reads the inputs (the forward's pass C does):
+  // a separate pass does
+  const DomainArgs dom{beta, (size_t)B * H * T * d_v, in_dtype == PALIMPSA_BF16, d_t, (size_t)B * H * T, nullptr,
+                       0, A, I_prior, H, st};
+  if (launch_domain_check(dom, static_cast<cudaStream_t>(cuda_stream)) != cudaSuccess) return PALIMPSA_ERR_CUDA;
   StreamOrderedScratch scratch;
   if (launch_segment_summary(a, summary, gamma, static_cast<cudaStream_t>(cuda_stream), &scratch) != cudaSuccess)
     return PALIMPSA_ERR_CUDA;
@@ -448,10 +453,10 @@ palimpsa_status backward_impl(const void* q, const void* k, const void* v, const
   BwdArgs a{q, k, v, beta, d_t, A, I_prior, mu0, I0, dy, dmu_T, dI_T, dq, dk, dv, dbeta, dd_t, dA, dI_prior,
             dmu0, dI0, B, H, T, d_k, d_v, in_dtype == PALIMPSA_BF16};
   a.ckpt_in = ckpt;
+  if (palimpsa_status st = status_word(&a.status)) return st;
   if (packed) {
     a.cu_seqlens = cu_seqlens;
     a.total_T = total_T;
-    if (palimpsa_status st = status_word(&a.status)) return st;
   }
   const size_t tok = packed ? (size_t)H * total_T : (size_t)B * H * T;
   // outputs that the kernel accumulates into start at zero
@@ -462,6 +467,10 @@ palimpsa_status backward_impl(const void* q, const void* k, const void* v, const
   if (cudaMemsetAsync(dA, 0, (size_t)H * sizeof(float), s) != cudaSuccess ||
       cudaMemsetAsync(dI_prior, 0, (size_t)H * sizeof(float), s) != cudaSuccess)
     return PALIMPSA_ERR_CUDA;
+  // the kernel does not test the preconditions as it reads the inputs: a separate pass does
+  const DomainArgs dom{beta, tok * (size_t)d_v, in_dtype == PALIMPSA_BF16, d_t, tok, I0,
+                       (size_t)B * H * d_v * d_k, A, I_prior, H, a.status};
+  if (launch_domain_check(dom, s) != cudaSuccess) return PALIMPSA_ERR_CUDA;
   StreamOrderedScratch scratch;
   float* ck = nullptr;
   const size_t bytes = backward_scratch_bytes(a);

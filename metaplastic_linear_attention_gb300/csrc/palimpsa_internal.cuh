@@ -208,6 +208,23 @@ cudaError_t launch_forward_without_meta(const FwdArgs& a, cudaStream_t s, Scratc
 size_t backward_scratch_bytes(const BwdArgs& a);
 cudaError_t launch_backward(const BwdArgs& a, float* scratch, cudaStream_t s);
 
+// The domain preconditions of a call's inputs, checked by a separate pass for
+// the entry points whose kernels do not test them as they read them.
+struct DomainArgs {
+  const void* beta;       // [n_beta] in the call's input dtype
+  size_t n_beta;
+  bool bf16;
+  const float* d_t;       // [n_dt]
+  size_t n_dt;
+  const float* I0;        // [n_state], or null
+  size_t n_state;
+  const float* A;         // [H]
+  const float* I_prior;   // [H]
+  int H;
+  unsigned int* status;   // latched: kStatusDomain
+};
+cudaError_t launch_domain_check(const DomainArgs& a, cudaStream_t s);
+
 // ------------------------------------------------------------------ device helpers
 #if defined(__CUDACC__)
 

@@ -296,6 +296,57 @@ def test_domain_violation_is_reported_not_faulted():
     _fwd(gi)
 
 
+@pytest.mark.parametrize("what", ["beta", "d_t", "A", "I_prior", "I0"])
+def test_backward_domain_violation_is_reported_not_faulted(what):
+    """The backward reports a broken precondition of its inputs (beta >= 0, d_t >= 0,
+    A > 0, I_prior > 0, I0 > 0) as PALIMPSA_ERR_DOMAIN without a fault; the next
+    call is clean."""
+    wl = syn.WORKLOADS["small_layer"].with_(B=1, H=2, T=70)
+    gi = _gpu(syn.sequence_inputs(wl))
+    mu0, I0 = (t.to(DEV) for t in _random_state(1, 2, wl.d_v, wl.d_k, 11))
+    dy = torch.randn((1, 2, 70, wl.d_v), device=DEV)
+    bad = {k: v.clone() for k, v in gi.items()}
+    bad_I0 = I0.clone()
+    if what == "beta":
+        bad["beta"][0, 1, 37, 5] = -0.5
+    elif what == "d_t":
+        bad["d_t"][0, 0, 3] = -1.0
+    elif what == "A":
+        bad["A"][1] = -0.5
+    elif what == "I_prior":
+        bad["I_prior"][0] = 0.0
+    else:
+        bad_I0[0, 1, 3, 7] = -2.0
+    pal.palimpsa_backward(bad["q"], bad["k"], bad["v"], bad["beta"], bad["d_t"], bad["A"], bad["I_prior"], mu0,
+                          bad_I0, dy)
+    assert pal.palimpsa_get_device_status() == 5          # PALIMPSA_ERR_DOMAIN
+    pal.palimpsa_backward(gi["q"], gi["k"], gi["v"], gi["beta"], gi["d_t"], gi["A"], gi["I_prior"], mu0, I0, dy)
+    assert pal.palimpsa_get_device_status() == 0
+
+
+@pytest.mark.parametrize("what", ["beta", "d_t", "A"])
+def test_segment_summary_domain_violation_is_reported_not_faulted(what):
+    """The segment summary reports a broken precondition of its inputs (checked before pass A)."""
+    wl = syn.WORKLOADS["small_layer"].with_(B=1, H=2, T=300)
+    gi = _gpu(syn.sequence_inputs(wl))
+    bad = {k: v.clone() for k, v in gi.items()}
+    if what == "beta":
+        bad["beta"][0, 0, 200, 9] = -1.0
+    elif what == "d_t":
+        bad["d_t"][0, 1, 17] = float("nan")
+    else:
+        bad["A"][0] = 0.0
+    pal.palimpsa_set_forward_segments(3)
+    try:
+        pal.palimpsa_segment_summary(bad["q"], bad["k"], bad["v"], bad["beta"], bad["d_t"], bad["A"],
+                                     bad["I_prior"])
+        assert pal.palimpsa_get_device_status() == 5      # PALIMPSA_ERR_DOMAIN
+        pal.palimpsa_segment_summary(gi["q"], gi["k"], gi["v"], gi["beta"], gi["d_t"], gi["A"], gi["I_prior"])
+        assert pal.palimpsa_get_device_status() == 0
+    finally:
+        pal.palimpsa_set_forward_segments(0)
+
+
 @pytest.mark.parametrize("S", [1, 3])
 def test_withheld_copy_times_out_and_context_survives(S):
     """A staged copy that never arrives: the bounded mbarrier wait gives up, the
