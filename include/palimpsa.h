@@ -40,8 +40,9 @@
  * - Domain: A > 0, I_prior > 0, d_t >= 0, beta >= 0 and I0 > 0 (all finite)
  *   are preconditions. They are tested on the device: by the forward and step
  *   kernels as they read the inputs, and, for palimpsa_backward (and its
- *   checkpointed and packed forms) and palimpsa_segment_summary, by a short
- *   separate pass over the inputs enqueued before their kernels. A violation
+ *   checkpointed and packed forms), palimpsa_segment_summary and
+ *   palimpsa_state_combine, by a short separate pass over the inputs enqueued
+ *   before their kernels. A violation
  *   leaves that call's outputs unspecified and latches PALIMPSA_ERR_DOMAIN into
  *   the device status word (palimpsa_get_device_status).
  * - Errors are returned as status codes; nothing aborts and no C++ exception

@@ -366,6 +366,11 @@ palimpsa_status palimpsa_state_combine(const float* summaries, const float* gamm
   for (const void* p : a4)
     if (p && !aligned(p, 4)) return PALIMPSA_ERR_ALIGN;
   const long long heads = (long long)B * H, DVK = (long long)d_v * d_k;
+  unsigned int* st = nullptr;
+  if (palimpsa_status s = status_word(&st)) return s;
+  // the preconditions this call reads (I_prior > 0, I0 > 0), checked by a separate pass
+  const DomainArgs dom{nullptr, 0, false, nullptr, 0, I0, I0 ? (size_t)(heads * DVK) : 0, nullptr, I_prior, H, st};
+  if (launch_domain_check(dom, static_cast<cudaStream_t>(cuda_stream)) != cudaSuccess) return PALIMPSA_ERR_CUDA;
   const FoldArgs f{summaries, gammas, heads * 2 * DVK, 2 * DVK, heads, 1, R, heads, H, (int)DVK, true, I_prior,
                    mu0, I0, mu_out, I_out, nullptr, DVK};
   if (launch_fold(f, static_cast<cudaStream_t>(cuda_stream)) != cudaSuccess) return PALIMPSA_ERR_CUDA;

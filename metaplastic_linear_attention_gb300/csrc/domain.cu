@@ -1,7 +1,7 @@
 // Domain check of a call's inputs, for the entry points whose kernels do not
 // test the preconditions as they read them (the backward and the segment
 // summary: their inner loops are register-bound, and a test there measured a
-// few percent slower). One grid-stride pass over the arrays; any violation
+// few percent slower; the state combine, a plain stream over the summaries). One grid-stride pass over the arrays; any violation
 // latches PALIMPSA_ERR_DOMAIN into the device status word. Nothing faults and
 // nothing else is written.
 //
@@ -50,7 +50,7 @@ __global__ void __launch_bounds__(256) palimpsa_domain_kernel(DomainArgs a) {
   for (size_t i = t0; i < a.n_dt; i += stride) bad |= !nonneg_finite(a.d_t[i]);
   if (a.I0)
     for (size_t i = t0; i < a.n_state; i += stride) bad |= !pos_finite(a.I0[i]);
-  for (size_t i = t0; i < (size_t)a.H; i += stride) bad |= !(pos_finite(a.A[i]) && pos_finite(a.I_prior[i]));
+  for (size_t i = t0; i < (size_t)a.H; i += stride) bad |= !((!a.A || pos_finite(a.A[i])) && pos_finite(a.I_prior[i]));
   if (__any_sync(0xffffffffu, bad) && (threadIdx.x & 31) == 0) latch_status(a.status, kStatusDomain);
 }
 

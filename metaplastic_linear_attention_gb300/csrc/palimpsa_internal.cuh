@@ -218,7 +218,7 @@ struct DomainArgs {
   size_t n_dt;
   const float* I0;        // [n_state], or null
   size_t n_state;
-  const float* A;         // [H]
+  const float* A;         // [H], or null
   const float* I_prior;   // [H]
   int H;
   unsigned int* status;   // latched: kStatusDomain

@@ -107,3 +107,21 @@ def test_state_combine_of_nothing_is_the_initial_state_in_place():
     assert rel_l2(mu.cpu().numpy(), mu_keep.cpu().numpy()) < 2e-7   # (I0 mu0) / I0
     mu_d, I_d = pal.palimpsa_state_combine(S, G, Ip)
     assert torch.count_nonzero(mu_d) == 0 and torch.equal(I_d, torch.ones_like(I_d))
+
+
+def test_state_combine_domain_violation_is_reported_not_faulted():
+    """palimpsa_state_combine reports a non-positive I_prior or I0 without a fault."""
+    g = torch.Generator().manual_seed(5)
+    summ = torch.rand((1, 1, 2, 2, 64, 128), generator=g).to(DEV)   # R = 1, B = 1, H = 2
+    gam = torch.rand((1, 1, 2), generator=g).to(DEV)
+    I_prior = torch.ones(2, device=DEV)
+    mu0 = torch.zeros((1, 2, 64, 128), device=DEV)
+    I0 = torch.ones((1, 2, 64, 128), device=DEV)
+    bad_I0 = I0.clone()
+    bad_I0[0, 1, 5, 6] = -1.0
+    pal.palimpsa_state_combine(summ, gam, I_prior, mu0, bad_I0)
+    assert pal.palimpsa_get_device_status() == 5          # PALIMPSA_ERR_DOMAIN
+    pal.palimpsa_state_combine(summ, gam, torch.tensor([1.0, 0.0], device=DEV), mu0, I0)
+    assert pal.palimpsa_get_device_status() == 5
+    pal.palimpsa_state_combine(summ, gam, I_prior, mu0, I0)
+    assert pal.palimpsa_get_device_status() == 0
