@@ -48,10 +48,11 @@
 // dq, dk (the library zeroes them first; one level fewer measured faster). Row
 // sums (d(bv), sum gI k^2) finish over the 8 column lanes with shuffles and
 // over the 4 warps through shared memory once per 8-token window; each lane's
-// sum of gI goes to shared memory as it is and is summed over the CTA's 128
-// lanes once per window. Then one warp turns the window's per-token sums into
-// the alpha gradients with the F recursion above (a suffix sum over the
-// window's tokens), while the other warps go on to the next window.
+// part of J (the sum of its gI injections) goes to shared memory as it is and
+// is summed over the CTA's 128 lanes once per window. Then one warp turns the
+// window's per-token sums into the alpha gradients with the F recursion above
+// (a suffix sum over the window's tokens), while the other warps go on to the
+// next window.
 //
 // Staging: every operand a segment needs (q, k and the CTA's 8 rows of v, beta,
 // dy, plus d_t) is copied into shared memory once per CTA with cp.async, into
