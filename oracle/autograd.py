@@ -54,6 +54,10 @@ def gradients(inputs: dict, dy, dmu_T=None, dI_T=None):
     if dI_T is not None:
         L = L + (I * torch.tensor(np.asarray(dI_T, dtype=np.float64))).sum()
     leaves = [n for n in NAMES if t[n] is not None]
+    if not L.requires_grad:
+        # L reaches no input (an empty sequence with no final-state cotangent, or
+        # one whose final state is a constant): every gradient is zero
+        return {n: np.zeros(t[n].shape) for n in leaves}
     grads = torch.autograd.grad(L, [t[n] for n in leaves], allow_unused=True)
     out = {}
     for n, gr in zip(leaves, grads):

@@ -52,3 +52,39 @@ def pick(t: torch.Tensor, heads):
     bs = [b for b, _ in heads]
     hs = [h for _, h in heads]
     return as_float64_numpy(t)[bs, hs][None]
+
+
+
+U32 = 2.0 ** -24  # fp32 unit roundoff
+
+
+def dA_within_bar(got_dA, ref_dA, got_dd_t, ref_dd_t, d_t, A, rel=TIGHT):
+    """Per-head check of dA against the oracle, through dd_t.
+
+    A and d_t enter the recurrence only through alpha = exp(-A d_t), so
+    dA_h = sum over the head's tokens of dd_t * d_t / A_h, both for the exact
+    gradients and (up to fp32 rounding) for the kernel's, which forms dd_t and dA
+    from the same per-token alpha adjoint. An error in dA is then bounded by the
+    error in dd_t carried through that linear map, ||delta dd_t,h|| ||d_t,h|| / A_h
+    (Cauchy-Schwarz), plus the probabilistic fp32 summation bound
+    4 sqrt(n) u sum|dd_t d_t| / A_h (Higham and Mary, "A new approach to
+    probabilistic rounding error analysis", 2019), plus the relative bar (which
+    also covers the rounding of the kernel's per-CTA partials of the map). dd_t
+    itself is held to the relative bar elsewhere, so this passes dA exactly when it
+    is the consistent image of a dd_t that passed, and a wrong dA term (a wrong
+    token's d_t, a dropped factor) fails it. A relative bar on dA alone cannot be
+    met in any precision where the exact dA vanishes by cancellation: on the first
+    token from the prior state neither I nor mu depends on alpha.
+
+    dA arrays [H]; dd_t, d_t [B, H, T] (head on axis 1) or [H, T] (axis 0); A [H].
+    Returns (ok, detail)."""
+    f = lambda x: np.asarray(x, dtype=np.float64)
+    got, ref, gdd, rdd, dt, A = f(got_dA), f(ref_dA), f(got_dd_t), f(ref_dd_t), f(d_t), f(A)
+    if dt.ndim == 3:
+        gdd, rdd, dt = (np.moveaxis(x, 1, 0).reshape(x.shape[1], -1) for x in (gdd, rdd, dt))
+    n = dt.shape[1]
+    cs = np.linalg.norm(gdd - rdd, axis=1) * np.linalg.norm(dt, axis=1) / A
+    slack = 4.0 * np.sqrt(max(n, 1)) * U32 * np.abs(gdd * dt).sum(axis=1) / A
+    bar = rel * np.abs(ref) + (1.0 + rel) * cs + slack
+    err = np.abs(got - ref)
+    return bool(np.all(err <= bar)), dict(err=err.tolist(), bar=bar.tolist())

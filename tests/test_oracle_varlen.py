@@ -137,3 +137,33 @@ def test_packed_gradients_of_empty_sequences_and_unused_tokens():
         np.testing.assert_array_equal(g["I0"][n], dI[n])
     for name in ("q", "k", "v", "beta", "d_t"):
         assert not g[name][:, 5:].any(), name
+
+
+def test_packed_gradients_when_the_loss_reaches_no_input():
+    """Empty sequences with no final-state cotangent: the loss does not depend on
+    their inputs, so their gradients are zero (with and without an initial state),
+    and A and I_prior get exactly the non-empty sequence's own gradients."""
+    from oracle import autograd as ag
+    rng = np.random.default_rng(13)
+    H, lengths, dk, dv = 2, [0, 4, 0], 4, 3
+    q, k, v, beta, d_t, A, Ip, cu = _packed(rng, H, lengths, dk, dv)
+    N = len(lengths)
+    for with_state in (False, True):
+        x = dict(q=q, k=k, v=v, beta=beta, d_t=d_t, A=A, I_prior=Ip,
+                 mu0=rng.standard_normal((N, H, dv, dk)) if with_state else None,
+                 I0=rng.uniform(0.5, 2.0, (N, H, dv, dk)) if with_state else None)
+        dy = rng.standard_normal(v.shape)
+        g = ovl.gradients(x, cu, dy)
+        one = {n: x[n][None] for n in ("q", "k", "v", "beta", "d_t")}
+        one.update(A=A, I_prior=Ip, mu0=None if x["mu0"] is None else x["mu0"][1:2],
+                   I0=None if x["I0"] is None else x["I0"][1:2])
+        g1 = ag.gradients(one, dy[None])
+        for name in ("A", "I_prior"):
+            np.testing.assert_array_equal(g[name], g1[name], err_msg=name)
+        if with_state:
+            for n in (0, 2):
+                assert not g["mu0"][n].any() and not g["I0"][n].any()
+    # a single empty sequence with no cotangent at all
+    q, k, v, beta, d_t, A, Ip, cu = _packed(rng, H, [0], dk, dv)
+    g = ovl.gradients(dict(q=q, k=k, v=v, beta=beta, d_t=d_t, A=A, I_prior=Ip), cu, np.zeros(v.shape))
+    assert not g["A"].any() and not g["I_prior"].any()
