@@ -21,9 +21,12 @@
 // Structure: one CTA per (head, segment), 8 warps. The raw k, v, beta of each
 // 32-token chunk arrive by bulk async copy into a 2-deep ring (bounded
 // mbarrier waits). Warp 0 forms the chunk's suffix products W; all threads
-// build the bf16 operand tiles (K-major, no swizzle: 8-row x 16-byte core
-// matrices) into one of two operand buffers; one thread issues the MMAs and a
-// tcgen05.commit that frees the buffer again. The accumulators stay in TMEM
+// build the bf16 operand tiles into one of two operand buffers; one thread
+// issues the MMAs and a tcgen05.commit that frees the buffer again. The tiles
+// are MN-major without swizzle, the layout in which the staged rows already
+// lie: a 16-byte row holds 8 consecutive key columns (or value rows) of one
+// token, so building a tile moves whole 16-byte pieces of the staged k, v and
+// beta and never transposes within one. The accumulators stay in TMEM
 // (2 d_v columns) for the whole segment and are read back once with
 // tcgen05.ld. Every wait is bounded; on a timeout the CTA records it, drains
 // its copies and MMAs (bounded), frees its TMEM and returns.
@@ -44,8 +47,8 @@ constexpr int kTcDK = 128;   // key columns = MMA M
 struct TcSmem {
   size_t raw_k, raw_v, raw_b, raw_bytes;    // one raw stage (k, v, beta of a chunk)
   size_t ops, op_bytes;                      // two operand buffers
-  size_t kt, k2h, k2l, xh, xl, yh, yl;       // tiles inside an operand buffer (two K-steps each)
-  size_t a_tile, b_tile;                     // bytes of one K-step of an M- / N-side tile
+  size_t kt, k2h, k2l, xh, xl, yh, yl;       // tiles inside an operand buffer (one chunk each)
+  size_t a_tile, b_tile;                     // bytes of one chunk's M- / N-side tile
   size_t wf, ns, carry, bars, mbars, slot, flag, total;
 
   __host__ __device__ explicit TcSmem(int DV) {
@@ -54,16 +57,16 @@ struct TcSmem {
     raw_b = align_up(raw_v + (size_t)kTcC * DV * 2, 16);
     raw_bytes = align_up(raw_b + (size_t)kTcC * DV * 2, 128);
     ops = align_up(2 * raw_bytes, 1024);
-    a_tile = (size_t)kTcDK * 16 * 2;
-    b_tile = (size_t)DV * 16 * 2;
+    a_tile = (size_t)kTcDK * kTcC * 2;
+    b_tile = (size_t)DV * kTcC * 2;
     kt = 0;
-    k2h = kt + 2 * a_tile;
-    k2l = k2h + 2 * a_tile;
-    xh = k2l + 2 * a_tile;
-    xl = xh + 2 * b_tile;
-    yh = xl + 2 * b_tile;
-    yl = yh + 2 * b_tile;
-    op_bytes = align_up(yl + 2 * b_tile, 1024);
+    k2h = kt + a_tile;
+    k2l = k2h + a_tile;
+    xh = k2l + a_tile;
+    xl = xh + b_tile;
+    yh = xl + b_tile;
+    yl = yh + b_tile;
+    op_bytes = align_up(yl + b_tile, 1024);
     size_t o = ops + 2 * op_bytes;
     wf = o;    o += kTcC * 4;
     ns = o;    o += kTcC * 4;     // per-token 1 / ||k_t|| (q/k norm) or 1
@@ -76,26 +79,45 @@ struct TcSmem {
   }
 };
 
-// Byte offset of the 16-byte core-matrix row holding (row r, tokens k0 .. k0+7)
-// of a K-major, non-swizzled tile of one K = 16 step: core matrices of 8 rows x
-// 16 bytes, two per 8-row group along K (leading byte offset 128), 8-row groups
-// 256 bytes apart (stride byte offset 256).
-__device__ __forceinline__ uint32_t kmajor_off(int r, int k0) {
-  return (uint32_t)(((r >> 3) * 2 + (k0 >> 3)) * 128 + (r & 7) * 16);
-}
+// A chunk's operand tile, MN-major without swizzle: the 16-byte row of 8
+// consecutive MN elements (key columns j = 8 grp .. 8 grp + 7, or value rows)
+// of token t sits at grp * 512 + t * 16. Along K (tokens), core matrices of
+// 8 tokens x 16 bytes are 128 bytes apart (leading byte offset); along MN,
+// groups of 8 elements are 512 bytes apart (stride byte offset). One K = 16
+// step of the MMA starts 256 bytes further per step.
+constexpr uint32_t kMnGroupBytes = kTcC * 16;
+__device__ __forceinline__ uint32_t mn_off(int grp, int t) { return (uint32_t)(grp * kMnGroupBytes + t * 16); }
 
 // tcgen05 shared-memory matrix descriptor: start address, leading byte offset
-// 128 (next core matrix along K), stride byte offset 256 (next 8 rows), the
+// 128 (next 8 tokens along K), stride byte offset 512 (next 8 MN elements), the
 // sm_100-family version field (bits 46-47 = 1), no swizzle.
 __device__ __forceinline__ uint64_t smem_desc(const void* p) {
   const uint64_t a = (smem_u32(p) & 0x3FFFFu) >> 4;
-  return a | ((uint64_t)(128 >> 4) << 16) | ((uint64_t)(256 >> 4) << 32) | (1ull << 46);
+  return a | ((uint64_t)(128 >> 4) << 16) | ((uint64_t)(kMnGroupBytes >> 4) << 32) | (1ull << 46);
 }
 
-// Instruction descriptor, kind::f16: D fp32, A and B bf16, both K-major,
-// N = n (multiple of 16), M = 128.
+// Instruction descriptor, kind::f16: D fp32, A and B bf16, both MN-major
+// (bits 15 and 16), N = n (multiple of 16), M = 128.
 __host__ __device__ constexpr uint32_t idesc_bf16(int n) {
-  return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(n >> 3) << 17) | ((uint32_t)(128 >> 4) << 24);
+  return (1u << 4) | (1u << 7) | (1u << 10) | (1u << 15) | (1u << 16) | ((uint32_t)(n >> 3) << 17) |
+         ((uint32_t)(128 >> 4) << 24);
+}
+
+// Item it of a tile build -> (token t, 8-element group grp) such that the 8
+// items of a shared-memory access phase (consecutive it) have distinct t mod 8
+// (the tile stores, 16 bytes each at t * 16) and distinct grp mod 8 (the staged
+// reads at t * row_bytes + grp * 16, row_bytes a multiple of 128): both
+// conflict-free. Needs the group count G to be a multiple of 8; otherwise
+// group-major order.
+__device__ __forceinline__ void tile_item(int it, int G, int& t, int& grp) {
+  if (G % 8 == 0) {
+    const int i = it & 7, j = it >> 3;
+    t = 8 * (j & 3) + i;
+    grp = 8 * (j >> 5) + ((i + (j >> 2)) & 7);
+  } else {
+    t = it % kTcC;
+    grp = it / kTcC;
+  }
 }
 
 __device__ __forceinline__ void tc_mma(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc, int accumulate) {
@@ -154,28 +176,25 @@ __device__ __forceinline__ void tc_stage(unsigned char* st, const TcSmem& L, uin
 }
 
 // All threads: the M-side tiles of one chunk (tokens >= tc are zero): K^T, and
-// k^2 split into bf16 hi + lo. One item = one key column j and 8 tokens = one
-// 16-byte core-matrix row of each tile.
+// k^2 split into bf16 hi + lo. One item = 8 key columns of one token = one
+// 16-byte row of each tile, read from the staged k as one 16-byte piece.
 __device__ __forceinline__ void build_key_tiles(const unsigned char* raw, unsigned char* ob, const TcSmem& L,
                                                 int tc) {
-  const uint16_t* rk = reinterpret_cast<const uint16_t*>(raw + L.raw_k);
-  for (int it = threadIdx.x; it < kTcDK * (kTcC / 8); it += kTcThreads) {
-    const int j = it % kTcDK, g = it / kTcDK;   // key column, 8-token group
-    uint32_t kt[4], kh[4], kl[4];
+  constexpr int G = kTcDK / 8;
+  for (int it = threadIdx.x; it < G * kTcC; it += kTcThreads) {
+    int t, grp;
+    tile_item(it, G, t, grp);
+    uint4 w = make_uint4(0u, 0u, 0u, 0u);
+    if (t < tc) w = *reinterpret_cast<const uint4*>(raw + L.raw_k + (size_t)t * kTcDK * 2 + grp * 16);
+    const uint32_t kw[4] = {w.x, w.y, w.z, w.w};
+    uint32_t kh[4], kl[4];
 #pragma unroll
-    for (int u = 0; u < 8; u += 2) {
-      uint32_t b[2];
-#pragma unroll
-      for (int e = 0; e < 2; ++e) {
-        const int t = 8 * g + u + e;
-        b[e] = t < tc ? rk[t * kTcDK + j] : 0u;
-      }
-      const float k0 = __uint_as_float(b[0] << 16), k1 = __uint_as_float(b[1] << 16);
-      kt[u / 2] = b[0] | (b[1] << 16);
-      split_bf16x2(k0 * k0, k1 * k1, kh[u / 2], kl[u / 2]);  // k^2 is exact in fp32 and in hi + lo
+    for (int q = 0; q < 4; ++q) {
+      const float k0 = __uint_as_float(kw[q] << 16), k1 = __uint_as_float(kw[q] & 0xffff0000u);
+      split_bf16x2(k0 * k0, k1 * k1, kh[q], kl[q]);  // k^2 is exact in fp32 and in hi + lo
     }
-    const uint32_t off = (uint32_t)((g >> 1) * L.a_tile) + kmajor_off(j, (g & 1) * 8);
-    *reinterpret_cast<uint4*>(ob + L.kt + off) = make_uint4(kt[0], kt[1], kt[2], kt[3]);
+    const uint32_t off = mn_off(grp, t);
+    *reinterpret_cast<uint4*>(ob + L.kt + off) = w;
     *reinterpret_cast<uint4*>(ob + L.k2h + off) = make_uint4(kh[0], kh[1], kh[2], kh[3]);
     *reinterpret_cast<uint4*>(ob + L.k2l + off) = make_uint4(kl[0], kl[1], kl[2], kl[3]);
   }
@@ -190,32 +209,31 @@ __device__ __forceinline__ void build_key_tiles(const unsigned char* raw, unsign
 __device__ __forceinline__ void build_row_tiles(const unsigned char* raw, unsigned char* ob, const TcSmem& L,
                                                 const float* wf, const float* ns, int tc, int DV, const Prologue& pro,
                                                 float bsc) {
-  const uint16_t* rv = reinterpret_cast<const uint16_t*>(raw + L.raw_v);
-  const uint16_t* rb = reinterpret_cast<const uint16_t*>(raw + L.raw_b);
-  for (int it = threadIdx.x; it < DV * (kTcC / 8); it += kTcThreads) {
-    const int i = it % DV, g = it / DV;
-    uint32_t xh[4], xl[4], yh[4], yl[4];
+  const int G = DV / 8;
+  for (int it = threadIdx.x; it < G * kTcC; it += kTcThreads) {
+    int t, grp;
+    tile_item(it, G, t, grp);
+    uint32_t xh[4] = {0u, 0u, 0u, 0u}, xl[4] = {0u, 0u, 0u, 0u}, yh[4] = {0u, 0u, 0u, 0u}, yl[4] = {0u, 0u, 0u, 0u};
+    if (t < tc) {
+      const size_t ro = (size_t)t * DV * 2 + grp * 16;
+      const uint4 vw = *reinterpret_cast<const uint4*>(raw + L.raw_v + ro);
+      const uint4 bw = *reinterpret_cast<const uint4*>(raw + L.raw_b + ro);
+      const uint32_t vv[4] = {vw.x, vw.y, vw.z, vw.w}, bb[4] = {bw.x, bw.y, bw.z, bw.w};
+      const float s = ns[t], ws = wf[t] * s, wss = ws * s;
 #pragma unroll
-    for (int u = 0; u < 8; u += 2) {
-      float x[2], y[2];
-#pragma unroll
-      for (int e = 0; e < 2; ++e) {
-        const int t = 8 * g + u + e;
-        x[e] = 0.f;
-        y[e] = 0.f;
-        if (t < tc) {
-          float b = __uint_as_float((uint32_t)rb[t * DV + i] << 16);
-          const float v = __uint_as_float((uint32_t)rv[t * DV + i] << 16);
-          if (pro.on) b = bsc * sigmoid_f(b);
-          const float ws = wf[t] * ns[t];
-          y[e] = ws * ns[t] * b;
-          x[e] = pro.v_star ? ws * v : ws * b * v;
+      for (int q = 0; q < 4; ++q) {
+        float b0 = __uint_as_float(bb[q] << 16), b1 = __uint_as_float(bb[q] & 0xffff0000u);
+        const float v0 = __uint_as_float(vv[q] << 16), v1 = __uint_as_float(vv[q] & 0xffff0000u);
+        if (pro.on) {
+          b0 = bsc * sigmoid_f(b0);
+          b1 = bsc * sigmoid_f(b1);
         }
+        const float x0 = pro.v_star ? ws * v0 : ws * b0 * v0, x1 = pro.v_star ? ws * v1 : ws * b1 * v1;
+        split_bf16x2(x0, x1, xh[q], xl[q]);
+        split_bf16x2(wss * b0, wss * b1, yh[q], yl[q]);
       }
-      split_bf16x2(x[0], x[1], xh[u / 2], xl[u / 2]);
-      split_bf16x2(y[0], y[1], yh[u / 2], yl[u / 2]);
     }
-    const uint32_t off = (uint32_t)((g >> 1) * L.b_tile) + kmajor_off(i, (g & 1) * 8);
+    const uint32_t off = mn_off(grp, t);
     *reinterpret_cast<uint4*>(ob + L.xh + off) = make_uint4(xh[0], xh[1], xh[2], xh[3]);
     *reinterpret_cast<uint4*>(ob + L.xl + off) = make_uint4(xl[0], xl[1], xl[2], xl[3]);
     *reinterpret_cast<uint4*>(ob + L.yh + off) = make_uint4(yh[0], yh[1], yh[2], yh[3]);
@@ -230,8 +248,8 @@ __device__ __forceinline__ void issue_chunk_mmas(const unsigned char* ob, const 
   const uint32_t dM = tmem, dI = tmem + (uint32_t)DV;
 #pragma unroll
   for (int ks = 0; ks < 2; ++ks) {
-    const unsigned char* a0 = ob + ks * L.a_tile;
-    const unsigned char* b0 = ob + ks * L.b_tile;
+    const unsigned char* a0 = ob + ks * 256;  // tokens 16 ks .. 16 ks + 15 of every 8-element group
+    const unsigned char* b0 = ob + ks * 256;
     const int acc = (first && ks == 0) ? 0 : 1;
     tc_mma(dM, smem_desc(a0 + L.kt), smem_desc(b0 + L.xh), idesc, acc);
     tc_mma(dM, smem_desc(a0 + L.kt), smem_desc(b0 + L.xl), idesc, 1);
