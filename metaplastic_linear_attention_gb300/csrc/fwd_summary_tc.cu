@@ -18,15 +18,18 @@
 //   D_M += K^T X_hi + K^T X_lo,   D_I += (K^2)_hi^T Y_hi + (K^2)_hi^T Y_lo + (K^2)_lo^T Y_hi
 // (the dropped (K^2)_lo^T Y_lo term is below 2^-16 relative).
 //
-// Structure: one CTA per (head, segment), 8 warps. The raw k, v, beta of each
-// 32-token chunk arrive by bulk async copy into a 2-deep ring (bounded
-// mbarrier waits). Warp 0 forms the chunk's suffix products W; all threads
-// build the bf16 operand tiles into one of two operand buffers; one thread
-// issues the MMAs and a tcgen05.commit that frees the buffer again. The tiles
-// are MN-major without swizzle, the layout in which the staged rows already
-// lie: a 16-byte row holds 8 consecutive key columns (or value rows) of one
-// token, so building a tile moves whole 16-byte pieces of the staged k, v and
-// beta and never transposes within one. The accumulators stay in TMEM
+// Structure: one CTA per (head, segment), 8 warps with two roles. The raw k,
+// v, beta of each 32-token chunk arrive by bulk async copy into a 2-deep ring.
+// Warp 0 is the control warp: one of its threads issues the copies, and the
+// MMAs of a chunk once its operand tiles are complete, followed by a
+// tcgen05.commit that frees the operand buffer again. Warps 1-7 build the
+// tiles: each forms the chunk's suffix products W itself (a warp scan over the
+// 32 tokens), so no CTA barrier sits in the chunk loop; the roles meet only at
+// mbarriers (raw stage full, operand buffer full, operand buffer free). The
+// tiles are MN-major without swizzle, the layout in which the staged rows
+// already lie: a 16-byte row holds 8 consecutive key columns (or value rows)
+// of one token, so building a tile moves whole 16-byte pieces of the staged k,
+// v and beta and never transposes within one. The accumulators stay in TMEM
 // (2 d_v columns) for the whole segment and are read back once with
 // tcgen05.ld. Every wait is bounded; on a timeout the CTA records it, drains
 // its copies and MMAs (bounded), frees its TMEM and returns.
@@ -40,6 +43,7 @@ namespace {
 using namespace fwd;
 
 constexpr int kTcThreads = 256;
+constexpr int kTcBuilders = kTcThreads - 32;  // warps 1-7 build the operand tiles
 constexpr int kTcC = 32;     // tokens per chunk: two K = 16 MMA steps
 constexpr int kTcDK = 128;   // key columns = MMA M
 
@@ -49,7 +53,7 @@ struct TcSmem {
   size_t ops, op_bytes;                      // two operand buffers
   size_t kt, k2h, k2l, xh, xl, yh, yl;       // tiles inside an operand buffer (one chunk each)
   size_t a_tile, b_tile;                     // bytes of one chunk's M- / N-side tile
-  size_t wf, ns, carry, bars, mbars, slot, flag, total;
+  size_t ns, gam, bars, fbars, mbars, nbars, slot, flag, issued, total;
 
   __host__ __device__ explicit TcSmem(int DV) {
     raw_k = 0;
@@ -68,13 +72,15 @@ struct TcSmem {
     yl = yh + b_tile;
     op_bytes = align_up(yl + b_tile, 1024);
     size_t o = ops + 2 * op_bytes;
-    wf = o;    o += kTcC * 4;
-    ns = o;    o += kTcC * 4;     // per-token 1 / ||k_t|| (q/k norm) or 1
-    carry = o; o += 16;
-    bars = o;  o += 2 * 8;    // raw ring
-    mbars = o; o += 2 * 8;    // MMA completion per operand buffer
-    slot = o;  o += 16;       // TMEM base address
-    flag = o;  o += 16;
+    ns = o;    o += 2 * kTcC * 4;  // per-token 1 / ||k_t|| (q/k norm), two chunks
+    gam = o;   o += 16;            // Gamma of the segment
+    bars = o;  o += 2 * 8;         // raw stage full (copy bytes)
+    fbars = o; o += 2 * 8;         // operand buffer full (builder arrivals)
+    mbars = o; o += 2 * 8;         // operand buffer free (MMA completion)
+    nbars = o; o += 2 * 8;         // key-norm scales of a chunk written (builder arrivals)
+    slot = o;  o += 16;            // TMEM base address
+    flag = o;  o += 16;            // a wait timed out
+    issued = o; o += 16;           // chunks whose MMAs were issued
     total = align_up(o, 128);
   }
 };
@@ -179,9 +185,9 @@ __device__ __forceinline__ void tc_stage(unsigned char* st, const TcSmem& L, uin
 // k^2 split into bf16 hi + lo. One item = 8 key columns of one token = one
 // 16-byte row of each tile, read from the staged k as one 16-byte piece.
 __device__ __forceinline__ void build_key_tiles(const unsigned char* raw, unsigned char* ob, const TcSmem& L,
-                                                int tc) {
+                                                int tc, int btid) {
   constexpr int G = kTcDK / 8;
-  for (int it = threadIdx.x; it < G * kTcC; it += kTcThreads) {
+  for (int it = btid; it < G * kTcC; it += kTcBuilders) {
     int t, grp;
     tile_item(it, G, t, grp);
     uint4 w = make_uint4(0u, 0u, 0u, 0u);
@@ -207,19 +213,23 @@ __device__ __forceinline__ void build_key_tiles(const unsigned char* raw, unsign
 // keeps K exact in bf16); beta through the fused prologue when it is on.
 // Tokens >= tc are zero.
 __device__ __forceinline__ void build_row_tiles(const unsigned char* raw, unsigned char* ob, const TcSmem& L,
-                                                const float* wf, const float* ns, int tc, int DV, const Prologue& pro,
-                                                float bsc) {
+                                                float w_lane, const float* ns, int tc, int DV, const Prologue& pro,
+                                                float bsc, int btid) {
   const int G = DV / 8;
-  for (int it = threadIdx.x; it < G * kTcC; it += kTcThreads) {
+  // the same trip count on every lane: W_t comes from lane t of the warp by a shuffle
+  for (int base = 0; base < G * kTcC; base += kTcBuilders) {
+    const int it = base + btid;
     int t, grp;
     tile_item(it, G, t, grp);
+    const float wt = __shfl_sync(0xffffffffu, w_lane, t & (kTcC - 1));
+    if (it >= G * kTcC) continue;
     uint32_t xh[4] = {0u, 0u, 0u, 0u}, xl[4] = {0u, 0u, 0u, 0u}, yh[4] = {0u, 0u, 0u, 0u}, yl[4] = {0u, 0u, 0u, 0u};
     if (t < tc) {
       const size_t ro = (size_t)t * DV * 2 + grp * 16;
       const uint4 vw = *reinterpret_cast<const uint4*>(raw + L.raw_v + ro);
       const uint4 bw = *reinterpret_cast<const uint4*>(raw + L.raw_b + ro);
       const uint32_t vv[4] = {vw.x, vw.y, vw.z, vw.w}, bb[4] = {bw.x, bw.y, bw.z, bw.w};
-      const float s = ns[t], ws = wf[t] * s, wss = ws * s;
+      const float s = ns ? ns[t] : 1.f, ws = wt * s, wss = ws * s;
 #pragma unroll
       for (int q = 0; q < 4; ++q) {
         float b0 = __uint_as_float(bb[q] << 16), b1 = __uint_as_float(bb[q] & 0xffff0000u);
@@ -272,12 +282,13 @@ palimpsa_fwd_summary_tc_kernel(FwdArgs a, int nslot, int seg_len, float* __restr
   const TcSmem L(DV);
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L.bars);
+  uint64_t* fbars = reinterpret_cast<uint64_t*>(smem + L.fbars);
   uint64_t* mbars = reinterpret_cast<uint64_t*>(smem + L.mbars);
+  uint64_t* nbars = reinterpret_cast<uint64_t*>(smem + L.nbars);
   uint32_t* slot = reinterpret_cast<uint32_t*>(smem + L.slot);
   volatile int* flag = reinterpret_cast<volatile int*>(smem + L.flag);
-  float* wf = reinterpret_cast<float*>(smem + L.wf);
-  float* ns = reinterpret_cast<float*>(smem + L.ns);
-  float* carry = reinterpret_cast<float*>(smem + L.carry);
+  int* issued_s = reinterpret_cast<int*>(smem + L.issued);
+  float* gam = reinterpret_cast<float*>(smem + L.gam);
   const float A_h = a.A[tl.h];
   const float bsc = a.pro.b_scale ? a.pro.b_scale[tl.h] : 1.f;
   const int nch = (tl.tn + kTcC - 1) / kTcC;
@@ -286,12 +297,15 @@ palimpsa_fwd_summary_tc_kernel(FwdArgs a, int nslot, int seg_len, float* __restr
   const float* gd = a.d_t + tok_base;
 
   if (threadIdx.x == 0) {
-    mbar_init(&bars[0], 1);
-    mbar_init(&bars[1], 1);
-    mbar_init(&mbars[0], 1);
-    mbar_init(&mbars[1], 1);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&bars[i], 1);
+      mbar_init(&fbars[i], kTcBuilders);
+      mbar_init(&mbars[i], 1);
+      mbar_init(&nbars[i], kTcBuilders);
+    }
     *flag = 0;
-    carry[0] = 1.f;
+    *issued_s = 0;
+    gam[0] = 1.f;
     fence_mbar_init();
   }
   if (warp == 0) {
@@ -306,44 +320,57 @@ palimpsa_fwd_summary_tc_kernel(FwdArgs a, int nslot, int seg_len, float* __restr
   const uint32_t tmem = *slot;
 
   // Processing chunk c is segment-local chunk nch - 1 - c (W is a suffix product).
-  bool pend[2] = {false, false};  // thread 0: raw copies in flight per stage, for a clean exit
-  uint32_t ppar[2] = {0u, 0u};
-  if (threadIdx.x == 0) {
-    for (int c = 0; c < 2 && c < nch; ++c) {
-      if (c == 0 && a.withhold_first_copy) continue;
-      const int t0 = (nch - 1 - c) * kTcC;
-      tc_stage(smem + (size_t)(c & 1) * L.raw_bytes, L, &bars[c & 1], a, tok_base + t0, min(kTcC, tl.tn - t0));
-      pend[c & 1] = true;
-      ppar[c & 1] = (uint32_t)(c >> 1) & 1u;
+  if (warp == 0) {
+    // ---- control: copies into the raw ring, and the MMAs of each complete chunk
+    if (lane == 0) {
+      bool pend[2] = {false, false};  // raw copies in flight per stage, for a clean exit
+      uint32_t ppar[2] = {0u, 0u};
+      for (int c = 0; c < 2 && c < nch; ++c) {
+        if (c == 0 && a.withhold_first_copy) continue;
+        const int t0 = (nch - 1 - c) * kTcC;
+        tc_stage(smem + (size_t)(c & 1) * L.raw_bytes, L, &bars[c & 1], a, tok_base + t0, min(kTcC, tl.tn - t0));
+        pend[c & 1] = true;
+        ppar[c & 1] = (uint32_t)(c >> 1) & 1u;
+      }
+      int c = 0;
+      for (; c < nch && !*flag; ++c) {
+        // the builders are done with raw stage c & 1 and operand buffer c & 1 is complete
+        if (!mbar_wait_bounded(&fbars[c & 1], (uint32_t)(c >> 1) & 1u, a.wait_timeout_ns)) {
+          *flag = 1;
+          break;
+        }
+        pend[c & 1] = false;  // the builders waited for this stage's bytes
+        if (c + 2 < nch) {
+          const int t2 = (nch - 1 - (c + 2)) * kTcC;
+          tc_stage(smem + (size_t)(c & 1) * L.raw_bytes, L, &bars[c & 1], a, tok_base + t2, min(kTcC, tl.tn - t2));
+          pend[c & 1] = true;
+          ppar[c & 1] = (uint32_t)((c + 2) >> 1) & 1u;
+        }
+        tc_fence_after();
+        issue_chunk_mmas(smem + L.ops + (size_t)(c & 1) * L.op_bytes, L, tmem, DV, c == 0);
+        tc_commit(&mbars[c & 1]);
+      }
+      *issued_s = c;
+      // copies still in flight (a timeout upstream) land before the CTA may exit
+      if (*flag) {
+        if (pend[0]) mbar_wait_bounded(&bars[0], ppar[0], 1000000000ull);
+        if (pend[1]) mbar_wait_bounded(&bars[1], ppar[1], 1000000000ull);
+      }
     }
-  }
-  int c = 0;
-  bool failed = false;
-  // d_t one chunk ahead (warp 0, lane t = token t), so its load lands during a chunk of compute
-  float d_next = 0.f;
-  if (warp == 0 && nch > 0) {
-    const int t0n = (nch - 1) * kTcC;
-    if (lane < min(kTcC, tl.tn - t0n)) d_next = gd[t0n + lane];
-  }
-  for (; c < nch; ++c) {
-    const int t0 = (nch - 1 - c) * kTcC, tc = min(kTcC, tl.tn - t0);
-    const float d_cur = d_next;
-    if (warp == 0 && c + 1 < nch) {
-      const int t0n = (nch - 2 - c) * kTcC;  // chunks before the last are whole
-      d_next = gd[t0n + lane];
+  } else {
+    // ---- builders (warps 1-7)
+    const int btid = threadIdx.x - 32;
+    float carry = 1.f;  // product of the alphas of the chunks already processed (later tokens)
+    float d_next = 0.f;  // d_t one chunk ahead, lane t = token t
+    if (nch > 0) {
+      const int t0n = (nch - 1) * kTcC;
+      if (lane < min(kTcC, tl.tn - t0n)) d_next = gd[t0n + lane];
     }
-    if (!mbar_wait_bounded(&bars[c & 1], (uint32_t)(c >> 1) & 1u, a.wait_timeout_ns)) *flag = 1;
-    // operand buffer c & 1 was last read by the MMAs of chunk c - 2
-    if (c >= 2 && !mbar_wait_bounded(&mbars[c & 1], (uint32_t)((c - 2) >> 1) & 1u, a.wait_timeout_ns)) *flag = 1;
-    __syncthreads();
-    if (*flag) {
-      failed = true;
-      break;
-    }
-    if (threadIdx.x == 0) pend[c & 1] = false;
-    const unsigned char* raw = smem + (size_t)(c & 1) * L.raw_bytes;
-    unsigned char* ob = smem + L.ops + (size_t)(c & 1) * L.op_bytes;
-    if (warp == 0) {  // W_t = carry * prod_{t < u < tc} alpha_u (suffix products inside the chunk)
+    for (int c = 0; c < nch; ++c) {
+      const int t0 = (nch - 1 - c) * kTcC, tc = min(kTcC, tl.tn - t0);
+      const float d_cur = d_next;
+      if (c + 1 < nch) d_next = gd[(nch - 2 - c) * kTcC + lane];  // chunks before the last are whole
+      // W_t = carry * prod_{t < u < tc} alpha_u (lane t), while the copies land
       float d = lane < tc ? d_cur : 0.f;
       if (a.pro.on) d = softplus_f(d);
       const float al = lane < tc ? expf(-A_h * d) : 1.f;
@@ -354,56 +381,63 @@ palimpsa_fwd_summary_tc_kernel(FwdArgs a, int nslot, int seg_len, float* __restr
         if (lane + off < 32) p *= o;
       }
       const float excl = __shfl_down_sync(0xffffffffu, p, 1);
-      const float cin = carry[0];
-      if (lane < tc) wf[lane] = cin * (lane + 1 < tc ? excl : 1.f);
-      __syncwarp();
-      if (lane == 0) carry[0] = cin * p;
-    }
-    // key-norm scales: warp w takes tokens w, w + 8, ... (each lane 4 of the 128 columns)
-    for (int t = warp; t < kTcC; t += kTcThreads / 32) {
-      float sc = 1.f;
-      if (a.pro.qk_norm && t < tc) {
-        const uint2 w2 = *reinterpret_cast<const uint2*>(raw + L.raw_k + ((size_t)t * kTcDK + 4 * lane) * 2);
-        const float k0 = bf16_lo(w2.x), k1 = bf16_hi(w2.x), k2 = bf16_lo(w2.y), k3 = bf16_hi(w2.y);
-        float ss = fmaf(k0, k0, fmaf(k1, k1, fmaf(k2, k2, k3 * k3)));
+      const float w_lane = lane < tc ? carry * (lane + 1 < tc ? excl : 1.f) : 0.f;
+      carry *= __shfl_sync(0xffffffffu, p, 0);
+      bool ok = mbar_wait_bounded(&bars[c & 1], (uint32_t)(c >> 1) & 1u, a.wait_timeout_ns);
+      // operand buffer c & 1 was last read by the MMAs of chunk c - 2
+      if (ok && c >= 2) ok = mbar_wait_bounded(&mbars[c & 1], (uint32_t)((c - 2) >> 1) & 1u, a.wait_timeout_ns);
+      if (!ok) *flag = 1;
+      if (*flag) break;  // the arrivals of this chunk never come: the control warp times out too
+      const unsigned char* raw = smem + (size_t)(c & 1) * L.raw_bytes;
+      unsigned char* ob = smem + L.ops + (size_t)(c & 1) * L.op_bytes;
+      const float* nsc = nullptr;
+      if (a.pro.qk_norm) {
+        // key-norm scales of the chunk (builder warp b takes tokens b - 1, b + 6, ...; each lane
+        // 4 of the 128 columns), two chunks' worth so that a slow warp still reads its own
+        float* ns = reinterpret_cast<float*>(smem + L.ns) + (c & 1) * kTcC;
+        for (int t = warp - 1; t < kTcC; t += kTcBuilders / 32) {
+          float sc = 1.f;
+          if (t < tc) {
+            const uint2 w2 = *reinterpret_cast<const uint2*>(raw + L.raw_k + ((size_t)t * kTcDK + 4 * lane) * 2);
+            const float k0 = bf16_lo(w2.x), k1 = bf16_hi(w2.x), k2 = bf16_lo(w2.y), k3 = bf16_hi(w2.y);
+            float ss = fmaf(k0, k0, fmaf(k1, k1, fmaf(k2, k2, k3 * k3)));
 #pragma unroll
-        for (int m = 16; m > 0; m >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, m);
-        sc = rsqrtf(fmaxf(ss, kNormFloorSq));
+            for (int m = 16; m > 0; m >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, m);
+            sc = rsqrtf(fmaxf(ss, kNormFloorSq));
+          }
+          if (lane == 0) ns[t] = sc;
+        }
+        // every builder's scales are in place (a bounded wait, as every wait here)
+        asm volatile("mbarrier.arrive.release.cta.shared::cta.b64 _, [%0];" ::"r"(smem_u32(&nbars[c & 1]))
+                     : "memory");
+        if (!mbar_wait_bounded(&nbars[c & 1], (uint32_t)(c >> 1) & 1u, a.wait_timeout_ns)) {
+          *flag = 1;
+          break;
+        }
+        nsc = ns;
       }
-      if (lane == 0) ns[t] = sc;
+      build_key_tiles(raw, ob, L, tc, btid);
+      build_row_tiles(raw, ob, L, w_lane, nsc, tc, DV, a.pro, bsc, btid);
+      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // generic-proxy writes -> tensor cores
+      asm volatile("mbarrier.arrive.release.cta.shared::cta.b64 _, [%0];" ::"r"(smem_u32(&fbars[c & 1]))
+                   : "memory");
     }
-    build_key_tiles(raw, ob, L, tc);
-    __syncthreads();  // W and the norm scales ready
-    build_row_tiles(raw, ob, L, wf, ns, tc, DV, a.pro, bsc);
-    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // generic-proxy writes -> tensor cores
-    __syncthreads();  // operands complete; the raw stage is free
-    if (threadIdx.x == 0) {
-      if (c + 2 < nch) {
-        const int t2 = (nch - 1 - (c + 2)) * kTcC;
-        tc_stage(smem + (size_t)(c & 1) * L.raw_bytes, L, &bars[c & 1], a, tok_base + t2, min(kTcC, tl.tn - t2));
-        pend[c & 1] = true;
-        ppar[c & 1] = (uint32_t)((c + 2) >> 1) & 1u;
-      }
-      tc_fence_after();
-      issue_chunk_mmas(ob, L, tmem, DV, c == 0);
-      tc_commit(&mbars[c & 1]);
-    }
-  }
-
-  // MMAs of chunks max(0, c - 2) .. c - 1 may still run: wait (bounded) before
-  // reading or freeing the accumulators.
-  const unsigned long long drain_ns = failed ? 1000000000ull : a.wait_timeout_ns;
-  bool mma_ok = true;
-  for (int k = c - 2 > 0 ? c - 2 : 0; k < c; ++k)
-    if (!mbar_wait_bounded(&mbars[k & 1], (uint32_t)(k >> 1) & 1u, drain_ns)) mma_ok = false;
-  if (threadIdx.x == 0 && (failed || !mma_ok)) {
-    latch_status(a.status, kStatusTimeout);
-    if (pend[0]) mbar_wait_bounded(&bars[0], ppar[0], 1000000000ull);
-    if (pend[1]) mbar_wait_bounded(&bars[1], ppar[1], 1000000000ull);
+    if (warp == 1 && lane == 0) gam[0] = carry;
   }
   __syncthreads();
+  const bool failed = *flag != 0;
+  const int issued = *issued_s;
+
+  // MMAs of chunks max(0, issued - 2) .. issued - 1 may still run: wait (bounded)
+  // before reading or freeing the accumulators.
+  const unsigned long long drain_ns = failed ? 1000000000ull : a.wait_timeout_ns;
+  bool mma_ok = true;
+  for (int k = issued - 2 > 0 ? issued - 2 : 0; k < issued; ++k)
+    if (!mbar_wait_bounded(&mbars[k & 1], (uint32_t)(k >> 1) & 1u, drain_ns)) mma_ok = false;
+  if (threadIdx.x == 0 && (failed || !mma_ok)) latch_status(a.status, kStatusTimeout);
+  __syncthreads();
   tc_fence_after();
-  if (!failed && __all_sync(0xffffffffu, mma_ok)) {
+  if (!failed && __syncthreads_and(mma_ok)) {
     // warps 0-3 read dM^T, warps 4-7 dIbar^T; TMEM lane = key column j
     const int part = warp >> 2;
     const int j = 32 * (warp & 3) + lane;
@@ -419,7 +453,7 @@ palimpsa_fwd_summary_tc_kernel(FwdArgs a, int nslot, int seg_len, float* __restr
 #pragma unroll
       for (int q = 0; q < 32; ++q) out[(size_t)(cb + q) * kTcDK + j] = v[q];
     }
-    if (threadIdx.x == 0) seg_gamma[(size_t)tl.bh * nslot + tl.seg] = carry[0];
+    if (threadIdx.x == 0) seg_gamma[(size_t)tl.bh * nslot + tl.seg] = gam[0];
   }
   tc_fence_before();
   __syncthreads();
