@@ -299,9 +299,9 @@ palimpsa_fwd_summary_tc_kernel(FwdArgs a, int nslot, int seg_len, float* __restr
   if (threadIdx.x == 0) {
     for (int i = 0; i < 2; ++i) {
       mbar_init(&bars[i], 1);
-      mbar_init(&fbars[i], kTcBuilders);
+      mbar_init(&fbars[i], kTcBuilders / 32);  // one arrival per builder warp
       mbar_init(&mbars[i], 1);
-      mbar_init(&nbars[i], kTcBuilders);
+      mbar_init(&nbars[i], kTcBuilders / 32);
     }
     *flag = 0;
     *issued_s = 0;
@@ -386,8 +386,12 @@ palimpsa_fwd_summary_tc_kernel(FwdArgs a, int nslot, int seg_len, float* __restr
       bool ok = mbar_wait_bounded(&bars[c & 1], (uint32_t)(c >> 1) & 1u, a.wait_timeout_ns);
       // operand buffer c & 1 was last read by the MMAs of chunk c - 2
       if (ok && c >= 2) ok = mbar_wait_bounded(&mbars[c & 1], (uint32_t)((c - 2) >> 1) & 1u, a.wait_timeout_ns);
-      if (!ok) *flag = 1;
-      if (*flag) break;  // the arrivals of this chunk never come: the control warp times out too
+      // leave together (the loop holds warp shuffles); the arrivals of this chunk then
+      // never come, and the control warp's wait for them times out too
+      if (__any_sync(0xffffffffu, !ok || *flag)) {
+        *flag = 1;
+        break;
+      }
       const unsigned char* raw = smem + (size_t)(c & 1) * L.raw_bytes;
       unsigned char* ob = smem + L.ops + (size_t)(c & 1) * L.op_bytes;
       const float* nsc = nullptr;
@@ -408,9 +412,11 @@ palimpsa_fwd_summary_tc_kernel(FwdArgs a, int nslot, int seg_len, float* __restr
           if (lane == 0) ns[t] = sc;
         }
         // every builder's scales are in place (a bounded wait, as every wait here)
-        asm volatile("mbarrier.arrive.release.cta.shared::cta.b64 _, [%0];" ::"r"(smem_u32(&nbars[c & 1]))
-                     : "memory");
-        if (!mbar_wait_bounded(&nbars[c & 1], (uint32_t)(c >> 1) & 1u, a.wait_timeout_ns)) {
+        __syncwarp();
+        if (lane == 0)
+          asm volatile("mbarrier.arrive.release.cta.shared::cta.b64 _, [%0];" ::"r"(smem_u32(&nbars[c & 1]))
+                       : "memory");
+        if (__any_sync(0xffffffffu, !mbar_wait_bounded(&nbars[c & 1], (uint32_t)(c >> 1) & 1u, a.wait_timeout_ns))) {
           *flag = 1;
           break;
         }
@@ -419,8 +425,10 @@ palimpsa_fwd_summary_tc_kernel(FwdArgs a, int nslot, int seg_len, float* __restr
       build_key_tiles(raw, ob, L, tc, btid);
       build_row_tiles(raw, ob, L, w_lane, nsc, tc, DV, a.pro, bsc, btid);
       asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // generic-proxy writes -> tensor cores
-      asm volatile("mbarrier.arrive.release.cta.shared::cta.b64 _, [%0];" ::"r"(smem_u32(&fbars[c & 1]))
-                   : "memory");
+      __syncwarp();  // the warp's tiles (and its reads of the raw stage) are done: one arrival for the warp
+      if (lane == 0)
+        asm volatile("mbarrier.arrive.release.cta.shared::cta.b64 _, [%0];" ::"r"(smem_u32(&fbars[c & 1]))
+                     : "memory");
     }
     if (warp == 1 && lane == 0) gam[0] = carry;
   }
