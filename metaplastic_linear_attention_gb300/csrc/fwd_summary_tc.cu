@@ -295,7 +295,17 @@ palimpsa_fwd_summary_tc_kernel(FwdArgs a, int nslot, int seg_len, float* __restr
   const uint32_t ncols = DV * 2 <= 64 ? 64u : DV * 2 <= 128 ? 128u : 256u;
   const size_t tok_base = tl.head_tok + tl.tb;
   const float* gd = a.d_t + tok_base;
+  // builders: d_t one chunk ahead (lane t = token t); the first chunk's load is
+  // issued before the set-up below, so that it lands meanwhile
+  float d_next = 0.f;
+  if (warp > 0 && nch > 0) {
+    const int t0n = (nch - 1) * kTcC;
+    if (lane < min(kTcC, tl.tn - t0n)) d_next = gd[t0n + lane];
+  }
 
+  // thread 0: raw copies in flight per stage (for a clean exit), and their phases
+  bool pend[2] = {false, false};
+  uint32_t ppar[2] = {0u, 0u};
   if (threadIdx.x == 0) {
     for (int i = 0; i < 2; ++i) {
       mbar_init(&bars[i], 1);
@@ -307,6 +317,15 @@ palimpsa_fwd_summary_tc_kernel(FwdArgs a, int nslot, int seg_len, float* __restr
     *issued_s = 0;
     gam[0] = 1.f;
     fence_mbar_init();
+    // the first two chunks' copies go out now and land during the set-up below
+    // (processing chunk c is segment-local chunk nch - 1 - c: W is a suffix product)
+    for (int c = 0; c < 2 && c < nch; ++c) {
+      if (c == 0 && a.withhold_first_copy) continue;
+      const int t0 = (nch - 1 - c) * kTcC;
+      tc_stage(smem + (size_t)(c & 1) * L.raw_bytes, L, &bars[c & 1], a, tok_base + t0, min(kTcC, tl.tn - t0));
+      pend[c & 1] = true;
+      ppar[c & 1] = (uint32_t)(c >> 1) & 1u;
+    }
   }
   if (warp == 0) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(slot)),
@@ -319,19 +338,9 @@ palimpsa_fwd_summary_tc_kernel(FwdArgs a, int nslot, int seg_len, float* __restr
   tc_fence_after();
   const uint32_t tmem = *slot;
 
-  // Processing chunk c is segment-local chunk nch - 1 - c (W is a suffix product).
   if (warp == 0) {
     // ---- control: copies into the raw ring, and the MMAs of each complete chunk
     if (lane == 0) {
-      bool pend[2] = {false, false};  // raw copies in flight per stage, for a clean exit
-      uint32_t ppar[2] = {0u, 0u};
-      for (int c = 0; c < 2 && c < nch; ++c) {
-        if (c == 0 && a.withhold_first_copy) continue;
-        const int t0 = (nch - 1 - c) * kTcC;
-        tc_stage(smem + (size_t)(c & 1) * L.raw_bytes, L, &bars[c & 1], a, tok_base + t0, min(kTcC, tl.tn - t0));
-        pend[c & 1] = true;
-        ppar[c & 1] = (uint32_t)(c >> 1) & 1u;
-      }
       int c = 0;
       for (; c < nch && !*flag; ++c) {
         // the builders are done with raw stage c & 1 and operand buffer c & 1 is complete
@@ -361,11 +370,6 @@ palimpsa_fwd_summary_tc_kernel(FwdArgs a, int nslot, int seg_len, float* __restr
     // ---- builders (warps 1-7)
     const int btid = threadIdx.x - 32;
     float carry = 1.f;  // product of the alphas of the chunks already processed (later tokens)
-    float d_next = 0.f;  // d_t one chunk ahead, lane t = token t
-    if (nch > 0) {
-      const int t0n = (nch - 1) * kTcC;
-      if (lane < min(kTcC, tl.tn - t0n)) d_next = gd[t0n + lane];
-    }
     for (int c = 0; c < nch; ++c) {
       const int t0 = (nch - 1 - c) * kTcC, tc = min(kTcC, tl.tn - t0);
       const float d_cur = d_next;
