@@ -25,7 +25,8 @@
 // tcgen05.commit that frees the operand buffer again. Warps 1-7 build the
 // tiles: each forms the chunk's suffix products W itself (a warp scan over the
 // 32 tokens), so no CTA barrier sits in the chunk loop; the roles meet only at
-// mbarriers (raw stage full, operand buffer full, operand buffer free). The
+// mbarriers (raw stage full, operand buffer full, operand buffer free, and
+// among the builders the key-norm scales of the fused prologue). The
 // tiles are MN-major without swizzle, the layout in which the staged rows
 // already lie: a 16-byte row holds 8 consecutive key columns (or value rows)
 // of one token, so building a tile moves whole 16-byte pieces of the staged k,
