@@ -33,6 +33,12 @@ FALLBACK_HBM_GBS = 6800.0
 # The ALU-bound kernels (chunked forward, backward) spend one SFU reciprocal per
 # element-token; their roofline is the reciprocal rate per clock and SM, measured
 # live by the library's issue-rate probe, x the SM count x the maximum SM clock.
+# The backward is also set against the FP32 arithmetic it cannot avoid, per
+# element-token: one forward step to recover the state (I and M: two FMA each),
+# mu = M r, the adjoint step (q r, dy q r, its product with mu, and the two carried
+# FMAs of gM and gI) and the gradient sums (dq: 1, dk: 2, the two row sums, and J:
+# 1), 16 operations at the probe's FP32 FMA rate.
+BWD_MIN_FP32_OPS = 16
 
 # DRAM bytes per launch (dram__bytes_read.sum + dram__bytes_write.sum) of a kernel from one ncu
 # capture, valid only while the kernel's source file is byte-identical to the one captured
@@ -507,13 +513,24 @@ def run_ours(args, ws, rank, local):
             "over_dense_pair": pair_var_ms / (fwd_ck_ms + bwd_ck_ms), "sequences": len(lengths), "max_seqlen": mx,
             "note": "checkpointed packed forward + packed backward from its checkpoints over the varlen line's "
                     "ragged batch; timed after the timed region"}
-        kernels["palimpsa_backward"] = {"avg_ms": bwd_ms, "head_tokens_per_s": B * H * T / (bwd_ms / 1e3),
-                                        "over_forward": bwd_ms / fwd_avg_ms,
-                                        "checkpointed_forward_ms": fwd_ck_ms,
-                                        "from_checkpoints_ms": bwd_ck_ms,
-                                        "note": "gradients of <dy, y> w.r.t. q, k, v, beta, d_t, A, I_prior; "
-                                                "from_checkpoints: reading the states a checkpointed forward "
-                                                "wrote; timed after the timed region"}
+        fp32_peak = n_sms * rates["ffma"] * sm_max * 1e6 / BWD_MIN_FP32_OPS / 1e9  # G element-tokens/s
+        bwd_rate = {name: E_fwd / (ms / 1e3) / 1e9 for name, ms in (("recomputing", bwd_ms),
+                                                                      ("from_checkpoints", bwd_ck_ms))}
+        kernels["palimpsa_backward"] = {
+            "avg_ms": bwd_ms, "head_tokens_per_s": B * H * T / (bwd_ms / 1e3),
+            "over_forward": bwd_ms / fwd_avg_ms,
+            "checkpointed_forward_ms": fwd_ck_ms,
+            "from_checkpoints_ms": bwd_ck_ms,
+            "sfu": {"achieved": bwd_rate, "peak": alu_peak, "unit": "G element-tokens/s",
+                    "frac": {k: v / alu_peak for k, v in bwd_rate.items()}},
+            "fp32": {"achieved": bwd_rate, "peak": fp32_peak, "unit": "G element-tokens/s",
+                     "frac": {k: v / fp32_peak for k, v in bwd_rate.items()},
+                     "ops_per_element_token": BWD_MIN_FP32_OPS,
+                     "peak_source": f"{n_sms} SMs x {rates['ffma']:.1f} FP32 FMA/clk/SM (probe) x {sm_max:.0f} MHz "
+                                    f"/ {BWD_MIN_FP32_OPS} ops"},
+            "note": "gradients of <dy, y> w.r.t. q, k, v, beta, d_t, A, I_prior; "
+                    "from_checkpoints: reading the states a checkpointed forward "
+                    "wrote; timed after the timed region"}
 
     e2e = None
     if not args.no_e2e:
