@@ -163,3 +163,60 @@ def test_random_packed_batch_forward_and_training_pair(i):
         assert rel_l2(grads[n].cpu().numpy(), rg[m]) <= TIGHT, (n, c)
     ok, detail = dA_within_bar(grads["dA"].cpu(), rg["A"], grads["dd_t"].cpu(), rg["d_t"], x["d_t"], x["A"])
     assert ok, ("dA", detail, c)
+
+
+# ------------------------------------------------------------ the tensor-core summaries
+N_TC = 24
+
+
+def _draw_tc(i):
+    """A time split whose summaries run on the tensor cores (bf16 inputs, d_k = 128,
+    d_v a multiple of 32 up to 128), with ragged segment ends and, for half the
+    draws, the fused prologue (its q/k norm and v* modes reach the summaries too)."""
+    r = np.random.default_rng(9800 + i)
+    fused = bool(r.integers(0, 2))
+    return dict(B=int(r.integers(1, 3)), H=int(r.integers(1, 4)), T=int(r.choice([33, 65, 100, 257, 511, 700])),
+                d_v=int(r.choice([32, 64, 96, 128])), segments=int(r.integers(2, 10)),
+                dt_mean=float(r.choice([-2.0, -1.0, 0.0])), with_state=bool(r.integers(0, 2)), fused=fused,
+                qk_norm=fused and bool(r.integers(0, 2)), v_star=fused and bool(r.integers(0, 2)),
+                seed=int(r.integers(1, 1 << 30)))
+
+
+@pytest.mark.parametrize("i", range(N_TC))
+def test_random_time_split_on_the_tensor_cores(i):
+    from oracle import prologue as opro
+    c = _draw_tc(i)
+    wl = syn.WORKLOADS["small_layer"].with_(B=c["B"], H=c["H"], T=c["T"], d_k=128, d_v=c["d_v"], bf16=True,
+                                            dt_mean=c["dt_mean"], seed=c["seed"])
+    plan = pal.palimpsa_forward_plan(c["B"], c["H"], c["T"], 128, c["d_v"], bf16=True)
+    g = torch.Generator().manual_seed(c["seed"] + 1)
+    shape = (c["B"], c["H"], c["d_v"], 128)
+    mu0 = torch.randn(shape, generator=g) if c["with_state"] else None
+    I0 = (0.5 + 3.0 * torch.rand(shape, generator=g)) if c["with_state"] else None
+    d = lambda t: None if t is None else t.to(DEV)
+    f = syn.as_float64_numpy
+    fo = lambda t: None if t is None else f(t)
+    pal.palimpsa_set_forward_segments(c["segments"])
+    try:
+        seg = pal.palimpsa_forward_plan(c["B"], c["H"], c["T"], 128, c["d_v"], bf16=True)["segments"]
+        if c["fused"]:
+            inp = syn.sequence_inputs(wl, raw=True)
+            gi = {k: d(v) for k, v in inp.items()}
+            out = pal.palimpsa_forward_fused(gi["q"], gi["k"], gi["v"], gi["beta_raw"], gi["d_raw"], gi["A"],
+                                             gi["I_prior"], gi["b_scale"], d(mu0), d(I0), qk_norm=c["qk_norm"],
+                                             v_star=c["v_star"])
+            ref = opro.forward(f(inp["q"]), f(inp["k"]), f(inp["v"]), f(inp["beta_raw"]), f(inp["d_raw"]),
+                               f(inp["A"]), f(inp["I_prior"]), b_scale=f(inp["b_scale"]), mu0=fo(mu0), I0=fo(I0),
+                               qk_norm=c["qk_norm"], v_star=c["v_star"])
+        else:
+            inp = syn.sequence_inputs(wl)
+            gi = {k: d(v) for k, v in inp.items()}
+            out = pal.palimpsa_forward_chunked(gi["q"], gi["k"], gi["v"], gi["beta"], gi["d_t"], gi["A"],
+                                               gi["I_prior"], d(mu0), d(I0))
+            ref = oracle_forward_from(inp, mu0, I0)
+    finally:
+        pal.palimpsa_set_forward_segments(0)
+    assert seg > 1, (c, plan)
+    assert pal.palimpsa_get_device_status() == 0, c
+    for name, got, want in zip(("y", "mu_T", "I_T"), out, ref):
+        assert rel_l2(got.cpu().numpy(), want) <= TIGHT, (name, c)
