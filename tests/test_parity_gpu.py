@@ -816,6 +816,52 @@ def test_backward_full_size_small_layer_sampled_head():
         assert rel_l2(out[n][h:h + 1].cpu().numpy(), ref[m]) <= TIGHT, n
 
 
+@pytest.mark.parametrize("name,b,h,r0", [("layer_760m", 7, 23, 60), ("long_context", 0, 17, 12)])
+def test_backward_full_size_sampled_rows(name, b, h, r0):
+    """The backward at the full size of the 760M layer (8 x 24 x 4096) and of the long
+    context (32 x 32768, long memory), with the loss on four value rows of one
+    sequence: rows are independent in Eq. (5), so every gradient of that loss is the
+    fp64 autograd of the four-row problem, and all other rows, sequences and heads get
+    exactly zero. dA (a sum over 4096 or 32768 tokens) is held through dd_t."""
+    from oracle import autograd as ag
+    from tests._helpers import dA_within_bar
+    wl = syn.WORKLOADS[name]
+    inp = syn.sequence_inputs(wl)
+    rows = slice(r0, r0 + 4)
+    g = torch.Generator().manual_seed(4343)
+    dy = torch.zeros((wl.B, wl.H, wl.T, wl.d_v))
+    dy[b, h, :, rows] = torch.randn((wl.T, 4), generator=g)
+    gi = _gpu(inp)
+    out = pal.palimpsa_backward(gi["q"], gi["k"], gi["v"], gi["beta"], gi["d_t"], gi["A"], gi["I_prior"], None,
+                                None, dy.to(DEV), want_state_grads=False)
+    assert pal.palimpsa_get_device_status() == 0
+    f = syn.as_float64_numpy
+    one = lambda t: f(t[b:b + 1, h:h + 1])
+    sub = dict(q=one(inp["q"]), k=one(inp["k"]), v=one(inp["v"])[..., rows], beta=one(inp["beta"])[..., rows],
+               d_t=one(inp["d_t"]), A=f(inp["A"][h:h + 1]), I_prior=f(inp["I_prior"][h:h + 1]), mu0=None, I0=None)
+    ref = ag.gradients(sub, f(dy[b:b + 1, h:h + 1, :, rows]))
+    for n, m in (("dq", "q"), ("dk", "k"), ("dd_t", "d_t")):
+        assert rel_l2(out[n][b:b + 1, h:h + 1].cpu().numpy(), ref[m]) <= TIGHT, n
+    for n, m in (("dv", "v"), ("dbeta", "beta")):
+        assert rel_l2(out[n][b:b + 1, h:h + 1, :, rows].cpu().numpy(), ref[m]) <= TIGHT, n
+    assert rel_l2(out["dI_prior"][h:h + 1].cpu().numpy(), ref["I_prior"]) <= TIGHT
+    ok, detail = dA_within_bar(out["dA"][h:h + 1].cpu(), ref["A"], out["dd_t"][b:b + 1, h:h + 1].cpu(), ref["d_t"],
+                               one(inp["d_t"]), f(inp["A"][h:h + 1]))
+    assert ok, detail
+    # nothing leaks into rows, sequences or heads without a loss
+    mask = torch.zeros((wl.B, wl.H), dtype=torch.bool)
+    mask[b, h] = True
+    for n in ("dq", "dk", "dd_t"):
+        assert not out[n][~mask.to(DEV)].any(), n
+    for n in ("dv", "dbeta"):
+        t = out[n].clone()
+        t[b, h, :, rows] = 0
+        assert not t.any(), n
+    others = torch.ones(wl.H, dtype=torch.bool)
+    others[h] = False
+    assert not out["dA"][others.to(DEV)].any() and not out["dI_prior"][others.to(DEV)].any()
+
+
 def test_host_inputs_on_a_side_stream():
     """Host inputs with a caller's stream: the copies in, the kernels and the
     copies out all run on that stream, so the results equal the device path's."""
