@@ -52,10 +52,13 @@ using namespace fwd;
 
 // ------------------------------------------------------------------ pass C
 // The recurrence with the readout over one segment (the whole sequence when
-// S = 1), from the segment's true initial state.
-template <int DK, bool BF16, int RG, int R>
+// S = 1), from the segment's true initial state. The chunk length C is a
+// compile-time constant (16 or 32 tokens), so that the per-token operand
+// arrays lie at fixed distances from one another in shared memory and one
+// address per token serves all of a token's loads.
+template <int DK, bool BF16, int RG, int R, int C>
 __global__ void __launch_bounds__(RG / (4 * R) * 32)
-palimpsa_fwd_chunked_kernel(FwdArgs a, int C, int nseg, int seg_len, const float* __restrict__ seg_state) {
+palimpsa_fwd_chunked_kernel(FwdArgs a, int nseg, int seg_len, const float* __restrict__ seg_state) {
   constexpr int NV = DK / 32;                 // float4 column blocks per thread
   constexpr int NTH = RG / (4 * R) * 32;      // threads per CTA
   constexpr int ES = BF16 ? 2 : 4;
@@ -489,28 +492,37 @@ struct Kernels {
   static size_t smem(const FwdArgs& a, int C) { return FwdSmem(C, DK, a.d_v, RG, BF16 ? 2 : 4).total; }
 
   static int ctas_per_sm(const FwdArgs& a, int C) {
-    auto kern = palimpsa_fwd_chunked_kernel<DK, BF16, RG, kRowsPerThread>;
-    const size_t sm = smem(a, C);
+    return C == 16 ? ctas_per_sm_c<16>(a) : ctas_per_sm_c<32>(a);
+  }
+  template <int CC>
+  static int ctas_per_sm_c(const FwdArgs& a) {
+    auto kern = palimpsa_fwd_chunked_kernel<DK, BF16, RG, kRowsPerThread, CC>;
+    const size_t sm = smem(a, CC);
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm) != cudaSuccess) return 1;
     int n = 1;
     if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kern, kThreads, sm) != cudaSuccess || n < 1) n = 1;
     return n;
   }
 
+  // The chunk is 16 or 32 tokens (the planner's choice).
   static cudaError_t run(const FwdArgs& a, int C, int nseg, int seg_len, float* scratch, cudaStream_t s) {
-    const size_t sm = smem(a, C);
+    return C == 16 ? run_c<16>(a, nseg, seg_len, scratch, s) : run_c<32>(a, nseg, seg_len, scratch, s);
+  }
+  template <int CC>
+  static cudaError_t run_c(const FwdArgs& a, int nseg, int seg_len, float* scratch, cudaStream_t s) {
+    const size_t sm = smem(a, CC);
     const long groups = a.d_v / RG;
     const long heads = (long)a.B * a.H;
-    auto main_k = palimpsa_fwd_chunked_kernel<DK, BF16, RG, kRowsPerThread>;
+    auto main_k = palimpsa_fwd_chunked_kernel<DK, BF16, RG, kRowsPerThread, CC>;
     cudaError_t e = cudaFuncSetAttribute(main_k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
     if (e != cudaSuccess) return e;
-    if (nseg > 1 && (e = prefix(a, C, nseg, seg_len, scratch, s)) != cudaSuccess) return e;
+    if (nseg > 1 && (e = prefix(a, CC, nseg, seg_len, scratch, s)) != cudaSuccess) return e;
     if (nseg > 1) {
-      e = launch_dependent(main_k, dim3((unsigned)(heads * nseg * groups)), dim3(kThreads), sm, s, a, C, nseg,
-                           seg_len, (const float*)scratch);
+      e = launch_dependent(main_k, dim3((unsigned)(heads * nseg * groups)), dim3(kThreads), sm, s, a, nseg, seg_len,
+                           (const float*)scratch);
       return e != cudaSuccess ? e : cudaGetLastError();
     }
-    main_k<<<(unsigned)(heads * nseg * groups), kThreads, sm, s>>>(a, C, nseg, seg_len, scratch);
+    main_k<<<(unsigned)(heads * nseg * groups), kThreads, sm, s>>>(a, nseg, seg_len, scratch);
     return cudaGetLastError();
   }
 
