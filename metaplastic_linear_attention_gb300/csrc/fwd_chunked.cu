@@ -246,12 +246,14 @@ palimpsa_fwd_chunked_kernel(FwdArgs a, int nseg, int seg_len, const float* __res
         float yk = (hi ? y1 : y0) + __shfl_xor_sync(0xffffffffu, hi ? y0 : y1, 4);
         yk += __shfl_xor_sync(0xffffffffu, yk, 2);
         yk += __shfl_xor_sync(0xffffffffu, yk, 1);
-        if ((cg & 3) == 0) gy[(size_t)(t0 + t) * DV + (cg >> 2)] = yk;
+        // the four lanes of each half hold the same sum (a butterfly; IEEE addition
+        // commutes), so all of them store it: no branch around the store
+        gy[(size_t)(t0 + t) * DV + (cg >> 2)] = yk;
       } else {
         float yv = acc[0].x + acc[0].y;
 #pragma unroll
         for (int m = 1; m < kLanesPerRow; m <<= 1) yv += __shfl_xor_sync(0xffffffffu, yv, m);
-        if (cg == 0) gy[(size_t)(t0 + t) * DV] = yv;
+        gy[(size_t)(t0 + t) * DV] = yv;  // every lane of the team holds the same sum
       }
     }
     // (the barrier at the top of the next chunk orders these reads before the

@@ -144,7 +144,8 @@ palimpsa_fwd_nometa_kernel(FwdArgs a, int C, int nseg, int seg_len, const float*
 #pragma unroll
         for (int m = 1; m < kLanesPerRow; m <<= 1) yv[r] += __shfl_xor_sync(0xffffffffu, yv[r], m);
       }
-      if (cg == 0) *reinterpret_cast<float2*>(gy + (size_t)(t0 + t) * DV) = make_float2(yv[0], yv[1]);
+      // every lane of the row team holds the same sums (a butterfly), so all store them
+      *reinterpret_cast<float2*>(gy + (size_t)(t0 + t) * DV) = make_float2(yv[0], yv[1]);
     }
     __syncthreads();  // operands of this chunk fully read before the next conversion
   }
