@@ -400,7 +400,16 @@ palimpsa_bwd_kernel(BwdArgs a, float* __restrict__ ckpt) {
       store_rows<NP>(cp, 2 * DK, M);
       store_rows<NP>(cp + DK, 2 * DK, I);
       __syncthreads();  // gates ready
-      for (int u = 0; u < tn; ++u) {
+      const int whole = tn / kWin * kWin;  // 8 tokens at a time without a per-token branch
+      for (int u0 = 0; u0 < whole; u0 += kWin) {
+#pragma unroll
+        for (int uu = 0; uu < kWin; ++uu) {
+          float2 k[NP];
+          lane_pairs<NP>(kf, DK, u0 + uu, c0, k);
+          step_rows<NP>(M, I, k, tok2(bsm, L, u0 + uu, g));
+        }
+      }
+      for (int u = whole; u < tn; ++u) {
         float2 k[NP];
         lane_pairs<NP>(kf, DK, u, c0, k);
         step_rows<NP>(M, I, k, tok2(bsm, L, u, g));
@@ -449,7 +458,19 @@ palimpsa_bwd_kernel(BwdArgs a, float* __restrict__ ckpt) {
           win_at(wi, 1, r, p) = I[r][p];
         }
     };
-    for (int u = 0; u < stop; ++u) {
+    // whole windows with their tokens unrolled (no per-token branch), then the
+    // sequence's last, partial window when the re-run goes on to the end
+    const int whole = stop / kWin;
+    for (int wr = 0; wr < whole; ++wr) {
+      keep_start(wr);
+#pragma unroll
+      for (int uu = 0; uu < kWin; ++uu) {
+        float2 k[NP];
+        lane_pairs<NP>(kf, DK, wr * kWin + uu, c0, k);
+        step_rows<NP>(M, I, k, tok2(bsm, L, wr * kWin + uu, g));
+      }
+    }
+    for (int u = whole * kWin; u < stop; ++u) {
       if (u % kWin == 0) keep_start(u / kWin);
       float2 k[NP];
       lane_pairs<NP>(kf, DK, u, c0, k);
