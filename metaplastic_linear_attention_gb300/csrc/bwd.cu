@@ -119,9 +119,11 @@ __device__ __forceinline__ void cp_async_wait_1() { asm volatile("cp.async.wait_
 // Addresses: a token of q or k is d_k * ES bytes (a multiple of 16); the CTA's
 // 8 rows of v or beta are 8 * ES contiguous bytes at row0 * ES (row0 is a
 // multiple of 8), and of dy 32 bytes; d_t goes 4 bytes at a time.
+// Without q_dy (the forward sweep's segments, except its last, which the
+// adjoint sweep reuses) q and dy are not copied.
 template <int DK, int ES>
 __device__ __forceinline__ void stage_segment(unsigned char* st, const BwdSmem& L, const BwdArgs& a, size_t head_tok,
-                                              int row0, int ts, int tn) {
+                                              int row0, int ts, int tn, bool q_dy = true) {
   const int DV = a.d_v;
   const size_t tok0 = head_tok + ts;
   const int kq = tn * DK * ES / 16;
@@ -129,7 +131,7 @@ __device__ __forceinline__ void stage_segment(unsigned char* st, const BwdSmem& 
   const char* gq = static_cast<const char*>(a.q) + tok0 * DK * ES;
   for (int i = threadIdx.x; i < kq; i += kThreads) {
     cp_async16(st + L.k + 16 * (size_t)i, gk + 16 * (size_t)i);
-    cp_async16(st + L.q + 16 * (size_t)i, gq + 16 * (size_t)i);
+    if (q_dy) cp_async16(st + L.q + 16 * (size_t)i, gq + 16 * (size_t)i);
   }
   constexpr int RP = kRowsPerCta * ES / 16;   // 16-byte pieces of one token's rows (v, beta)
   for (int i = threadIdx.x; i < tn * RP; i += kThreads) {
@@ -139,7 +141,7 @@ __device__ __forceinline__ void stage_segment(unsigned char* st, const BwdSmem& 
     cp_async16(st + L.b + (size_t)u * kRowsPerCta * ES + 16 * pc, static_cast<const char*>(a.beta) + g);
   }
   constexpr int DP = kRowsPerCta * 4 / 16;    // pieces of one token's dy rows
-  for (int i = threadIdx.x; i < tn * DP; i += kThreads) {
+  for (int i = threadIdx.x; q_dy && i < tn * DP; i += kThreads) {
     const int u = i / DP, pc = i % DP;
     cp_async16(st + L.dy + (size_t)u * kRowsPerCta * 4 + 16 * pc,
                reinterpret_cast<const char*>(a.dy + (tok0 + u) * DV + row0) + 16 * pc);
@@ -181,9 +183,9 @@ __device__ __forceinline__ void rs_level(float (&x)[V], int lane, int m) {
 
 // All threads, once per staged segment: the gate table (alpha, (1 - alpha)
 // I_prior, 1 - alpha per token, one 16-byte load), the row tables (beta_i, beta_i v_i of the CTA's 8 rows)
-// and, for bf16 inputs, fp32 copies of k and q. Callers order this with
-// barriers on both sides.
-template <int DK, bool BF16>
+// and, for bf16 inputs, fp32 copies of k and (WITH_Q: the adjoint sweep reads it) q.
+// Callers order this with barriers on both sides.
+template <int DK, bool BF16, bool WITH_Q = true>
 __device__ __forceinline__ void prepare_segment(const unsigned char* st, unsigned char* bsm, const BwdSmem& L, int tn,
                                                 float A_h, float Ip) {
   const float* dt = reinterpret_cast<const float*>(st + L.dt);
@@ -206,7 +208,7 @@ __device__ __forceinline__ void prepare_segment(const unsigned char* st, unsigne
     const int n4 = tn * DK / 4;
     for (int x = threadIdx.x; x < n4; x += kThreads) {
 #pragma unroll
-      for (int which = 0; which < 2; ++which) {
+      for (int which = 0; which < (WITH_Q ? 2 : 1); ++which) {
         const uint2 w = reinterpret_cast<const uint2*>(st + (which ? L.q : L.k))[x];
         reinterpret_cast<float4*>(bsm + (which ? L.qf : L.kf))[x] =
             make_float4(bf16_lo(w.x), bf16_hi(w.x), bf16_lo(w.y), bf16_hi(w.y));
@@ -383,18 +385,18 @@ palimpsa_bwd_kernel(BwdArgs a, float* __restrict__ ckpt) {
                             T - (nseg - 1) * kSeg);
     cp_async_commit();
   } else {
-    if (nseg > 0) stage_segment<DK, ES>(bsm, L, a, head_tok, row0, 0, min(kSeg, T));
+    if (nseg > 0) stage_segment<DK, ES>(bsm, L, a, head_tok, row0, 0, min(kSeg, T), nseg == 1);
     cp_async_commit();
     for (int s = 0; s < nseg; ++s) {
       const int ts = s * kSeg, tn = min(kSeg, T - ts);
       if (s + 1 < nseg)
         stage_segment<DK, ES>(bsm + (size_t)((s + 1) & 1) * L.stage, L, a, head_tok, row0, ts + kSeg,
-                              min(kSeg, T - ts - kSeg));
+                              min(kSeg, T - ts - kSeg), s + 1 == nseg - 1);
       cp_async_commit();
       cp_async_wait_1();
       __syncthreads();  // segment s staged by every thread
       const unsigned char* st = bsm + (size_t)(s & 1) * L.stage;
-      prepare_segment<DK, BF16>(st, bsm, L, tn, A_h, Ip);
+      prepare_segment<DK, BF16, false>(st, bsm, L, tn, A_h, Ip);  // the forward sweep reads no q
       const float* kf = reinterpret_cast<const float*>(BF16 ? bsm + L.kf : st + L.k);
       float* cp = ck_out + (size_t)s * ck_step;
       store_rows<NP>(cp, 2 * DK, M);
