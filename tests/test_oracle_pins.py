@@ -371,3 +371,24 @@ def test_autograd_gradients_equal_finite_differences_of_the_c_oracle(with_state)
             dm[name][idx] -= h
             fd[idx] = (loss(dp) - loss(dm)) / (2 * h)
         np.testing.assert_allclose(g[name], fd, rtol=2e-6, atol=2e-7, err_msg=name)
+
+
+def test_autograd_gradients_of_an_empty_sequence():
+    """T = 0: the final state is the initial one, so dmu0 = dmu_T and dI0 = dI_T
+    exactly (mu_T = mu0, I_T = I0); with no final-state cotangent the loss is a
+    constant and every gradient is zero, A and I_prior included."""
+    from oracle import autograd as ag
+    rng = _rng(90)
+    B, H, dk, dv = 1, 2, 3, 2
+    q, k, v, beta, d_t, A, I_prior = _random_problem(rng, B, H, 0, dk, dv, unit_keys=False)
+    inp = dict(q=q, k=k, v=v, beta=beta, d_t=d_t, A=A, I_prior=I_prior,
+               mu0=rng.standard_normal((B, H, dv, dk)), I0=rng.uniform(0.5, 2.0, (B, H, dv, dk)))
+    dmu = rng.standard_normal((B, H, dv, dk))
+    dI = rng.standard_normal((B, H, dv, dk))
+    g = ag.gradients(inp, np.zeros((B, H, 0, dv)), dmu, dI)
+    np.testing.assert_array_equal(g["mu0"], dmu)
+    np.testing.assert_array_equal(g["I0"], dI)
+    assert not g["A"].any() and not g["I_prior"].any()
+    g0 = ag.gradients(inp, np.zeros((B, H, 0, dv)))
+    for name in ("mu0", "I0", "A", "I_prior"):
+        assert not g0[name].any(), name
