@@ -206,13 +206,19 @@ __device__ __forceinline__ void prepare_segment(const unsigned char* st, unsigne
     // 4 bf16 values (8 bytes) in, one float4 out per item: consecutive threads store
     // consecutive 16 bytes, so the stores are free of bank conflicts
     const int n4 = tn * DK / 4;
-    for (int x = threadIdx.x; x < n4; x += kThreads) {
+    auto convert = [&](const int x) {
 #pragma unroll
       for (int which = 0; which < (WITH_Q ? 2 : 1); ++which) {
         const uint2 w = reinterpret_cast<const uint2*>(st + (which ? L.q : L.k))[x];
         reinterpret_cast<float4*>(bsm + (which ? L.qf : L.kf))[x] =
             make_float4(bf16_lo(w.x), bf16_hi(w.x), bf16_lo(w.y), bf16_hi(w.y));
       }
+    };
+    if (tn == kSeg) {  // a whole segment: a fixed count per thread, unrolled so the loads go out together
+#pragma unroll
+      for (int i = 0; i < kSeg * DK / 4 / kThreads; ++i) convert(threadIdx.x + i * kThreads);
+    } else {
+      for (int x = threadIdx.x; x < n4; x += kThreads) convert(x);
     }
   }
 }
