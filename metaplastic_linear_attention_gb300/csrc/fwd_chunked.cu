@@ -179,7 +179,7 @@ palimpsa_fwd_chunked_kernel(FwdArgs a, int nseg, int seg_len, const float* __res
     // ---- convert the staged chunk to fp32 operands shared by all rows
     const unsigned char* raw = pipe.raw(c);
     convert_keys<DK, BF16, true, NTH>(raw, L, smem, tc, a.pro.qk_norm);
-    for (int it = threadIdx.x; it < tc * RG; it += NTH) {
+    auto row_item = [&](const int it) {
       const int t = it / RG, r = it % RG;
       const size_t e = (size_t)t * DV + tl.row0 + r;
       const float vv = raw_elem<BF16>(raw + L.raw_v, e);
@@ -188,6 +188,13 @@ palimpsa_fwd_chunked_kernel(FwdArgs a, int nseg, int seg_len, const float* __res
       domain_bad |= !nonneg_finite(bb);
       bvf[it] = a.pro.v_star ? vv : bb * vv;
       bfv[it] = bb;
+    };
+    if (tc == C) {  // a whole chunk: a fixed count per thread, unrolled so the loads go out together
+      static_assert(C * RG % NTH == 0, "whole chunks split evenly over the threads");
+#pragma unroll
+      for (int i = 0; i < C * RG / NTH; ++i) row_item((int)threadIdx.x + i * NTH);
+    } else {
+      for (int it = threadIdx.x; it < tc * RG; it += NTH) row_item(it);
     }
     for (int t = threadIdx.x; t < tc; t += NTH) {  // one token per thread at most (tc <= 32 <= NTH)
       float d = d_cur;
